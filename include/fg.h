@@ -1,0 +1,200 @@
+/*
+ * fg.h -- C ABI of libfg.so: the OPT-style transformer layer of FlexGen on
+ * weights and KV cache stored in fine-grained asymmetric 4-bit groups of 64,
+ * for one NVIDIA GB300 (sm_103a).
+ *
+ * Sources (FlexGen notes, papercache.org, "FlexGen: High-Throughput Generative
+ * Inference of Large Language Models with a Single GPU"):
+ *   [BG]  section "背景知识" (Background): the prefill equations
+ *         x_K = x w_K, x_V = x w_V, x_Q = x w_Q,
+ *         x_Out = Softmax(x_Q x_K^T / sqrt(h1)) x_V w_O + x,
+ *         x' = relu(x_Out w_1) w_2 + x_Out,
+ *         and the decode equations with KV Concat for t in R^{b x 1 x h1}.
+ *   [S5]  section "5. 近似方法" (Approximate Methods): group-wise asymmetric
+ *         quantization x_q = round((x - min)/(max - min) * (2^b - 1)), b = 4,
+ *         g = 64, weights grouped along the output channel, KV along the
+ *         hidden dimension, stored quantized and converted back to FP16
+ *         before compute.
+ *   [S4]  section "4. 卸载策略": the zig-zag block schedule -- one load of a
+ *         layer's weights serves every sequence of the block.
+ *
+ * Conventions for every entry point:
+ *   - All pointers named "device" are CUDA device pointers on the current
+ *     device; the caller owns every buffer.  The library never allocates
+ *     device memory and keeps no per-call state on the host.
+ *   - Calls are asynchronous on `stream` (0 = legacy default stream).
+ *     Argument errors are returned synchronously before anything is
+ *     launched; a failed launch returns FG_ERR_CUDA.  Errors raised inside a
+ *     kernel (a bounded wait that ran out) are reported by fg_sync_status.
+ *   - Grouping is always along the innermost, contiguous dimension of the
+ *     tensor named, in groups of 64 consecutive elements.  A 4-bit tensor
+ *     of logical shape [R][C] is three arrays:
+ *         codes  uint8 [R][C/2]   byte j = q[2j] | q[2j+1] << 4
+ *         mins   fp32  [R][C/64]  group minimum
+ *         scales fp32  [R][C/64]  (max - min) / 15
+ *     and element (r, c) is restored as fmaf(q, scale, min) in fp32
+ *     (then rounded to fp16 when the consumer computes in fp16).
+ *   - Codes and activations must be 16-byte aligned (FG_ERR_ALIGN), mins and
+ *     scales 4-byte aligned.
+ *   - No CPU fallback exists: every operation runs in the library's CUDA
+ *     kernels.
+ */
+#ifndef FG_H_
+#define FG_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FG_OK = 0,
+  FG_ERR_ARG = 1,             /* null pointer, negative size, bad enum      */
+  FG_ERR_SHAPE = 2,           /* a dimension breaks a divisibility rule     */
+  FG_ERR_ALIGN = 3,           /* pointer alignment                          */
+  FG_ERR_CAPACITY = 4,        /* KV slot outside [0, capacity)              */
+  FG_ERR_WORKSPACE = 5,       /* workspace null or smaller than required   */
+  FG_ERR_CUDA = 6,            /* a CUDA runtime call or launch failed       */
+  FG_ERR_DEVICE_TIMEOUT = 7,  /* a kernel gave up a bounded wait            */
+  FG_ERR_UNSUPPORTED = 8      /* valid, but not implemented (e.g. head_dim) */
+} fg_status;
+
+typedef enum { FG_F16 = 0, FG_F32 = 1 } fg_dtype;               /* activations */
+typedef enum { FG_CODEC_NONE = 0, FG_CODEC_Q4G64 = 1 } fg_codec; /* storage     */
+
+/* One weight matrix w in R^{K x N}, used as x . w ([BG]); K = input
+ * features, N = output features.  With FG_CODEC_Q4G64: codes [K][N/2],
+ * mins and scales [K][N/64] -- each group is 64 consecutive output channels
+ * at one input index ([S5]: "along the output-channel dimension").  With
+ * FG_CODEC_NONE: dense [K][N] in the layer's activation dtype.  Device. */
+typedef struct {
+  const uint8_t* codes;
+  const float* mins;
+  const float* scales;
+  const void* dense;
+  int64_t K, N;
+} fg_wmat;
+
+/* One transformer layer ([BG]): w_Q, w_K, w_V, w_O in R^{h1 x h1},
+ * w_1 in R^{h1 x h2}, w_2 in R^{h2 x h1}; `heads` attention heads of
+ * head_dim = h1 / heads (score scale 1/sqrt(head_dim); heads = 1 is the
+ * page's 1/sqrt(h1)).  h1 and h2 must be multiples of 64; head_dim must be
+ * 64 or 128. */
+typedef struct {
+  fg_wmat wq, wk, wv, wo, w1, w2;
+  int64_t h1, h2;
+  int32_t heads;
+  fg_codec codec;
+  fg_dtype dtype;
+} fg_layer;
+
+/* One layer's KV cache for b sequences ([BG] x_K, x_V, grown by Concat).
+ * Layout [b][heads][capacity][head_dim]; a token's K (or V) row of h1 =
+ * heads * head_dim values is quantized in groups of 64 along the hidden
+ * dimension ([S5]), which never straddle heads because head_dim % 64 == 0.
+ *   FG_CODEC_Q4G64: {k,v}_codes uint8 [b][H][cap][d/2],
+ *                   {k,v}_mins, {k,v}_scales fp32 [b][H][cap][d/64]
+ *   FG_CODEC_NONE:  {k,v}_dense [b][H][cap][d] in `dtype`.
+ * Device memory owned by the caller; slot p holds the token at position p. */
+typedef struct {
+  uint8_t* k_codes;
+  uint8_t* v_codes;
+  float* k_mins;
+  float* k_scales;
+  float* v_mins;
+  float* v_scales;
+  void* k_dense;
+  void* v_dense;
+  int64_t b, capacity;
+  int32_t heads, head_dim;
+  fg_codec codec;
+  fg_dtype dtype;
+} fg_kv;
+
+/* [S5] quantization equation.  x: device [rows][cols] of dtype `dt`
+ * (fp16 or fp32), cols % 64 == 0.  Writes codes [rows][cols/2], mins and
+ * scales [rows][cols/64].  Per group, in IEEE fp32 with round-to-nearest-
+ * even and no contraction: min/max in the total order of non-NaN values
+ * (-0 < +0; an all-NaN group gives NaN), r = max - min, scale = r / 15,
+ * q = clamp(rint(((x - min) / r) * 15), 0, 15) with a NaN quotient -> 0.
+ * rows == 0 is a no-op. */
+fg_status fg_quantize_g64(const void* x, fg_dtype dt, int64_t rows, int64_t cols,
+                          uint8_t* codes, float* mins, float* scales, cudaStream_t stream);
+
+/* [S5] "converted back to FP16 before compute".  Inverse of the layout
+ * above: out[r][c] = fmaf(q, scale, min) in fp32, stored as `dt` (fp16:
+ * round-to-nearest-even).  out: device [rows][cols]. */
+fg_status fg_dequant_g64(const uint8_t* codes, const float* mins, const float* scales,
+                         int64_t rows, int64_t cols, void* out, fg_dtype dt,
+                         cudaStream_t stream);
+
+/* [BG] decode, "x_K <- Concat(x_K, t w_K); x_V <- Concat(x_V, t w_V)":
+ * store the rows k_new, v_new (device [kv->b][h1], kv->dtype) at slot `pos`
+ * of every sequence, quantizing each 64-group of the hidden dimension with
+ * the fg_quantize_g64 arithmetic when kv->codec is FG_CODEC_Q4G64.
+ * pos outside [0, capacity) -> FG_ERR_CAPACITY. */
+fg_status fg_kv_append(const fg_kv* kv, const void* k_new, const void* v_new, int64_t pos,
+                       cudaStream_t stream);
+
+/* Workspace (device bytes) that fg_prefill_layer / fg_prefill_block need for
+ * b sequences of s tokens, and that fg_decode_step / fg_decode_block_step
+ * need for b sequences with a cache of `capacity` slots.  Pure host
+ * functions; 0 on invalid arguments. */
+size_t fg_prefill_workspace_bytes(const fg_layer* L, int64_t b, int64_t s);
+size_t fg_decode_workspace_bytes(const fg_layer* L, int64_t b, int64_t capacity);
+
+/* [BG] prefill of one layer.  x: device [b][s][h1] (L->dtype); y: device
+ * [b][s][h1] output x^{i+1}, must not overlap x.  Writes K/V rows of the s
+ * prompt tokens into slots 0..s-1 of kv (quantized per [S5]); attention is
+ * causal and reads K/V back through the codec, so the new tokens see the
+ * same values a later decode step reads.  Requires kv->b == b,
+ * s <= kv->capacity, and ws_bytes >= fg_prefill_workspace_bytes(L, b, s). */
+fg_status fg_prefill_layer(const fg_layer* L, const void* x, int64_t b, int64_t s,
+                           const fg_kv* kv, void* y, void* ws, size_t ws_bytes,
+                           cudaStream_t stream);
+
+/* [BG] one decode step of one layer for the whole block (zig-zag reuse [S4]:
+ * each weight is read once for all b sequences).  t: device [b][h1]; appends
+ * t w_K, t w_V at slot `pos` (Concat), attends over slots 0..pos and writes
+ * t^{i+1} to y (device [b][h1], must not overlap t).  pos outside
+ * [0, capacity) -> FG_ERR_CAPACITY. */
+fg_status fg_decode_step(const fg_layer* L, const void* t, int64_t b, int64_t pos,
+                         const fg_kv* kv, void* y, void* ws, size_t ws_bytes,
+                         cudaStream_t stream);
+
+/* [S4] zig-zag block, prefill half: run the prompt x (device [b][s][h1])
+ * through layers[0..l-1] with caches kvs[0..l-1]; the last layer's output
+ * goes to y (device [b][s][h1]).  Workspace as for fg_prefill_layer plus
+ * 2*b*s*h1 activation elements (see fg_prefill_block_workspace_bytes). */
+size_t fg_prefill_block_workspace_bytes(const fg_layer* L, int64_t b, int64_t s);
+fg_status fg_prefill_block(const fg_layer* layers, int32_t l, const void* x, int64_t b,
+                           int64_t s, const fg_kv* kvs, void* y, void* ws, size_t ws_bytes,
+                           cudaStream_t stream);
+
+/* [S4] zig-zag block, one generation step: feed t (device [b][h1]) through
+ * every layer at slot `pos`; the last layer's output goes to y. */
+size_t fg_decode_block_workspace_bytes(const fg_layer* L, int64_t b, int64_t capacity);
+fg_status fg_decode_block_step(const fg_layer* layers, int32_t l, const void* t, int64_t b,
+                               int64_t pos, const fg_kv* kvs, void* y, void* ws,
+                               size_t ws_bytes, cudaStream_t stream);
+
+/* Synchronize `stream`, then report (and clear) the device error word that
+ * kernels raise when a bounded wait runs out: FG_ERR_DEVICE_TIMEOUT, or
+ * FG_ERR_CUDA if the synchronization itself failed. */
+fg_status fg_sync_status(cudaStream_t stream);
+
+/* Human-readable name of a status, and the detail message of the most recent
+ * failing call on this host thread ("" if none). */
+const char* fg_status_str(fg_status s);
+const char* fg_last_error(void);
+
+/* Library version, e.g. "fg 0.1 sm_103a". */
+const char* fg_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FG_H_ */

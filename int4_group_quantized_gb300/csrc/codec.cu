@@ -1,0 +1,328 @@
+// The 4-bit group codec (FlexGen notes, "5. 近似方法", group-wise quantization
+// equation, b = 4, g = 64) and the KV-cache writes that use it.
+//
+// Every operation of the quantizer is an explicitly rounded fp32 intrinsic
+// (__fsub_rn, __fdiv_rn, __fmul_rn, rintf), so nothing can be contracted into
+// an FMA and the codes are bit-identical to an IEEE fp32 evaluation of
+// ((x - min) / (max - min)) * 15 rounded half-to-even.
+//
+// Layout of the work: a group of 64 consecutive elements is spread over 8
+// consecutive lanes, 8 elements each (one 16-byte load of fp16, two of fp32);
+// the group min/max is reduced with three xor-shuffles on order-preserving
+// integer keys, which makes the result independent of reduction order and
+// gives -0 < +0.  Each lane writes one 32-bit word of codes (8 nibbles); the
+// first lane of the group writes (min, scale).
+#include "fg_internal.cuh"
+
+namespace fg {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+// Monotone map from non-NaN floats to unsigned keys: a < b (with -0 < +0)
+// iff key(a) < key(b).
+__device__ __forceinline__ uint32_t order_key(float f) {
+  uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_to_float(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// Quantizes the 64-group held by the 8 lanes {8j .. 8j+7} of the warp (lane
+// 8j+p holds elements 8p .. 8p+7 in v).  All 32 lanes must call it.
+__device__ __forceinline__ uint32_t quantize_group8(const float (&v)[8], float& mn_out,
+                                                   float& scale_out) {
+  uint32_t kmin = 0xffffffffu, kmax = 0u;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    if (!isnan(v[i])) {
+      uint32_t k = order_key(v[i]);
+      kmin = min(kmin, k);
+      kmax = max(kmax, k);
+    }
+  }
+#pragma unroll
+  for (int off = 1; off < 8; off <<= 1) {
+    kmin = min(kmin, __shfl_xor_sync(kFull, kmin, off));
+    kmax = max(kmax, __shfl_xor_sync(kFull, kmax, off));
+  }
+  float mn, mx;
+  if (kmin == 0xffffffffu) {  // every member is NaN
+    mn = mx = __uint_as_float(0x7fffffffu);
+  } else {
+    mn = key_to_float(kmin);
+    mx = key_to_float(kmax);
+  }
+  const float r = __fsub_rn(mx, mn);
+  uint32_t packed = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float u = __fmul_rn(__fdiv_rn(__fsub_rn(v[i], mn), r), 15.0f);
+    const float q = fminf(fmaxf(rintf(u), 0.0f), 15.0f);  // NaN -> 0
+    packed |= static_cast<uint32_t>(q) << (4 * i);
+  }
+  mn_out = mn;
+  scale_out = __fdiv_rn(r, 15.0f);
+  return packed;
+}
+
+__device__ __forceinline__ void load8(const __half* p, float (&v)[8]) {
+  const uint4 raw = *reinterpret_cast<const uint4*>(p);
+  const __half2* h = reinterpret_cast<const __half2*>(&raw);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __half22float2(h[i]);
+    v[2 * i] = f.x;
+    v[2 * i + 1] = f.y;
+  }
+}
+__device__ __forceinline__ void load8(const float* p, float (&v)[8]) {
+  const float4 a = *reinterpret_cast<const float4*>(p);
+  const float4 b = *reinterpret_cast<const float4*>(p + 4);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+
+__device__ __forceinline__ void store8(__half* p, const float (&v)[8]) {
+  uint4 raw;
+  __half2* h = reinterpret_cast<__half2*>(&raw);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) h[i] = __floats2half2_rn(v[2 * i], v[2 * i + 1]);
+  *reinterpret_cast<uint4*>(p) = raw;
+}
+__device__ __forceinline__ void store8(float* p, const float (&v)[8]) {
+  *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+  *reinterpret_cast<float4*>(p + 4) = make_float4(v[4], v[5], v[6], v[7]);
+}
+
+// x viewed as ngroups consecutive groups of 64.
+template <typename T>
+__global__ void __launch_bounds__(256) quantize_kernel(const T* __restrict__ x, int64_t ngroups,
+                                                       uint32_t* __restrict__ codes,
+                                                       float* __restrict__ mins,
+                                                       float* __restrict__ scales) {
+  const int lane = threadIdx.x & 31;
+  const int part = lane & 7;
+  const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t base = warp * 4; base < ngroups; base += nwarps * 4) {
+    const int64_t g = base + (lane >> 3);
+    const bool valid = g < ngroups;
+    float v[8];
+    if (valid) {
+      load8(x + g * 64 + part * 8, v);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(0x7fffffffu);
+    }
+    float mn, sc;
+    const uint32_t packed = quantize_group8(v, mn, sc);
+    if (valid) {
+      codes[g * 8 + part] = packed;
+      if (part == 0) {
+        mins[g] = mn;
+        scales[g] = sc;
+      }
+    }
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) dequant_kernel(const uint32_t* __restrict__ codes,
+                                                      const float* __restrict__ mins,
+                                                      const float* __restrict__ scales,
+                                                      int64_t nwords, T* __restrict__ out) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t w = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; w < nwords;
+       w += stride) {
+    const uint32_t c = codes[w];
+    const int64_t g = w >> 3;  // 8 words of codes per group
+    const float mn = mins[g], sc = scales[g];
+    float v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __fmaf_rn(static_cast<float>((c >> (4 * i)) & 15u), sc, mn);
+    store8(out + w * 8, v);
+  }
+}
+
+// KV rows of T tokens per sequence -> cache slots pos0..pos0+T-1.  One
+// quantization group = 64 hidden values of one token of one of K/V.
+struct KVDst {
+  uint32_t* codes[2];
+  float* mins[2];
+  float* scales[2];
+};
+
+template <typename T>
+__global__ void __launch_bounds__(256) kv_store_q4_kernel(const T* __restrict__ ksrc,
+                                                          const T* __restrict__ vsrc, int64_t ld,
+                                                          int64_t b, int64_t ntok, int64_t pos0,
+                                                          int h1, int heads, int d, int64_t cap,
+                                                          KVDst dst) {
+  const int lane = threadIdx.x & 31;
+  const int part = lane & 7;
+  const int gpr = h1 >> 6;  // groups per token row
+  const int64_t ngroups = 2 * b * ntok * gpr;
+  const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t base = warp * 4; base < ngroups; base += nwarps * 4) {
+    int64_t g = base + (lane >> 3);
+    const bool valid = g < ngroups;
+    if (!valid) g = 0;
+    const int gi = static_cast<int>(g % gpr);
+    int64_t rest = g / gpr;
+    const int64_t row = rest % (b * ntok);  // bi * ntok + ti
+    const int which = static_cast<int>(rest / (b * ntok));
+    const int64_t bi = row / ntok, ti = row % ntok;
+    float v[8];
+    if (valid) {
+      load8((which ? vsrc : ksrc) + row * ld + gi * 64 + part * 8, v);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = 0.0f;
+    }
+    float mn, sc;
+    const uint32_t packed = quantize_group8(v, mn, sc);
+    if (valid) {
+      const int head = (gi * 64) / d;
+      const int wg = ((gi * 64) % d) >> 6;
+      const int64_t slot = (bi * heads + head) * cap + pos0 + ti;
+      dst.codes[which][(slot * (d >> 1) + wg * 32) / 4 + part] = packed;
+      if (part == 0) {
+        dst.mins[which][slot * (d >> 6) + wg] = mn;
+        dst.scales[which][slot * (d >> 6) + wg] = sc;
+      }
+    }
+  }
+}
+
+// Codec off: copy rows into the dense cache, 8 elements per thread.
+template <typename T>
+__global__ void kv_store_dense_kernel(const T* __restrict__ ksrc, const T* __restrict__ vsrc,
+                                      int64_t ld, int64_t b, int64_t ntok, int64_t pos0, int h1,
+                                      int heads, int d, int64_t cap, T* kd, T* vd) {
+  const int64_t n8 = 2 * b * ntok * (h1 / 8);
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
+       i += stride) {
+    const int c8 = static_cast<int>(i % (h1 / 8));
+    const int64_t rest = i / (h1 / 8);
+    const int64_t row = rest % (b * ntok);
+    const int which = static_cast<int>(rest / (b * ntok));
+    const int64_t bi = row / ntok, ti = row % ntok;
+    float v[8];
+    load8((which ? vsrc : ksrc) + row * ld + c8 * 8, v);
+    const int col = c8 * 8, head = col / d, dd = col % d;
+    T* out = which ? vd : kd;
+    store8(out + ((bi * heads + head) * cap + pos0 + ti) * d + dd, v);
+  }
+}
+
+int grid_for(int64_t items, int per_block) {
+  const int64_t want = (items + per_block - 1) / per_block;
+  const int64_t cap = static_cast<int64_t>(num_sms()) * 16;
+  return static_cast<int>(want < 1 ? 1 : (want > cap ? cap : want));
+}
+
+}  // namespace
+
+fg_status quantize_rows(const void* x, fg_dtype dt, int64_t rows, int64_t cols, uint8_t* codes,
+                        float* mins, float* scales, cudaStream_t st) {
+  const int64_t ngroups = rows * (cols / 64);
+  if (ngroups == 0) return FG_OK;
+  const int grid = grid_for(ngroups, 32);  // 8 warps x 4 groups per block
+  if (dt == FG_F16)
+    quantize_kernel<__half><<<grid, 256, 0, st>>>(static_cast<const __half*>(x), ngroups,
+                                                  reinterpret_cast<uint32_t*>(codes), mins, scales);
+  else
+    quantize_kernel<float><<<grid, 256, 0, st>>>(static_cast<const float*>(x), ngroups,
+                                                 reinterpret_cast<uint32_t*>(codes), mins, scales);
+  return check_launch("quantize_kernel");
+}
+
+fg_status dequant_rows(const uint8_t* codes, const float* mins, const float* scales,
+                       int64_t rows, int64_t cols, void* out, fg_dtype dt, cudaStream_t st) {
+  const int64_t nwords = rows * cols / 8;
+  if (nwords == 0) return FG_OK;
+  const int grid = grid_for(nwords, 256);
+  const uint32_t* c = reinterpret_cast<const uint32_t*>(codes);
+  if (dt == FG_F16)
+    dequant_kernel<__half><<<grid, 256, 0, st>>>(c, mins, scales, nwords, static_cast<__half*>(out));
+  else
+    dequant_kernel<float><<<grid, 256, 0, st>>>(c, mins, scales, nwords, static_cast<float*>(out));
+  return check_launch("dequant_kernel");
+}
+
+fg_status kv_store(const fg_kv& kv, const void* ksrc, const void* vsrc, int64_t ld, int64_t b,
+                   int64_t ntok, int64_t pos0, cudaStream_t st) {
+  const int h1 = kv.heads * kv.head_dim;
+  if (b == 0 || ntok == 0) return FG_OK;
+  if (kv.codec == FG_CODEC_Q4G64) {
+    KVDst dst;
+    dst.codes[0] = reinterpret_cast<uint32_t*>(kv.k_codes);
+    dst.codes[1] = reinterpret_cast<uint32_t*>(kv.v_codes);
+    dst.mins[0] = kv.k_mins;
+    dst.mins[1] = kv.v_mins;
+    dst.scales[0] = kv.k_scales;
+    dst.scales[1] = kv.v_scales;
+    const int64_t ngroups = 2 * b * ntok * (h1 / 64);
+    const int grid = grid_for(ngroups, 32);
+    if (kv.dtype == FG_F16)
+      kv_store_q4_kernel<__half><<<grid, 256, 0, st>>>(
+          static_cast<const __half*>(ksrc), static_cast<const __half*>(vsrc), ld, b, ntok, pos0,
+          h1, kv.heads, kv.head_dim, kv.capacity, dst);
+    else
+      kv_store_q4_kernel<float><<<grid, 256, 0, st>>>(
+          static_cast<const float*>(ksrc), static_cast<const float*>(vsrc), ld, b, ntok, pos0, h1,
+          kv.heads, kv.head_dim, kv.capacity, dst);
+    return check_launch("kv_store_q4_kernel");
+  }
+  const int64_t n8 = 2 * b * ntok * (h1 / 8);
+  const int grid = grid_for(n8, 256);
+  if (kv.dtype == FG_F16)
+    kv_store_dense_kernel<__half><<<grid, 256, 0, st>>>(
+        static_cast<const __half*>(ksrc), static_cast<const __half*>(vsrc), ld, b, ntok, pos0, h1,
+        kv.heads, kv.head_dim, kv.capacity, static_cast<__half*>(kv.k_dense),
+        static_cast<__half*>(kv.v_dense));
+  else
+    kv_store_dense_kernel<float><<<grid, 256, 0, st>>>(
+        static_cast<const float*>(ksrc), static_cast<const float*>(vsrc), ld, b, ntok, pos0, h1,
+        kv.heads, kv.head_dim, kv.capacity, static_cast<float*>(kv.k_dense),
+        static_cast<float*>(kv.v_dense));
+  return check_launch("kv_store_dense_kernel");
+}
+
+}  // namespace fg
+
+// ---------------------------------------------------------------------------
+// C ABI
+// ---------------------------------------------------------------------------
+using fg::aligned;
+using fg::fail;
+
+extern "C" fg_status fg_quantize_g64(const void* x, fg_dtype dt, int64_t rows, int64_t cols,
+                                     uint8_t* codes, float* mins, float* scales,
+                                     cudaStream_t stream) {
+  if (dt != FG_F16 && dt != FG_F32) return fail(FG_ERR_ARG, "dtype %d", static_cast<int>(dt));
+  if (rows < 0 || cols < 0) return fail(FG_ERR_ARG, "negative size");
+  if (cols % 64 != 0) return fail(FG_ERR_SHAPE, "cols %lld is not a multiple of 64", (long long)cols);
+  if (rows == 0 || cols == 0) return FG_OK;
+  if (!x || !codes || !mins || !scales) return fail(FG_ERR_ARG, "null pointer");
+  if (!aligned(x, 16) || !aligned(codes, 16) || !aligned(mins, 4) || !aligned(scales, 4))
+    return fail(FG_ERR_ALIGN, "x and codes need 16-byte, mins/scales 4-byte alignment");
+  return fg::quantize_rows(x, dt, rows, cols, codes, mins, scales, stream);
+}
+
+extern "C" fg_status fg_dequant_g64(const uint8_t* codes, const float* mins, const float* scales,
+                                    int64_t rows, int64_t cols, void* out, fg_dtype dt,
+                                    cudaStream_t stream) {
+  if (dt != FG_F16 && dt != FG_F32) return fail(FG_ERR_ARG, "dtype %d", static_cast<int>(dt));
+  if (rows < 0 || cols < 0) return fail(FG_ERR_ARG, "negative size");
+  if (cols % 64 != 0) return fail(FG_ERR_SHAPE, "cols %lld is not a multiple of 64", (long long)cols);
+  if (rows == 0 || cols == 0) return FG_OK;
+  if (!out || !codes || !mins || !scales) return fail(FG_ERR_ARG, "null pointer");
+  if (!aligned(out, 16) || !aligned(codes, 16) || !aligned(mins, 4) || !aligned(scales, 4))
+    return fail(FG_ERR_ALIGN, "out and codes need 16-byte, mins/scales 4-byte alignment");
+  return fg::dequant_rows(codes, mins, scales, rows, cols, out, dt, stream);
+}

@@ -1,0 +1,90 @@
+// Internal declarations shared by the libfg.so translation units.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "fg.h"
+
+namespace fg {
+
+// ---- host-side error reporting -------------------------------------------
+// Records a printf-style detail for fg_last_error() and returns `s`.
+fg_status fail(fg_status s, const char* fmt, ...);
+// Maps cudaGetLastError() after a launch to FG_OK / FG_ERR_CUDA.
+fg_status check_launch(const char* what);
+inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+inline size_t dtype_bytes(fg_dtype d) { return d == FG_F16 ? 2 : 4; }
+// Number of SMs of the current device (cached per device).
+int num_sms();
+// Device address of the library's error word on the current device; kernels
+// that run bounded waits OR an error code into it.
+unsigned int* device_error_word();
+
+enum DeviceError : unsigned int { DEV_ERR_WAIT_TIMEOUT = 1u };
+
+// ---- weight operand of a product -----------------------------------------
+// A product's B operand may be split into up to three matrices laid side by
+// side along N (w_Q | w_K | w_V share one launch); each segment's N is a
+// multiple of 64 and its columns start at `n0` in the output.
+struct WSeg {
+  const uint8_t* codes;
+  const float* mins;
+  const float* scales;
+  const void* dense;
+  int64_t N;
+  int64_t n0;
+};
+
+struct GemmArgs {
+  const void* X;     // [M][K], row stride ldx (elements)
+  int64_t ldx;
+  int64_t M, K;
+  WSeg seg[3];
+  int nseg;
+  int64_t N;         // total columns = sum of segment N
+  void* Y;           // [M][N], row stride ldy
+  int64_t ldy;
+  const void* R;     // optional residual [M][N], row stride ldr
+  int64_t ldr;
+  int relu;
+  int quant;         // 1: segments are Q4G64, 0: dense
+  fg_dtype dtype;
+};
+
+// CUDA-core product (any M, fp16 or fp32).
+fg_status gemm_simt(const GemmArgs& a, cudaStream_t st);
+// Y = epilogue(X . W); chooses the kernel for the shape.  Scratch: `ws`
+// (device, may be null when ws_bytes == 0) for split-K partial sums.
+fg_status gemm(const GemmArgs& a, void* ws, size_t ws_bytes, cudaStream_t st);
+size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, fg_dtype dt, int quant);
+
+// ---- KV cache --------------------------------------------------------------
+// Store K/V rows of `T` tokens per sequence at slots pos0..pos0+T-1.  The
+// row of sequence bi, token ti starts at ksrc + (bi*T + ti)*ld (elements of
+// the cache dtype), likewise for vsrc.
+fg_status kv_store(const fg_kv& kv, const void* ksrc, const void* vsrc, int64_t ld, int64_t b,
+                   int64_t T, int64_t pos0, cudaStream_t st);
+
+// ---- attention -------------------------------------------------------------
+// Decode: one query per (sequence, head) at slot pos over slots 0..pos.
+// q: [b][ldq] (head h at columns h*d..), out: [b][ldo].
+fg_status decode_attention(const fg_kv& kv, const void* q, int64_t ldq, int64_t b, int64_t pos,
+                           void* out, int64_t ldo, void* ws, size_t ws_bytes, cudaStream_t st);
+size_t decode_attention_workspace_bytes(int64_t b, int32_t heads, int32_t head_dim,
+                                        int64_t capacity);
+fg_status decode_attention_simt(const fg_kv& kv, const void* q, int64_t ldq, int64_t b,
+                                int64_t pos, void* out, int64_t ldo, cudaStream_t st);
+// Prefill: causal attention of s queries per sequence over slots 0..s-1.
+// q: [b*s][ldq]; out: [b*s][ldo].
+fg_status prefill_attention(const fg_kv& kv, const void* q, int64_t ldq, int64_t b, int64_t s,
+                            void* out, int64_t ldo, cudaStream_t st);
+
+// ---- codec -----------------------------------------------------------------
+fg_status quantize_rows(const void* x, fg_dtype dt, int64_t rows, int64_t cols, uint8_t* codes,
+                        float* mins, float* scales, cudaStream_t st);
+fg_status dequant_rows(const uint8_t* codes, const float* mins, const float* scales,
+                       int64_t rows, int64_t cols, void* out, fg_dtype dt, cudaStream_t st);
+
+}  // namespace fg

@@ -1,0 +1,383 @@
+// The OPT-style layer and the zig-zag block loop (FlexGen notes, "背景知识"
+// prefill and decode equations; "4. 卸载策略" zig-zag block schedule with the
+// whole block resident, so one pass over a layer's weights serves every
+// sequence of the block).  Argument validation, workspace layout and the
+// sequence of kernel launches live here; the arithmetic is in the kernels.
+#include "fg_internal.cuh"
+
+namespace fg {
+namespace {
+
+constexpr size_t kAlign = 256;
+inline size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+fg_status check_wmat(const fg_wmat& w, int64_t K, int64_t N, fg_codec codec, const char* name) {
+  if (w.K != K || w.N != N)
+    return fail(FG_ERR_SHAPE, "%s is %lldx%lld, expected %lldx%lld", name, (long long)w.K,
+                (long long)w.N, (long long)K, (long long)N);
+  if (codec == FG_CODEC_Q4G64) {
+    if (!w.codes || !w.mins || !w.scales) return fail(FG_ERR_ARG, "%s: null 4-bit arrays", name);
+    if (!aligned(w.codes, 16) || !aligned(w.mins, 4) || !aligned(w.scales, 4))
+      return fail(FG_ERR_ALIGN, "%s: codes need 16-byte alignment", name);
+  } else {
+    if (!w.dense) return fail(FG_ERR_ARG, "%s: null dense weights", name);
+    if (!aligned(w.dense, 16)) return fail(FG_ERR_ALIGN, "%s: dense weights need 16-byte alignment", name);
+  }
+  return FG_OK;
+}
+
+fg_status check_layer(const fg_layer* L) {
+  if (!L) return fail(FG_ERR_ARG, "null layer");
+  if (L->dtype != FG_F16 && L->dtype != FG_F32) return fail(FG_ERR_ARG, "layer dtype");
+  if (L->codec != FG_CODEC_NONE && L->codec != FG_CODEC_Q4G64) return fail(FG_ERR_ARG, "layer codec");
+  if (L->h1 <= 0 || L->h2 <= 0 || L->heads <= 0) return fail(FG_ERR_ARG, "layer sizes");
+  if (L->h1 % 64 || L->h2 % 64) return fail(FG_ERR_SHAPE, "h1 and h2 must be multiples of 64");
+  if (L->h1 % L->heads) return fail(FG_ERR_SHAPE, "heads must divide h1");
+  const int64_t d = L->h1 / L->heads;
+  if (d != 64 && d != 128) return fail(FG_ERR_UNSUPPORTED, "head_dim %lld (64 or 128)", (long long)d);
+  fg_status s;
+  const int64_t h1 = L->h1, h2 = L->h2;
+  if ((s = check_wmat(L->wq, h1, h1, L->codec, "w_Q")) != FG_OK) return s;
+  if ((s = check_wmat(L->wk, h1, h1, L->codec, "w_K")) != FG_OK) return s;
+  if ((s = check_wmat(L->wv, h1, h1, L->codec, "w_V")) != FG_OK) return s;
+  if ((s = check_wmat(L->wo, h1, h1, L->codec, "w_O")) != FG_OK) return s;
+  if ((s = check_wmat(L->w1, h1, h2, L->codec, "w_1")) != FG_OK) return s;
+  if ((s = check_wmat(L->w2, h2, h1, L->codec, "w_2")) != FG_OK) return s;
+  return FG_OK;
+}
+
+fg_status check_kv(const fg_kv* kv, int64_t b, int32_t heads, int64_t d, fg_codec codec,
+                   fg_dtype dt) {
+  if (!kv) return fail(FG_ERR_ARG, "null kv");
+  if (kv->codec != codec || kv->dtype != dt) return fail(FG_ERR_ARG, "kv codec/dtype differ from the layer");
+  if (kv->heads != heads || kv->head_dim != d)
+    return fail(FG_ERR_SHAPE, "kv heads/head_dim %d/%d, layer %d/%lld", kv->heads, kv->head_dim,
+                heads, (long long)d);
+  if (kv->b != b) return fail(FG_ERR_SHAPE, "kv holds %lld sequences, call has %lld", (long long)kv->b, (long long)b);
+  if (kv->capacity <= 0) return fail(FG_ERR_ARG, "kv capacity");
+  if (codec == FG_CODEC_Q4G64) {
+    if (!kv->k_codes || !kv->v_codes || !kv->k_mins || !kv->k_scales || !kv->v_mins || !kv->v_scales)
+      return fail(FG_ERR_ARG, "kv: null 4-bit arrays");
+    if (!aligned(kv->k_codes, 16) || !aligned(kv->v_codes, 16) || !aligned(kv->k_mins, 4) ||
+        !aligned(kv->k_scales, 4) || !aligned(kv->v_mins, 4) || !aligned(kv->v_scales, 4))
+      return fail(FG_ERR_ALIGN, "kv: codes need 16-byte alignment");
+  } else {
+    if (!kv->k_dense || !kv->v_dense) return fail(FG_ERR_ARG, "kv: null dense arrays");
+    if (!aligned(kv->k_dense, 16) || !aligned(kv->v_dense, 16)) return fail(FG_ERR_ALIGN, "kv: dense arrays need 16-byte alignment");
+  }
+  return FG_OK;
+}
+
+WSeg seg_of(const fg_wmat& w, int64_t n0) {
+  WSeg s;
+  s.codes = w.codes;
+  s.mins = w.mins;
+  s.scales = w.scales;
+  s.dense = w.dense;
+  s.N = w.N;
+  s.n0 = n0;
+  return s;
+}
+
+GemmArgs product(const fg_layer& L, const void* X, int64_t ldx, int64_t M, const fg_wmat* ws,
+                 int nseg, void* Y, int64_t ldy, const void* R, int64_t ldr, int relu) {
+  GemmArgs a{};
+  a.X = X;
+  a.ldx = ldx;
+  a.M = M;
+  a.K = ws[0].K;
+  int64_t n0 = 0;
+  for (int i = 0; i < nseg; ++i) {
+    a.seg[i] = seg_of(ws[i], n0);
+    n0 += ws[i].N;
+  }
+  a.nseg = nseg;
+  a.N = n0;
+  a.Y = Y;
+  a.ldy = ldy;
+  a.R = R;
+  a.ldr = ldr;
+  a.relu = relu;
+  a.quant = L.codec == FG_CODEC_Q4G64;
+  a.dtype = L.dtype;
+  return a;
+}
+
+// Workspace carve-up shared by prefill (M = b*s) and decode (M = b).
+struct Buffers {
+  char* qkv;  // [M][3 h1]
+  char* att;  // [M][h1]
+  char* xo;   // [M][h1]
+  char* hid;  // [M][h2]
+  char* scratch;
+  size_t scratch_bytes;
+};
+
+size_t activations_bytes(const fg_layer& L, int64_t M) {
+  const size_t e = dtype_bytes(L.dtype);
+  return up(M * 3 * L.h1 * e) + up(M * L.h1 * e) * 2 + up(M * L.h2 * e);
+}
+
+size_t scratch_bytes(const fg_layer& L, int64_t M, int64_t capacity, bool decode) {
+  const int quant = L.codec == FG_CODEC_Q4G64;
+  size_t s = gemm_workspace_bytes(M, 3 * L.h1, L.h1, L.dtype, quant);
+  size_t t;
+  t = gemm_workspace_bytes(M, L.h2, L.h1, L.dtype, quant);
+  s = t > s ? t : s;
+  t = gemm_workspace_bytes(M, L.h1, L.h2, L.dtype, quant);
+  s = t > s ? t : s;
+  if (decode) {
+    t = decode_attention_workspace_bytes(M, L.heads, static_cast<int32_t>(L.h1 / L.heads), capacity);
+    s = t > s ? t : s;
+  }
+  return up(s);
+}
+
+Buffers carve(const fg_layer& L, int64_t M, void* ws) {
+  const size_t e = dtype_bytes(L.dtype);
+  Buffers B;
+  char* p = static_cast<char*>(ws);
+  B.qkv = p;
+  p += up(M * 3 * L.h1 * e);
+  B.att = p;
+  p += up(M * L.h1 * e);
+  B.xo = p;
+  p += up(M * L.h1 * e);
+  B.hid = p;
+  p += up(M * L.h2 * e);
+  B.scratch = p;
+  return B;
+}
+
+#define FG_TRY(expr)                 \
+  do {                               \
+    fg_status _s = (expr);           \
+    if (_s != FG_OK) return _s;      \
+  } while (0)
+
+fg_status run_prefill(const fg_layer& L, const void* x, int64_t b, int64_t s, const fg_kv& kv,
+                      void* y, void* ws, size_t scratch, cudaStream_t st) {
+  const int64_t M = b * s, h1 = L.h1, h2 = L.h2;
+  Buffers B = carve(L, M, ws);
+  const fg_wmat qkv[3] = {L.wq, L.wk, L.wv};
+  // x_Q, x_K, x_V = x w_Q, x w_K, x w_V (one pass over the three matrices)
+  FG_TRY(gemm(product(L, x, h1, M, qkv, 3, B.qkv, 3 * h1, nullptr, 0, 0), B.scratch, scratch, st));
+  // cache the prompt's K/V (quantized per token along the hidden dimension)
+  const size_t e = dtype_bytes(L.dtype);
+  FG_TRY(kv_store(kv, B.qkv + h1 * e, B.qkv + 2 * h1 * e, 3 * h1, b, s, 0, st));
+  // Softmax(x_Q x_K^T / sqrt(d)) x_V, causal, K/V read back through the codec
+  FG_TRY(prefill_attention(kv, B.qkv, 3 * h1, b, s, B.att, h1, st));
+  // x_Out = (...) w_O + x
+  FG_TRY(gemm(product(L, B.att, h1, M, &L.wo, 1, B.xo, h1, x, h1, 0), B.scratch, scratch, st));
+  // relu(x_Out w_1)
+  FG_TRY(gemm(product(L, B.xo, h1, M, &L.w1, 1, B.hid, h2, nullptr, 0, 1), B.scratch, scratch, st));
+  // x^{i+1} = (...) w_2 + x_Out
+  FG_TRY(gemm(product(L, B.hid, h2, M, &L.w2, 1, y, h1, B.xo, h1, 0), B.scratch, scratch, st));
+  return FG_OK;
+}
+
+fg_status run_decode(const fg_layer& L, const void* t, int64_t b, int64_t pos, const fg_kv& kv,
+                     void* y, void* ws, size_t scratch, cudaStream_t st) {
+  const int64_t h1 = L.h1, h2 = L.h2;
+  Buffers B = carve(L, b, ws);
+  const fg_wmat qkv[3] = {L.wq, L.wk, L.wv};
+  // t_Q, t w_K, t w_V: every weight read once for the whole block
+  FG_TRY(gemm(product(L, t, h1, b, qkv, 3, B.qkv, 3 * h1, nullptr, 0, 0), B.scratch, scratch, st));
+  // Concat: append t w_K, t w_V at slot pos
+  const size_t e = dtype_bytes(L.dtype);
+  FG_TRY(kv_store(kv, B.qkv + h1 * e, B.qkv + 2 * h1 * e, 3 * h1, b, 1, pos, st));
+  // Softmax(t_Q x_K^T / sqrt(d)) x_V over slots 0..pos
+  FG_TRY(decode_attention(kv, B.qkv, 3 * h1, b, pos, B.att, h1, B.scratch, scratch, st));
+  FG_TRY(gemm(product(L, B.att, h1, b, &L.wo, 1, B.xo, h1, t, h1, 0), B.scratch, scratch, st));
+  FG_TRY(gemm(product(L, B.xo, h1, b, &L.w1, 1, B.hid, h2, nullptr, 0, 1), B.scratch, scratch, st));
+  FG_TRY(gemm(product(L, B.hid, h2, b, &L.w2, 1, y, h1, B.xo, h1, 0), B.scratch, scratch, st));
+  return FG_OK;
+}
+
+fg_status check_act(const void* p, const char* name) {
+  if (!p) return fail(FG_ERR_ARG, "%s is null", name);
+  if (!aligned(p, 16)) return fail(FG_ERR_ALIGN, "%s needs 16-byte alignment", name);
+  return FG_OK;
+}
+
+}  // namespace
+
+// The decode attention with its workspace (split over tokens when the block
+// has too few (sequence, head) pairs to fill the GPU).
+fg_status decode_attention(const fg_kv& kv, const void* q, int64_t ldq, int64_t b, int64_t pos,
+                           void* out, int64_t ldo, void* ws, size_t ws_bytes, cudaStream_t st) {
+  (void)ws;
+  (void)ws_bytes;
+  return decode_attention_simt(kv, q, ldq, b, pos, out, ldo, st);
+}
+
+size_t decode_attention_workspace_bytes(int64_t b, int32_t heads, int32_t head_dim,
+                                        int64_t capacity) {
+  (void)b;
+  (void)heads;
+  (void)head_dim;
+  (void)capacity;
+  return 0;
+}
+
+fg_status gemm(const GemmArgs& a, void* ws, size_t ws_bytes, cudaStream_t st) {
+  (void)ws;
+  (void)ws_bytes;
+  return gemm_simt(a, st);
+}
+
+size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, fg_dtype dt, int quant) {
+  (void)M;
+  (void)N;
+  (void)K;
+  (void)dt;
+  (void)quant;
+  return 0;
+}
+
+}  // namespace fg
+
+using namespace fg;
+
+extern "C" {
+
+size_t fg_prefill_workspace_bytes(const fg_layer* L, int64_t b, int64_t s) {
+  if (check_layer(L) != FG_OK || b < 0 || s < 0) return 0;
+  return activations_bytes(*L, b * s) + scratch_bytes(*L, b * s, s, false);
+}
+
+size_t fg_decode_workspace_bytes(const fg_layer* L, int64_t b, int64_t capacity) {
+  if (check_layer(L) != FG_OK || b < 0 || capacity < 0) return 0;
+  return activations_bytes(*L, b) + scratch_bytes(*L, b, capacity, true);
+}
+
+size_t fg_prefill_block_workspace_bytes(const fg_layer* L, int64_t b, int64_t s) {
+  if (check_layer(L) != FG_OK || b < 0 || s < 0) return 0;
+  return fg_prefill_workspace_bytes(L, b, s) + 2 * up(b * s * L->h1 * dtype_bytes(L->dtype));
+}
+
+size_t fg_decode_block_workspace_bytes(const fg_layer* L, int64_t b, int64_t capacity) {
+  if (check_layer(L) != FG_OK || b < 0 || capacity < 0) return 0;
+  return fg_decode_workspace_bytes(L, b, capacity) + 2 * up(b * L->h1 * dtype_bytes(L->dtype));
+}
+
+fg_status fg_kv_append(const fg_kv* kv, const void* k_new, const void* v_new, int64_t pos,
+                       cudaStream_t stream) {
+  if (!kv) return fail(FG_ERR_ARG, "null kv");
+  if (kv->heads <= 0 || kv->head_dim <= 0 || kv->b < 0) return fail(FG_ERR_ARG, "kv sizes");
+  if (kv->head_dim % 64) return fail(FG_ERR_SHAPE, "head_dim must be a multiple of 64");
+  FG_TRY(check_kv(kv, kv->b, kv->heads, kv->head_dim, kv->codec, kv->dtype));
+  if (pos < 0 || pos >= kv->capacity)
+    return fail(FG_ERR_CAPACITY, "pos %lld outside [0, %lld)", (long long)pos, (long long)kv->capacity);
+  if (kv->b == 0) return FG_OK;
+  FG_TRY(check_act(k_new, "k_new"));
+  FG_TRY(check_act(v_new, "v_new"));
+  const int64_t h1 = static_cast<int64_t>(kv->heads) * kv->head_dim;
+  return kv_store(*kv, k_new, v_new, h1, kv->b, 1, pos, stream);
+}
+
+fg_status fg_prefill_layer(const fg_layer* L, const void* x, int64_t b, int64_t s, const fg_kv* kv,
+                           void* y, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  FG_TRY(check_layer(L));
+  if (b < 0 || s < 0) return fail(FG_ERR_ARG, "negative size");
+  FG_TRY(check_kv(kv, b, L->heads, L->h1 / L->heads, L->codec, L->dtype));
+  if (s > kv->capacity) return fail(FG_ERR_CAPACITY, "s %lld exceeds capacity %lld", (long long)s, (long long)kv->capacity);
+  if (b == 0 || s == 0) return FG_OK;
+  FG_TRY(check_act(x, "x"));
+  FG_TRY(check_act(y, "y"));
+  const size_t need = fg_prefill_workspace_bytes(L, b, s);
+  if (!ws || ws_bytes < need)
+    return fail(FG_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes, need);
+  if (!aligned(ws, kAlign)) return fail(FG_ERR_ALIGN, "workspace needs 256-byte alignment");
+  return run_prefill(*L, x, b, s, *kv, y, ws, scratch_bytes(*L, b * s, s, false), stream);
+}
+
+fg_status fg_decode_step(const fg_layer* L, const void* t, int64_t b, int64_t pos, const fg_kv* kv,
+                         void* y, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  FG_TRY(check_layer(L));
+  if (b < 0) return fail(FG_ERR_ARG, "negative size");
+  FG_TRY(check_kv(kv, b, L->heads, L->h1 / L->heads, L->codec, L->dtype));
+  if (pos < 0 || pos >= kv->capacity)
+    return fail(FG_ERR_CAPACITY, "pos %lld outside [0, %lld)", (long long)pos, (long long)kv->capacity);
+  if (b == 0) return FG_OK;
+  FG_TRY(check_act(t, "t"));
+  FG_TRY(check_act(y, "y"));
+  const size_t need = fg_decode_workspace_bytes(L, b, kv->capacity);
+  if (!ws || ws_bytes < need)
+    return fail(FG_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes, need);
+  if (!aligned(ws, kAlign)) return fail(FG_ERR_ALIGN, "workspace needs 256-byte alignment");
+  return run_decode(*L, t, b, pos, *kv, y, ws, scratch_bytes(*L, b, kv->capacity, true), stream);
+}
+
+fg_status fg_prefill_block(const fg_layer* layers, int32_t l, const void* x, int64_t b, int64_t s,
+                           const fg_kv* kvs, void* y, void* ws, size_t ws_bytes,
+                           cudaStream_t stream) {
+  if (!layers || !kvs || l <= 0) return fail(FG_ERR_ARG, "layers/kvs/l");
+  for (int32_t i = 0; i < l; ++i) {
+    FG_TRY(check_layer(&layers[i]));
+    if (layers[i].h1 != layers[0].h1 || layers[i].dtype != layers[0].dtype)
+      return fail(FG_ERR_SHAPE, "layers differ in h1/dtype");
+    FG_TRY(check_kv(&kvs[i], b, layers[i].heads, layers[i].h1 / layers[i].heads, layers[i].codec,
+                    layers[i].dtype));
+    if (s > kvs[i].capacity) return fail(FG_ERR_CAPACITY, "s exceeds capacity");
+  }
+  if (b == 0 || s == 0) return FG_OK;
+  FG_TRY(check_act(x, "x"));
+  FG_TRY(check_act(y, "y"));
+  size_t layer_ws = 0;
+  for (int32_t i = 0; i < l; ++i) {
+    const size_t w = fg_prefill_workspace_bytes(&layers[i], b, s);
+    layer_ws = w > layer_ws ? w : layer_ws;
+  }
+  const size_t act = up(b * s * layers[0].h1 * dtype_bytes(layers[0].dtype));
+  const size_t need = up(layer_ws) + 2 * act;
+  if (!ws || ws_bytes < need) return fail(FG_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes, need);
+  if (!aligned(ws, kAlign)) return fail(FG_ERR_ALIGN, "workspace needs 256-byte alignment");
+  char* ping[2] = {static_cast<char*>(ws) + up(layer_ws), static_cast<char*>(ws) + up(layer_ws) + act};
+  const void* in = x;
+  for (int32_t i = 0; i < l; ++i) {
+    void* out = (i == l - 1) ? y : ping[i & 1];
+    FG_TRY(run_prefill(layers[i], in, b, s, kvs[i], out, ws,
+                       scratch_bytes(layers[i], b * s, s, false), stream));
+    in = out;
+  }
+  return FG_OK;
+}
+
+fg_status fg_decode_block_step(const fg_layer* layers, int32_t l, const void* t, int64_t b,
+                               int64_t pos, const fg_kv* kvs, void* y, void* ws, size_t ws_bytes,
+                               cudaStream_t stream) {
+  if (!layers || !kvs || l <= 0) return fail(FG_ERR_ARG, "layers/kvs/l");
+  for (int32_t i = 0; i < l; ++i) {
+    FG_TRY(check_layer(&layers[i]));
+    if (layers[i].h1 != layers[0].h1 || layers[i].dtype != layers[0].dtype)
+      return fail(FG_ERR_SHAPE, "layers differ in h1/dtype");
+    FG_TRY(check_kv(&kvs[i], b, layers[i].heads, layers[i].h1 / layers[i].heads, layers[i].codec,
+                    layers[i].dtype));
+    if (pos < 0 || pos >= kvs[i].capacity)
+      return fail(FG_ERR_CAPACITY, "pos %lld outside [0, %lld)", (long long)pos, (long long)kvs[i].capacity);
+  }
+  if (b == 0) return FG_OK;
+  FG_TRY(check_act(t, "t"));
+  FG_TRY(check_act(y, "y"));
+  size_t layer_ws = 0;
+  for (int32_t i = 0; i < l; ++i) {
+    const size_t w = fg_decode_workspace_bytes(&layers[i], b, kvs[i].capacity);
+    layer_ws = w > layer_ws ? w : layer_ws;
+  }
+  const size_t act = up(b * layers[0].h1 * dtype_bytes(layers[0].dtype));
+  const size_t need = up(layer_ws) + 2 * act;
+  if (!ws || ws_bytes < need) return fail(FG_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes, need);
+  if (!aligned(ws, kAlign)) return fail(FG_ERR_ALIGN, "workspace needs 256-byte alignment");
+  char* ping[2] = {static_cast<char*>(ws) + up(layer_ws), static_cast<char*>(ws) + up(layer_ws) + act};
+  const void* in = t;
+  for (int32_t i = 0; i < l; ++i) {
+    void* out = (i == l - 1) ? y : ping[i & 1];
+    FG_TRY(run_decode(layers[i], in, b, pos, kvs[i], out, ws,
+                      scratch_bytes(layers[i], b, kvs[i].capacity, true), stream));
+    in = out;
+  }
+  return FG_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,109 @@
+"""CPU checks of the C ABI: libfg.so builds, loads, exports every function
+include/fg.h declares, and rejects bad arguments on the host before any
+CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def fg():
+    import __graft_entry__
+    __graft_entry__.build()
+    import int4_group_quantized_gb300 as fg
+    return fg
+
+
+def _declared():
+    names = set()
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", f)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(fg_[a-z0-9_]+)\s*\(", src))
+    return names
+
+
+def test_exports_every_declared_symbol(fg):
+    names = _declared()
+    assert {"fg_quantize_g64", "fg_dequant_g64", "fg_prefill_layer", "fg_decode_step",
+            "fg_kv_append"} <= names
+    for n in sorted(names):
+        assert hasattr(fg.lib, n), n
+
+
+def test_version_and_status_strings(fg):
+    assert "sm_103a" in fg.fg_version()
+    for code, name in fg.STATUS.items():
+        assert fg.lib.fg_status_str(code).decode() == name
+
+
+def test_codec_argument_errors(fg):
+    L = fg.lib
+    p = ctypes.c_void_p(16)
+    assert L.fg_quantize_g64(p, 0, 2, 65, p, p, p, None) == 2          # FG_ERR_SHAPE
+    assert b"multiple of 64" in L.fg_last_error()
+    assert L.fg_quantize_g64(p, 7, 2, 64, p, p, p, None) == 1          # bad dtype
+    assert L.fg_quantize_g64(None, 0, 2, 64, p, p, p, None) == 1       # null x
+    assert L.fg_quantize_g64(ctypes.c_void_p(18), 0, 2, 64, p, p, p, None) == 3  # misaligned
+    assert L.fg_quantize_g64(None, 0, 0, 64, None, None, None, None) == 0        # empty: no-op
+    assert L.fg_dequant_g64(p, p, p, 1, 100, p, 0, None) == 2
+
+
+def _layer(fg, h1=128, h2=256, heads=2, codec=1, dtype=0):
+    P = 4096
+    wm = lambda K, N: fg.fg_wmat(P, P, P, P, K, N)
+    return fg.fg_layer(wm(h1, h1), wm(h1, h1), wm(h1, h1), wm(h1, h1), wm(h1, h2), wm(h2, h1),
+                       h1, h2, heads, codec, dtype)
+
+
+def _kv(fg, b=2, cap=16, heads=2, d=64, codec=1, dtype=0):
+    P = 4096
+    return fg.fg_kv(P, P, P, P, P, P, P, P, b, cap, heads, d, codec, dtype)
+
+
+def test_layer_argument_errors(fg):
+    L = fg.lib
+    lay, kv = _layer(fg), _kv(fg)
+    P = ctypes.c_void_p(4096)
+    ws = fg.lib.fg_decode_workspace_bytes(ctypes.byref(lay), 2, 16)
+    assert ws > 0
+    # pos at capacity
+    assert L.fg_decode_step(ctypes.byref(lay), P, 2, 16, ctypes.byref(kv), P, P, ws, None) == 4
+    assert L.fg_decode_step(ctypes.byref(lay), P, 2, -1, ctypes.byref(kv), P, P, ws, None) == 4
+    # workspace too small
+    assert L.fg_decode_step(ctypes.byref(lay), P, 2, 3, ctypes.byref(kv), P, P, ws - 1, None) == 5
+    # b differs from the cache
+    assert L.fg_decode_step(ctypes.byref(lay), P, 3, 3, ctypes.byref(kv), P, P, ws, None) == 2
+    # head_dim 96 is not implemented
+    bad = _layer(fg, h1=192, heads=2)
+    assert L.fg_prefill_layer(ctypes.byref(bad), P, 2, 4, ctypes.byref(kv), P, P, ws, None) == 8
+    # h2 not a multiple of 64
+    bad = _layer(fg, h2=200)
+    assert L.fg_prefill_layer(ctypes.byref(bad), P, 2, 4, ctypes.byref(kv), P, P, ws, None) == 2
+    # wrong matrix shape
+    bad = _layer(fg)
+    bad.w1.N = 128
+    assert L.fg_prefill_layer(ctypes.byref(bad), P, 2, 4, ctypes.byref(kv), P, P, ws, None) == 2
+    # s beyond capacity
+    assert L.fg_prefill_layer(ctypes.byref(lay), P, 2, 17, ctypes.byref(kv), P, P, 1 << 30, None) == 4
+    # cache codec differs from layer codec
+    kv2 = _kv(fg, codec=0)
+    assert L.fg_prefill_layer(ctypes.byref(lay), P, 2, 4, ctypes.byref(kv2), P, P, 1 << 30, None) == 1
+    # kv append outside capacity
+    assert L.fg_kv_append(ctypes.byref(kv), P, P, 16, None) == 4
+    # misaligned activation
+    assert L.fg_decode_step(ctypes.byref(lay), ctypes.c_void_p(4098), 2, 3, ctypes.byref(kv), P, P, ws,
+                            None) == 3
+
+
+def test_workspace_sizes_grow_with_tokens(fg):
+    lay = _layer(fg)
+    a = fg.lib.fg_prefill_workspace_bytes(ctypes.byref(lay), 2, 8)
+    b = fg.lib.fg_prefill_workspace_bytes(ctypes.byref(lay), 2, 16)
+    assert 0 < a < b
+    assert fg.lib.fg_prefill_block_workspace_bytes(ctypes.byref(lay), 2, 8) > a

@@ -1,0 +1,151 @@
+"""GPU parity of the layer and block entry points against the fp64 oracle
+(FlexGen notes, "背景知识" prefill and decode equations on 4-bit weights and
+KV, "5. 近似方法").
+
+Bar: max|gpu - oracle| / max|oracle| <= 1e-5 for the fp32 one-layer check,
+<= 1e-2 with fp16 activations, per output.  Sequences of a block are
+independent, so full-size blocks run on the GPU and the oracle recomputes a
+sample of sequences.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import layer as olayer
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def fg():
+    import int4_group_quantized_gb300 as fg
+    return fg
+
+
+def rel_err(got, ref):
+    got = np.asarray(got, dtype=np.float64)
+    return float(np.max(np.abs(got - ref)) / max(np.max(np.abs(ref)), 1e-30))
+
+
+def run_gpu_block(fg, w, layers_raw, quant, x, tin, per_layer_api=False):
+    """Prefill x through the layers, then len(tin) decode steps.  Returns the
+    last layer's prefill output, per-step outputs and the caches."""
+    dev = x.device
+    dt = synth.torch_dtype(w.act)
+    b, s = x.shape[0], x.shape[1]
+    n = tin.shape[0]
+    layers = [fg.Layer.from_dense(r, w.heads, quantized=quant) for r in layers_raw]
+    kvs = [fg.KVCache(b, w.heads, w.head_dim, s + n, quant, dt, dev) for _ in layers]
+    y = torch.empty_like(x)
+    outs = []
+    if per_layer_api:
+        ws = fg.workspace(max(fg.fg_prefill_workspace_bytes(layers[0], b, s),
+                              fg.fg_decode_workspace_bytes(layers[0], b, s + n)), dev)
+        cur = x
+        for L, kv in zip(layers, kvs):
+            nxt = torch.empty_like(x)
+            fg.fg_prefill_layer(L, cur, kv, nxt, ws)
+            cur = nxt
+        y = cur
+        for t in range(n):
+            cur = tin[t]
+            for L, kv in zip(layers, kvs):
+                nxt = torch.empty_like(tin[t])
+                fg.fg_decode_step(L, cur, s + t, kv, nxt, ws)
+                cur = nxt
+            outs.append(cur)
+    else:
+        blk = fg.Block(layers, kvs)
+        ws = fg.workspace(max(fg.fg_prefill_block_workspace_bytes(layers[0], b, s),
+                              fg.fg_decode_block_workspace_bytes(layers[0], b, s + n)), dev)
+        fg.fg_prefill_block(blk, x, y, ws)
+        for t in range(n):
+            o = torch.empty_like(tin[t])
+            fg.fg_decode_block_step(blk, tin[t], s + t, o, ws)
+            outs.append(o)
+    fg.fg_sync_status()
+    return y, outs, kvs
+
+
+def oracle_block(w, layers_raw, quant, x, tin, seqs):
+    ow = [olayer.Weights.prepare({k: v.cpu().numpy() for k, v in r.items()}, quant, w.act)
+          for r in layers_raw]
+    xs = x[seqs].cpu().numpy().astype(np.float64)
+    ts = tin[:, seqs].cpu().numpy().astype(np.float64)
+    return olayer.run_block(xs, ts, ow, w.heads, quant, w.act)
+
+
+def _compare(w, y, outs, ref, seqs, tol):
+    ry, routs, _ = ref
+    e = rel_err(y[seqs].cpu().numpy(), ry)
+    assert e <= tol, f"prefill rel err {e}"
+    for t in range(len(outs)):
+        e = rel_err(outs[t][seqs].cpu().numpy(), routs[t])
+        assert e <= tol, f"decode step {t} rel err {e}"
+
+
+@pytest.mark.parametrize("quant", [True, False])
+@pytest.mark.parametrize("per_layer_api", [False, True])
+def test_tiny_exact_formula(fg, quant, per_layer_api):
+    w = synth.WORKLOADS["tiny"]
+    raw = [synth.layer_weights(w, 0, "cuda")]
+    x = synth.prompt(w, device="cuda")
+    tin = synth.decode_inputs(w, device="cuda")
+    y, outs, kvs = run_gpu_block(fg, w, raw, quant, x, tin, per_layer_api)
+    ref = oracle_block(w, raw, quant, x, tin, list(range(w.b)))
+    _compare(w, y, outs, ref, list(range(w.b)), 1e-5)
+    if quant:   # cache codes: identical except where fp32 rounding moved a value across a code step
+        oc = ref[2][0]
+        mism = np.mean(kvs[0].k_codes.cpu().numpy() != oc.k_codes) + np.mean(kvs[0].v_codes.cpu().numpy() != oc.v_codes)
+        assert mism < 0.01
+
+
+def test_tiny_multi_head_and_ragged(fg):
+    """A ragged prompt (s not a multiple of any tile) with 2 heads of 64."""
+    w = synth.Workload("tiny2", 9, 2, 128, 256, 2, 3, 37, 5, "f32")
+    raw = [synth.layer_weights(w, i, "cuda") for i in range(w.l)]
+    x = synth.prompt(w, device="cuda")
+    tin = synth.decode_inputs(w, device="cuda")
+    y, outs, _ = run_gpu_block(fg, w, raw, True, x, tin)
+    _compare(w, y, outs, oracle_block(w, raw, True, x, tin, list(range(w.b))), list(range(w.b)), 1e-5)
+
+
+def test_fp16_small_ragged(fg):
+    w = synth.Workload("small16", 9, 2, 256, 512, 2, 5, 77, 6, "f16")
+    raw = [synth.layer_weights(w, i, "cuda") for i in range(w.l)]
+    x = synth.prompt(w, device="cuda")
+    tin = synth.decode_inputs(w, device="cuda")
+    y, outs, _ = run_gpu_block(fg, w, raw, True, x, tin)
+    _compare(w, y, outs, oracle_block(w, raw, True, x, tin, list(range(w.b))), list(range(w.b)), 1e-2)
+
+
+def test_opt125m_two_layer_chain(fg):
+    """Two chained layers of the OPT-125M shape at the full block (b=32,
+    s=512, n=32); the oracle recomputes sequences 0, 17 and 31.  Deeper
+    chains are checked layer by layer: in the oracle itself a 2^-11
+    relative perturbation of the prompt grows to ~0.5% after 2 layers, ~6%
+    after 8 and ~10% after 12 (4-bit KV codes flip and the unnormalised
+    activations grow), so no implementation can meet 1e-2 end to end there."""
+    w = synth.WORKLOADS["opt-125m"]
+    raw = [synth.layer_weights(w, i, "cuda") for i in range(2)]
+    x = synth.prompt(w, device="cuda")
+    tin = synth.decode_inputs(w, device="cuda")
+    y, outs, _ = run_gpu_block(fg, w, raw, True, x, tin)
+    seqs = [0, 17, 31]
+    _compare(w, y, outs, oracle_block(w, raw, True, x, tin, seqs), seqs, 1e-2)
+
+
+@pytest.mark.parametrize("name,layer", [("opt-125m", 0), ("opt-125m", 6), ("opt-125m", 11),
+                                        ("opt-6.7b", 0), ("opt-6.7b", 31)])
+def test_layer_local_full_block(fg, name, layer):
+    """One layer of a large shape at the full block size and prompt length,
+    with its own N(0,1) inputs (the stack overflows fp16 past a few layers
+    without normalisation, so parity is checked layer by layer)."""
+    w = synth.WORKLOADS[name]
+    raw = [synth.layer_weights(w, layer, "cuda")]
+    x = synth.prompt(w, device="cuda", seed_offset=layer)
+    tin = synth.decode_inputs(w, n=w.n if w.h1 < 2048 else 4, device="cuda", seed_offset=layer)
+    y, outs, _ = run_gpu_block(fg, w, raw, True, x, tin)
+    seqs = [0, w.b - 1]
+    _compare(w, y, outs, oracle_block(w, raw, True, x, tin, seqs), seqs, 1e-2)
