@@ -1,0 +1,418 @@
+#!/usr/bin/env python
+"""Decode throughput of the int4 group-64 OPT layer stack on one GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config opt-6.7b]
+                    [--impl ours|reference]
+
+One step is one zig-zag block of the FlexGen notes ("4. 卸载策略"): the
+b-sequence prompt (s tokens) through all l layers, then n decode steps, each
+through all l layers, with weights and KV cache in 4-bit groups of 64
+("5. 近似方法").  Inputs are seeded synthetic tensors of the OPT shapes
+(weights N(0, 0.02), prompt and per-step embeddings N(0, 1)); everything is
+resident in HBM before the timed region.  The reported value is decode
+tokens/s: b*n*K (times the number of ranks) over the device time of the
+decode phases of the K timed steps (max over ranks).
+
+With --impl reference the CPU oracle (the plain fp64/fp32 restatement of the
+page, under oracle/) is timed on the host cores on a bounded sample of the
+same workload and printed in the same format.
+
+Multi-GPU (torchrun): replicas only; every rank runs its own block (its own
+prompt seeds, the same weights) with no collective on the data path; the
+timing is the max over ranks and the value sums all ranks' tokens.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "decode tokens/s (OPT-6.7B shape, int4 W+KV); achieved HBM GB/s vs ~8 TB/s"
+Q4 = 0.5 + 8.0 / 64.0   # bytes per element: 4-bit code + fp32 (min, scale) per 64
+
+
+def peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "tflops": d["bf16_tflops"],
+                "tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "tflops": 1900.0, "tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ---------------------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device: int):
+        self.rows = []
+        self.proc = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(device).uuid)
+            ident = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception:
+            ident = str(device)
+        self.cmd = ["nvidia-smi", "-i", ident, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                    "-lms", "200"]
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.th = threading.Thread(target=self._read, daemon=True)
+            self.th.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) == 7:
+                self.rows.append(parts)
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for r in self.rows:
+            try:
+                sm.append(float(r[0]))
+                mx = float(r[1])
+            except ValueError:
+                continue
+            for nm, v in zip(names, r[3:]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------------------
+# algorithmic work (FlexGen notes "背景知识" memory formulas, "附录 A.3" compute terms)
+# ---------------------------------------------------------------------------------------
+
+def decode_product_bytes(w, b) -> float:
+    """One decode step of one layer, all four products: every 4-bit weight
+    once for the whole block plus fp16 activations in, out and residual."""
+    h1, h2 = w.h1, w.h2
+    weights = (4 * h1 * h1 + 2 * h1 * h2) * Q4
+    act = 2 * b * ((h1 + 3 * h1) + (h1 + h1 + h1) + (h1 + h2) + (h2 + h1 + h1))
+    return weights + act
+
+
+def decode_product_flops(w, b) -> float:
+    return 2.0 * b * (4 * w.h1 * w.h1 + 2 * w.h1 * w.h2)
+
+
+def decode_attn_bytes(w, b, length) -> float:
+    """Read K and V of `length` tokens (4-bit), read q, write the output."""
+    return 2 * b * w.h1 * length * Q4 + 2 * b * w.h1 * 2
+
+
+def prefill_product_flops(w, b, s) -> float:
+    return 2.0 * b * s * (4 * w.h1 * w.h1 + 2 * w.h1 * w.h2)
+
+
+def prefill_attn_flops(w, b, s) -> float:
+    return 4.0 * b * w.h1 * (s * (s + 1) / 2)
+
+
+def decode_step_bytes(w, b, length) -> float:
+    return decode_product_bytes(w, b) + decode_attn_bytes(w, b, length) + 2 * b * w.h1 * Q4
+
+
+# ---------------------------------------------------------------------------------------
+# CPU oracle timing (the reference arm and the cpu_baseline)
+# ---------------------------------------------------------------------------------------
+
+def oracle_decode_sample(w, budget_s: float = 20.0) -> dict:
+    """Times the oracle on one decode step of one layer for the whole block at
+    cache length s + n/2, including the dequantization of that layer's 4-bit
+    weights (stored quantized, converted back before compute).  Returns
+    decode tokens/s of the full l-layer model on this host."""
+    from oracle import codec as ocodec
+    from oracle import layer as olayer
+
+    raw = synth.layer_weights(w, 0, "cpu")
+    stored = {}
+    for m in synth.MATS:     # model preparation, not timed
+        a = raw[m].numpy()
+        parts = [ocodec.quantize_g64(a[r:r + 64]) for r in range(0, a.shape[0], 64)]
+        stored[m] = tuple(np.concatenate([p[i] for p in parts]) for i in range(3))
+    length = w.s + w.n // 2
+    cache = olayer.KVCache(w.b, w.heads, w.head_dim, length + 1, True, w.act)
+    rng = np.random.default_rng(0)
+    cache.k_val[:, :, :length] = rng.standard_normal((w.b, w.heads, length, w.head_dim))
+    cache.v_val[:, :, :length] = rng.standard_normal((w.b, w.heads, length, w.head_dim))
+    t_in = synth.decode_inputs(w, n=1, device="cpu")[0].numpy().astype(np.float64)
+    act = np.float16 if w.act == "f16" else np.float32
+    times = []
+    t_start = time.perf_counter()
+    while True:
+        t0 = time.perf_counter()
+        wts = olayer.Weights(**{m: olayer.dequant_weight(*stored[m], w.act) for m in synth.MATS})
+        olayer.decode_layer(t_in, wts, cache, length)
+        times.append(time.perf_counter() - t0)
+        if time.perf_counter() - t_start > budget_s or len(times) >= 3:
+            break
+    t = statistics.median(times)
+    return {"value": w.b / (t * w.l), "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+            "threads": os.environ.get("OMP_NUM_THREADS") or os.environ.get("OPENBLAS_NUM_THREADS") or "blas default",
+            "sample": (f"one decode step of one {w.name} layer for all b={w.b} sequences at cache length "
+                       f"{length}, weight dequantization included, median of {len(times)}; scaled to "
+                       f"l={w.l} layers"),
+            "seconds_per_layer_step": t}
+
+
+def run_reference(args, w, rank, world):
+    if rank != 0:
+        return
+    res = oracle_decode_sample(w)
+    line = {"impl": "reference", "metric": METRIC, "value": res["value"], "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": res["seconds_per_layer_step"] * w.l * w.n * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "l": w.l, "h1": w.h1, "h2": w.h2, "heads": w.heads, "b": w.b,
+                       "s": w.s, "n": w.n},
+            "cpu_baseline": {k: res[k] for k in ("value", "unit", "cores", "kind", "sample", "threads")},
+            "e2e": {"value": res["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------------------
+# the CUDA path
+# ---------------------------------------------------------------------------------------
+
+def run_ours(args, w, rank, world, device):
+    import int4_group_quantized_gb300 as fg
+
+    dt = synth.torch_dtype(w.act)
+    torch.cuda.set_device(device)
+    dev = torch.device("cuda", device)
+    st = torch.cuda.current_stream()
+
+    # model preparation (not timed): fp16 weights drawn on the device one layer
+    # at a time, quantized by the library's codec kernel, fp16 copy freed
+    layers, kvs = [], []
+    qbytes, qtime = 0, 0.0
+    for i in range(w.l):
+        raw = synth.layer_weights(w, i, dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        L = fg.Layer.from_dense(raw, w.heads, quantized=True)
+        e1.record()
+        e1.synchronize()
+        qtime += e0.elapsed_time(e1) / 1e3
+        qbytes += sum(t.numel() for t in raw.values()) * (2 + Q4)
+        layers.append(L)
+        del raw
+        kvs.append(fg.KVCache(w.b, w.heads, w.head_dim, w.s + w.n, True, dt, dev))
+    blk = fg.Block(layers, kvs)
+    ws = fg.workspace(max(fg.fg_prefill_block_workspace_bytes(layers[0], w.b, w.s),
+                          fg.fg_decode_block_workspace_bytes(layers[0], w.b, w.s + w.n)), dev)
+    x = synth.prompt(w, device=dev, seed_offset=rank)
+    tin = synth.decode_inputs(w, device=dev, seed_offset=rank)
+    y = torch.empty_like(x)
+    outs = torch.empty_like(tin)
+
+    def step(evs=None):
+        if evs:
+            evs[0].record(st)
+        fg.fg_profile_phase(0) if args._prof else None
+        fg.fg_prefill_block(blk, x, y, ws, st)
+        if evs:
+            evs[1].record(st)
+        fg.fg_profile_phase(1) if args._prof else None
+        for t in range(w.n):
+            fg.fg_decode_block_step(blk, tin[t], w.s + t, outs[t], ws, st)
+        if evs:
+            evs[2].record(st)
+
+    args._prof = False
+    for _ in range(args.warmup):
+        step()
+    fg.fg_sync_status(st)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    launches_per_step = w.l * 8 + w.n * w.l * 8
+    fg.fg_profile_start(args.steps * launches_per_step + 64)
+    args._prof = True
+    n0 = fg.fg_launch_count()
+    with ClockSampler(device) as clk:
+        t_wall = time.perf_counter()
+        for k in range(args.steps):
+            step(evs[k])
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    n_launch = fg.fg_launch_count() - n0
+    prof = fg.fg_profile_stop()
+    args._prof = False
+    fg.fg_sync_status(st)
+    pre_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    dec_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    tot_ms = [e[0].elapsed_time(e[2]) for e in evs]
+    dec_total = sum(dec_ms) / 1e3
+    tot_total = sum(tot_ms) / 1e3
+    pre_total = sum(pre_ms) / 1e3
+    if world > 1:
+        t = torch.tensor([dec_total, tot_total, pre_total], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        dec_total, tot_total, pre_total = t.tolist()
+    nonfinite = int((~torch.isfinite(outs)).sum().item())
+
+    # end to end through the public API with host buffers: the prompt and each
+    # step's embedding come from pinned host memory, each step's output goes back
+    x_h = x.cpu().pin_memory()
+    tin_h = tin.cpu().pin_memory()
+    out_h = torch.empty(outs.shape, dtype=outs.dtype, pin_memory=True)
+    x_d = torch.empty_like(x)
+    t_d = torch.empty_like(tin[0])
+    e2e_ms = []
+    for k in range(args.steps):
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        x_d.copy_(x_h, non_blocking=True)
+        fg.fg_prefill_block(blk, x_d, y, ws, st)
+        e[0].record(st)
+        for t in range(w.n):
+            t_d.copy_(tin_h[t], non_blocking=True)
+            fg.fg_decode_block_step(blk, t_d, w.s + t, outs[t], ws, st)
+            out_h[t].copy_(outs[t], non_blocking=True)
+        e[1].record(st)
+        torch.cuda.synchronize()
+        e2e_ms.append(e[0].elapsed_time(e[1]))
+    e2e_dec = sum(e2e_ms) / 1e3
+    if world > 1:
+        t = torch.tensor([e2e_dec], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_dec = t.item()
+
+    if rank != 0:
+        return
+    pk = peaks()
+    K = args.steps
+    tokens = w.b * w.n * K * world
+    value = tokens / dec_total
+    # roofline of the decode phase's dominant kernel class
+    mean_len = statistics.mean(w.s + t + 1 for t in range(w.n))
+    dec_prof = prof.get(1, {})
+    pre_prof = prof.get(0, {})
+    work = {}
+    for name, (cnt, ms) in dec_prof.items():
+        if name.startswith("gemm"):
+            flops = decode_product_flops(w, w.b) * w.l * w.n * K
+            byts = decode_product_bytes(w, w.b) * w.l * w.n * K
+            # split-K reduction launches belong to the products they finish
+            work[name] = (byts, flops, ms, cnt)
+        elif name == "attn_decode":
+            work[name] = (decode_attn_bytes(w, w.b, mean_len) * w.l * w.n * K, 4.0 * w.b * w.h1 * mean_len * w.l * w.n * K, ms, cnt)
+    dom = max(dec_prof.items(), key=lambda kv: kv[1][1])[0] if dec_prof else None
+    roof = None
+    if dom in work:
+        byts, flops, ms, cnt = work[dom]
+        if dom.startswith("gemm") and w.b >= 128:
+            ach = flops / (ms / 1e3) / 1e12
+            roof = {"bound": "tensor", "achieved": ach, "peak": pk["tflops_sustained"], "unit": "TFLOP/s",
+                    "frac": ach / pk["tflops_sustained"], "traffic": None, "kernel": dom}
+        else:
+            ach = byts / (ms / 1e3) / 1e9
+            roof = {"bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                    "frac": ach / pk["hbm_gbs"], "traffic": None, "kernel": dom}
+        roof.update({"launches": cnt, "avg_launch_us": ms / cnt * 1e3,
+                     "algorithmic_per_launch": (byts if roof["unit"] == "GB/s" else flops) / cnt,
+                     "peak_source": pk["source"] + (" sustained" if roof["unit"] == "TFLOP/s" else "")})
+    roof_pre = None
+    g_pre = {k: v for k, v in pre_prof.items() if k.startswith("gemm")}
+    if g_pre:
+        ms = sum(v[1] for v in g_pre.values())
+        cnt = sum(v[0] for v in g_pre.values())
+        ach = prefill_product_flops(w, w.b, w.s) * w.l * K / (ms / 1e3) / 1e12
+        roof_pre = {"bound": "tensor", "achieved": ach, "peak": pk["tflops_sustained"], "unit": "TFLOP/s",
+                    "frac": ach / pk["tflops_sustained"], "traffic": None, "kernel": "+".join(sorted(g_pre)),
+                    "launches": cnt, "avg_launch_us": ms / cnt * 1e3}
+    dec_bytes = sum(decode_step_bytes(w, w.b, w.s + t + 1) for t in range(w.n)) * w.l * K * world
+    cpu = oracle_decode_sample(w, budget_s=args.cpu_budget) if not args.no_cpu else None
+    clocks = clk.summary()
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": tot_total / K * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": {"workload": w.name, "l": w.l, "h1": w.h1, "h2": w.h2, "heads": w.heads, "b": w.b,
+                   "s": w.s, "n": w.n, "weights": "int4 g64 (fp32 min/scale)", "kv": "int4 g64",
+                   "l2": "inputs larger than L2 (%.1f GB of 4-bit weights + %.1f GB of 4-bit KV)" % (
+                       sum(L.nbytes() for L in layers) / 1e9, sum(c.nbytes() for c in kvs) / 1e9),
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "value_definition": "b*n*steps*ranks / decode-phase device time (max over ranks)"},
+        "roofline": roof, "roofline_prefill": roof_pre,
+        "decode_achieved_gbs_step": dec_bytes / dec_total / 1e9,
+        "prefill_tok_s": w.b * w.s * K * world / pre_total,
+        "generation_tok_s": w.b * w.n * K * world / tot_total,
+        "decode_ms_per_step": dec_total / K * 1e3, "prefill_ms_per_step": pre_total / K * 1e3,
+        "quantize_gbs": qbytes / qtime / 1e9 if qtime else None,
+        "kernels": {f"{'prefill' if p == 0 else 'decode'}:{k}": {"launches": v[0], "ms": round(v[1], 3)}
+                    for p, d in prof.items() for k, v in d.items()},
+        "gpu_launches": int(n_launch), "nonfinite_decode_outputs": nonfinite,
+        "cpu_baseline": cpu and {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample", "threads")},
+        "e2e": {"value": w.b * w.n * K * world / e2e_dec, "unit": "tokens/s",
+                "h2d_bytes_per_step": x.numel() * x.element_size() + tin.numel() * tin.element_size(),
+                "d2h_bytes_per_step": outs.numel() * outs.element_size(),
+                "definition": "decode phase with per-step host->device input and device->host output copies"},
+        "clocks": clocks, "wall_s_timed": t_wall,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--config", default="opt-6.7b", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu", action="store_true", help="skip the oracle timing")
+    ap.add_argument("--cpu-budget", type=float, default=20.0)
+    args = ap.parse_args()
+    w = synth.WORKLOADS[args.config]
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, w, rank, world)
+        return
+    if world > 1:
+        torch.cuda.set_device(local)
+        torch.distributed.init_process_group("nccl")
+    run_ours(args, w, rank, world, local)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

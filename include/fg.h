@@ -191,6 +191,27 @@ fg_status fg_sync_status(cudaStream_t stream);
 const char* fg_status_str(fg_status s);
 const char* fg_last_error(void);
 
+/* Launch accounting (measurement support, not part of the method).
+ * fg_profile_start(max_launches): from now on every kernel launch of the
+ * library gets a pair of CUDA events on its own stream (host-side event
+ * objects, no device memory), up to max_launches launches; later launches
+ * are counted as dropped.  fg_profile_stop(): waits for the recorded events
+ * and accumulates per (phase, kernel class) (FG_ERR_WORKSPACE if launches
+ * were dropped).  fg_profile_phase(p), 0 <= p < 4: tags the following
+ * launches with phase p (0 after start), e.g. prefill vs decode.
+ * fg_profile_query(p, i, ...): launches and total milliseconds of class i
+ * (0 <= i < fg_profile_kernel_classes()) in phase p, named by
+ * fg_profile_kernel_name(i).  Not thread-safe against concurrent
+ * start/stop.  fg_launch_count(): kernels launched since the library
+ * was loaded. */
+fg_status fg_profile_start(int32_t max_launches);
+fg_status fg_profile_phase(int32_t phase);
+fg_status fg_profile_stop(void);
+int32_t fg_profile_kernel_classes(void);
+const char* fg_profile_kernel_name(int32_t i);
+fg_status fg_profile_query(int32_t phase, int32_t i, int64_t* launches, double* total_ms);
+uint64_t fg_launch_count(void);
+
 /* Library version, e.g. "fg 0.1 sm_103a". */
 const char* fg_version(void);
 

@@ -94,6 +94,14 @@ _sig("fg_sync_status", _INT, _P)
 _sig("fg_status_str", ctypes.c_char_p, _INT)
 _sig("fg_last_error", ctypes.c_char_p)
 _sig("fg_version", ctypes.c_char_p)
+_sig("fg_profile_start", _INT, ctypes.c_int32)
+_sig("fg_profile_stop", _INT)
+_sig("fg_profile_kernel_classes", ctypes.c_int32)
+_sig("fg_profile_kernel_name", ctypes.c_char_p, ctypes.c_int32)
+_sig("fg_profile_phase", _INT, ctypes.c_int32)
+_sig("fg_profile_query", _INT, ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(ctypes.c_int64),
+     ctypes.POINTER(ctypes.c_double))
+_sig("fg_launch_count", ctypes.c_uint64)
 
 lib = _lib
 
@@ -314,6 +322,32 @@ def fg_decode_block_step(block: Block, t: torch.Tensor, pos: int, y: torch.Tenso
 
 def fg_sync_status(stream=None) -> None:
     _check(_lib.fg_sync_status(_stream(stream)), "fg_sync_status")
+
+
+def fg_profile_start(max_launches: int) -> None:
+    _check(_lib.fg_profile_start(int(max_launches)), "fg_profile_start")
+
+
+def fg_profile_phase(phase: int) -> None:
+    _check(_lib.fg_profile_phase(int(phase)), "fg_profile_phase")
+
+
+def fg_profile_stop(phases: int = 4) -> dict:
+    """Stops launch tracing; returns {phase: {kernel class: (launches, total ms)}}."""
+    st = _lib.fg_profile_stop()
+    out = {}
+    for p in range(phases):
+        for i in range(_lib.fg_profile_kernel_classes()):
+            n, ms = ctypes.c_int64(), ctypes.c_double()
+            _lib.fg_profile_query(p, i, ctypes.byref(n), ctypes.byref(ms))
+            if n.value:
+                out.setdefault(p, {})[_lib.fg_profile_kernel_name(i).decode()] = (n.value, ms.value)
+    _check(st, "fg_profile_stop")
+    return out
+
+
+def fg_launch_count() -> int:
+    return int(_lib.fg_launch_count())
 
 
 def fg_version() -> str:

@@ -261,6 +261,7 @@ KVSrc make_src(const fg_kv& kv) {
 template <typename T, bool QUANT, int D>
 void launch_decode(const fg_kv& kv, const void* q, int64_t ldq, int64_t b, int64_t pos, void* out,
                    int64_t ldo, cudaStream_t st) {
+  Trace tr(KC_ATTN_DECODE, st);
   decode_attn_simt_kernel<T, QUANT, D><<<static_cast<unsigned>(b * kv.heads), 128, 0, st>>>(
       make_src(kv), static_cast<const T*>(q), ldq, pos, static_cast<T*>(out), ldo, kv.heads,
       kv.capacity);
@@ -270,6 +271,7 @@ template <typename T, bool QUANT, int D>
 void launch_prefill(const fg_kv& kv, const void* q, int64_t ldq, int64_t b, int64_t s, void* out,
                     int64_t ldo, cudaStream_t st) {
   const int64_t nqb = (s + 15) / 16;
+  Trace tr(KC_ATTN_PREFILL, st);
   prefill_attn_simt_kernel<T, QUANT, D><<<static_cast<unsigned>(b * kv.heads * nqb), 128, 0, st>>>(
       make_src(kv), static_cast<const T*>(q), ldq, s, static_cast<T*>(out), ldo, kv.heads,
       kv.capacity);

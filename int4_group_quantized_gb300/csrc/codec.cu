@@ -232,6 +232,7 @@ fg_status quantize_rows(const void* x, fg_dtype dt, int64_t rows, int64_t cols, 
   const int64_t ngroups = rows * (cols / 64);
   if (ngroups == 0) return FG_OK;
   const int grid = grid_for(ngroups, 32);  // 8 warps x 4 groups per block
+  Trace tr(KC_QUANTIZE, st);
   if (dt == FG_F16)
     quantize_kernel<__half><<<grid, 256, 0, st>>>(static_cast<const __half*>(x), ngroups,
                                                   reinterpret_cast<uint32_t*>(codes), mins, scales);
@@ -246,6 +247,7 @@ fg_status dequant_rows(const uint8_t* codes, const float* mins, const float* sca
   const int64_t nwords = rows * cols / 8;
   if (nwords == 0) return FG_OK;
   const int grid = grid_for(nwords, 256);
+  Trace tr(KC_DEQUANT, st);
   const uint32_t* c = reinterpret_cast<const uint32_t*>(codes);
   if (dt == FG_F16)
     dequant_kernel<__half><<<grid, 256, 0, st>>>(c, mins, scales, nwords, static_cast<__half*>(out));
@@ -268,6 +270,7 @@ fg_status kv_store(const fg_kv& kv, const void* ksrc, const void* vsrc, int64_t 
     dst.scales[1] = kv.v_scales;
     const int64_t ngroups = 2 * b * ntok * (h1 / 64);
     const int grid = grid_for(ngroups, 32);
+    Trace tr(KC_KV_STORE, st);
     if (kv.dtype == FG_F16)
       kv_store_q4_kernel<__half><<<grid, 256, 0, st>>>(
           static_cast<const __half*>(ksrc), static_cast<const __half*>(vsrc), ld, b, ntok, pos0,
@@ -280,6 +283,7 @@ fg_status kv_store(const fg_kv& kv, const void* ksrc, const void* vsrc, int64_t 
   }
   const int64_t n8 = 2 * b * ntok * (h1 / 8);
   const int grid = grid_for(n8, 256);
+  Trace tr(KC_KV_STORE, st);
   if (kv.dtype == FG_F16)
     kv_store_dense_kernel<__half><<<grid, 256, 0, st>>>(
         static_cast<const __half*>(ksrc), static_cast<const __half*>(vsrc), ld, b, ntok, pos0, h1,

@@ -3,6 +3,10 @@
 #include <stdarg.h>
 #include <stdio.h>
 
+#include <atomic>
+#include <mutex>
+#include <vector>
+
 #include "fg_internal.cuh"
 
 namespace fg {
@@ -51,9 +55,120 @@ unsigned int* device_error_word() {
   return cache[dev];
 }
 
+// ---- launch tracing ----------------------------------------------------------
+namespace {
+const char* const kClassNames[KC_COUNT] = {
+    "quantize_g64", "dequant_g64", "kv_store_q4", "gemm_simt", "gemm_tc_q4",
+    "gemm_splitk_reduce", "attn_decode", "attn_decode_combine", "attn_prefill"};
+
+struct Profiler {
+  std::mutex mu;
+  bool on = false;
+  std::vector<cudaEvent_t> ev;   // 2 per launch
+  std::vector<int> cls;          // class + KC_COUNT * phase
+  size_t used = 0;
+  int64_t dropped = 0;
+  int phase = 0;
+  int64_t launches[kProfilePhases * KC_COUNT] = {0};
+  double ms[kProfilePhases * KC_COUNT] = {0};
+};
+Profiler g_prof;
+std::atomic<uint64_t> g_launches{0};
+thread_local int t_open_slot = -1;
+}  // namespace
+
+void trace_begin(int c, cudaStream_t st) {
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  t_open_slot = -1;
+  if (!g_prof.on) return;
+  std::lock_guard<std::mutex> lk(g_prof.mu);
+  if (!g_prof.on) return;
+  if (g_prof.used >= g_prof.cls.size()) {
+    ++g_prof.dropped;
+    return;
+  }
+  const size_t i = g_prof.used++;
+  g_prof.cls[i] = c + KC_COUNT * g_prof.phase;
+  cudaEventRecord(g_prof.ev[2 * i], st);
+  t_open_slot = static_cast<int>(i);
+}
+
+void trace_end(int c, cudaStream_t st) {
+  (void)c;
+  if (t_open_slot < 0) return;
+  std::lock_guard<std::mutex> lk(g_prof.mu);
+  cudaEventRecord(g_prof.ev[2 * t_open_slot + 1], st);
+  t_open_slot = -1;
+}
+
 }  // namespace fg
 
 extern "C" {
+
+fg_status fg_profile_start(int32_t max_launches) {
+  using fg::g_prof;
+  if (max_launches <= 0) return fg::fail(FG_ERR_ARG, "max_launches");
+  std::lock_guard<std::mutex> lk(g_prof.mu);
+  if (g_prof.on) return fg::fail(FG_ERR_ARG, "profiling already active");
+  const size_t need = 2 * static_cast<size_t>(max_launches);
+  while (g_prof.ev.size() < need) {
+    cudaEvent_t e;
+    if (cudaEventCreate(&e) != cudaSuccess) return fg::fail(FG_ERR_CUDA, "cudaEventCreate");
+    g_prof.ev.push_back(e);
+  }
+  g_prof.cls.assign(max_launches, 0);
+  g_prof.used = 0;
+  g_prof.dropped = 0;
+  for (int i = 0; i < fg::kProfilePhases * fg::KC_COUNT; ++i) {
+    g_prof.launches[i] = 0;
+    g_prof.ms[i] = 0;
+  }
+  g_prof.phase = 0;
+  g_prof.on = true;
+  return FG_OK;
+}
+
+fg_status fg_profile_stop(void) {
+  using fg::g_prof;
+  std::lock_guard<std::mutex> lk(g_prof.mu);
+  if (!g_prof.on) return fg::fail(FG_ERR_ARG, "profiling not active");
+  g_prof.on = false;
+  for (size_t i = 0; i < g_prof.used; ++i) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(g_prof.ev[2 * i + 1]) != cudaSuccess ||
+        cudaEventElapsedTime(&ms, g_prof.ev[2 * i], g_prof.ev[2 * i + 1]) != cudaSuccess)
+      return fg::fail(FG_ERR_CUDA, "event timing");
+    g_prof.launches[g_prof.cls[i]] += 1;
+    g_prof.ms[g_prof.cls[i]] += ms;
+  }
+  return g_prof.dropped ? fg::fail(FG_ERR_WORKSPACE, "%lld launches not timed (pool full)",
+                                   (long long)g_prof.dropped)
+                        : FG_OK;
+}
+
+int32_t fg_profile_kernel_classes(void) { return fg::KC_COUNT; }
+
+const char* fg_profile_kernel_name(int32_t i) {
+  return (i >= 0 && i < fg::KC_COUNT) ? fg::kClassNames[i] : "";
+}
+
+fg_status fg_profile_phase(int32_t phase) {
+  if (phase < 0 || phase >= fg::kProfilePhases) return fg::fail(FG_ERR_ARG, "phase");
+  std::lock_guard<std::mutex> lk(fg::g_prof.mu);
+  fg::g_prof.phase = phase;
+  return FG_OK;
+}
+
+fg_status fg_profile_query(int32_t phase, int32_t i, int64_t* launches, double* total_ms) {
+  if (phase < 0 || phase >= fg::kProfilePhases || i < 0 || i >= fg::KC_COUNT || !launches ||
+      !total_ms)
+    return fg::fail(FG_ERR_ARG, "phase/class");
+  *launches = fg::g_prof.launches[phase * fg::KC_COUNT + i];
+  *total_ms = fg::g_prof.ms[phase * fg::KC_COUNT + i];
+  return FG_OK;
+}
+
+uint64_t fg_launch_count(void) { return fg::g_launches.load(); }
 
 const char* fg_status_str(fg_status s) {
   switch (s) {

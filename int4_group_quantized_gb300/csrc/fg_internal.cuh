@@ -24,6 +24,32 @@ unsigned int* device_error_word();
 
 enum DeviceError : unsigned int { DEV_ERR_WAIT_TIMEOUT = 1u };
 
+// ---- launch tracing ----------------------------------------------------------
+// Every kernel launch is bracketed by a Trace; while fg_profile_start() is
+// active each launch gets a pair of CUDA events on its stream, accumulated per
+// kernel class by fg_profile_stop().  A launch counter runs always.
+enum KernelClass : int {
+  KC_QUANTIZE = 0,
+  KC_DEQUANT,
+  KC_KV_STORE,
+  KC_GEMM_SIMT,
+  KC_GEMM_TC,
+  KC_GEMM_REDUCE,
+  KC_ATTN_DECODE,
+  KC_ATTN_COMBINE,
+  KC_ATTN_PREFILL,
+  KC_COUNT
+};
+constexpr int kProfilePhases = 4;
+void trace_begin(int cls, cudaStream_t st);
+void trace_end(int cls, cudaStream_t st);
+struct Trace {
+  int cls;
+  cudaStream_t st;
+  Trace(int c, cudaStream_t s) : cls(c), st(s) { trace_begin(c, s); }
+  ~Trace() { trace_end(cls, st); }
+};
+
 // ---- weight operand of a product -----------------------------------------
 // A product's B operand may be split into up to three matrices laid side by
 // side along N (w_Q | w_K | w_V share one launch); each segment's N is a

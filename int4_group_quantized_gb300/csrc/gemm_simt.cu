@@ -129,6 +129,7 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmArgs a) {
 fg_status gemm_simt(const GemmArgs& a, cudaStream_t st) {
   if (a.M == 0 || a.N == 0) return FG_OK;
   dim3 grid(static_cast<unsigned>(a.N / BN), static_cast<unsigned>((a.M + BM - 1) / BM));
+  Trace tr(KC_GEMM_SIMT, st);
   if (a.dtype == FG_F16) {
     if (a.quant) gemm_simt_kernel<__half, true><<<grid, 256, 0, st>>>(a);
     else gemm_simt_kernel<__half, false><<<grid, 256, 0, st>>>(a);

@@ -49,11 +49,12 @@ def _act_np(act_dtype: str):
 
 
 def weight_for_compute(w: np.ndarray, quantized: bool, act_dtype: str,
-                       rows_per_chunk: int = 2048) -> np.ndarray:
+                       rows_per_chunk: int = 64) -> np.ndarray:
     """w: [K=in][N=out] in the storage type of the generated weights.
     Returns the matrix the layer multiplies by, in fp64: the raw weights,
     or dequant(quant(w)) grouped along the output channel (the last axis)
-    and converted to the activation type."""
+    and converted to the activation type.  Rows are processed in chunks only
+    to bound the size of temporaries."""
     if not quantized:
         return np.asarray(w).astype(np.float64)
     out = np.empty(w.shape, dtype=np.float64)
@@ -61,6 +62,19 @@ def weight_for_compute(w: np.ndarray, quantized: bool, act_dtype: str,
         blk = np.asarray(w[r0:r0 + rows_per_chunk])
         c, m, s = codec.quantize_g64(blk)
         out[r0:r0 + rows_per_chunk] = codec.dequant_g64(c, m, s, _act_np(act_dtype))
+    return out
+
+
+def dequant_weight(codes: np.ndarray, mins: np.ndarray, scales: np.ndarray, act_dtype: str,
+                   rows_per_chunk: int = 64) -> np.ndarray:
+    """A stored 4-bit weight ([K][N/2] codes, [K][N/64] mins and scales)
+    converted back to the activation type, as fp64 (row chunks only bound
+    the temporaries)."""
+    K = codes.shape[0]
+    out = np.empty((K, codes.shape[1] * 2), dtype=np.float64)
+    for r0 in range(0, K, rows_per_chunk):
+        sl = slice(r0, r0 + rows_per_chunk)
+        out[sl] = codec.dequant_g64(codes[sl], mins[sl], scales[sl], _act_np(act_dtype))
     return out
 
 
