@@ -139,6 +139,20 @@ fg_status fg_dequant_g64(const uint8_t* codes, const float* mins, const float* s
 fg_status fg_kv_append(const fg_kv* kv, const void* k_new, const void* v_new, int64_t pos,
                        cudaStream_t stream);
 
+/* [BG] one product of the layer with its epilogue, on weights stored per
+ * [S5]: y = act(x . w + r), act = relu if `relu` != 0 else identity.
+ * x: device [M][w->K] (dtype), r: device [M][w->N] or NULL, y: device
+ * [M][w->N]; y must not overlap x or r.
+ * codec FG_CODEC_Q4G64 uses w->codes/mins/scales (dequantized on the fly,
+ * rounded to the compute dtype), FG_CODEC_NONE uses w->dense ([K][N] in
+ * dtype).  K and N must be multiples of 64.  fp16 with M >= 64 runs on the
+ * tensor cores (split over K when the output has too few tiles, using ws);
+ * other cases on the CUDA cores.  ws_bytes >= fg_linear_workspace_bytes. */
+size_t fg_linear_workspace_bytes(int64_t M, int64_t K, int64_t N, fg_codec codec, fg_dtype dtype);
+fg_status fg_linear(const fg_wmat* w, fg_codec codec, fg_dtype dtype, const void* x, int64_t M,
+                    const void* r, int32_t relu, void* y, void* ws, size_t ws_bytes,
+                    cudaStream_t stream);
+
 /* Workspace (device bytes) that fg_prefill_layer / fg_prefill_block need for
  * b sequences of s tokens, and that fg_decode_step / fg_decode_block_step
  * need for b sequences with a cache of `capacity` slots.  Pure host

@@ -352,3 +352,26 @@ def fg_launch_count() -> int:
 
 def fg_version() -> str:
     return _lib.fg_version().decode()
+
+
+_sig("fg_linear_workspace_bytes", _SZ, _I64, _I64, _I64, _INT, _INT)
+_sig("fg_linear", _INT, ctypes.POINTER(fg_wmat), _INT, _INT, _P, _I64, _P, ctypes.c_int32, _P, _P, _SZ, _P)
+
+
+def fg_linear_workspace_bytes(M: int, K: int, N: int, quantized: bool, dtype: torch.dtype) -> int:
+    return _lib.fg_linear_workspace_bytes(int(M), int(K), int(N), FG_CODEC_Q4G64 if quantized else FG_CODEC_NONE,
+                                          FG_F16 if dtype == torch.float16 else FG_F32)
+
+
+def fg_linear(w: QuantWeight, x: torch.Tensor, y: torch.Tensor, r: torch.Tensor | None = None, relu: bool = False,
+              ws: torch.Tensor | None = None, stream=None) -> None:
+    """y = act(x . w + r) through the library's product kernels."""
+    quant = w.codes is not None
+    M = x.shape[0]
+    if ws is None:
+        need = fg_linear_workspace_bytes(M, w.K, w.N, quant, x.dtype)
+        ws = workspace(need, x.device) if need else None
+    s = w.struct()
+    _check(_lib.fg_linear(ctypes.byref(s), FG_CODEC_Q4G64 if quant else FG_CODEC_NONE, _dt(x), _ptr(x), M, _ptr(r),
+                          1 if relu else 0, _ptr(y), _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)),
+           "fg_linear")

@@ -81,6 +81,11 @@ struct GemmArgs {
 
 // CUDA-core product (any M, fp16 or fp32).
 fg_status gemm_simt(const GemmArgs& a, cudaStream_t st);
+// Tensor-core product (fp16, M >= 64); Q4 segments are dequantized in shared
+// memory, dense segments are loaded by TMA.
+bool gemm_tc_supported(const GemmArgs& a);
+fg_status gemm_tc(const GemmArgs& a, void* ws, size_t ws_bytes, cudaStream_t st);
+size_t gemm_tc_workspace_bytes(int64_t M, int64_t N, int64_t K, bool q4);
 // Y = epilogue(X . W); chooses the kernel for the shape.  Scratch: `ws`
 // (device, may be null when ws_bytes == 0) for split-K partial sums.
 fg_status gemm(const GemmArgs& a, void* ws, size_t ws_bytes, cudaStream_t st);

@@ -118,10 +118,26 @@ size_t activations_bytes(const fg_layer& L, int64_t M) {
   return up(M * 3 * L.h1 * e) + up(M * L.h1 * e) * 2 + up(M * L.h2 * e);
 }
 
+// Prefill with fp16 activations runs its products on the tensor cores from
+// fp16 weights: the layer's six 4-bit matrices are dequantized once into the
+// workspace (each weight then feeds all b*s rows).
+bool prefill_dequantizes(const fg_layer& L, int64_t M) {
+  return L.dtype == FG_F16 && L.codec == FG_CODEC_Q4G64 && M >= 128;
+}
+size_t w16_bytes(const fg_layer& L) {
+  return up(L.h1 * L.h1 * 2) * 4 + up(L.h1 * L.h2 * 2) * 2;
+}
+
 size_t scratch_bytes(const fg_layer& L, int64_t M, int64_t capacity, bool decode) {
-  const int quant = L.codec == FG_CODEC_Q4G64;
+  int quant = L.codec == FG_CODEC_Q4G64;
+  size_t w16 = 0;
+  if (!decode && prefill_dequantizes(L, M)) {
+    w16 = w16_bytes(L);
+    quant = 0;
+  }
   size_t s = gemm_workspace_bytes(M, 3 * L.h1, L.h1, L.dtype, quant);
-  size_t t;
+  size_t t = gemm_workspace_bytes(M, L.h1, L.h1, L.dtype, quant);
+  s = t > s ? t : s;
   t = gemm_workspace_bytes(M, L.h2, L.h1, L.dtype, quant);
   s = t > s ? t : s;
   t = gemm_workspace_bytes(M, L.h1, L.h2, L.dtype, quant);
@@ -130,7 +146,7 @@ size_t scratch_bytes(const fg_layer& L, int64_t M, int64_t capacity, bool decode
     t = decode_attention_workspace_bytes(M, L.heads, static_cast<int32_t>(L.h1 / L.heads), capacity);
     s = t > s ? t : s;
   }
-  return up(s);
+  return w16 + up(s);
 }
 
 Buffers carve(const fg_layer& L, int64_t M, void* ws) {
@@ -159,20 +175,36 @@ fg_status run_prefill(const fg_layer& L, const void* x, int64_t b, int64_t s, co
                       void* y, void* ws, size_t scratch, cudaStream_t st) {
   const int64_t M = b * s, h1 = L.h1, h2 = L.h2;
   Buffers B = carve(L, M, ws);
-  const fg_wmat qkv[3] = {L.wq, L.wk, L.wv};
+  fg_layer Lc = L;   // the layer as the products see it
+  if (prefill_dequantizes(L, M)) {
+    // "converted back to FP16 before compute": once per layer, into the workspace
+    char* w = B.scratch;
+    fg_wmat* mats[6] = {&Lc.wq, &Lc.wk, &Lc.wv, &Lc.wo, &Lc.w1, &Lc.w2};
+    for (fg_wmat* m : mats) {
+      FG_TRY(dequant_rows(m->codes, m->mins, m->scales, m->K, m->N, w, FG_F16, st));
+      m->dense = w;
+      m->codes = nullptr;
+      w += up(m->K * m->N * 2);
+    }
+    Lc.codec = FG_CODEC_NONE;
+    scratch -= w16_bytes(L);
+    B.scratch = w;
+  }
+  const fg_layer& P = Lc;
+  const fg_wmat qkv[3] = {P.wq, P.wk, P.wv};
   // x_Q, x_K, x_V = x w_Q, x w_K, x w_V (one pass over the three matrices)
-  FG_TRY(gemm(product(L, x, h1, M, qkv, 3, B.qkv, 3 * h1, nullptr, 0, 0), B.scratch, scratch, st));
+  FG_TRY(gemm(product(P, x, h1, M, qkv, 3, B.qkv, 3 * h1, nullptr, 0, 0), B.scratch, scratch, st));
   // cache the prompt's K/V (quantized per token along the hidden dimension)
   const size_t e = dtype_bytes(L.dtype);
   FG_TRY(kv_store(kv, B.qkv + h1 * e, B.qkv + 2 * h1 * e, 3 * h1, b, s, 0, st));
   // Softmax(x_Q x_K^T / sqrt(d)) x_V, causal, K/V read back through the codec
   FG_TRY(prefill_attention(kv, B.qkv, 3 * h1, b, s, B.att, h1, st));
   // x_Out = (...) w_O + x
-  FG_TRY(gemm(product(L, B.att, h1, M, &L.wo, 1, B.xo, h1, x, h1, 0), B.scratch, scratch, st));
+  FG_TRY(gemm(product(P, B.att, h1, M, &P.wo, 1, B.xo, h1, x, h1, 0), B.scratch, scratch, st));
   // relu(x_Out w_1)
-  FG_TRY(gemm(product(L, B.xo, h1, M, &L.w1, 1, B.hid, h2, nullptr, 0, 1), B.scratch, scratch, st));
+  FG_TRY(gemm(product(P, B.xo, h1, M, &P.w1, 1, B.hid, h2, nullptr, 0, 1), B.scratch, scratch, st));
   // x^{i+1} = (...) w_2 + x_Out
-  FG_TRY(gemm(product(L, B.hid, h2, M, &L.w2, 1, y, h1, B.xo, h1, 0), B.scratch, scratch, st));
+  FG_TRY(gemm(product(P, B.hid, h2, M, &P.w2, 1, y, h1, B.xo, h1, 0), B.scratch, scratch, st));
   return FG_OK;
 }
 
@@ -221,18 +253,13 @@ size_t decode_attention_workspace_bytes(int64_t b, int32_t heads, int32_t head_d
 }
 
 fg_status gemm(const GemmArgs& a, void* ws, size_t ws_bytes, cudaStream_t st) {
-  (void)ws;
-  (void)ws_bytes;
+  if (gemm_tc_supported(a)) return gemm_tc(a, ws, ws_bytes, st);
   return gemm_simt(a, st);
 }
 
 size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, fg_dtype dt, int quant) {
-  (void)M;
-  (void)N;
-  (void)K;
-  (void)dt;
-  (void)quant;
-  return 0;
+  if (dt != FG_F16 || M < 64) return 0;
+  return gemm_tc_workspace_bytes(M, N, K, quant != 0);
 }
 
 }  // namespace fg
@@ -259,6 +286,34 @@ size_t fg_prefill_block_workspace_bytes(const fg_layer* L, int64_t b, int64_t s)
 size_t fg_decode_block_workspace_bytes(const fg_layer* L, int64_t b, int64_t capacity) {
   if (check_layer(L) != FG_OK || b < 0 || capacity < 0) return 0;
   return fg_decode_workspace_bytes(L, b, capacity) + 2 * up(b * L->h1 * dtype_bytes(L->dtype));
+}
+
+size_t fg_linear_workspace_bytes(int64_t M, int64_t K, int64_t N, fg_codec codec, fg_dtype dtype) {
+  if (M < 0 || K <= 0 || N <= 0) return 0;
+  return gemm_workspace_bytes(M, N, K, dtype, codec == FG_CODEC_Q4G64);
+}
+
+fg_status fg_linear(const fg_wmat* w, fg_codec codec, fg_dtype dtype, const void* x, int64_t M,
+                    const void* r, int32_t relu, void* y, void* ws, size_t ws_bytes,
+                    cudaStream_t stream) {
+  if (!w) return fail(FG_ERR_ARG, "null weight");
+  if (dtype != FG_F16 && dtype != FG_F32) return fail(FG_ERR_ARG, "dtype");
+  if (codec != FG_CODEC_NONE && codec != FG_CODEC_Q4G64) return fail(FG_ERR_ARG, "codec");
+  if (M < 0 || w->K <= 0 || w->N <= 0) return fail(FG_ERR_ARG, "sizes");
+  if (w->K % 64 || w->N % 64) return fail(FG_ERR_SHAPE, "K and N must be multiples of 64");
+  FG_TRY(check_wmat(*w, w->K, w->N, codec, "w"));
+  if (M == 0) return FG_OK;
+  FG_TRY(check_act(x, "x"));
+  FG_TRY(check_act(y, "y"));
+  if (r && !aligned(r, 16)) return fail(FG_ERR_ALIGN, "r needs 16-byte alignment");
+  if (r == y || x == y) return fail(FG_ERR_ARG, "y must not alias x or r");
+  const size_t need = fg_linear_workspace_bytes(M, w->K, w->N, codec, dtype);
+  if (need && (!ws || ws_bytes < need)) return fail(FG_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes, need);
+  fg_layer L{};
+  L.codec = codec;
+  L.dtype = dtype;
+  GemmArgs a = product(L, x, w->K, M, w, 1, y, w->N, r, w->N, relu ? 1 : 0);
+  return gemm(a, ws, ws_bytes, stream);
 }
 
 fg_status fg_kv_append(const fg_kv* kv, const void* k_new, const void* v_new, int64_t pos,
