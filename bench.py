@@ -262,9 +262,6 @@ def run_ours(args, w, rank, world, device):
     torch.cuda.synchronize()
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    launches_per_step = w.l * 8 + w.n * w.l * 8
-    fg.fg_profile_start(args.steps * launches_per_step + 64)
-    args._prof = True
     n0 = fg.fg_launch_count()
     with ClockSampler(device) as clk:
         t_wall = time.perf_counter()
@@ -273,9 +270,18 @@ def run_ours(args, w, rank, world, device):
         torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall
     n_launch = fg.fg_launch_count() - n0
+    fg.fg_sync_status(st)
+
+    # per-kernel device times: the same K steps again with an event pair
+    # around every library launch (kept out of the timed region above)
+    launches_per_step = w.l * 16 + w.n * w.l * 16
+    fg.fg_profile_start(args.steps * launches_per_step + 64)
+    args._prof = True
+    for k in range(args.steps):
+        step()
+    torch.cuda.synchronize()
     prof = fg.fg_profile_stop()
     args._prof = False
-    fg.fg_sync_status(st)
     pre_ms = [e[0].elapsed_time(e[1]) for e in evs]
     dec_ms = [e[1].elapsed_time(e[2]) for e in evs]
     tot_ms = [e[0].elapsed_time(e[2]) for e in evs]
@@ -354,9 +360,13 @@ def run_ours(args, w, rank, world, device):
         ms = sum(v[1] for v in g_pre.values())
         cnt = sum(v[0] for v in g_pre.values())
         ach = prefill_product_flops(w, w.b, w.s) * w.l * K / (ms / 1e3) / 1e12
-        roof_pre = {"bound": "tensor", "achieved": ach, "peak": pk["tflops_sustained"], "unit": "TFLOP/s",
-                    "frac": ach / pk["tflops_sustained"], "traffic": None, "kernel": "+".join(sorted(g_pre)),
-                    "launches": cnt, "avg_launch_us": ms / cnt * 1e3}
+        # the products alternate with attention inside the prefill, and the SM
+        # clock stays at its maximum there: the burst figure is the fair peak
+        roof_pre = {"bound": "tensor", "achieved": ach, "peak": pk["tflops"], "unit": "TFLOP/s",
+                    "frac": ach / pk["tflops"], "traffic": None, "kernel": "+".join(sorted(g_pre)),
+                    "launches": cnt, "avg_launch_us": ms / cnt * 1e3,
+                    "peak_source": pk["source"] + " burst (fp16 and bf16 share the dense rate)",
+                    "frac_of_sustained": ach / pk["tflops_sustained"]}
     dec_bytes = sum(decode_step_bytes(w, w.b, w.s + t + 1) for t in range(w.n)) * w.l * K * world
     cpu = oracle_decode_sample(w, budget_s=args.cpu_budget) if not args.no_cpu else None
     clocks = clk.summary()

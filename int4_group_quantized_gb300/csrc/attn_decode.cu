@@ -1,0 +1,477 @@
+// Decode attention over the 4-bit KV cache with the new token's K/V appended
+// in the same launch (FlexGen notes, "背景知识": x_K <- Concat(x_K, t w_K),
+// x_V <- Concat(x_V, t w_V), t_Out = Softmax(t_Q x_K^T / sqrt(h1)) x_V;
+// "5. 近似方法": K/V stored in 4-bit groups of 64 along the hidden dimension).
+//
+// The path is HBM-bound (one query per (sequence, head) against ~0.6 bytes
+// per cached value), so the design goal is to convert codes with as few
+// instructions as possible.  Codes never become full fp16 values:
+//   * a lop3 with 0x6400 in the exponent turns a nibble c into the exact
+//     fp16 number 1024 + c (or 1024 + 16c for the upper nibble of a byte);
+//   * the legacy warp-level tensor-core MMA (m16n8k16, fp32 accumulate)
+//     forms the dot products on these biased integers; the bias is removed
+//     once per group: sum_j q_j (1024 + c_j) = sum_j q_j c_j + 1024 sum_j q_j;
+//   * the per-token (min, scale) pair is applied to the group's integer dot
+//     product: k.q = scale * sum_j c_j q_j + min * sum_j q_j, and for the
+//     values sum_t p_t (c_t scale_t + min_t) = sum_t (p_t scale_t) c_t +
+//     sum_t p_t min_t.
+// That is ~0.7 integer instructions per cached element; the MMAs carry the
+// multiply-adds.
+//
+// One CTA (4 warps) per (sequence, head, token split).  Each warp walks its
+// tokens 16 at a time with an online softmax in base 2 (q is pre-scaled by
+// log2(e)/sqrt(d)); warps, then splits, are merged with the usual
+// max/sum rescaling.
+#include <math.h>
+
+#include "codec_dev.cuh"
+#include "fg_internal.cuh"
+
+namespace fg {
+namespace {
+
+struct DecodeArgs {
+  uint8_t* kc;   // codes [b*H][cap][D/2]
+  uint8_t* vc;
+  float* kmin;   // [b*H][cap][D/64]
+  float* kscale;
+  float* vmin;
+  float* vscale;
+  const __half* q;     // row bi at q + bi*ldq, head h at + h*D
+  int64_t ldq;
+  const __half* knew;  // new token's K/V rows (nullptr: nothing to append)
+  const __half* vnew;
+  int64_t ldnew;
+  int64_t pos;         // slot of the new token; attend over 0..pos
+  __half* out;         // [b][ldo]
+  int64_t ldo;
+  float* part;         // splits > 1: [b*H][splits][D + 2]
+  int heads;
+  int64_t cap;
+  int splits;
+  int tps;             // tokens per split (multiple of 16)
+};
+
+__device__ __forceinline__ uint32_t lop_mask_or(uint32_t x, uint32_t mask, uint32_t magic) {
+  uint32_t r;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(x), "r"(mask), "r"(magic));  // (x & mask) | magic
+  return r;
+}
+
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+__device__ __forceinline__ float2 unpack_h2(uint32_t v) {
+  return __half22float2(*reinterpret_cast<const __half2*>(&v));
+}
+
+// Registers holding one 16-token block of the cache as a lane needs it.
+template <int NG>
+struct KVBlock {
+  uint2 kw[2][NG];      // K codes of tokens gq, gq+8 (8 bytes per group)
+  uint32_t vw[4][NG];   // V codes of tokens 2tig, 2tig+1, 2tig+8, 2tig+9 (4 bytes per group)
+  float ksc[2][NG], kmn[2][NG], vsc[2][NG], vmn[2][NG];   // (scale, min) of tokens gq, gq+8
+};
+
+constexpr uint32_t kMagic = 0x64006400u;   // fp16 1024.0 in both halves
+constexpr uint32_t kLoNib = 0x000F000Fu;   // nibble 0 of bytes 0 and 2
+constexpr uint32_t kHiNib = 0x00F000F0u;   // nibble 1 of bytes 0 and 2 (value x16)
+
+template <int D>
+__global__ void __launch_bounds__(128) decode_attn_mma_kernel(const DecodeArgs a) {
+  constexpr int NG = D / 64;   // 64-groups per head row
+  constexpr int NT = D / 16;   // m16 tiles of value dims
+  __shared__ float red_m[4], red_l[4];
+  __shared__ float red_o[4][D];
+
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int gq = lane >> 2, tig = lane & 3;
+  const int bh = blockIdx.x / a.splits, sp = blockIdx.x % a.splits;
+  const int64_t bi = bh / a.heads;
+  const int h = bh % a.heads;
+  const int64_t len = a.pos + 1;
+  const int64_t t0 = static_cast<int64_t>(sp) * a.tps;
+  const int64_t t1 = min(len, t0 + a.tps);
+  const int64_t slot0 = static_cast<int64_t>(bh) * a.cap;
+
+  // ---- Concat: quantize the new token's K and V into slot pos -----------------
+  if (a.knew != nullptr && a.pos >= t0 && a.pos < t1) {
+    if (warp == 0) {
+      const int gi = lane >> 3, part = lane & 7;
+      const bool valid = gi < 2 * NG;
+      const int which = gi / NG, grp = gi % NG;
+      float v[8];
+      if (valid) {
+        const __half* src = (which ? a.vnew : a.knew) + bi * a.ldnew + h * D + grp * 64 + part * 8;
+        const uint4 raw = *reinterpret_cast<const uint4*>(src);
+        const __half2* hh = reinterpret_cast<const __half2*>(&raw);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 f = __half22float2(hh[i]);
+          v[2 * i] = f.x;
+          v[2 * i + 1] = f.y;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = 0.0f;
+      }
+      float mn, sc;
+      const uint32_t packed = codec::quantize_group8(v, mn, sc);
+      if (valid) {
+        const int64_t slot = slot0 + a.pos;
+        *reinterpret_cast<uint32_t*>((which ? a.vc : a.kc) + slot * (D / 2) + grp * 32 + part * 4) = packed;
+        if (part == 0) {
+          (which ? a.vmin : a.kmin)[slot * NG + grp] = mn;
+          (which ? a.vscale : a.kscale)[slot * NG + grp] = sc;
+        }
+      }
+    }
+    __syncthreads();
+  }
+
+  // ---- q as B fragments (replicated across the 8 columns) -------------------
+  // lane (gq, tig) supplies k-indices {2tig, 2tig+1, 2tig+8, 2tig+9} of every
+  // k-step; they stand for its own dims: per group, dims 16*tig .. 16*tig+15,
+  // taken from two 32-bit code words as (0,4),(1,5)x16 | (2,6),(3,7)x16.
+  uint32_t qb[NG][4][2];
+  float bias[NG], qsum[NG];
+  {
+    const float qscale = 1.4426950408889634f / sqrtf(static_cast<float>(D));
+    const __half* qrow = a.q + bi * a.ldq + h * D;
+#pragma unroll
+    for (int g = 0; g < NG; ++g) {
+      float qv[16];
+      const uint4* src = reinterpret_cast<const uint4*>(qrow + g * 64 + 16 * tig);
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const uint4 raw = src[c];
+        const __half2* hh = reinterpret_cast<const __half2*>(&raw);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 f = __half22float2(hh[i]);
+          qv[8 * c + 2 * i] = f.x * qscale;
+          qv[8 * c + 2 * i + 1] = f.y * qscale;
+        }
+      }
+      float bsum = 0.0f, qs = 0.0f;
+#pragma unroll
+      for (int w = 0; w < 2; ++w) {
+        const float* d = qv + 8 * w;
+        qb[g][2 * w][0] = pack_h2(d[0], d[4]);
+        qb[g][2 * w][1] = pack_h2(d[1] * 0.0625f, d[5] * 0.0625f);
+        qb[g][2 * w + 1][0] = pack_h2(d[2], d[6]);
+        qb[g][2 * w + 1][1] = pack_h2(d[3] * 0.0625f, d[7] * 0.0625f);
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+          const float2 x = unpack_h2(qb[g][2 * w + s][0]);
+          const float2 y = unpack_h2(qb[g][2 * w + s][1]);
+          bsum += x.x + x.y + y.x + y.y;
+          qs += x.x + x.y + 16.0f * (y.x + y.y);
+        }
+      }
+      bsum += __shfl_xor_sync(0xffffffffu, bsum, 1);
+      bsum += __shfl_xor_sync(0xffffffffu, bsum, 2);
+      qs += __shfl_xor_sync(0xffffffffu, qs, 1);
+      qs += __shfl_xor_sync(0xffffffffu, qs, 2);
+      bias[g] = 1024.0f * bsum;
+      qsum[g] = qs;
+    }
+  }
+
+  // ---- this warp's tokens -------------------------------------------------------
+  const int nblk = static_cast<int>((t1 - t0 + 15) / 16);
+  const int wb0 = warp * nblk / 4, wb1 = (warp + 1) * nblk / 4;
+  float run_m = -INFINITY, run_l = 0.0f;
+  float ps[NG], cmn[NG];
+  float acc[NT][4];
+#pragma unroll
+  for (int g = 0; g < NG; ++g) ps[g] = cmn[g] = 0.0f;
+#pragma unroll
+  for (int i = 0; i < NT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
+
+  // loads of one 16-token block (issued a block ahead of its use)
+  auto load = [&](int blk, KVBlock<NG>& B) {
+    const int64_t tb = t0 + static_cast<int64_t>(blk) * 16;
+    // K rows of tokens gq and gq+8: per group, 8 bytes at 16*tig dims
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int64_t tok = tb + gq + 8 * r;
+      const int64_t slot = slot0 + tok;
+#pragma unroll
+      for (int g = 0; g < NG; ++g) {
+        if (tok < t1) {
+          B.kw[r][g] = __ldcs(reinterpret_cast<const uint2*>(a.kc + slot * (D / 2) + g * 32 + 8 * tig));
+          B.ksc[r][g] = a.kscale[slot * NG + g];
+          B.kmn[r][g] = a.kmin[slot * NG + g];
+          B.vsc[r][g] = a.vscale[slot * NG + g];
+          B.vmn[r][g] = a.vmin[slot * NG + g];
+        } else {
+          B.kw[r][g] = make_uint2(0u, 0u);
+          B.ksc[r][g] = B.kmn[r][g] = B.vsc[r][g] = B.vmn[r][g] = 0.0f;
+        }
+      }
+    }
+    // V words of tokens 2tig, 2tig+1, 2tig+8, 2tig+9: per group, 4 bytes at 8*gq dims
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int64_t tok = tb + 2 * tig + (r & 1) + 8 * (r >> 1);
+      const int64_t slot = slot0 + tok;
+#pragma unroll
+      for (int g = 0; g < NG; ++g)
+        B.vw[r][g] =
+            tok < t1 ? __ldcs(reinterpret_cast<const unsigned int*>(a.vc + slot * (D / 2) + g * 32 + 4 * gq)) : 0u;
+    }
+  };
+
+  auto process = [&](int blk, const KVBlock<NG>& B) {
+    const int64_t tb = t0 + static_cast<int64_t>(blk) * 16;
+    const bool kval[2] = {tb + gq < t1, tb + gq + 8 < t1};
+    const auto& kw = B.kw;
+    const auto& vw = B.vw;
+    const auto& ksc = B.ksc;
+    const auto& kmn = B.kmn;
+    const auto& vsc = B.vsc;
+    const auto& vmn = B.vmn;
+
+    // scores (base 2) of tokens gq and gq+8
+    float sc0 = 0.0f, sc1 = 0.0f;
+#pragma unroll
+    for (int g = 0; g < NG; ++g) {
+      float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+      for (int w = 0; w < 2; ++w) {
+        const uint32_t x0 = w ? kw[0][g].y : kw[0][g].x;
+        const uint32_t x1 = w ? kw[1][g].y : kw[1][g].x;
+        mma16816(d, lop_mask_or(x0, kLoNib, kMagic), lop_mask_or(x1, kLoNib, kMagic),
+                 lop_mask_or(x0, kHiNib, kMagic), lop_mask_or(x1, kHiNib, kMagic), qb[g][2 * w][0],
+                 qb[g][2 * w][1]);
+        const uint32_t y0 = x0 >> 8, y1 = x1 >> 8;
+        mma16816(d, lop_mask_or(y0, kLoNib, kMagic), lop_mask_or(y1, kLoNib, kMagic),
+                 lop_mask_or(y0, kHiNib, kMagic), lop_mask_or(y1, kHiNib, kMagic), qb[g][2 * w + 1][0],
+                 qb[g][2 * w + 1][1]);
+      }
+      sc0 += ksc[0][g] * (d[0] - bias[g]) + kmn[0][g] * qsum[g];
+      sc1 += ksc[1][g] * (d[2] - bias[g]) + kmn[1][g] * qsum[g];
+    }
+    if (!kval[0]) sc0 = -INFINITY;
+    if (!kval[1]) sc1 = -INFINITY;
+
+    // online softmax over the block
+    float m = fmaxf(sc0, sc1);
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+    const float new_m = fmaxf(run_m, m);
+    const float alpha = exp2f(run_m - new_m);
+    const float p0 = exp2f(sc0 - new_m), p1 = exp2f(sc1 - new_m);
+    float l = p0 + p1;
+    l += __shfl_xor_sync(0xffffffffu, l, 4);
+    l += __shfl_xor_sync(0xffffffffu, l, 8);
+    l += __shfl_xor_sync(0xffffffffu, l, 16);
+    run_l = run_l * alpha + l;
+    run_m = new_m;
+
+    // value weights p*scale per group, as B fragments for tokens
+    // (2tig, 2tig+1 | 2tig+8, 2tig+9), and the min term sum p*min
+    uint32_t vb[NG][2];
+#pragma unroll
+    for (int g = 0; g < NG; ++g) {
+      const float w0 = p0 * vsc[0][g], w1 = p1 * vsc[1][g];
+      const float a0 = __shfl_sync(0xffffffffu, w0, 8 * tig);
+      const float a1 = __shfl_sync(0xffffffffu, w0, 8 * tig + 4);
+      const float a8 = __shfl_sync(0xffffffffu, w1, 8 * tig);
+      const float a9 = __shfl_sync(0xffffffffu, w1, 8 * tig + 4);
+      vb[g][0] = pack_h2(a0, a1);
+      vb[g][1] = pack_h2(a8, a9);
+      const float2 u = unpack_h2(vb[g][0]), v = unpack_h2(vb[g][1]);
+      float s = u.x + u.y + v.x + v.y;   // the fp16 weights the MMA multiplies
+      s += __shfl_xor_sync(0xffffffffu, s, 1);
+      s += __shfl_xor_sync(0xffffffffu, s, 2);
+      ps[g] = ps[g] * alpha + s;
+      float c = p0 * vmn[0][g] + p1 * vmn[1][g];
+      c += __shfl_xor_sync(0xffffffffu, c, 4);
+      c += __shfl_xor_sync(0xffffffffu, c, 8);
+      c += __shfl_xor_sync(0xffffffffu, c, 16);
+      cmn[g] = cmn[g] * alpha + c;
+    }
+
+    // O^T[dim] += sum_t V^T[dim][t] * (p scale)[t]; tile i covers dims
+    // 64*(i/4) + 8*gq + 2*(i%4) (+1 for the upper row, scaled x16)
+#pragma unroll
+    for (int i = 0; i < NT; ++i) {
+      const int g = i / 4, ii = i % 4;
+      acc[i][0] *= alpha;
+      acc[i][1] *= alpha;
+      acc[i][2] *= alpha;
+      acc[i][3] *= alpha;
+      const uint32_t sel = static_cast<uint32_t>(ii) | (static_cast<uint32_t>(ii + 4) << 8);
+      const uint32_t x01 = __byte_perm(vw[0][g], vw[1][g], sel);
+      const uint32_t x89 = __byte_perm(vw[2][g], vw[3][g], sel);
+      mma16816(acc[i], lop_mask_or(x01, kLoNib, kMagic), lop_mask_or(x01, kHiNib, kMagic),
+               lop_mask_or(x89, kLoNib, kMagic), lop_mask_or(x89, kHiNib, kMagic), vb[g][0], vb[g][1]);
+    }
+  };
+
+  // two block buffers: the next block's loads are in flight while this one computes
+  KVBlock<NG> buf0, buf1;
+  if (wb0 < wb1) load(wb0, buf0);
+  for (int blk = wb0; blk < wb1; blk += 2) {
+    if (blk + 1 < wb1) load(blk + 1, buf1);
+    process(blk, buf0);
+    if (blk + 1 >= wb1) break;
+    if (blk + 2 < wb1) load(blk + 2, buf0);
+    process(blk + 1, buf1);
+  }
+
+  // ---- merge the 4 warps --------------------------------------------------------
+  if (tig == 0) {
+#pragma unroll
+    for (int i = 0; i < NT; ++i) {
+      const int g = i / 4, ii = i % 4;
+      const int dim = 64 * g + 8 * gq + 2 * ii;
+      red_o[warp][dim] = (acc[i][0] - 1024.0f * ps[g]) + cmn[g];
+      red_o[warp][dim + 1] = (acc[i][2] - 1024.0f * ps[g]) * 0.0625f + cmn[g];
+    }
+  }
+  if (lane == 0) {
+    red_m[warp] = run_m;
+    red_l[warp] = run_l;
+  }
+  __syncthreads();
+  if (threadIdx.x < D) {
+    const int dim = threadIdx.x;
+    float M = fmaxf(fmaxf(red_m[0], red_m[1]), fmaxf(red_m[2], red_m[3]));
+    float L = 0.0f, O = 0.0f;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const float f = red_m[w] == -INFINITY ? 0.0f : exp2f(red_m[w] - M);
+      L += f * red_l[w];
+      O += f * red_o[w][dim];
+    }
+    if (a.splits == 1) {
+      a.out[bi * a.ldo + h * D + dim] = __float2half_rn(O / L);
+    } else {
+      float* p = a.part + (static_cast<int64_t>(bh) * a.splits + sp) * (D + 2);
+      p[dim] = O;
+      if (dim == 0) {
+        p[D] = M;
+        p[D + 1] = L;
+      }
+    }
+  }
+}
+
+// Merge the token splits of each (sequence, head).
+template <int D>
+__global__ void decode_attn_combine_kernel(const float* __restrict__ part, int splits, int heads,
+                                           __half* __restrict__ out, int64_t ldo) {
+  const int bh = blockIdx.x, dim = threadIdx.x;
+  const float* p = part + static_cast<int64_t>(bh) * splits * (D + 2);
+  float M = -INFINITY;
+  for (int s = 0; s < splits; ++s) M = fmaxf(M, p[s * (D + 2) + D]);
+  float L = 0.0f, O = 0.0f;
+  for (int s = 0; s < splits; ++s) {
+    const float m = p[s * (D + 2) + D];
+    const float f = m == -INFINITY ? 0.0f : exp2f(m - M);
+    L += f * p[s * (D + 2) + D + 1];
+    O += f * p[s * (D + 2) + dim];
+  }
+  out[static_cast<int64_t>(bh / heads) * ldo + (bh % heads) * D + dim] = __float2half_rn(O / L);
+}
+
+// Token splits per (sequence, head): enough CTAs for ~6 per SM, at least 64
+// tokens each.  Depends on the shape only.
+int attn_splits(int64_t bh, int64_t len) {
+  const int64_t target = 148 * 6;
+  int64_t s = (target + bh - 1) / bh;
+  const int64_t by_len = (len + 63) / 64;
+  if (s > by_len) s = by_len;
+  if (s > 32) s = 32;
+  return static_cast<int>(s < 1 ? 1 : s);
+}
+
+template <int D>
+fg_status launch_mma(const fg_kv& kv, const void* q, int64_t ldq, const void* knew, const void* vnew,
+                     int64_t ldnew, int64_t b, int64_t pos, void* out, int64_t ldo, void* ws,
+                     size_t ws_bytes, cudaStream_t st) {
+  DecodeArgs a;
+  a.kc = kv.k_codes;
+  a.vc = kv.v_codes;
+  a.kmin = kv.k_mins;
+  a.kscale = kv.k_scales;
+  a.vmin = kv.v_mins;
+  a.vscale = kv.v_scales;
+  a.q = static_cast<const __half*>(q);
+  a.ldq = ldq;
+  a.knew = static_cast<const __half*>(knew);
+  a.vnew = static_cast<const __half*>(vnew);
+  a.ldnew = ldnew;
+  a.pos = pos;
+  a.out = static_cast<__half*>(out);
+  a.ldo = ldo;
+  a.heads = kv.heads;
+  a.cap = kv.capacity;
+  const int64_t bh = b * kv.heads, len = pos + 1;
+  const int want = attn_splits(bh, len);
+  a.tps = static_cast<int>(((len + want - 1) / want + 15) / 16 * 16);
+  a.splits = static_cast<int>((len + a.tps - 1) / a.tps);
+  a.part = nullptr;
+  if (a.splits > 1) {
+    const size_t need = static_cast<size_t>(bh) * a.splits * (D + 2) * sizeof(float);
+    if (!ws || ws_bytes < need) return fail(FG_ERR_WORKSPACE, "attention split partials need %zu bytes", need);
+    a.part = static_cast<float*>(ws);
+  }
+  {
+    Trace tr(KC_ATTN_DECODE, st);
+    decode_attn_mma_kernel<D><<<static_cast<unsigned>(bh * a.splits), 128, 0, st>>>(a);
+  }
+  {
+    const fg_status s = check_launch("decode_attn_mma_kernel");
+    if (s != FG_OK) return s;
+  }
+  if (a.splits > 1) {
+    Trace tr(KC_ATTN_COMBINE, st);
+    decode_attn_combine_kernel<D><<<static_cast<unsigned>(bh), D, 0, st>>>(a.part, a.splits, kv.heads,
+                                                                           a.out, ldo);
+    return check_launch("decode_attn_combine_kernel");
+  }
+  return FG_OK;
+}
+
+}  // namespace
+
+size_t decode_attention_workspace_bytes(int64_t b, int32_t heads, int32_t head_dim, int64_t capacity) {
+  const int64_t bh = b * heads;
+  const int s = attn_splits(bh, capacity);
+  return s > 1 ? static_cast<size_t>(bh) * s * (head_dim + 2) * sizeof(float) : 0;
+}
+
+fg_status decode_attention(const fg_kv& kv, const void* q, int64_t ldq, const void* knew,
+                           const void* vnew, int64_t ldnew, int64_t b, int64_t pos, void* out,
+                           int64_t ldo, void* ws, size_t ws_bytes, cudaStream_t st) {
+  if (b == 0) return FG_OK;
+  if (kv.codec == FG_CODEC_Q4G64 && kv.dtype == FG_F16) {
+    if (kv.head_dim == 128)
+      return launch_mma<128>(kv, q, ldq, knew, vnew, ldnew, b, pos, out, ldo, ws, ws_bytes, st);
+    if (kv.head_dim == 64)
+      return launch_mma<64>(kv, q, ldq, knew, vnew, ldnew, b, pos, out, ldo, ws, ws_bytes, st);
+  }
+  // fp32 activations or an uncompressed cache: append, then CUDA-core attention
+  if (knew) {
+    fg_status s = kv_store(kv, knew, vnew, ldnew, b, 1, pos, st);
+    if (s != FG_OK) return s;
+  }
+  return decode_attention_simt(kv, q, ldq, b, pos, out, ldo, st);
+}
+
+}  // namespace fg

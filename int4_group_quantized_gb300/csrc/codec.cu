@@ -12,60 +12,13 @@
 // integer keys, which makes the result independent of reduction order and
 // gives -0 < +0.  Each lane writes one 32-bit word of codes (8 nibbles); the
 // first lane of the group writes (min, scale).
+#include "codec_dev.cuh"
 #include "fg_internal.cuh"
 
 namespace fg {
 namespace {
 
-constexpr unsigned kFull = 0xffffffffu;
-
-// Monotone map from non-NaN floats to unsigned keys: a < b (with -0 < +0)
-// iff key(a) < key(b).
-__device__ __forceinline__ uint32_t order_key(float f) {
-  uint32_t u = __float_as_uint(f);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-__device__ __forceinline__ float key_to_float(uint32_t k) {
-  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
-}
-
-// Quantizes the 64-group held by the 8 lanes {8j .. 8j+7} of the warp (lane
-// 8j+p holds elements 8p .. 8p+7 in v).  All 32 lanes must call it.
-__device__ __forceinline__ uint32_t quantize_group8(const float (&v)[8], float& mn_out,
-                                                   float& scale_out) {
-  uint32_t kmin = 0xffffffffu, kmax = 0u;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    if (!isnan(v[i])) {
-      uint32_t k = order_key(v[i]);
-      kmin = min(kmin, k);
-      kmax = max(kmax, k);
-    }
-  }
-#pragma unroll
-  for (int off = 1; off < 8; off <<= 1) {
-    kmin = min(kmin, __shfl_xor_sync(kFull, kmin, off));
-    kmax = max(kmax, __shfl_xor_sync(kFull, kmax, off));
-  }
-  float mn, mx;
-  if (kmin == 0xffffffffu) {  // every member is NaN
-    mn = mx = __uint_as_float(0x7fffffffu);
-  } else {
-    mn = key_to_float(kmin);
-    mx = key_to_float(kmax);
-  }
-  const float r = __fsub_rn(mx, mn);
-  uint32_t packed = 0;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const float u = __fmul_rn(__fdiv_rn(__fsub_rn(v[i], mn), r), 15.0f);
-    const float q = fminf(fmaxf(rintf(u), 0.0f), 15.0f);  // NaN -> 0
-    packed |= static_cast<uint32_t>(q) << (4 * i);
-  }
-  mn_out = mn;
-  scale_out = __fdiv_rn(r, 15.0f);
-  return packed;
-}
+using codec::quantize_group8;
 
 __device__ __forceinline__ void load8(const __half* p, float (&v)[8]) {
   const uint4 raw = *reinterpret_cast<const uint4*>(p);

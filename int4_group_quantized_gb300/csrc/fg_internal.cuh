@@ -86,8 +86,14 @@ fg_status gemm_simt(const GemmArgs& a, cudaStream_t st);
 bool gemm_tc_supported(const GemmArgs& a);
 fg_status gemm_tc(const GemmArgs& a, void* ws, size_t ws_bytes, cudaStream_t st);
 size_t gemm_tc_workspace_bytes(int64_t M, int64_t N, int64_t K, bool q4);
-// Y = epilogue(X . W); chooses the kernel for the shape.  Scratch: `ws`
-// (device, may be null when ws_bytes == 0) for split-K partial sums.
+// Decode product on 4-bit weights for M <= 256 rows (weights as the MMA's
+// M operand; K splits of a tile reduced through distributed shared memory
+// inside a thread-block cluster, so no global scratch).
+bool gemm_q4dec_supported(const GemmArgs& a);
+fg_status gemm_q4dec(const GemmArgs& a, cudaStream_t st);
+
+// Y = epilogue(X . W); chooses the kernel for the shape.  `ws` (ws_bytes >=
+// gemm_workspace_bytes) holds split-K partial sums where a kernel needs them.
 fg_status gemm(const GemmArgs& a, void* ws, size_t ws_bytes, cudaStream_t st);
 size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, fg_dtype dt, int quant);
 
@@ -100,9 +106,12 @@ fg_status kv_store(const fg_kv& kv, const void* ksrc, const void* vsrc, int64_t 
 
 // ---- attention -------------------------------------------------------------
 // Decode: one query per (sequence, head) at slot pos over slots 0..pos.
-// q: [b][ldq] (head h at columns h*d..), out: [b][ldo].
-fg_status decode_attention(const fg_kv& kv, const void* q, int64_t ldq, int64_t b, int64_t pos,
-                           void* out, int64_t ldo, void* ws, size_t ws_bytes, cudaStream_t st);
+// q: [b][ldq] (head h at columns h*d..), out: [b][ldo].  When knew/vnew are
+// given ([b][ldnew] rows), the new token's K/V are first written to slot pos
+// (fused into the attention launch on the tensor-core path).
+fg_status decode_attention(const fg_kv& kv, const void* q, int64_t ldq, const void* knew,
+                           const void* vnew, int64_t ldnew, int64_t b, int64_t pos, void* out,
+                           int64_t ldo, void* ws, size_t ws_bytes, cudaStream_t st);
 size_t decode_attention_workspace_bytes(int64_t b, int32_t heads, int32_t head_dim,
                                         int64_t capacity);
 fg_status decode_attention_simt(const fg_kv& kv, const void* q, int64_t ldq, int64_t b,

@@ -24,6 +24,7 @@
 #include <string.h>
 
 #include "fg_internal.cuh"
+#include "q4_dev.cuh"
 #include "tc_ptx.cuh"
 
 namespace fg {
@@ -32,10 +33,12 @@ namespace {
 using namespace tc;
 
 constexpr int BK = 64;             // k per pipeline stage (one 128-byte swizzle row of fp16)
-constexpr int kThreads = 256;
-constexpr int kDequantWarp0 = 2;   // warps 2..7
-constexpr int kDequantThreads = kThreads - 32 * kDequantWarp0;
-constexpr int kEpiWarp0 = 4;       // warps 4..7
+constexpr int kDenseThreads = 256;
+constexpr int kQ4Threads = 384;
+constexpr int kDequantWarp0 = 4;   // Q4: warps 4..11 dequantize
+constexpr int kDequantThreads = kQ4Threads - 32 * kDequantWarp0;
+constexpr int kEpiWarp0 = 4;       // warps 4..7 drain TMEM
+__host__ __device__ constexpr int cta_threads(bool q4) { return q4 ? kQ4Threads : kDenseThreads; }
 constexpr uint32_t kWaitLimit = 1u << 24;
 
 struct TcParams {
@@ -79,24 +82,10 @@ struct Smem {
 
 __device__ __forceinline__ void raise(const TcParams& p) { atomicOr(p.err, DEV_ERR_WAIT_TIMEOUT); }
 
-// Decode: 8 codes (one 32-bit word, consecutive output channels of one input
-// row and one 64-group) -> 8 fp16 weights fmaf(q, scale, min) rounded to
-// nearest even, packed for one 16-byte store.
-__device__ __forceinline__ uint4 dequant8(uint32_t c, float mn, float sc) {
-  uint4 out;
-  uint32_t* o = reinterpret_cast<uint32_t*>(&out);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float lo = __fmaf_rn(static_cast<float>((c >> (8 * i)) & 15u), sc, mn);
-    const float hi = __fmaf_rn(static_cast<float>((c >> (8 * i + 4)) & 15u), sc, mn);
-    const __half2 h = __floats2half2_rn(lo, hi);
-    o[i] = *reinterpret_cast<const uint32_t*>(&h);
-  }
-  return out;
-}
+using namespace q4;
 
 template <int MT, int BN, bool Q4>
-__global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ TcParams p) {
+__global__ void __launch_bounds__(cta_threads(Q4), 1) gemm_tc_kernel(const __grid_constant__ TcParams p) {
   using S = Smem<MT, BN, Q4>;
   constexpr int STAGES = S::kStages;
   constexpr uint32_t kTmemCols = MT * BN;   // 128, 256 or 512
@@ -229,7 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
       mma_commit(done);
       if (!ok) raise(p);
     }
-  } else if (Q4) {
+  } else if (Q4 && warp >= kDequantWarp0) {
     // ---- dequantization warps ---------------------------------------------------
     const int t = threadIdx.x - 32 * kDequantWarp0;
     bool ok = true;
@@ -240,21 +229,29 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
            mbar_wait(&bempty[j], ((i / S::kNB) & 1) ^ 1, kWaitLimit, abort_flag);
       if (!ok) break;
       const uint8_t* st = stage_base + s * S::kStage;
-      const uint32_t* codes = reinterpret_cast<const uint32_t*>(st + S::kA);
+      const uint2* codes = reinterpret_cast<const uint2*>(st + S::kA);
       const float* mins = reinterpret_cast<const float*>(st + S::kA + S::kCodes);
       const float* scales = mins + BK * 4;
       const int g0 = (nl & 255) >> 6;   // first group of this tile inside the 256-column meta tile
       uint8_t* b = bbuf_base + j * S::kB;
-      constexpr int kUnits = BK * BN / 8;
-      for (int u = t; u < kUnits; u += kDequantThreads) {
-        const int k = u / (BN / 8);
-        const int c8 = u % (BN / 8);
-        const int n = c8 * 8;
-        const float mn = mins[k * 4 + g0 + n / 64];
-        const float sc = scales[k * 4 + g0 + n / 64];
-        const uint4 v = dequant8(codes[k * (BN / 8) + c8], mn, sc);
+      // unit = 16 consecutive channels of one input row (one 64-bit code
+      // word, one (min, scale) pair) -> two swizzled 16-byte chunks
+      constexpr int kUnits = BK * BN / 16;
+      static_assert(kUnits % kDequantThreads == 0, "units split evenly over the dequant threads");
+#pragma unroll
+      for (int it = 0; it < kUnits / kDequantThreads; ++it) {
+        const int u = t + it * kDequantThreads;
+        const int k = u / (BN / 16);
+        const int n = (u % (BN / 16)) * 16;
+        const int gi = k * 4 + g0 + n / 64;
+        const uint32_t s2 = bcast_h2(scales[gi]), m2 = bcast_h2(mins[gi]);
+        const uint2 c = codes[k * (BN / 16) + n / 16];
+        const uint4 v0 = dequant8(c.x, s2, m2);
+        const uint4 v1 = dequant8(c.y, s2, m2);
         const int chunk = (n & 63) >> 3;
-        *reinterpret_cast<uint4*>(b + (n >> 6) * (BK * 128) + k * 128 + ((chunk ^ (k & 7)) << 4)) = v;
+        uint8_t* row = b + (n >> 6) * (BK * 128) + k * 128;
+        *reinterpret_cast<uint4*>(row + ((chunk ^ (k & 7)) << 4)) = v0;
+        *reinterpret_cast<uint4*>(row + (((chunk + 1) ^ (k & 7)) << 4)) = v1;
       }
       fence_proxy_async_smem();
       mbar_arrive(&bfull[j]);
@@ -276,6 +273,23 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
           tmem_ld_wait();
           if (m >= p.M) continue;
           const int n = n0 + c0;
+          if (Q4) {
+            // accumulator column order inside each 8-chunk is channel
+            // (0,4,1,5,2,6,3,7): put it back
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              const uint32_t c[8] = {r[8 * v], r[8 * v + 1], r[8 * v + 2], r[8 * v + 3],
+                                     r[8 * v + 4], r[8 * v + 5], r[8 * v + 6], r[8 * v + 7]};
+              r[8 * v + 0] = c[0];
+              r[8 * v + 1] = c[2];
+              r[8 * v + 2] = c[4];
+              r[8 * v + 3] = c[6];
+              r[8 * v + 4] = c[1];
+              r[8 * v + 5] = c[3];
+              r[8 * v + 6] = c[5];
+              r[8 * v + 7] = c[7];
+            }
+          }
           if (p.splits > 1) {
             float4* dst = reinterpret_cast<float4*>(p.partial + (static_cast<size_t>(split) * p.M + m) * p.N + n);
 #pragma unroll
@@ -410,11 +424,16 @@ fg_status launch(TcParams& p, cudaStream_t st) {
   }
   const int grid = p.m_tiles * p.n_tiles * p.splits;
   Trace tr(KC_GEMM_TC, st);
-  gemm_tc_kernel<MT, BN, Q4><<<grid, kThreads, S::kTotal, st>>>(p);
+  gemm_tc_kernel<MT, BN, Q4><<<grid, cta_threads(Q4), S::kTotal, st>>>(p);
   return check_launch("gemm_tc_kernel");
 }
 
 }  // namespace
+
+bool tc_make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+                 uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
+  return make_map(m, dt, base, inner, outer, row_bytes, box_inner, box_outer, sw);
+}
 
 // Column tile of the tensor-core path, and the split-K factor it uses for a
 // product (fixed by the shape only, so workspace sizes do not depend on the

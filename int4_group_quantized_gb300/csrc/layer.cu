@@ -215,11 +215,11 @@ fg_status run_decode(const fg_layer& L, const void* t, int64_t b, int64_t pos, c
   const fg_wmat qkv[3] = {L.wq, L.wk, L.wv};
   // t_Q, t w_K, t w_V: every weight read once for the whole block
   FG_TRY(gemm(product(L, t, h1, b, qkv, 3, B.qkv, 3 * h1, nullptr, 0, 0), B.scratch, scratch, st));
-  // Concat: append t w_K, t w_V at slot pos
+  // Concat (t w_K, t w_V into slot pos), then Softmax(t_Q x_K^T / sqrt(d)) x_V
+  // over slots 0..pos
   const size_t e = dtype_bytes(L.dtype);
-  FG_TRY(kv_store(kv, B.qkv + h1 * e, B.qkv + 2 * h1 * e, 3 * h1, b, 1, pos, st));
-  // Softmax(t_Q x_K^T / sqrt(d)) x_V over slots 0..pos
-  FG_TRY(decode_attention(kv, B.qkv, 3 * h1, b, pos, B.att, h1, B.scratch, scratch, st));
+  FG_TRY(decode_attention(kv, B.qkv, 3 * h1, B.qkv + h1 * e, B.qkv + 2 * h1 * e, 3 * h1, b, pos,
+                          B.att, h1, B.scratch, scratch, st));
   FG_TRY(gemm(product(L, B.att, h1, b, &L.wo, 1, B.xo, h1, t, h1, 0), B.scratch, scratch, st));
   FG_TRY(gemm(product(L, B.xo, h1, b, &L.w1, 1, B.hid, h2, nullptr, 0, 1), B.scratch, scratch, st));
   FG_TRY(gemm(product(L, B.hid, h2, b, &L.w2, 1, y, h1, B.xo, h1, 0), B.scratch, scratch, st));
@@ -234,31 +234,14 @@ fg_status check_act(const void* p, const char* name) {
 
 }  // namespace
 
-// The decode attention with its workspace (split over tokens when the block
-// has too few (sequence, head) pairs to fill the GPU).
-fg_status decode_attention(const fg_kv& kv, const void* q, int64_t ldq, int64_t b, int64_t pos,
-                           void* out, int64_t ldo, void* ws, size_t ws_bytes, cudaStream_t st) {
-  (void)ws;
-  (void)ws_bytes;
-  return decode_attention_simt(kv, q, ldq, b, pos, out, ldo, st);
-}
-
-size_t decode_attention_workspace_bytes(int64_t b, int32_t heads, int32_t head_dim,
-                                        int64_t capacity) {
-  (void)b;
-  (void)heads;
-  (void)head_dim;
-  (void)capacity;
-  return 0;
-}
-
 fg_status gemm(const GemmArgs& a, void* ws, size_t ws_bytes, cudaStream_t st) {
+  if (gemm_q4dec_supported(a)) return gemm_q4dec(a, st);
   if (gemm_tc_supported(a)) return gemm_tc(a, ws, ws_bytes, st);
   return gemm_simt(a, st);
 }
 
 size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, fg_dtype dt, int quant) {
-  if (dt != FG_F16 || M < 64) return 0;
+  if (dt != FG_F16 || M < 64 || (quant && M <= 256)) return 0;
   return gemm_tc_workspace_bytes(M, N, K, quant != 0);
 }
 
@@ -309,6 +292,7 @@ fg_status fg_linear(const fg_wmat* w, fg_codec codec, fg_dtype dtype, const void
   if (r == y || x == y) return fail(FG_ERR_ARG, "y must not alias x or r");
   const size_t need = fg_linear_workspace_bytes(M, w->K, w->N, codec, dtype);
   if (need && (!ws || ws_bytes < need)) return fail(FG_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes, need);
+  if (!aligned(ws, kAlign)) return fail(FG_ERR_ALIGN, "workspace needs 256-byte alignment");
   fg_layer L{};
   L.codec = codec;
   L.dtype = dtype;
@@ -405,8 +389,8 @@ fg_status fg_decode_block_step(const fg_layer* layers, int32_t l, const void* t,
   if (!layers || !kvs || l <= 0) return fail(FG_ERR_ARG, "layers/kvs/l");
   for (int32_t i = 0; i < l; ++i) {
     FG_TRY(check_layer(&layers[i]));
-    if (layers[i].h1 != layers[0].h1 || layers[i].dtype != layers[0].dtype)
-      return fail(FG_ERR_SHAPE, "layers differ in h1/dtype");
+    if (layers[i].h1 != layers[0].h1 || layers[i].h2 != layers[0].h2 || layers[i].dtype != layers[0].dtype)
+      return fail(FG_ERR_SHAPE, "layers differ in h1/h2/dtype");
     FG_TRY(check_kv(&kvs[i], b, layers[i].heads, layers[i].h1 / layers[i].heads, layers[i].codec,
                     layers[i].dtype));
     if (pos < 0 || pos >= kvs[i].capacity)
