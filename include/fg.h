@@ -153,6 +153,19 @@ fg_status fg_linear(const fg_wmat* w, fg_codec codec, fg_dtype dtype, const void
                     const void* r, int32_t relu, void* y, void* ws, size_t ws_bytes,
                     cudaStream_t stream);
 
+/* [BG] decode attention alone: for every sequence and head,
+ * Softmax(q K^T / sqrt(head_dim)) V over cache slots 0..pos of kv (nothing
+ * is appended), K/V read through the codec.  q: device [kv->b][ldq] with
+ * head h at columns h*head_dim (dtype kv->dtype); out: device [kv->b][ldo],
+ * same layout.  ldq and ldo are multiples of 8 and at least h1.  The cache
+ * is split over tokens when there are too few (sequence, head) pairs to fill
+ * the GPU; the split partials use ws (device, ws_bytes >=
+ * fg_decode_attention_workspace_bytes(kv), 0 when no split is needed).
+ * pos outside [0, capacity) -> FG_ERR_CAPACITY. */
+size_t fg_decode_attention_workspace_bytes(const fg_kv* kv);
+fg_status fg_decode_attention(const fg_kv* kv, const void* q, int64_t ldq, int64_t pos, void* out,
+                              int64_t ldo, void* ws, size_t ws_bytes, cudaStream_t stream);
+
 /* Workspace (device bytes) that fg_prefill_layer / fg_prefill_block need for
  * b sequences of s tokens, and that fg_decode_step / fg_decode_block_step
  * need for b sequences with a cache of `capacity` slots.  Pure host

@@ -375,3 +375,23 @@ def fg_linear(w: QuantWeight, x: torch.Tensor, y: torch.Tensor, r: torch.Tensor 
     _check(_lib.fg_linear(ctypes.byref(s), FG_CODEC_Q4G64 if quant else FG_CODEC_NONE, _dt(x), _ptr(x), M, _ptr(r),
                           1 if relu else 0, _ptr(y), _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)),
            "fg_linear")
+
+
+_sig("fg_decode_attention_workspace_bytes", _SZ, ctypes.POINTER(fg_kv))
+_sig("fg_decode_attention", _INT, ctypes.POINTER(fg_kv), _P, _I64, _I64, _P, _I64, _P, _SZ, _P)
+
+
+def fg_decode_attention_workspace_bytes(kv: KVCache) -> int:
+    return _lib.fg_decode_attention_workspace_bytes(ctypes.byref(kv.struct))
+
+
+def fg_decode_attention(kv: KVCache, q: torch.Tensor, pos: int, out: torch.Tensor, ws: torch.Tensor | None = None,
+                        stream=None) -> None:
+    """out[b][h*d:(h+1)*d] = softmax(q_h K_h^T / sqrt(d)) V_h over cache slots 0..pos."""
+    if ws is None:
+        need = fg_decode_attention_workspace_bytes(kv)
+        ws = workspace(need, q.device) if need else None
+    _check(_lib.fg_decode_attention(ctypes.byref(kv.struct), _ptr(q), q.stride(0), int(pos), _ptr(out), out.stride(0),
+                                    _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)),
+           "fg_decode_attention")
+

@@ -300,6 +300,32 @@ fg_status fg_linear(const fg_wmat* w, fg_codec codec, fg_dtype dtype, const void
   return gemm(a, ws, ws_bytes, stream);
 }
 
+size_t fg_decode_attention_workspace_bytes(const fg_kv* kv) {
+  if (!kv || kv->b < 0 || kv->heads <= 0 || kv->head_dim <= 0 || kv->capacity <= 0) return 0;
+  if (kv->codec != FG_CODEC_Q4G64 || kv->dtype != FG_F16) return 0;
+  return decode_attention_workspace_bytes(kv->b, kv->heads, kv->head_dim, kv->capacity);
+}
+
+fg_status fg_decode_attention(const fg_kv* kv, const void* q, int64_t ldq, int64_t pos, void* out,
+                              int64_t ldo, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (!kv) return fail(FG_ERR_ARG, "null kv");
+  if (kv->heads <= 0 || kv->head_dim <= 0 || kv->b < 0) return fail(FG_ERR_ARG, "kv sizes");
+  if (kv->head_dim != 64 && kv->head_dim != 128)
+    return fail(FG_ERR_UNSUPPORTED, "head_dim %d (64 or 128)", kv->head_dim);
+  FG_TRY(check_kv(kv, kv->b, kv->heads, kv->head_dim, kv->codec, kv->dtype));
+  if (pos < 0 || pos >= kv->capacity)
+    return fail(FG_ERR_CAPACITY, "pos %lld outside [0, %lld)", (long long)pos, (long long)kv->capacity);
+  const int64_t h1 = static_cast<int64_t>(kv->heads) * kv->head_dim;
+  if (ldq < h1 || ldo < h1 || ldq % 8 || ldo % 8) return fail(FG_ERR_SHAPE, "ldq/ldo must be >= h1 and multiples of 8");
+  if (kv->b == 0) return FG_OK;
+  FG_TRY(check_act(q, "q"));
+  FG_TRY(check_act(out, "out"));
+  const size_t need = fg_decode_attention_workspace_bytes(kv);
+  if (need && (!ws || ws_bytes < need)) return fail(FG_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes, need);
+  if (need && !aligned(ws, 16)) return fail(FG_ERR_ALIGN, "workspace needs 16-byte alignment");
+  return decode_attention(*kv, q, ldq, nullptr, nullptr, 0, kv->b, pos, out, ldo, ws, ws_bytes, stream);
+}
+
 fg_status fg_kv_append(const fg_kv* kv, const void* k_new, const void* v_new, int64_t pos,
                        cudaStream_t stream) {
   if (!kv) return fail(FG_ERR_ARG, "null kv");
