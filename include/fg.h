@@ -166,6 +166,24 @@ size_t fg_decode_attention_workspace_bytes(const fg_kv* kv);
 fg_status fg_decode_attention(const fg_kv* kv, const void* q, int64_t ldq, int64_t pos, void* out,
                               int64_t ldo, void* ws, size_t ws_bytes, cudaStream_t stream);
 
+/* fg_decode_attention for callers that cannot allocate device memory: code
+ * embedded in a host application that owns the GPU memory pool and forbids
+ * other allocations, or a latency-critical loop that cannot afford the
+ * device-wide synchronization a cudaMalloc/cudaFree may imply.  (The FlexGen
+ * notes have no counterpart; this is an interface convenience.)
+ * Same arguments and results as fg_decode_attention, without a workspace:
+ * the split partials go to a 1 MiB array built into libfg.so, which every
+ * GPU that loads the library holds until the process exits.  Caches whose
+ * fg_decode_attention_workspace_bytes exceeds 1 MiB are rejected with
+ * FG_ERR_WORKSPACE (the split rule needs at most ~0.9 MB, so none is
+ * today).  The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture.  Calls share the array, so calls whose kernels
+ * overlap on the GPU (concurrent streams) race; nothing in the array needs
+ * to start at zero.  Allocates nothing, on the device or the host. */
+fg_status fg_decode_attention_noalloc(const fg_kv* kv, const void* q, int64_t ldq, int64_t pos,
+                                      void* out, int64_t ldo, cudaStream_t stream);
+
 /* Workspace (device bytes) that fg_prefill_layer / fg_prefill_block need for
  * b sequences of s tokens, and that fg_decode_step / fg_decode_block_step
  * need for b sequences with a cache of `capacity` slots.  Pure host

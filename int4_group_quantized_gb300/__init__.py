@@ -395,3 +395,15 @@ def fg_decode_attention(kv: KVCache, q: torch.Tensor, pos: int, out: torch.Tenso
                                     _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)),
            "fg_decode_attention")
 
+
+_sig("fg_decode_attention_noalloc", _INT, ctypes.POINTER(fg_kv), _P, _I64, _I64, _P, _I64, _P)
+
+
+def fg_decode_attention_noalloc(kv: KVCache, q: torch.Tensor, pos: int, out: torch.Tensor, stream=None) -> None:
+    """fg_decode_attention without a workspace, for callers that cannot
+    allocate device memory: the split partials use a fixed array inside
+    libfg.so (shared by all calls; overlapping calls race)."""
+    _check(_lib.fg_decode_attention_noalloc(ctypes.byref(kv.struct), _ptr(q), q.stride(0), int(pos), _ptr(out),
+                                            out.stride(0), _stream(stream)),
+           "fg_decode_attention_noalloc")
+

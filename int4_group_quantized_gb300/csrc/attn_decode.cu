@@ -475,3 +475,53 @@ fg_status decode_attention(const fg_kv& kv, const void* q, int64_t ldq, const vo
 }
 
 }  // namespace fg
+
+// ---------------------------------------------------------------------------
+// Decode attention for callers that cannot allocate device memory.
+//
+// The split-over-tokens partial results normally live in a workspace the
+// caller allocates.  This entry point uses instead a fixed array compiled
+// into the library, which every GPU that loads libfg.so holds until the
+// process exits.  Its device address is looked up once per device (with
+// that device current) by the first call on that device; make that first
+// call before any stream capture.  Every call shares the array: calls whose
+// kernels overlap on the GPU race on it.  Nothing in it needs to start at
+// zero (each split writes its partial before the merge reads it).
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+// The split rule above asks for at most ~0.9 MB (b*H*splits*(d+2)*4 bytes,
+// largest near b*H = 888/2 with head_dim 128), so 1 MiB covers every cache.
+static constexpr size_t kNoAllocScratchBytes = size_t(1) << 20;   // 1 MiB
+static __device__ __align__(256) unsigned char g_decode_attn_scratch[kNoAllocScratchBytes];
+
+static fg_status noalloc_scratch(void** ptr) {
+  static std::mutex mu;
+  static void* cache[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return fg::fail(FG_ERR_CUDA, "cudaGetDevice");
+  std::lock_guard<std::mutex> lk(mu);
+  if (cache[dev] == nullptr) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_decode_attn_scratch);
+    if (e != cudaSuccess) return fg::fail(FG_ERR_CUDA, "cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+    cache[dev] = p;
+  }
+  *ptr = cache[dev];
+  return FG_OK;
+}
+
+extern "C" fg_status fg_decode_attention_noalloc(const fg_kv* kv, const void* q, int64_t ldq, int64_t pos,
+                                                 void* out, int64_t ldo, cudaStream_t stream) {
+  if (!kv) return fg::fail(FG_ERR_ARG, "null kv");
+  const size_t need = fg_decode_attention_workspace_bytes(kv);
+  if (need > kNoAllocScratchBytes)
+    return fg::fail(FG_ERR_WORKSPACE,
+                    "this cache needs %zu bytes of split scratch; the built-in array holds %zu "
+                    "(use fg_decode_attention with a caller workspace)",
+                    need, kNoAllocScratchBytes);
+  void* scratch = nullptr;
+  const fg_status s = noalloc_scratch(&scratch);
+  if (s != FG_OK) return s;
+  return fg_decode_attention(kv, q, ldq, pos, out, ldo, scratch, kNoAllocScratchBytes, stream);
+}
