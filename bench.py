@@ -399,6 +399,88 @@ def run_ours(args, w, rank, world, device):
     print(json.dumps(line), flush=True)
 
 
+CASES = ("linear-qkv", "linear-o", "linear-fc1", "linear-fc2", "prefill-linear-fc1", "attn-decode",
+         "prefill-layer")
+
+
+def run_case(args, w, device):
+    """One kernel class at the workload's shapes, with a small device
+    footprint (one layer): the command the ncu summaries under profiles/ are
+    taken with.  Enough weight copies (or caches) rotate that the inputs of
+    consecutive calls exceed L2; the calls are captured once in a CUDA graph
+    and the graph is replayed `--steps` times after `--warmup` replays, so the
+    printed time per call is device time without host launch overhead."""
+    import int4_group_quantized_gb300 as fg
+    torch.cuda.set_device(device)
+    dev = torch.device("cuda", device)
+    dt = synth.torch_dtype(w.act)
+    name = args.case
+    l2 = 3 * 129 * 2 ** 20
+    if name.startswith("linear") or name.startswith("prefill-linear"):
+        mat = {"qkv": "wq", "o": "wo", "fc1": "w1", "fc2": "w2"}[name.split("-")[-1]]
+        K, N = synth.weight_shape(w, mat)
+        if mat == "wq":
+            N *= 3
+        prefill = name.startswith("prefill")
+        M = min(w.b * w.s, 8192) if prefill else w.b      # a few GB at most on the device
+        per = K * N * (2 if prefill else 0.5625)
+        copies = 1 if prefill else max(2, min(32, int(-(-l2 // per))))
+        Ws = []
+        for c in range(copies):
+            w16 = synth.normal((K, N), 7 + c, synth.WEIGHT_STD, dt, dev)
+            Ws.append(fg.QuantWeight.from_dense(w16, not prefill))
+            del w16
+        x = synth.normal((M, K), 8, 1.0, dt, dev)
+        y = torch.empty((M, N), dtype=dt, device=dev)
+        ws = fg.workspace(max(fg.fg_linear_workspace_bytes(M, K, N, not prefill, dt), 1), dev)
+        calls = [lambda W=W: fg.fg_linear(W, x, y, ws=ws) for W in Ws]
+        shape = {"M": M, "K": K, "N": N, "copies": copies}
+    else:
+        L = fg.Layer.from_dense(synth.layer_weights(w, 0, dev), w.heads, True)
+        x = synth.prompt(w, device=dev)
+        y = torch.empty_like(x)
+        ws = fg.workspace(max(fg.fg_prefill_workspace_bytes(L, w.b, w.s),
+                              fg.fg_decode_workspace_bytes(L, w.b, w.s + w.n)), dev)
+        if name == "attn-decode":
+            kv_bytes = 2 * w.b * w.h1 * (w.s + w.n) * 0.625
+            kvs = [fg.KVCache(w.b, w.heads, w.head_dim, w.s + w.n, True, dt, dev)
+                   for _ in range(max(2, int(-(-l2 // kv_bytes))))]
+            for kv in kvs:
+                fg.fg_prefill_layer(L, x, kv, y, ws)       # fills slots 0..s-1
+            q = synth.normal((w.b, w.h1), 9, 1.0, dt, dev)
+            out = torch.empty_like(q)
+            pos = w.s + w.n // 2
+            calls = [lambda kv=kv: fg.fg_decode_attention(kv, q, pos, out) for kv in kvs]
+        else:
+            kv = fg.KVCache(w.b, w.heads, w.head_dim, w.s + w.n, True, dt, dev)
+            calls = [lambda: fg.fg_prefill_layer(L, x, kv, y, ws)]
+        shape = {"b": w.b, "s": w.s, "h1": w.h1, "heads": w.heads, "copies": len(calls)}
+    reps = max(1, 16 // len(calls)) * len(calls) if len(calls) < 16 else len(calls)
+    side = torch.cuda.Stream(device=dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        for k in range(reps):
+            calls[k % len(calls)]()
+        torch.cuda.synchronize()
+        graph.capture_begin()
+        for k in range(reps):
+            calls[k % len(calls)]()
+        graph.capture_end()
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        graph.replay()
+    e1.record()
+    e1.synchronize()
+    fg.fg_sync_status()
+    print(json.dumps({"case": name, "workload": w.name, "shape": shape, "calls_per_replay": reps,
+                      "us_per_call": e0.elapsed_time(e1) / (args.steps * reps) * 1e3}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -408,6 +490,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle timing")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--case", choices=CASES, default=None,
+                    help="time one kernel class at the workload's shapes (for profilers)")
     args = ap.parse_args()
     w = synth.WORKLOADS[args.config]
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -415,6 +499,9 @@ def main():
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         run_reference(args, w, rank, world)
+        return
+    if args.case:
+        run_case(args, w, local)
         return
     if world > 1:
         torch.cuda.set_device(local)

@@ -69,13 +69,16 @@ typedef enum { FG_CODEC_NONE = 0, FG_CODEC_Q4G64 = 1 } fg_codec; /* storage     
  * features, N = output features.  With FG_CODEC_Q4G64: codes [K][N/2],
  * mins and scales [K][N/64] -- each group is 64 consecutive output channels
  * at one input index ([S5]: "along the output-channel dimension").  With
- * FG_CODEC_NONE: dense [K][N] in the layer's activation dtype.  Device. */
+ * FG_CODEC_NONE: dense [K][N] in the layer's activation dtype.  Device.
+ * packed (optional, may be NULL): the decode copy written by fg_pack_weight;
+ * fp16 products of up to 256 rows read it instead of codes/mins/scales. */
 typedef struct {
   const uint8_t* codes;
   const float* mins;
   const float* scales;
   const void* dense;
   int64_t K, N;
+  const uint8_t* packed;
 } fg_wmat;
 
 /* One transformer layer ([BG]): w_Q, w_K, w_V, w_O in R^{h1 x h1},
@@ -152,6 +155,26 @@ size_t fg_linear_workspace_bytes(int64_t M, int64_t K, int64_t N, fg_codec codec
 fg_status fg_linear(const fg_wmat* w, fg_codec codec, fg_dtype dtype, const void* x, int64_t M,
                     const void* r, int32_t relu, void* y, void* ws, size_t ws_bytes,
                     cudaStream_t stream);
+
+/* The decode copy of a Q4G64 weight ([S5] storage; [BG] x . w with one
+ * weight read for the whole block), fg_pack_weight_bytes(K, N) = K*N/2 +
+ * K*N/16 bytes: one 4608-byte block per (128-channel tile t, 64-k tile u),
+ * block (t, u) at byte offset (t * K/64 + u) * 4608, so the k tiles of a
+ * channel tile are one contiguous run:
+ *   bytes 0..4095: codes; channel r of the tile in bytes r*32 .. r*32+31,
+ *     its two 16-byte halves (k 0..31 of the tile, k 32..63) stored swapped
+ *     when bit 2 of r is set; within each 32-bit word (8 consecutive k) the
+ *     nibbles from the low end hold k0 k2 k4 k6 k1 k3 k5 k7, so one mask
+ *     turns a word into fp16 pairs of consecutive k;
+ *   bytes 4096..4607: for the tile's two 64-channel groups (lower first) and
+ *     j = 0..31, fp16x2 (scale[2j], scale[2j+1]) then fp16x2 (min[2j],
+ *     min[2j+1]) of the tile's k, each rounded to nearest -- the precision
+ *     the decode products apply them in.
+ * packed: device, 16-byte aligned, owned by the caller, then stored in
+ * w->packed.  K a multiple of 64 and N of 128, else FG_ERR_SHAPE; null
+ * arrays -> FG_ERR_ARG.  Asynchronous on `stream`. */
+size_t fg_pack_weight_bytes(int64_t K, int64_t N);
+fg_status fg_pack_weight(const fg_wmat* w, uint8_t* packed, cudaStream_t stream);
 
 /* [BG] decode attention alone: for every sequence and head,
  * Softmax(q K^T / sqrt(head_dim)) V over cache slots 0..pos of kv (nothing

@@ -43,7 +43,8 @@ class FGError(RuntimeError):
 
 class fg_wmat(ctypes.Structure):
     _fields_ = [("codes", ctypes.c_void_p), ("mins", ctypes.c_void_p), ("scales", ctypes.c_void_p),
-                ("dense", ctypes.c_void_p), ("K", ctypes.c_int64), ("N", ctypes.c_int64)]
+                ("dense", ctypes.c_void_p), ("K", ctypes.c_int64), ("N", ctypes.c_int64),
+                ("packed", ctypes.c_void_p)]
 
 
 class fg_layer(ctypes.Structure):
@@ -102,6 +103,8 @@ _sig("fg_profile_phase", _INT, ctypes.c_int32)
 _sig("fg_profile_query", _INT, ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(ctypes.c_int64),
      ctypes.POINTER(ctypes.c_double))
 _sig("fg_launch_count", ctypes.c_uint64)
+_sig("fg_pack_weight_bytes", _SZ, _I64, _I64)
+_sig("fg_pack_weight", _INT, ctypes.POINTER(fg_wmat), _P, _P)
 
 lib = _lib
 
@@ -169,25 +172,51 @@ class QuantWeight:
     """w in R^{K x N} (x . w) as stored: Q4G64 (codes/mins/scales, grouped
     along N = the output channel) or dense."""
 
-    def __init__(self, K, N, codes=None, mins=None, scales=None, dense=None):
+    def __init__(self, K, N, codes=None, mins=None, scales=None, dense=None, packed=None):
         self.K, self.N = int(K), int(N)
         self.codes, self.mins, self.scales, self.dense = codes, mins, scales, dense
+        self.packed = packed
 
     @staticmethod
-    def from_dense(w: torch.Tensor, quantize_it: bool = True, stream=None) -> "QuantWeight":
+    def from_dense(w: torch.Tensor, quantize_it: bool = True, stream=None, pack: bool | None = None) -> "QuantWeight":
+        """pack (default: fp16 weights with N a multiple of 128) adds the
+        decode copy the decode products read (fg_pack_weight)."""
         K, N = w.shape
         if not quantize_it:
             return QuantWeight(K, N, dense=w.contiguous())
         codes, mins, scales = quantize(w.contiguous(), stream)
-        return QuantWeight(K, N, codes, mins, scales)
+        q = QuantWeight(K, N, codes, mins, scales)
+        if pack if pack is not None else (w.dtype == torch.float16 and N % 128 == 0):
+            q.pack(stream)
+        return q
+
+    def pack(self, stream=None) -> "QuantWeight":
+        self.packed = torch.empty(fg_pack_weight_bytes(self.K, self.N), dtype=torch.uint8,
+                                  device=self.codes.device)
+        fg_pack_weight(self, self.packed, stream)
+        return self
 
     def struct(self) -> fg_wmat:
         return fg_wmat(_ptr(self.codes), _ptr(self.mins), _ptr(self.scales), _ptr(self.dense), self.K,
-                       self.N)
+                       self.N, _ptr(self.packed))
 
     def nbytes(self) -> int:
+        """Bytes of the stored format (the packed copy is counted apart: packed_nbytes)."""
         ts = [self.codes, self.mins, self.scales, self.dense]
         return sum(t.numel() * t.element_size() for t in ts if t is not None)
+
+    def packed_nbytes(self) -> int:
+        return 0 if self.packed is None else self.packed.numel()
+
+
+def fg_pack_weight_bytes(K: int, N: int) -> int:
+    return int(_lib.fg_pack_weight_bytes(K, N))
+
+
+def fg_pack_weight(w: "QuantWeight", packed: torch.Tensor, stream=None) -> None:
+    s = w.struct()
+    s.packed = None
+    _check(_lib.fg_pack_weight(ctypes.byref(s), _ptr(packed), _stream(stream)), "fg_pack_weight")
 
 
 class Layer:

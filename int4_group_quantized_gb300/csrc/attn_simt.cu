@@ -294,8 +294,8 @@ fg_status decode_attention_simt(const fg_kv& kv, const void* q, int64_t ldq, int
   return check_launch("decode_attn_simt_kernel");
 }
 
-fg_status prefill_attention(const fg_kv& kv, const void* q, int64_t ldq, int64_t b, int64_t s,
-                            void* out, int64_t ldo, cudaStream_t st) {
+fg_status prefill_attention_simt(const fg_kv& kv, const void* q, int64_t ldq, int64_t b, int64_t s,
+                                 void* out, int64_t ldo, cudaStream_t st) {
   if (b == 0 || s == 0) return FG_OK;
   const bool qz = kv.codec == FG_CODEC_Q4G64;
   const bool h = kv.dtype == FG_F16;

@@ -59,7 +59,8 @@ unsigned int* device_error_word() {
 namespace {
 const char* const kClassNames[KC_COUNT] = {
     "quantize_g64", "dequant_g64", "kv_store_q4", "gemm_simt", "gemm_tc_q4",
-    "gemm_splitk_reduce", "attn_decode", "attn_decode_combine", "attn_prefill"};
+    "gemm_splitk_reduce", "attn_decode", "attn_decode_combine", "attn_prefill", "gemm_q4_decode",
+    "pack_weight"};
 
 struct Profiler {
   std::mutex mu;

@@ -38,6 +38,8 @@ enum KernelClass : int {
   KC_ATTN_DECODE,
   KC_ATTN_COMBINE,
   KC_ATTN_PREFILL,
+  KC_GEMM_Q4DEC,
+  KC_PACK,
   KC_COUNT
 };
 constexpr int kProfilePhases = 4;
@@ -56,6 +58,7 @@ struct Trace {
 // multiple of 64 and its columns start at `n0` in the output.
 struct WSeg {
   const uint8_t* codes;
+  const uint8_t* packed;   // channel-major codes + fp16 (scale, min) pairs (fg_pack_weight) or null
   const float* mins;
   const float* scales;
   const void* dense;
@@ -91,6 +94,17 @@ size_t gemm_tc_workspace_bytes(int64_t M, int64_t N, int64_t K, bool q4);
 // inside a thread-block cluster, so no global scratch).
 bool gemm_q4dec_supported(const GemmArgs& a);
 fg_status gemm_q4dec(const GemmArgs& a, cudaStream_t st);
+int gemm_q4dec_splits(int64_t M, int64_t N, int64_t K);
+// Decode product on channel-major packed 4-bit weights for M <= 256 rows:
+// the weights are dequantized straight into tensor memory (the MMA's A
+// operand), so shared memory carries only codes, (min, scale) and X.
+// K splits go through `ws` (gemm_q4ts_workspace_bytes).
+bool gemm_q4ts_supported(const GemmArgs& a);
+fg_status gemm_q4ts(const GemmArgs& a, void* ws, size_t ws_bytes, cudaStream_t st);
+size_t gemm_q4ts_workspace_bytes(int64_t M, int64_t N, int64_t K);
+// The packed copy of a [K][N] 4-bit weight read by gemm_q4ts (fg_pack_weight).
+fg_status pack_weight(const uint8_t* codes, const float* mins, const float* scales, int64_t K, int64_t N,
+                      uint8_t* packed, cudaStream_t st);
 
 // Y = epilogue(X . W); chooses the kernel for the shape.  `ws` (ws_bytes >=
 // gemm_workspace_bytes) holds split-K partial sums where a kernel needs them.
@@ -117,9 +131,12 @@ size_t decode_attention_workspace_bytes(int64_t b, int32_t heads, int32_t head_d
 fg_status decode_attention_simt(const fg_kv& kv, const void* q, int64_t ldq, int64_t b,
                                 int64_t pos, void* out, int64_t ldo, cudaStream_t st);
 // Prefill: causal attention of s queries per sequence over slots 0..s-1.
-// q: [b*s][ldq]; out: [b*s][ldo].
+// q: [b*s][ldq]; out: [b*s][ldo].  Tensor cores for a 4-bit fp16 cache,
+// CUDA cores otherwise.
 fg_status prefill_attention(const fg_kv& kv, const void* q, int64_t ldq, int64_t b, int64_t s,
                             void* out, int64_t ldo, cudaStream_t st);
+fg_status prefill_attention_simt(const fg_kv& kv, const void* q, int64_t ldq, int64_t b, int64_t s,
+                                 void* out, int64_t ldo, cudaStream_t st);
 
 // ---- codec -----------------------------------------------------------------
 fg_status quantize_rows(const void* x, fg_dtype dt, int64_t rows, int64_t cols, uint8_t* codes,

@@ -113,10 +113,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_q4_decode_kernel(const __gri
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1 + kDqThreads);
+      mbar_init(&empty[i], 1 + kDqThreads / 32);   // the MMA commit + one arrival per dequant warp
     }
     for (int i = 0; i < NW; ++i) {
-      mbar_init(&wfull[i], kDqThreads);
+      mbar_init(&wfull[i], kDqThreads / 32);
       mbar_init(&wempty[i], 1);
     }
     mbar_init(done, 1);
@@ -214,9 +214,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_q4_decode_kernel(const __gri
         *reinterpret_cast<uint4*>(row + ((chunk ^ (k & 7)) << 4)) = v0;
         *reinterpret_cast<uint4*>(row + (((chunk + 1) ^ (k & 7)) << 4)) = v1;
       }
+      // each thread orders its own stores before the tensor core reads them;
+      // the warp then signals once
       fence_proxy_async_smem();
-      mbar_arrive(&wfull[j]);
-      mbar_arrive(&empty[s]);
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&wfull[j]);
+        mbar_arrive(&empty[s]);
+      }
     }
   }
 
@@ -321,7 +326,7 @@ int bt_for(int64_t M) { return M <= 64 ? 64 : (M <= 128 ? 128 : 256); }
 // per-CTA work; depends on the shape only.
 int gemm_q4dec_splits(int64_t M, int64_t N, int64_t K) {
   const int64_t tiles = N / BNC, ktiles = K / BK;
-  const int64_t slots = (M <= 128 ? 2 : 1) * 148;
+  const int64_t slots = (M <= 128 ? 2 : 1) * static_cast<int64_t>(num_sms());
   int64_t best = 1;
   double best_cost = 1e30;
   for (int64_t s = 1; s <= 8 && s <= ktiles / 2; ++s) {   // a cluster holds at most 8 CTAs
@@ -340,6 +345,7 @@ bool gemm_q4dec_supported(const GemmArgs& a) {
   for (int i = 0; i < a.nseg; ++i) {
     if (a.seg[i].N % BNC) return false;
     if (((a.seg[i].N / 64) * 4) % 16) return false;
+    if (!aligned(a.seg[i].codes, 16) || !aligned(a.seg[i].mins, 16) || !aligned(a.seg[i].scales, 16)) return false;
   }
   if ((a.ldx * 2) % 16) return false;
   return true;

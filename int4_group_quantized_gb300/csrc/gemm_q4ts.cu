@@ -1,0 +1,657 @@
+// Decode products on 4-bit weights with the weights in tensor memory
+// (FlexGen notes, "4. 卸载策略": zig-zag block, one read of a layer's weights
+// serves every sequence of the block; "5. 近似方法": 4-bit groups of 64 along
+// the output channel, converted back to FP16 before compute).
+//
+// Y^T = W^T X^T on tcgen05.mma kind::f16 with A taken from TMEM.  A CTA
+// owns RB row blocks of 128 output channels (RB = 2: one CTA per SM with all
+// 512 TMEM columns; RB = 1: two CTAs per SM):
+//   * A = 128 channels x 64 k per row block.  Dequantization warps turn the
+//     packed codes and fp16 (scale, min) pairs (fg_pack_weight) into fp16
+//     weights in registers and store them with tcgen05.st: TMEM lane =
+//     channel, column = two consecutive k.  A warp reaches only its own
+//     32-lane quarter of TMEM (warp % 4); two groups of 4*RB warps take
+//     alternate k tiles, so two tiles are in conversion at any time.
+//   * B = X tile [BT rows][64 k], K-major, 128-byte swizzle, by TMA, shared
+//     by the RB row blocks: the activations cross L2 once per 128*RB
+//     channels, which is what bounds this kernel at small RB.
+//   * D = RB accumulators of 128 lanes (channels) x BT columns (sequences).
+// Shared memory carries only what HBM delivers (codes, pairs) and X; the fp16
+// weights never touch it.  Stage i of the ring is one smem slot and RB
+// 32-column TMEM slots; one mbarrier per stage frees both (the MMA's commit
+// plus one arrival per warp of the converting group).
+//
+// K is split when there are too few channel tiles to fill the GPU: each
+// split writes its fp32 partial to the workspace, and the last CTA of a tile
+// to finish (a ticket counter per tile, library-owned and reset by that CTA)
+// sums the splits in index order and applies the epilogue.
+//
+// The kernel is launched with programmatic stream serialization: the weight
+// tiles of the first stages are requested and converted before
+// griddepcontrol.wait, so they stream while the previous kernel finishes; X,
+// the residual, the workspace and Y are touched only after it.
+//
+// Warp roles (128 + 256*RB threads): warp 0 issues the copies, warp 1 owns
+// TMEM and issues the MMAs, warps 4.. dequantize, and the first 4*RB of them
+// drain TMEM.  Every wait is bounded and raises the device error word on
+// timeout.
+#include <cudaTypedefs.h>
+#include <string.h>
+
+#include <algorithm>
+#include <atomic>
+
+#include "fg_internal.cuh"
+#include "q4_dev.cuh"
+#include "tc_ptx.cuh"
+
+namespace fg {
+
+// defined in gemm_tc.cu
+bool tc_make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+                 uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw);
+
+namespace {
+
+using namespace tc;
+using namespace q4;
+
+constexpr int BK = 64;
+constexpr int BNC = 128;               // channels per row block (the MMA's M)
+constexpr int kDqWarp0 = 4;            // dequantization warps start here
+constexpr int kGroups = 2;             // groups of dequantization warps, alternate k tiles
+constexpr uint32_t kWaitLimit = 1u << 24;
+
+// Split-K tickets: kSlices slices of one counter per 128-channel tile; each
+// launch takes the next slice, so launches in flight at the same time (up to
+// kSlices across all streams of a device) never share a counter.
+constexpr int kSlices = 64;
+constexpr int kSliceTiles = 1024;
+__device__ unsigned int g_tickets[kSlices * kSliceTiles];   // zero at load; reset by each tile's last CTA
+
+// ---- packing -------------------------------------------------------------------
+// The decode copy is one 4608-byte block per (128-channel tile nt, 64-k tile
+// kt), blocks in order nt-major, so a CTA streams one contiguous run of HBM
+// and fetches a stage with one bulk copy:
+//   bytes 0..4095: codes, channel r of the tile in bytes r*32..r*32+31, its
+//     two 16-byte halves (k 0..31, k 32..63) swapped when bit 2 of r is set
+//     (the order in which eight lanes reading rows r..r+7 hit distinct shared
+//     memory banks); in each 32-bit word (8 consecutive k) nibble slot p
+//     (from the low end) holds k = 2*(p & 3) + (p >> 2), so slots (p, p+4)
+//     are the pair (2p, 2p+1);
+//   bytes 4096..4607: for the tile's two 64-channel groups gl and j = 0..31,
+//     fp16x2 (scale[2j], scale[2j+1]) then fp16x2 (min[2j], min[2j+1]).
+constexpr int kTileCodes = BNC * BK / 2;             // 4096
+constexpr int kTilePairs = 2 * (BK / 2) * 8;         // 512
+constexpr int kTileBytes = kTileCodes + kTilePairs;  // 4608
+
+__global__ void pack_codes_kernel(const uint8_t* __restrict__ codes, int64_t K, int64_t N,
+                                  uint8_t* __restrict__ packed) {
+  const int64_t words = N * (K / 8), KT = K / BK;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < words;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t n = i % N, rest = i / N;   // threads along n: coalesced reads of a code row
+    const int wq = static_cast<int>(rest % 4), c = static_cast<int>((rest / 4) % 2);
+    const int64_t kt = rest / 8;
+    const int64_t k0 = kt * BK + 32 * c + 8 * wq;
+    uint32_t out = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t byte = codes[(k0 + j) * (N / 2) + n / 2];
+      const uint32_t q = (n & 1) ? (byte >> 4) : (byte & 15u);
+      out |= q << (4 * (((j & 1) << 2) | (j >> 1)));
+    }
+    const int64_t nt = n / BNC;
+    const int r = static_cast<int>(n % BNC);
+    uint8_t* tile = packed + (nt * KT + kt) * kTileBytes;
+    *reinterpret_cast<uint32_t*>(tile + r * 32 + 16 * (c ^ ((r >> 2) & 1)) + 4 * wq) = out;
+  }
+}
+
+__global__ void pack_pairs_kernel(const float* __restrict__ mins, const float* __restrict__ scales, int64_t K,
+                                  int64_t N, uint8_t* __restrict__ packed) {
+  const int64_t G = N / 64, total = G * (K / 2), KT = K / BK;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t g = i % G, jj = i / G;     // jj = global k pair; threads along g: coalesced reads
+    const __half2 s2 = __floats2half2_rn(scales[(2 * jj) * G + g], scales[(2 * jj + 1) * G + g]);
+    const __half2 m2 = __floats2half2_rn(mins[(2 * jj) * G + g], mins[(2 * jj + 1) * G + g]);
+    const int64_t kt = jj / (BK / 2), j = jj % (BK / 2);
+    uint8_t* tile = packed + ((g / 2) * KT + kt) * kTileBytes;
+    *reinterpret_cast<uint2*>(tile + kTileCodes + ((g % 2) * (BK / 2) + j) * 8) =
+        make_uint2(*reinterpret_cast<const uint32_t*>(&s2), *reinterpret_cast<const uint32_t*>(&m2));
+  }
+}
+
+struct TsParams {
+  CUtensorMap mapX;
+  const uint8_t* wp[3];     // decode copy of each segment
+  int seg_n0[4];
+  int nseg;
+  int M, N, K;
+  int n_tiles, splits, ktiles_per_split;
+  __half* Y;
+  int ldy;
+  const __half* R;
+  int ldr;
+  int relu;
+  float* part;              // [splits][M][N] fp32 when splits > 1
+  unsigned int* tickets;    // [n_tiles] of this launch's slice
+  unsigned int* err;
+};
+
+constexpr int cmin(int a, int b) { return a < b ? a : b; }
+constexpr int cmax(int a, int b) { return a > b ? a : b; }
+
+// Three rings, each released by the stage that last needs it, so that a slow
+// stage never holds back the requests of another: weights (released once the
+// dequantization warps hold them in registers), X (released by the MMAs that
+// read it) and TMEM A slots (released by the MMAs).  Ring depths follow what
+// each must cover: HBM latency for the weights, L2 latency for X.
+template <int BT, int RB>
+struct TsCfg {
+  static constexpr int kThreads = 128 + kGroups * 4 * RB * 32;   // warps 0..3, then the dequant groups
+  static constexpr int kGroupWarps = 4 * RB;
+  static constexpr int kX = BT * BK * 2;              // X tile, K-major, 128-byte swizzle
+  static constexpr int kW = RB * kTileBytes;          // the weights of one k tile: RB packed blocks
+  static constexpr int kAcc = BT < 32 ? 32 : BT;      // accumulator columns per row block
+  static constexpr uint32_t kTmemCols = (RB == 1 && BT <= 128) ? 256 : 512;
+  static constexpr int kMinBlocks = kTmemCols == 256 ? 2 : 1;
+  static constexpr int kBudget = kMinBlocks == 2 ? 104 * 1024 : 204 * 1024;
+  static constexpr int kAStages = cmin((static_cast<int>(kTmemCols) - RB * kAcc) / (32 * RB), 8);
+  static constexpr int kXStages = cmax(2, cmin(6, (kBudget / 2) / kX));
+  static constexpr int kWStages = cmin(16, (kBudget - kXStages * kX) / kW);
+  static constexpr int kXBytes = kXStages * kX;
+  static constexpr int kWBytes = kWStages * kW;
+  static constexpr int kBarBytes = (2 * (kXStages + kWStages + kAStages) + 2) * 8 + 16;   // + done, red
+  static constexpr int kTotal = 1024 + kXBytes + kWBytes + kBarBytes;
+  static_assert(kAStages >= 2 && kWStages >= 2, "pipeline needs two stages");
+  static_assert(kX % 1024 == 0, "X stages stay 1024-byte aligned");
+};
+
+template <int BT, int RB>
+__global__ void __launch_bounds__(TsCfg<BT, RB>::kThreads, TsCfg<BT, RB>::kMinBlocks)
+    gemm_q4ts_kernel(const __grid_constant__ TsParams p) {
+  using C = TsCfg<BT, RB>;
+  constexpr int SX = C::kXStages, SW = C::kWStages, SA = C::kAStages;
+  constexpr int kGW = C::kGroupWarps;
+  constexpr uint32_t kIdesc = idesc_f16(128, BT, 0, 0);   // A (TMEM) and B (X) K-major
+  constexpr uint32_t kACol = RB * C::kAcc;                // TMEM A slots follow the accumulators
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* xring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* wring = xring + C::kXBytes;
+  uint64_t* xfull = reinterpret_cast<uint64_t*>(wring + C::kWBytes);
+  uint64_t* xempty = xfull + SX;
+  uint64_t* wfull = xempty + SX;
+  uint64_t* wempty = wfull + SW;
+  uint64_t* afull = wempty + SW;
+  uint64_t* aempty = afull + SA;
+  uint64_t* done = aempty + SA;   // done + 1: the reduction barrier of the split-K epilogue
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* last_flag = abort_flag + 1;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int split = blockIdx.x % p.splits;
+  const int nt = blockIdx.x / p.splits;
+  const int n0 = nt * BNC * RB;
+  int seg = 0;
+  while (seg + 1 < p.nseg && n0 >= p.seg_n0[seg + 1]) ++seg;
+  const int nl = n0 - p.seg_n0[seg];
+  const int kt0 = split * p.ktiles_per_split;
+  const int kt1 = min(kt0 + p.ktiles_per_split, p.K / BK);
+  const int nk = kt1 - kt0;
+
+  griddep_launch();   // a dependent grid waits for this one before it reads Y
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < SX; ++i) {
+      mbar_init(&xfull[i], 1);
+      mbar_init(&xempty[i], 1);      // the MMA commit
+    }
+    for (int i = 0; i < SW; ++i) {
+      mbar_init(&wfull[i], 1);
+      mbar_init(&wempty[i], kGW);    // one arrival per warp of the converting group
+    }
+    for (int i = 0; i < SA; ++i) {
+      mbar_init(&afull[i], kGW);
+      mbar_init(&aempty[i], 1);      // the MMA commit
+    }
+    mbar_init(done, 1);
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, C::kTmemCols);
+  if (warp == 2 && lane == 0) tma_prefetch_desc(&p.mapX);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // weights: independent of the previous kernel, so they stream from the start;
+      // the k tiles of a 128-channel block are one contiguous run of packed blocks
+      const size_t run = static_cast<size_t>(p.K / BK) * kTileBytes;
+      const uint8_t* wsrc = p.wp[seg] + static_cast<size_t>(nl / BNC) * run + static_cast<size_t>(kt0) * kTileBytes;
+      int issued = 0;
+      for (int i = 0; i < nk; ++i) {
+        const int s = i % SW;
+        if (!mbar_wait(&wempty[s], ((i / SW) & 1) ^ 1, kWaitLimit, abort_flag)) break;
+        mbar_expect_tx(&wfull[s], C::kW);
+#pragma unroll
+        for (int rb = 0; rb < RB; ++rb)
+          bulk_load(wring + s * C::kW + rb * kTileBytes, wsrc + rb * run + static_cast<size_t>(i) * kTileBytes,
+                    kTileBytes, &wfull[s]);
+        ++issued;
+      }
+      for (int i = max(0, issued - SW); i < issued; ++i) {   // nothing in flight at exit
+        volatile int dummy = 0;
+        mbar_wait(&wfull[i % SW], (i / SW) & 1, kWaitLimit, &dummy);
+      }
+      if (*abort_flag) atomicOr(p.err, DEV_ERR_WAIT_TIMEOUT);
+    }
+  } else if (warp == 2) {
+    if (lane == 0) {
+      griddep_wait();   // X comes from the previous kernel
+      int issued = 0;
+      for (int i = 0; i < nk; ++i) {
+        const int s = i % SX;
+        if (!mbar_wait(&xempty[s], ((i / SX) & 1) ^ 1, kWaitLimit, abort_flag)) break;
+        mbar_expect_tx(&xfull[s], C::kX);
+        tma_load_2d(xring + s * C::kX, &p.mapX, (kt0 + i) * BK, 0, &xfull[s]);
+        ++issued;
+      }
+      for (int i = max(0, issued - SX); i < issued; ++i) {
+        volatile int dummy = 0;
+        mbar_wait(&xfull[i % SX], (i / SX) & 1, kWaitLimit, &dummy);
+      }
+      if (*abort_flag) atomicOr(p.err, DEV_ERR_WAIT_TIMEOUT);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      bool ok = true;
+      for (int i = 0; i < nk && ok; ++i) {
+        const int sx = i % SX, sa = i % SA;
+        ok = mbar_wait(&xfull[sx], (i / SX) & 1, kWaitLimit, abort_flag) &&
+             mbar_wait(&afull[sa], (i / SA) & 1, kWaitLimit, abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t xa = smem_u32(xring + sx * C::kX);
+#pragma unroll
+        for (int rb = 0; rb < RB; ++rb) {
+          const uint32_t ta = tmem_base + kACol + 32u * (sa * RB + rb);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            // B (X): K-major, 8-row groups 1 KiB apart; +32 bytes per 16-wide k step
+            const uint64_t bdesc = smem_desc_sw128(xa + kk * 32, 16, 1024);
+            mma_f16_ts(tmem_base + rb * C::kAcc, ta + 8u * kk, bdesc, kIdesc, (i > 0 || kk > 0) ? 1u : 0u);
+          }
+        }
+        mma_commit(&xempty[sx]);
+        mma_commit(&aempty[sa]);
+      }
+      mma_commit(done);
+      if (!ok) atomicOr(p.err, DEV_ERR_WAIT_TIMEOUT);
+    }
+  } else if (warp >= kDqWarp0) {
+    const int d = warp - kDqWarp0;
+    const int grp = d / kGW;                    // takes tiles i with i % kGroups == grp
+    const int rb = (d / 4) % RB;                // row block
+    const int q = warp & 3;                     // TMEM lane quarter of this warp
+    const int r = 32 * q + lane;                // channel in the row block = TMEM lane
+    const int sw = ((r >> 2) & 1) << 4;         // halves swapped in rows with bit 2 set
+    const uint32_t trow = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + kACol + 32u * rb;
+    bool ok = true;
+    for (int i = grp; i < nk && ok; i += kGroups) {
+      const int s = i % SW, sa = i % SA;
+      ok = mbar_wait(&wfull[s], (i / SW) & 1, kWaitLimit, abort_flag) &&
+           mbar_wait(&aempty[sa], ((i / SA) & 1) ^ 1, kWaitLimit, abort_flag);
+      ok = __all_sync(0xffffffffu, ok);   // the warp-wide tcgen05.st below needs every lane
+      if (!ok) break;
+      tc_fence_after();
+      const uint8_t* st = wring + s * C::kW + rb * kTileBytes;
+      const uint4 c0 = *reinterpret_cast<const uint4*>(st + r * 32 + (0 ^ sw));    // k 0..31
+      const uint4 c1 = *reinterpret_cast<const uint4*>(st + r * 32 + (16 ^ sw));   // k 32..63
+      const uint4* pr = reinterpret_cast<const uint4*>(st + kTileCodes + (q >> 1) * 256);   // this group's pairs
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {   // columns 16h .. 16h+15 (k 32h .. 32h+31)
+        const uint4 c = h ? c1 : c0;
+        const uint32_t words[4] = {c.x, c.y, c.z, c.w};
+        uint32_t a[16];
+#pragma unroll
+        for (int wd = 0; wd < 4; ++wd) {
+          const uint4 m01 = pr[8 * h + 2 * wd], m23 = pr[8 * h + 2 * wd + 1];   // (scale, min), 4 columns
+          const uint32_t x = words[wd], y = x >> 8;
+          a[4 * wd + 0] = hfma2_u(hfma2_u(lop_mask_or(x, 0x000F000Fu, kMagic), kOne, kNegMagic), m01.x, m01.y);
+          a[4 * wd + 1] = hfma2_u(hfma2_u(lop_mask_or(x, 0x00F000F0u, kMagic), kSixteenth, kNeg64), m01.z, m01.w);
+          a[4 * wd + 2] = hfma2_u(hfma2_u(lop_mask_or(y, 0x000F000Fu, kMagic), kOne, kNegMagic), m23.x, m23.y);
+          a[4 * wd + 3] = hfma2_u(hfma2_u(lop_mask_or(y, 0x00F000F0u, kMagic), kSixteenth, kNeg64), m23.z, m23.w);
+        }
+        if (h == 1) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&wempty[s]);   // this k tile's codes and pairs are in registers
+        }
+        tmem_st_32x32b_x16(trow + 32u * RB * sa + 16u * h, a);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&afull[sa]);
+    }
+  }
+
+  // ---- epilogue: TMEM lane = channel, column rb*kAcc + m = sequence m ---------------
+  const bool epi = warp >= kDqWarp0 && warp < kDqWarp0 + 4 * RB;
+  const int erb = (warp - kDqWarp0) >> 2;
+  const int q = warp & 3;
+  constexpr int NCH = RB * BNC;                 // channels of the tile
+  bool ok = true;
+  if (epi) {
+    ok = mbar_wait(done, 0, kWaitLimit, abort_flag);
+    tc_fence_after();
+    ok = ok && !*abort_flag;
+  }
+  griddep_wait();   // Y, the residual and the workspace belong to the stream order from here on
+  const uint32_t tlane = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + erb * C::kAcc;
+  const int lch = erb * BNC + 32 * q + lane;    // this lane's channel in the tile
+
+  if (p.splits == 1) {
+    if (epi) {
+      const int ch = n0 + lch;
+#pragma unroll 1
+      for (int c0 = 0; c0 < BT && c0 < p.M; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tlane + c0, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int m = c0 + e;
+          if (m < p.M && ok) {
+            float y = __uint_as_float(v[e]);
+            if (p.R) y += __half2float(p.R[static_cast<size_t>(m) * p.ldr + ch]);
+            if (p.relu) y = fmaxf(y, 0.0f);
+            p.Y[static_cast<size_t>(m) * p.ldy + ch] = __float2half_rn(y);
+          }
+        }
+      }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+      tc_fence_after();
+      tmem_dealloc(tmem_base, C::kTmemCols);
+    }
+    return;
+  }
+
+  // K splits.  Each split's partial, [M][NCH] fp32, goes to its own contiguous
+  // block of the workspace with one bulk copy from the drained rings; the
+  // tile's last CTA brings all blocks back the same way and sums them in
+  // split order.
+  float* stage = reinterpret_cast<float*>(xring);   // the rings are free: every load and MMA is done
+  const size_t blk = static_cast<size_t>(p.M) * NCH;   // floats per partial block
+  float* myblk = p.part + (static_cast<size_t>(split) * p.n_tiles + nt) * blk;
+  if (epi) {
+#pragma unroll 1
+    for (int c0 = 0; c0 < BT && c0 < p.M; c0 += 32) {
+      uint32_t v[32];
+      tmem_ld_32x32b_x32(tlane + c0, v);
+      tmem_ld_wait();
+#pragma unroll
+      for (int e = 0; e < 32; ++e)
+        if (c0 + e < p.M) stage[(c0 + e) * NCH + lch] = ok ? __uint_as_float(v[e]) : 0.0f;
+    }
+  }
+  fence_proxy_async_smem();   // the staged partial is visible to the bulk copy
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+  if (threadIdx.x == 0) {
+    bulk_store(myblk, stage, static_cast<uint32_t>(blk * 4));
+    bulk_commit();
+    bulk_wait_all();
+    fence_proxy_async_global();
+    __threadfence();   // this split's partial before its ticket
+    *last_flag = atomicAdd(&p.tickets[nt], 1u) == static_cast<unsigned>(p.splits - 1);
+  }
+  __syncthreads();
+  if (!*last_flag) return;
+
+  // The tile's last CTA.  Rows are taken in chunks small enough that the
+  // rings hold at least three chunk slots; per chunk, rounds bring as many
+  // splits as the slots hold, slot 0 keeping the running sum (split order).
+  constexpr int kRing = C::kXBytes + C::kWBytes;
+  const int rc = min(p.M, kRing / (3 * NCH * 4));      // rows per chunk
+  const int slots = kRing / (rc * NCH * 4);              // >= 3
+  const size_t slot_f = static_cast<size_t>(rc) * NCH;   // floats per slot
+  uint64_t* red = done + 1;
+  if (threadIdx.x == 0) {
+    mbar_init(red, 1);
+    mbar_fence_init();
+    __threadfence();            // every split's partial is visible to this CTA
+    fence_proxy_async_global();
+  }
+  __syncthreads();
+  uint32_t phase = 0;
+  bool good = true;
+  for (int m0 = 0; m0 < p.M && good; m0 += rc) {
+    const int rows = min(rc, p.M - m0);
+    const uint32_t bytes = static_cast<uint32_t>(rows) * NCH * 4;
+    const int nf4 = rows * NCH / 4;
+    for (int s0 = 0; s0 < p.splits && good;) {
+      const int first = s0 == 0 ? 0 : 1;                 // later rounds keep slot 0
+      const int n = min(p.splits - s0, slots - first);
+      if (threadIdx.x == 0) {
+        mbar_expect_tx(red, bytes * n);
+        for (int j = 0; j < n; ++j)
+          bulk_load(stage + (first + j) * slot_f,
+                    p.part + (static_cast<size_t>(s0 + j) * p.n_tiles + nt) * blk + static_cast<size_t>(m0) * NCH,
+                    bytes, red);
+      }
+      good = __syncthreads_and(mbar_wait(red, phase, kWaitLimit, abort_flag) ? 1 : 0) != 0;   // uniform
+      phase ^= 1;
+      if (!good) {
+        if (threadIdx.x == 0) atomicOr(p.err, DEV_ERR_WAIT_TIMEOUT);
+        break;
+      }
+      for (int e = threadIdx.x; e < nf4; e += C::kThreads) {
+        float4 a4 = reinterpret_cast<const float4*>(stage)[e];
+        for (int j = 1; j < first + n; ++j) {
+          const float4 v = reinterpret_cast<const float4*>(stage + j * slot_f)[e];
+          a4.x += v.x;
+          a4.y += v.y;
+          a4.z += v.z;
+          a4.w += v.w;
+        }
+        reinterpret_cast<float4*>(stage)[e] = a4;
+      }
+      __syncthreads();   // slot 0 complete; the other slots may be refilled
+      s0 += n;
+    }
+    // Y = epilogue(sum) for these rows, 4 channels per thread and pass
+    for (int e = threadIdx.x; e < nf4 && good; e += C::kThreads) {
+      const int m = m0 + e / (NCH / 4), ch = n0 + 4 * (e % (NCH / 4));
+      float4 a4 = reinterpret_cast<const float4*>(stage)[e];
+      if (p.R) {
+        const uint2 rr = *reinterpret_cast<const uint2*>(p.R + static_cast<size_t>(m) * p.ldr + ch);
+        const float2 r01 = __half22float2(*reinterpret_cast<const __half2*>(&rr.x));
+        const float2 r23 = __half22float2(*reinterpret_cast<const __half2*>(&rr.y));
+        a4.x += r01.x;
+        a4.y += r01.y;
+        a4.z += r23.x;
+        a4.w += r23.y;
+      }
+      if (p.relu) {
+        a4.x = fmaxf(a4.x, 0.0f);
+        a4.y = fmaxf(a4.y, 0.0f);
+        a4.z = fmaxf(a4.z, 0.0f);
+        a4.w = fmaxf(a4.w, 0.0f);
+      }
+      const __half2 y01 = __floats2half2_rn(a4.x, a4.y), y23 = __floats2half2_rn(a4.z, a4.w);
+      *reinterpret_cast<uint2*>(p.Y + static_cast<size_t>(m) * p.ldy + ch) =
+          make_uint2(*reinterpret_cast<const uint32_t*>(&y01), *reinterpret_cast<const uint32_t*>(&y23));
+    }
+    __syncthreads();   // slot 0 is read before the next chunk refills it
+  }
+  if (threadIdx.x == 0) p.tickets[nt] = 0;   // the slice is clean for its next launch
+}
+
+template <int BT, int RB>
+fg_status launch_ts(TsParams& p, cudaStream_t st) {
+  using C = TsCfg<BT, RB>;
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    if (cudaFuncSetAttribute(gemm_q4ts_kernel<BT, RB>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kTotal) !=
+        cudaSuccess)
+      return check_launch("gemm_q4ts smem attribute");
+    attr_set[dev] = true;
+  }
+  Trace tr(KC_GEMM_Q4DEC, st);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.n_tiles * p.splits));
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kTotal;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, gemm_q4ts_kernel<BT, RB>, p) != cudaSuccess)
+    return check_launch("gemm_q4ts_kernel (launch)");
+  return check_launch("gemm_q4ts_kernel");
+}
+
+int bt_for(int64_t M) { return M <= 32 ? 32 : (M <= 64 ? 64 : (M <= 128 ? 128 : 256)); }
+
+// One row block per CTA: measured at b = 64, two CTAs of 128 channels per SM
+// beat one of 256 (the X tile is re-read twice as often, but the two CTAs'
+// pipelines overlap each other's stalls).
+int rb_for(const GemmArgs&) { return 1; }
+
+unsigned int* ticket_slice() {
+  static std::atomic<unsigned> next{0};
+  static unsigned int* base[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (!base[dev]) {
+    void* a = nullptr;
+    if (cudaGetSymbolAddress(&a, g_tickets) != cudaSuccess) return nullptr;
+    base[dev] = static_cast<unsigned int*>(a);
+  }
+  return base[dev] + static_cast<size_t>(next.fetch_add(1) % kSlices) * kSliceTiles;
+}
+
+// Split count: K is cut so that the CTAs fill the GPU's slots (one per SM
+// with two row blocks, two per SM with one) with the fewest waves of per-CTA
+// k tiles, plus a charge per split for its partial's round trip through L2.
+// Depends on the shape only.
+int splits_for(int64_t M, int64_t N, int64_t K, int rb) {
+  const int64_t tiles = N / (BNC * rb), ktiles = K / BK;
+  const int64_t slots = (rb == 1 && M <= 128 ? 2 : 1) * static_cast<int64_t>(num_sms());
+  int64_t best = 1;
+  double best_cost = 1e30;
+  for (int64_t s = 1; s <= 16 && s <= ktiles / 2; ++s) {
+    const int64_t waves = (tiles * s + slots - 1) / slots;
+    const double cost = static_cast<double>(waves) * ((ktiles + s - 1) / s) + (s > 1 ? 2.0 + 0.5 * s : 0.0);
+    if (cost < best_cost) {
+      best_cost = cost;
+      best = s;
+    }
+  }
+  return static_cast<int>(best);
+}
+
+}  // namespace
+
+size_t gemm_q4ts_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  size_t need = 0;
+  for (int rb = 1; rb <= 2; ++rb) {   // whichever the weight segments allow
+    const int s = splits_for(M, N, K, rb);
+    if (s > 1) need = std::max(need, static_cast<size_t>(s) * M * N * 4);
+  }
+  return need;
+}
+
+bool gemm_q4ts_supported(const GemmArgs& a) {
+  if (a.dtype != FG_F16 || !a.quant || a.M < 1 || a.M > 256 || a.K % BK) return false;
+  if (a.N / BNC > kSliceTiles) return false;
+  for (int i = 0; i < a.nseg; ++i) {
+    const WSeg& s = a.seg[i];
+    if (!s.packed || s.N % BNC || !aligned(s.packed, 16)) return false;
+  }
+  if ((a.ldx * 2) % 16 || !aligned(a.X, 16)) return false;
+  if (a.ldy % 4 || !aligned(a.Y, 8) || (a.R && (a.ldr % 4 || !aligned(a.R, 8)))) return false;
+  return true;
+}
+
+fg_status gemm_q4ts(const GemmArgs& a, void* ws, size_t ws_bytes, cudaStream_t st) {
+  TsParams p;
+  memset(&p, 0, sizeof(p));
+  const int bt = bt_for(a.M);
+  const int rb = rb_for(a);
+  p.M = static_cast<int>(a.M);
+  p.N = static_cast<int>(a.N);
+  p.K = static_cast<int>(a.K);
+  p.nseg = a.nseg;
+  if (!tc_make_map(&p.mapX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.X, a.K, a.M, a.ldx * 2, BK, bt,
+                   CU_TENSOR_MAP_SWIZZLE_128B))
+    return fail(FG_ERR_CUDA, "tensor map for X");
+  for (int i = 0; i < a.nseg; ++i) {
+    p.seg_n0[i] = static_cast<int>(a.seg[i].n0);
+    p.wp[i] = a.seg[i].packed;
+  }
+  p.seg_n0[a.nseg] = static_cast<int>(a.N);
+  p.n_tiles = static_cast<int>(a.N / (BNC * rb));
+  {
+    const int ktiles = static_cast<int>(a.K / BK);
+    const int want = splits_for(a.M, a.N, a.K, rb);
+    p.ktiles_per_split = (ktiles + want - 1) / want;
+    p.splits = (ktiles + p.ktiles_per_split - 1) / p.ktiles_per_split;
+  }
+  if (p.splits > 1) {
+    const size_t need = static_cast<size_t>(p.splits) * a.M * a.N * 4;
+    if (!ws || ws_bytes < need) return fail(FG_ERR_WORKSPACE, "decode product needs %zu workspace bytes", need);
+    p.part = static_cast<float*>(ws);
+    p.tickets = ticket_slice();
+    if (!p.tickets) return fail(FG_ERR_CUDA, "split-K tickets");
+  }
+  p.Y = static_cast<__half*>(a.Y);
+  p.ldy = static_cast<int>(a.ldy);
+  p.R = static_cast<const __half*>(a.R);
+  p.ldr = static_cast<int>(a.ldr);
+  p.relu = a.relu;
+  p.err = device_error_word();
+  if (!p.err) return fail(FG_ERR_CUDA, "device error word");
+  switch (bt) {
+    case 32: return launch_ts<32, 1>(p, st);
+    case 64: return launch_ts<64, 1>(p, st);
+    case 128: return launch_ts<128, 1>(p, st);
+    default: return launch_ts<256, 1>(p, st);
+  }
+}
+
+fg_status pack_weight(const uint8_t* codes, const float* mins, const float* scales, int64_t K, int64_t N,
+                      uint8_t* packed, cudaStream_t st) {
+  if (K == 0 || N == 0) return FG_OK;
+  Trace tr(KC_PACK, st);
+  constexpr int kT = 256;
+  const int64_t cap = static_cast<int64_t>(num_sms()) * 16;
+  const int64_t words = N * (K / 8), pairs = (N / 64) * (K / 2);
+  pack_codes_kernel<<<static_cast<unsigned>(std::min<int64_t>((words + kT - 1) / kT, cap)), kT, 0, st>>>(
+      codes, K, N, packed);
+  const fg_status sc = check_launch("pack_codes_kernel");
+  if (sc != FG_OK) return sc;
+  pack_pairs_kernel<<<static_cast<unsigned>(std::min<int64_t>((pairs + kT - 1) / kT, cap)), kT, 0, st>>>(
+      mins, scales, K, N, packed);
+  return check_launch("pack_pairs_kernel");
+}
+
+}  // namespace fg

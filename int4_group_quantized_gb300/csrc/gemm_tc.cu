@@ -133,10 +133,10 @@ __global__ void __launch_bounds__(cta_threads(Q4), 1) gemm_tc_kernel(const __gri
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], Q4 ? 1 + kDequantThreads : 1);
+      mbar_init(&empty[i], Q4 ? 1 + kDequantThreads / 32 : 1);   // MMA commit + one per dequant warp
     }
     for (int i = 0; i < S::kNB; ++i) {
-      mbar_init(&bfull[i], kDequantThreads);
+      mbar_init(&bfull[i], kDequantThreads / 32);
       mbar_init(&bempty[i], 1);
     }
     mbar_init(done, 1);
@@ -254,8 +254,11 @@ __global__ void __launch_bounds__(cta_threads(Q4), 1) gemm_tc_kernel(const __gri
         *reinterpret_cast<uint4*>(row + (((chunk + 1) ^ (k & 7)) << 4)) = v1;
       }
       fence_proxy_async_smem();
-      mbar_arrive(&bfull[j]);
-      mbar_arrive(&empty[s]);
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&bfull[j]);
+        mbar_arrive(&empty[s]);
+      }
     }
   }
 

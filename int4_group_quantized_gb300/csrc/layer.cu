@@ -19,6 +19,7 @@ fg_status check_wmat(const fg_wmat& w, int64_t K, int64_t N, fg_codec codec, con
     if (!w.codes || !w.mins || !w.scales) return fail(FG_ERR_ARG, "%s: null 4-bit arrays", name);
     if (!aligned(w.codes, 16) || !aligned(w.mins, 4) || !aligned(w.scales, 4))
       return fail(FG_ERR_ALIGN, "%s: codes need 16-byte alignment", name);
+    if (w.packed && !aligned(w.packed, 16)) return fail(FG_ERR_ALIGN, "%s: packed copy needs 16-byte alignment", name);
   } else {
     if (!w.dense) return fail(FG_ERR_ARG, "%s: null dense weights", name);
     if (!aligned(w.dense, 16)) return fail(FG_ERR_ALIGN, "%s: dense weights need 16-byte alignment", name);
@@ -71,6 +72,7 @@ fg_status check_kv(const fg_kv* kv, int64_t b, int32_t heads, int64_t d, fg_code
 WSeg seg_of(const fg_wmat& w, int64_t n0) {
   WSeg s;
   s.codes = w.codes;
+  s.packed = w.packed;
   s.mins = w.mins;
   s.scales = w.scales;
   s.dense = w.dense;
@@ -235,12 +237,14 @@ fg_status check_act(const void* p, const char* name) {
 }  // namespace
 
 fg_status gemm(const GemmArgs& a, void* ws, size_t ws_bytes, cudaStream_t st) {
+  if (gemm_q4ts_supported(a)) return gemm_q4ts(a, ws, ws_bytes, st);
   if (gemm_q4dec_supported(a)) return gemm_q4dec(a, st);
   if (gemm_tc_supported(a)) return gemm_tc(a, ws, ws_bytes, st);
   return gemm_simt(a, st);
 }
 
 size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, fg_dtype dt, int quant) {
+  if (dt == FG_F16 && quant && M >= 1 && M <= 256) return gemm_q4ts_workspace_bytes(M, N, K);
   if (dt != FG_F16 || M < 64 || (quant && M <= 256)) return 0;
   return gemm_tc_workspace_bytes(M, N, K, quant != 0);
 }
@@ -298,6 +302,21 @@ fg_status fg_linear(const fg_wmat* w, fg_codec codec, fg_dtype dtype, const void
   L.dtype = dtype;
   GemmArgs a = product(L, x, w->K, M, w, 1, y, w->N, r, w->N, relu ? 1 : 0);
   return gemm(a, ws, ws_bytes, stream);
+}
+
+size_t fg_pack_weight_bytes(int64_t K, int64_t N) {
+  if (K <= 0 || N <= 0) return 0;
+  const size_t kn = static_cast<size_t>(K) * static_cast<size_t>(N);
+  return kn / 2 + kn / 16;
+}
+
+fg_status fg_pack_weight(const fg_wmat* w, uint8_t* packed, cudaStream_t stream) {
+  if (!w || !w->codes || !w->mins || !w->scales || !packed) return fail(FG_ERR_ARG, "null weight arrays or packed buffer");
+  if (w->K <= 0 || w->N <= 0) return fail(FG_ERR_ARG, "sizes");
+  if (w->K % 64 || w->N % 128) return fail(FG_ERR_SHAPE, "K must be a multiple of 64 and N of 128");
+  if (!aligned(w->codes, 16) || !aligned(packed, 16) || !aligned(w->mins, 4) || !aligned(w->scales, 4))
+    return fail(FG_ERR_ALIGN, "codes and the packed buffer need 16-byte alignment");
+  return pack_weight(w->codes, w->mins, w->scales, w->K, w->N, packed, stream);
 }
 
 size_t fg_decode_attention_workspace_bytes(const fg_kv* kv) {

@@ -36,19 +36,29 @@ CASES = [
     (5, 128, 64, True, True, True, torch.float16),            # small block: CUDA cores
     (32, 768, 2304, True, False, False, torch.float16),
     (7, 256, 192, True, False, True, torch.float32),          # fp32 activations
+    (1, 4096, 4096, True, False, True, torch.float16),        # one sequence (GEMV shape)
+    (33, 2048, 1536, True, True, False, torch.float16),       # ragged 64-row block
+    (64, 64, 1024, True, False, False, torch.float16),        # a single k tile
+    (130, 4096, 256, True, False, True, torch.float16),       # two tiles, eight K splits
 ]
 
+# quantized fp16 products with at most 256 rows run on the packed-weight
+# kernel when the weight carries its channel-major copy, on the shared-memory
+# kernel otherwise; both are checked
+PACKED = [c + (True,) for c in CASES if c[3] and c[6] == torch.float16 and c[0] <= 256 and c[2] % 128 == 0]
+ALL = [c + (False,) for c in CASES] + PACKED
 
-@pytest.mark.parametrize("case", CASES, ids=lambda c: "M%d_K%d_N%d_%s%s%s_%s" % (
+
+@pytest.mark.parametrize("case", ALL, ids=lambda c: "M%d_K%d_N%d_%s%s%s_%s%s" % (
     c[0], c[1], c[2], "q4" if c[3] else "dense", "_relu" if c[4] else "", "_res" if c[5] else "",
-    "f16" if c[6] == torch.float16 else "f32"))
+    "f16" if c[6] == torch.float16 else "f32", "_packed" if c[7] else ""))
 def test_linear_matches_oracle(fg, case):
-    M, K, N, quant, relu, res, dt = case
+    M, K, N, quant, relu, res, dt, packed = case
     w16 = synth.normal((K, N), 7 + K + N, synth.WEIGHT_STD, dt, "cuda")
     x = synth.normal((M, K), 11 + M, 1.0, dt, "cuda")
     r = synth.normal((M, N), 13 + M, 1.0, dt, "cuda") if res else None
     if quant:
-        W = fg.QuantWeight.from_dense(w16, True)
+        W = fg.QuantWeight.from_dense(w16, True, pack=packed)
         wref = olayer.weight_for_compute(w16.cpu().numpy(), True, "f16" if dt == torch.float16 else "f32")
     else:
         W = fg.QuantWeight.from_dense(w16, False)
@@ -67,13 +77,56 @@ def test_linear_matches_oracle(fg, case):
     assert err <= tol, f"rel err {err}"
 
 
-def test_linear_repeatable(fg):
+@pytest.mark.parametrize("packed", [False, True])
+def test_linear_repeatable(fg, packed):
     """Two calls give identical bits (no atomics in the reduction order)."""
     w16 = synth.normal((4096, 4096), 3, synth.WEIGHT_STD, torch.float16, "cuda")
-    W = fg.QuantWeight.from_dense(w16, True)
+    W = fg.QuantWeight.from_dense(w16, True, pack=packed)
     x = synth.normal((64, 4096), 4, 1.0, torch.float16, "cuda")
     y1 = torch.empty((64, 4096), dtype=torch.float16, device="cuda")
     y2 = torch.empty_like(y1)
     fg.fg_linear(W, x, y1)
     fg.fg_linear(W, x, y2)
     assert torch.equal(y1, y2)
+
+
+def test_pack_layout(fg):
+    """fg_pack_weight's layout as its declaration states it, rebuilt here in
+    numpy from the [K][N/2] codes and [K][N/64] (min, scale): 4608-byte
+    blocks per (128-channel tile, 64-k tile); channel r's 32 code bytes with
+    halves swapped when bit 2 of r is set, nibbles k0 k2 k4 k6 k1 k3 k5 k7
+    per word; then per (group, k pair) fp16 (scale, scale') and (min, min')."""
+    K, N = 192, 384
+    w16 = synth.normal((K, N), 5, synth.WEIGHT_STD, torch.float16, "cuda")
+    W = fg.QuantWeight.from_dense(w16, True, pack=True)
+    fg.fg_sync_status()
+    codes = W.codes.cpu().numpy()
+    nib = np.empty((K, N), dtype=np.uint32)
+    nib[:, 0::2] = codes & 15
+    nib[:, 1::2] = codes >> 4
+    slot_of_j = [0, 4, 1, 5, 2, 6, 3, 7]
+    words = np.zeros((N, K // 8), dtype=np.uint32)           # channel n, k = 8w..8w+7
+    for j in range(8):
+        words |= nib[j::8, :].T << np.uint32(4 * slot_of_j[j])
+    sc = W.scales.cpu().numpy().astype(np.float16)    # [K][N/64], rounded to nearest even
+    mn = W.mins.cpu().numpy().astype(np.float16)
+    packed = W.packed.cpu().numpy()
+    assert packed.size == K * N // 2 + K * N // 16
+    blocks = packed.reshape(N // 128, K // 64, 4608)
+    for t in range(N // 128):
+        for u in range(K // 64):
+            blk = blocks[t, u]
+            cw = blk[:4096].view(np.uint32).reshape(128, 2, 4)
+            for r in range(128):
+                sw = (r >> 2) & 1
+                for c in range(2):
+                    want = words[128 * t + r, 8 * u + 4 * c: 8 * u + 4 * c + 4]
+                    assert np.array_equal(cw[r, c ^ sw], want), (t, u, r, c)
+            pr = blk[4096:].view(np.float16).reshape(2, 32, 4)
+            for gl in range(2):
+                g = 2 * t + gl
+                ks = slice(64 * u, 64 * u + 64)
+                assert np.array_equal(pr[gl, :, 0].view(np.uint16), sc[ks, g][0::2].view(np.uint16))
+                assert np.array_equal(pr[gl, :, 1].view(np.uint16), sc[ks, g][1::2].view(np.uint16))
+                assert np.array_equal(pr[gl, :, 2].view(np.uint16), mn[ks, g][0::2].view(np.uint16))
+                assert np.array_equal(pr[gl, :, 3].view(np.uint16), mn[ks, g][1::2].view(np.uint16))
