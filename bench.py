@@ -42,6 +42,7 @@ import synth  # noqa: E402
 
 METRIC = "decode tokens/s (OPT-6.7B shape, int4 W+KV); achieved HBM GB/s vs ~8 TB/s"
 Q4 = 0.5 + 8.0 / 64.0   # bytes per element: 4-bit code + fp32 (min, scale) per 64
+Q4_PACKED = 0.5 + 4.0 / 64.0   # the decode copy of a weight: 4-bit code + fp16 (scale, min) per 64
 
 
 def peaks() -> dict:
@@ -118,9 +119,11 @@ class ClockSampler:
 
 def decode_product_bytes(w, b) -> float:
     """One decode step of one layer, all four products: every 4-bit weight
-    once for the whole block plus fp16 activations in, out and residual."""
+    once for the whole block, in the form the decode products read it (the
+    packed copy: 4-bit codes + one fp16 (scale, min) pair per group, Q4_PACKED
+    bytes per weight), plus fp16 activations in, out and residual."""
     h1, h2 = w.h1, w.h2
-    weights = (4 * h1 * h1 + 2 * h1 * h2) * Q4
+    weights = (4 * h1 * h1 + 2 * h1 * h2) * Q4_PACKED
     act = 2 * b * ((h1 + 3 * h1) + (h1 + h1 + h1) + (h1 + h2) + (h2 + h1 + h1))
     return weights + act
 
