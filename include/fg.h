@@ -260,12 +260,14 @@ const char* fg_status_str(fg_status s);
 const char* fg_last_error(void);
 
 /* Launch accounting (measurement support, not part of the method).
- * fg_profile_start(max_launches): from now on every kernel launch of the
- * library gets a pair of CUDA events on its own stream (host-side event
- * objects, no device memory), up to max_launches launches; later launches
- * are counted as dropped.  fg_profile_stop(): waits for the recorded events
- * and accumulates per (phase, kernel class) (FG_ERR_WORKSPACE if launches
- * were dropped).  fg_profile_phase(p), 0 <= p < 4: tags the following
+ * fg_profile_start(max_launches): from now on the library's kernel launches
+ * are timed with CUDA events on their own stream (host-side event objects,
+ * no device memory).  Launches of one class that follow one another on a
+ * stream form one run with one event pair, so that consecutive products
+ * keep their programmatic overlap; up to max_launches runs, later ones are
+ * counted as dropped.  fg_profile_stop(): waits for the recorded events and
+ * accumulates launches and time per (phase, kernel class)
+ * (FG_ERR_WORKSPACE if runs were dropped).  fg_profile_phase(p), 0 <= p < 4: tags the following
  * launches with phase p (0 after start), e.g. prefill vs decode.
  * fg_profile_query(p, i, ...): launches and total milliseconds of class i
  * (0 <= i < fg_profile_kernel_classes()) in phase p, named by

@@ -87,154 +87,32 @@ constexpr uint32_t kMagic = 0x64006400u;   // fp16 1024.0 in both halves
 constexpr uint32_t kLoNib = 0x000F000Fu;   // nibble 0 of bytes 0 and 2
 constexpr uint32_t kHiNib = 0x00F000F0u;   // nibble 1 of bytes 0 and 2 (value x16)
 
+// One 16-token block of the cache (tokens tb .. tb+15, valid below t1) into
+// a warp's running softmax state and output accumulators.
 template <int D>
-__global__ void __launch_bounds__(128) decode_attn_mma_kernel(const DecodeArgs a) {
-  constexpr int NG = D / 64;   // 64-groups per head row
-  constexpr int NT = D / 16;   // m16 tiles of value dims
-  __shared__ float red_m[4], red_l[4];
-  __shared__ float red_o[4][D];
-
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int gq = lane >> 2, tig = lane & 3;
-  const int bh = blockIdx.x / a.splits, sp = blockIdx.x % a.splits;
-  const int64_t bi = bh / a.heads;
-  const int h = bh % a.heads;
-  const int64_t len = a.pos + 1;
-  const int64_t t0 = static_cast<int64_t>(sp) * a.tps;
-  const int64_t t1 = min(len, t0 + a.tps);
-  const int64_t slot0 = static_cast<int64_t>(bh) * a.cap;
-
-  // ---- Concat: quantize the new token's K and V into slot pos -----------------
-  if (a.knew != nullptr && a.pos >= t0 && a.pos < t1) {
-    if (warp == 0) {
-      const int gi = lane >> 3, part = lane & 7;
-      const bool valid = gi < 2 * NG;
-      const int which = gi / NG, grp = gi % NG;
-      float v[8];
-      if (valid) {
-        const __half* src = (which ? a.vnew : a.knew) + bi * a.ldnew + h * D + grp * 64 + part * 8;
-        const uint4 raw = *reinterpret_cast<const uint4*>(src);
-        const __half2* hh = reinterpret_cast<const __half2*>(&raw);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float2 f = __half22float2(hh[i]);
-          v[2 * i] = f.x;
-          v[2 * i + 1] = f.y;
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = 0.0f;
-      }
-      float mn, sc;
-      const uint32_t packed = codec::quantize_group8(v, mn, sc);
-      if (valid) {
-        const int64_t slot = slot0 + a.pos;
-        *reinterpret_cast<uint32_t*>((which ? a.vc : a.kc) + slot * (D / 2) + grp * 32 + part * 4) = packed;
-        if (part == 0) {
-          (which ? a.vmin : a.kmin)[slot * NG + grp] = mn;
-          (which ? a.vscale : a.kscale)[slot * NG + grp] = sc;
-        }
-      }
-    }
-    __syncthreads();
-  }
-
-  // ---- q as B fragments (replicated across the 8 columns) -------------------
-  // lane (gq, tig) supplies k-indices {2tig, 2tig+1, 2tig+8, 2tig+9} of every
-  // k-step; they stand for its own dims: per group, dims 16*tig .. 16*tig+15,
-  // taken from two 32-bit code words as (0,4),(1,5)x16 | (2,6),(3,7)x16.
-  uint32_t qb[NG][4][2];
+struct WarpState {
+  static constexpr int NG = D / 64;
+  static constexpr int NT = D / 16;
+  uint32_t qb[NG][4][2];   // q as B fragments (biased-integer form, see the header)
   float bias[NG], qsum[NG];
-  {
-    const float qscale = 1.4426950408889634f / sqrtf(static_cast<float>(D));
-    const __half* qrow = a.q + bi * a.ldq + h * D;
-#pragma unroll
-    for (int g = 0; g < NG; ++g) {
-      float qv[16];
-      const uint4* src = reinterpret_cast<const uint4*>(qrow + g * 64 + 16 * tig);
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const uint4 raw = src[c];
-        const __half2* hh = reinterpret_cast<const __half2*>(&raw);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float2 f = __half22float2(hh[i]);
-          qv[8 * c + 2 * i] = f.x * qscale;
-          qv[8 * c + 2 * i + 1] = f.y * qscale;
-        }
-      }
-      float bsum = 0.0f, qs = 0.0f;
-#pragma unroll
-      for (int w = 0; w < 2; ++w) {
-        const float* d = qv + 8 * w;
-        qb[g][2 * w][0] = pack_h2(d[0], d[4]);
-        qb[g][2 * w][1] = pack_h2(d[1] * 0.0625f, d[5] * 0.0625f);
-        qb[g][2 * w + 1][0] = pack_h2(d[2], d[6]);
-        qb[g][2 * w + 1][1] = pack_h2(d[3] * 0.0625f, d[7] * 0.0625f);
-#pragma unroll
-        for (int s = 0; s < 2; ++s) {
-          const float2 x = unpack_h2(qb[g][2 * w + s][0]);
-          const float2 y = unpack_h2(qb[g][2 * w + s][1]);
-          bsum += x.x + x.y + y.x + y.y;
-          qs += x.x + x.y + 16.0f * (y.x + y.y);
-        }
-      }
-      bsum += __shfl_xor_sync(0xffffffffu, bsum, 1);
-      bsum += __shfl_xor_sync(0xffffffffu, bsum, 2);
-      qs += __shfl_xor_sync(0xffffffffu, qs, 1);
-      qs += __shfl_xor_sync(0xffffffffu, qs, 2);
-      bias[g] = 1024.0f * bsum;
-      qsum[g] = qs;
-    }
-  }
-
-  // ---- this warp's tokens -------------------------------------------------------
-  const int nblk = static_cast<int>((t1 - t0 + 15) / 16);
-  const int wb0 = warp * nblk / 4, wb1 = (warp + 1) * nblk / 4;
-  float run_m = -INFINITY, run_l = 0.0f;
+  float run_m, run_l;
   float ps[NG], cmn[NG];
   float acc[NT][4];
-#pragma unroll
-  for (int g = 0; g < NG; ++g) ps[g] = cmn[g] = 0.0f;
-#pragma unroll
-  for (int i = 0; i < NT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
+};
 
-  // loads of one 16-token block (issued a block ahead of its use)
-  auto load = [&](int blk, KVBlock<NG>& B) {
-    const int64_t tb = t0 + static_cast<int64_t>(blk) * 16;
-    // K rows of tokens gq and gq+8: per group, 8 bytes at 16*tig dims
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const int64_t tok = tb + gq + 8 * r;
-      const int64_t slot = slot0 + tok;
-#pragma unroll
-      for (int g = 0; g < NG; ++g) {
-        if (tok < t1) {
-          B.kw[r][g] = __ldcs(reinterpret_cast<const uint2*>(a.kc + slot * (D / 2) + g * 32 + 8 * tig));
-          B.ksc[r][g] = a.kscale[slot * NG + g];
-          B.kmn[r][g] = a.kmin[slot * NG + g];
-          B.vsc[r][g] = a.vscale[slot * NG + g];
-          B.vmn[r][g] = a.vmin[slot * NG + g];
-        } else {
-          B.kw[r][g] = make_uint2(0u, 0u);
-          B.ksc[r][g] = B.kmn[r][g] = B.vsc[r][g] = B.vmn[r][g] = 0.0f;
-        }
-      }
-    }
-    // V words of tokens 2tig, 2tig+1, 2tig+8, 2tig+9: per group, 4 bytes at 8*gq dims
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int64_t tok = tb + 2 * tig + (r & 1) + 8 * (r >> 1);
-      const int64_t slot = slot0 + tok;
-#pragma unroll
-      for (int g = 0; g < NG; ++g)
-        B.vw[r][g] =
-            tok < t1 ? __ldcs(reinterpret_cast<const unsigned int*>(a.vc + slot * (D / 2) + g * 32 + 4 * gq)) : 0u;
-    }
-  };
-
-  auto process = [&](int blk, const KVBlock<NG>& B) {
-    const int64_t tb = t0 + static_cast<int64_t>(blk) * 16;
+template <int D>
+__device__ __forceinline__ void process_block(WarpState<D>& W, int64_t tb, int64_t t1, const KVBlock<D / 64>& B,
+                                              int gq, int tig) {
+  constexpr int NG = D / 64;
+  constexpr int NT = D / 16;
+  auto& qb = W.qb;
+  auto& bias = W.bias;
+  auto& qsum = W.qsum;
+  auto& run_m = W.run_m;
+  auto& run_l = W.run_l;
+  auto& ps = W.ps;
+  auto& cmn = W.cmn;
+  auto& acc = W.acc;
     const bool kval[2] = {tb + gq < t1, tb + gq + 8 < t1};
     const auto& kw = B.kw;
     const auto& vw = B.vw;
@@ -307,34 +185,129 @@ __global__ void __launch_bounds__(128) decode_attn_mma_kernel(const DecodeArgs a
 
     // O^T[dim] += sum_t V^T[dim][t] * (p scale)[t]; tile i covers dims
     // 64*(i/4) + 8*gq + 2*(i%4) (+1 for the upper row, scaled x16)
+    // the running max is the same in every lane, and after the first blocks
+    // it rarely moves: the rescale is skipped when it did not
+    if (alpha != 1.0f) {
+#pragma unroll
+      for (int i = 0; i < NT; ++i) {
+        acc[i][0] *= alpha;
+        acc[i][1] *= alpha;
+        acc[i][2] *= alpha;
+        acc[i][3] *= alpha;
+      }
+    }
 #pragma unroll
     for (int i = 0; i < NT; ++i) {
       const int g = i / 4, ii = i % 4;
-      acc[i][0] *= alpha;
-      acc[i][1] *= alpha;
-      acc[i][2] *= alpha;
-      acc[i][3] *= alpha;
       const uint32_t sel = static_cast<uint32_t>(ii) | (static_cast<uint32_t>(ii + 4) << 8);
       const uint32_t x01 = __byte_perm(vw[0][g], vw[1][g], sel);
       const uint32_t x89 = __byte_perm(vw[2][g], vw[3][g], sel);
       mma16816(acc[i], lop_mask_or(x01, kLoNib, kMagic), lop_mask_or(x01, kHiNib, kMagic),
                lop_mask_or(x89, kLoNib, kMagic), lop_mask_or(x89, kHiNib, kMagic), vb[g][0], vb[g][1]);
     }
-  };
+}
 
-  // two block buffers: the next block's loads are in flight while this one computes
-  KVBlock<NG> buf0, buf1;
-  if (wb0 < wb1) load(wb0, buf0);
-  for (int blk = wb0; blk < wb1; blk += 2) {
-    if (blk + 1 < wb1) load(blk + 1, buf1);
-    process(blk, buf0);
-    if (blk + 1 >= wb1) break;
-    if (blk + 2 < wb1) load(blk + 2, buf0);
-    process(blk + 1, buf1);
+// Concat: warp 0 quantizes the new token's K and V rows into slot pos
+// (8 lanes per 64-group, the codec's rounding).
+template <int D>
+__device__ __forceinline__ void append_token(const DecodeArgs& a, int64_t slot0, int64_t bi, int h, int lane) {
+  constexpr int NG = D / 64;
+  const int gi = lane >> 3, part = lane & 7;
+  const bool valid = gi < 2 * NG;
+  const int which = gi / NG, grp = gi % NG;
+  float v[8];
+  if (valid) {
+    const __half* src = (which ? a.vnew : a.knew) + bi * a.ldnew + h * D + grp * 64 + part * 8;
+    const uint4 raw = *reinterpret_cast<const uint4*>(src);
+    const __half2* hh = reinterpret_cast<const __half2*>(&raw);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __half22float2(hh[i]);
+      v[2 * i] = f.x;
+      v[2 * i + 1] = f.y;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = 0.0f;
   }
+  float mn, sc;
+  const uint32_t packed = codec::quantize_group8(v, mn, sc);
+  if (valid) {
+    const int64_t slot = slot0 + a.pos;
+    *reinterpret_cast<uint32_t*>((which ? a.vc : a.kc) + slot * (D / 2) + grp * 32 + part * 4) = packed;
+    if (part == 0) {
+      (which ? a.vmin : a.kmin)[slot * NG + grp] = mn;
+      (which ? a.vscale : a.kscale)[slot * NG + grp] = sc;
+    }
+  }
+}
 
-  // ---- merge the 4 warps --------------------------------------------------------
-  if (tig == 0) {
+// q of one (sequence, head) as this lane's B fragments: lane (gq, tig)
+// supplies k-indices {2tig, 2tig+1, 2tig+8, 2tig+9} of every k-step; they
+// stand for its own dims: per group, dims 16*tig .. 16*tig+15, taken from two
+// 32-bit code words as (0,4),(1,5)x16 | (2,6),(3,7)x16.
+template <int D>
+__device__ __forceinline__ void setup_q(WarpState<D>& W, const __half* qrow, int tig) {
+  constexpr int NG = D / 64;
+  auto& qb = W.qb;
+  auto& bias = W.bias;
+  auto& qsum = W.qsum;
+  {
+    const float qscale = 1.4426950408889634f / sqrtf(static_cast<float>(D));
+#pragma unroll
+    for (int g = 0; g < NG; ++g) {
+      float qv[16];
+      const uint4* src = reinterpret_cast<const uint4*>(qrow + g * 64 + 16 * tig);
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const uint4 raw = src[c];
+        const __half2* hh = reinterpret_cast<const __half2*>(&raw);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 f = __half22float2(hh[i]);
+          qv[8 * c + 2 * i] = f.x * qscale;
+          qv[8 * c + 2 * i + 1] = f.y * qscale;
+        }
+      }
+      float bsum = 0.0f, qs = 0.0f;
+#pragma unroll
+      for (int w = 0; w < 2; ++w) {
+        const float* d = qv + 8 * w;
+        qb[g][2 * w][0] = pack_h2(d[0], d[4]);
+        qb[g][2 * w][1] = pack_h2(d[1] * 0.0625f, d[5] * 0.0625f);
+        qb[g][2 * w + 1][0] = pack_h2(d[2], d[6]);
+        qb[g][2 * w + 1][1] = pack_h2(d[3] * 0.0625f, d[7] * 0.0625f);
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+          const float2 x = unpack_h2(qb[g][2 * w + s][0]);
+          const float2 y = unpack_h2(qb[g][2 * w + s][1]);
+          bsum += x.x + x.y + y.x + y.y;
+          qs += x.x + x.y + 16.0f * (y.x + y.y);
+        }
+      }
+      bsum += __shfl_xor_sync(0xffffffffu, bsum, 1);
+      bsum += __shfl_xor_sync(0xffffffffu, bsum, 2);
+      qs += __shfl_xor_sync(0xffffffffu, qs, 1);
+      qs += __shfl_xor_sync(0xffffffffu, qs, 2);
+      bias[g] = 1024.0f * bsum;
+      qsum[g] = qs;
+    }
+  }
+}
+
+// Merge the 4 attention warps of a CTA (shared red_*), then write the result
+// (one split) or this split's partial (several).  Every thread of the CTA
+// calls it (it holds a CTA barrier); only attention warps stash.
+template <int D>
+__device__ __forceinline__ void merge_warps(const WarpState<D>& W, float* red_m, float* red_l, float (*red_o)[D],
+                                            const DecodeArgs& a, int64_t bi, int h, int bh, int sp, int warp,
+                                            int lane, int gq, int tig, bool stash = true) {
+  constexpr int NT = D / 16;
+  const auto& acc = W.acc;
+  const auto& ps = W.ps;
+  const auto& cmn = W.cmn;
+  const float run_m = W.run_m, run_l = W.run_l;
+  if (stash && tig == 0) {
 #pragma unroll
     for (int i = 0; i < NT; ++i) {
       const int g = i / 4, ii = i % 4;
@@ -343,7 +316,7 @@ __global__ void __launch_bounds__(128) decode_attn_mma_kernel(const DecodeArgs a
       red_o[warp][dim + 1] = (acc[i][2] - 1024.0f * ps[g]) * 0.0625f + cmn[g];
     }
   }
-  if (lane == 0) {
+  if (stash && lane == 0) {
     red_m[warp] = run_m;
     red_l[warp] = run_l;
   }
@@ -369,6 +342,100 @@ __global__ void __launch_bounds__(128) decode_attn_mma_kernel(const DecodeArgs a
       }
     }
   }
+}
+
+template <int D>
+__global__ void __launch_bounds__(128) decode_attn_mma_kernel(const DecodeArgs a) {
+  constexpr int NG = D / 64;   // 64-groups per head row
+  constexpr int NT = D / 16;   // m16 tiles of value dims
+  __shared__ float red_m[4], red_l[4];
+  __shared__ float red_o[4][D];
+
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int gq = lane >> 2, tig = lane & 3;
+  const int bh = blockIdx.x / a.splits, sp = blockIdx.x % a.splits;
+  const int64_t bi = bh / a.heads;
+  const int h = bh % a.heads;
+  const int64_t len = a.pos + 1;
+  const int64_t t0 = static_cast<int64_t>(sp) * a.tps;
+  const int64_t t1 = min(len, t0 + a.tps);
+  const int64_t slot0 = static_cast<int64_t>(bh) * a.cap;
+
+  // ---- Concat: quantize the new token's K and V into slot pos -----------------
+  if (a.knew != nullptr && a.pos >= t0 && a.pos < t1) {
+    if (warp == 0) append_token<D>(a, slot0, bi, h, lane);
+    __syncthreads();
+  }
+
+  // ---- q as B fragments ---------------------------------------------------------
+  WarpState<D> W;
+  setup_q<D>(W, a.q + bi * a.ldq + h * D, tig);
+
+  // ---- this warp's tokens -------------------------------------------------------
+  const int nblk = static_cast<int>((t1 - t0 + 15) / 16);
+  const int wb0 = warp * nblk / 4, wb1 = (warp + 1) * nblk / 4;
+  auto& run_m = W.run_m;
+  auto& run_l = W.run_l;
+  auto& ps = W.ps;
+  auto& cmn = W.cmn;
+  auto& acc = W.acc;
+  run_m = -INFINITY;
+  run_l = 0.0f;
+#pragma unroll
+  for (int g = 0; g < NG; ++g) ps[g] = cmn[g] = 0.0f;
+#pragma unroll
+  for (int i = 0; i < NT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
+
+  // loads of one 16-token block (issued a block ahead of its use)
+  auto load = [&](int blk, KVBlock<NG>& B) {
+    const int64_t tb = t0 + static_cast<int64_t>(blk) * 16;
+    // K rows of tokens gq and gq+8: per group, 8 bytes at 16*tig dims
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int64_t tok = tb + gq + 8 * r;
+      const int64_t slot = slot0 + tok;
+#pragma unroll
+      for (int g = 0; g < NG; ++g) {
+        if (tok < t1) {
+          B.kw[r][g] = __ldcs(reinterpret_cast<const uint2*>(a.kc + slot * (D / 2) + g * 32 + 8 * tig));
+          B.ksc[r][g] = a.kscale[slot * NG + g];
+          B.kmn[r][g] = a.kmin[slot * NG + g];
+          B.vsc[r][g] = a.vscale[slot * NG + g];
+          B.vmn[r][g] = a.vmin[slot * NG + g];
+        } else {
+          B.kw[r][g] = make_uint2(0u, 0u);
+          B.ksc[r][g] = B.kmn[r][g] = B.vsc[r][g] = B.vmn[r][g] = 0.0f;
+        }
+      }
+    }
+    // V words of tokens 2tig, 2tig+1, 2tig+8, 2tig+9: per group, 4 bytes at 8*gq dims
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int64_t tok = tb + 2 * tig + (r & 1) + 8 * (r >> 1);
+      const int64_t slot = slot0 + tok;
+#pragma unroll
+      for (int g = 0; g < NG; ++g)
+        B.vw[r][g] =
+            tok < t1 ? __ldcs(reinterpret_cast<const unsigned int*>(a.vc + slot * (D / 2) + g * 32 + 4 * gq)) : 0u;
+    }
+  };
+
+  auto process = [&](int blk, const KVBlock<NG>& B) {
+    process_block<D>(W, t0 + static_cast<int64_t>(blk) * 16, t1, B, gq, tig);
+  };
+
+  // two block buffers: the next block's loads are in flight while this one computes
+  KVBlock<NG> buf0, buf1;
+  if (wb0 < wb1) load(wb0, buf0);
+  for (int blk = wb0; blk < wb1; blk += 2) {
+    if (blk + 1 < wb1) load(blk + 1, buf1);
+    process(blk, buf0);
+    if (blk + 1 >= wb1) break;
+    if (blk + 2 < wb1) load(blk + 2, buf0);
+    process(blk + 1, buf1);
+  }
+
+  merge_warps<D>(W, red_m, red_l, red_o, a, bi, h, bh, sp, warp, lane, gq, tig);
 }
 
 // Merge the token splits of each (sequence, head).

@@ -62,44 +62,62 @@ const char* const kClassNames[KC_COUNT] = {
     "gemm_splitk_reduce", "attn_decode", "attn_decode_combine", "attn_prefill", "gemm_q4_decode",
     "pack_weight"};
 
+// Launches of the same class that follow one another on a stream form one
+// timed run (one event pair): events between them would break the overlap
+// that programmatic dependent launch gives consecutive products, and add each
+// launch's gap to its time.  A run ends at the next launch of another class,
+// at a phase change and at fg_profile_stop.
 struct Profiler {
   std::mutex mu;
   bool on = false;
-  std::vector<cudaEvent_t> ev;   // 2 per launch
-  std::vector<int> cls;          // class + KC_COUNT * phase
+  std::vector<cudaEvent_t> ev;   // 2 per run
+  std::vector<int> cls;          // class + KC_COUNT * phase, per run
+  std::vector<int64_t> count;    // launches per run
   size_t used = 0;
   int64_t dropped = 0;
   int phase = 0;
+  int open = -1;                 // run still accepting launches
+  cudaStream_t open_st = nullptr;
   int64_t launches[kProfilePhases * KC_COUNT] = {0};
   double ms[kProfilePhases * KC_COUNT] = {0};
 };
 Profiler g_prof;
 std::atomic<uint64_t> g_launches{0};
-thread_local int t_open_slot = -1;
+
+void close_run_locked() {
+  if (g_prof.open >= 0) {
+    cudaEventRecord(g_prof.ev[2 * g_prof.open + 1], g_prof.open_st);
+    g_prof.open = -1;
+  }
+}
 }  // namespace
 
 void trace_begin(int c, cudaStream_t st) {
   g_launches.fetch_add(1, std::memory_order_relaxed);
-  t_open_slot = -1;
   if (!g_prof.on) return;
   std::lock_guard<std::mutex> lk(g_prof.mu);
   if (!g_prof.on) return;
+  const int key = c + KC_COUNT * g_prof.phase;
+  if (g_prof.open >= 0 && g_prof.cls[g_prof.open] == key && g_prof.open_st == st) {
+    ++g_prof.count[g_prof.open];
+    return;
+  }
+  close_run_locked();
   if (g_prof.used >= g_prof.cls.size()) {
     ++g_prof.dropped;
     return;
   }
   const size_t i = g_prof.used++;
-  g_prof.cls[i] = c + KC_COUNT * g_prof.phase;
+  g_prof.cls[i] = key;
+  g_prof.count[i] = 1;
   cudaEventRecord(g_prof.ev[2 * i], st);
-  t_open_slot = static_cast<int>(i);
+  g_prof.open = static_cast<int>(i);
+  g_prof.open_st = st;
 }
 
 void trace_end(int c, cudaStream_t st) {
   (void)c;
-  if (t_open_slot < 0) return;
-  std::lock_guard<std::mutex> lk(g_prof.mu);
-  cudaEventRecord(g_prof.ev[2 * t_open_slot + 1], st);
-  t_open_slot = -1;
+  (void)st;   // runs are closed by the next launch of another class
 }
 
 }  // namespace fg
@@ -118,6 +136,8 @@ fg_status fg_profile_start(int32_t max_launches) {
     g_prof.ev.push_back(e);
   }
   g_prof.cls.assign(max_launches, 0);
+  g_prof.count.assign(max_launches, 0);
+  g_prof.open = -1;
   g_prof.used = 0;
   g_prof.dropped = 0;
   for (int i = 0; i < fg::kProfilePhases * fg::KC_COUNT; ++i) {
@@ -133,13 +153,14 @@ fg_status fg_profile_stop(void) {
   using fg::g_prof;
   std::lock_guard<std::mutex> lk(g_prof.mu);
   if (!g_prof.on) return fg::fail(FG_ERR_ARG, "profiling not active");
+  fg::close_run_locked();
   g_prof.on = false;
   for (size_t i = 0; i < g_prof.used; ++i) {
     float ms = 0.f;
     if (cudaEventSynchronize(g_prof.ev[2 * i + 1]) != cudaSuccess ||
         cudaEventElapsedTime(&ms, g_prof.ev[2 * i], g_prof.ev[2 * i + 1]) != cudaSuccess)
       return fg::fail(FG_ERR_CUDA, "event timing");
-    g_prof.launches[g_prof.cls[i]] += 1;
+    g_prof.launches[g_prof.cls[i]] += g_prof.count[i];
     g_prof.ms[g_prof.cls[i]] += ms;
   }
   return g_prof.dropped ? fg::fail(FG_ERR_WORKSPACE, "%lld launches not timed (pool full)",
@@ -156,6 +177,7 @@ const char* fg_profile_kernel_name(int32_t i) {
 fg_status fg_profile_phase(int32_t phase) {
   if (phase < 0 || phase >= fg::kProfilePhases) return fg::fail(FG_ERR_ARG, "phase");
   std::lock_guard<std::mutex> lk(fg::g_prof.mu);
+  fg::close_run_locked();
   fg::g_prof.phase = phase;
   return FG_OK;
 }

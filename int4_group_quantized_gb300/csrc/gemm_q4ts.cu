@@ -143,11 +143,18 @@ struct TsParams {
 constexpr int cmin(int a, int b) { return a < b ? a : b; }
 constexpr int cmax(int a, int b) { return a > b ? a : b; }
 
-// Three rings, each released by the stage that last needs it, so that a slow
-// stage never holds back the requests of another: weights (released once the
-// dequantization warps hold them in registers), X (released by the MMAs that
-// read it) and TMEM A slots (released by the MMAs).  Ring depths follow what
-// each must cover: HBM latency for the weights, L2 latency for X.
+// Rings, each released by the stage that last needs it: weights (released
+// once the dequantization warps hold them in registers; deep, to cover HBM
+// latency) and slots (an X tile in shared memory plus its TMEM A slot, both
+// released by the commit of the MMAs that read them).
+//
+// The issuing thread synchronises rarely: any acquire-ordered check it makes
+// (an mbarrier wait, an acquire load) stalls it behind its MMAs in flight
+// (~250 cycles each on this GPU, against ~50 cycles per 128x64x16 MMA).  So
+// the dequantization warps also wait for the X tile, then publish "slot
+// ready" with a release add on a per-slot counter, and the issuing thread
+// checks readiness once per batch of kBatch k tiles (the last tile of each
+// group: a group finishes its tiles in order).
 template <int BT, int RB>
 struct TsCfg {
   static constexpr int kThreads = 128 + kGroups * 4 * RB * 32;   // warps 0..3, then the dequant groups
@@ -158,22 +165,41 @@ struct TsCfg {
   static constexpr uint32_t kTmemCols = (RB == 1 && BT <= 128) ? 256 : 512;
   static constexpr int kMinBlocks = kTmemCols == 256 ? 2 : 1;
   static constexpr int kBudget = kMinBlocks == 2 ? 104 * 1024 : 204 * 1024;
-  static constexpr int kAStages = cmin((static_cast<int>(kTmemCols) - RB * kAcc) / (32 * RB), 8);
-  static constexpr int kXStages = cmax(2, cmin(6, (kBudget / 2) / kX));
-  static constexpr int kWStages = cmin(16, (kBudget - kXStages * kX) / kW);
-  static constexpr int kXBytes = kXStages * kX;
+  static constexpr int kSlots = cmin(cmin((static_cast<int>(kTmemCols) - RB * kAcc) / (32 * RB),
+                                          cmax(2, (kBudget / 2) / kX)), 8);
+  static constexpr int kBatch = cmax(1, cmin(4, kSlots - 2));
+  static constexpr int kWStages = cmin(16, (kBudget - kSlots * kX) / kW);
+  static constexpr int kXBytes = kSlots * kX;
   static constexpr int kWBytes = kWStages * kW;
-  static constexpr int kBarBytes = (2 * (kXStages + kWStages + kAStages) + 2) * 8 + 16;   // + done, red
+  static constexpr int kBarBytes = (2 * (kSlots + kWStages) + 2) * 8 + kSlots * 4 + 16;   // + done, red, counters
   static constexpr int kTotal = 1024 + kXBytes + kWBytes + kBarBytes;
-  static_assert(kAStages >= 2 && kWStages >= 2, "pipeline needs two stages");
-  static_assert(kX % 1024 == 0, "X stages stay 1024-byte aligned");
+  static_assert(kSlots >= 2 && kWStages >= 2, "pipeline needs two stages");
+  static_assert(kX % 1024 == 0, "X slots stay 1024-byte aligned");
 };
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+  return v;
+}
+__device__ __forceinline__ void add_release_u32(uint32_t* p, uint32_t v) {
+  asm volatile("red.release.cta.shared::cta.add.u32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
+}
+// Waits until *p >= target (acquire), bounded like the mbarrier waits.
+__device__ __forceinline__ bool wait_count(const uint32_t* p, uint32_t target, volatile int* abort) {
+  for (uint32_t i = 0; i < kWaitLimit; ++i) {
+    if (static_cast<int32_t>(ld_acquire_u32(p) - target) >= 0) return true;
+    if ((i & 1023u) == 1023u && *abort) return false;
+  }
+  *abort = 1;
+  return false;
+}
 
 template <int BT, int RB>
 __global__ void __launch_bounds__(TsCfg<BT, RB>::kThreads, TsCfg<BT, RB>::kMinBlocks)
     gemm_q4ts_kernel(const __grid_constant__ TsParams p) {
   using C = TsCfg<BT, RB>;
-  constexpr int SX = C::kXStages, SW = C::kWStages, SA = C::kAStages;
+  constexpr int SL = C::kSlots, SW = C::kWStages;
   constexpr int kGW = C::kGroupWarps;
   constexpr uint32_t kIdesc = idesc_f16(128, BT, 0, 0);   // A (TMEM) and B (X) K-major
   constexpr uint32_t kACol = RB * C::kAcc;                // TMEM A slots follow the accumulators
@@ -182,13 +208,12 @@ __global__ void __launch_bounds__(TsCfg<BT, RB>::kThreads, TsCfg<BT, RB>::kMinBl
   uint8_t* xring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* wring = xring + C::kXBytes;
   uint64_t* xfull = reinterpret_cast<uint64_t*>(wring + C::kWBytes);
-  uint64_t* xempty = xfull + SX;
-  uint64_t* wfull = xempty + SX;
+  uint64_t* consumed = xfull + SL;   // slot s read by its MMAs (X tile and TMEM A slot)
+  uint64_t* wfull = consumed + SL;
   uint64_t* wempty = wfull + SW;
-  uint64_t* afull = wempty + SW;
-  uint64_t* aempty = afull + SA;
-  uint64_t* done = aempty + SA;   // done + 1: the reduction barrier of the split-K epilogue
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 2);
+  uint64_t* done = wempty + SW;      // done + 1: the reduction barrier of the split-K epilogue
+  uint32_t* ready = reinterpret_cast<uint32_t*>(done + 2);   // [SL] warps that finished slot s, cumulative
+  uint32_t* tmem_slot = ready + SL;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* last_flag = abort_flag + 1;
 
@@ -206,17 +231,14 @@ __global__ void __launch_bounds__(TsCfg<BT, RB>::kThreads, TsCfg<BT, RB>::kMinBl
   griddep_launch();   // a dependent grid waits for this one before it reads Y
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < SX; ++i) {
+    for (int i = 0; i < SL; ++i) {
       mbar_init(&xfull[i], 1);
-      mbar_init(&xempty[i], 1);      // the MMA commit
+      mbar_init(&consumed[i], 1);    // the MMA commit
+      ready[i] = 0;
     }
     for (int i = 0; i < SW; ++i) {
       mbar_init(&wfull[i], 1);
       mbar_init(&wempty[i], kGW);    // one arrival per warp of the converting group
-    }
-    for (int i = 0; i < SA; ++i) {
-      mbar_init(&afull[i], kGW);
-      mbar_init(&aempty[i], 1);      // the MMA commit
     }
     mbar_init(done, 1);
     *abort_flag = 0;
@@ -257,40 +279,43 @@ __global__ void __launch_bounds__(TsCfg<BT, RB>::kThreads, TsCfg<BT, RB>::kMinBl
       griddep_wait();   // X comes from the previous kernel
       int issued = 0;
       for (int i = 0; i < nk; ++i) {
-        const int s = i % SX;
-        if (!mbar_wait(&xempty[s], ((i / SX) & 1) ^ 1, kWaitLimit, abort_flag)) break;
+        const int s = i % SL;
+        if (!mbar_wait(&consumed[s], ((i / SL) & 1) ^ 1, kWaitLimit, abort_flag)) break;
         mbar_expect_tx(&xfull[s], C::kX);
         tma_load_2d(xring + s * C::kX, &p.mapX, (kt0 + i) * BK, 0, &xfull[s]);
         ++issued;
       }
-      for (int i = max(0, issued - SX); i < issued; ++i) {
+      for (int i = max(0, issued - SL); i < issued; ++i) {
         volatile int dummy = 0;
-        mbar_wait(&xfull[i % SX], (i / SX) & 1, kWaitLimit, &dummy);
+        mbar_wait(&xfull[i % SL], (i / SL) & 1, kWaitLimit, &dummy);
       }
       if (*abort_flag) atomicOr(p.err, DEV_ERR_WAIT_TIMEOUT);
     }
   } else if (warp == 1) {
     if (lane == 0) {
       bool ok = true;
-      for (int i = 0; i < nk && ok; ++i) {
-        const int sx = i % SX, sa = i % SA;
-        ok = mbar_wait(&xfull[sx], (i / SX) & 1, kWaitLimit, abort_flag) &&
-             mbar_wait(&afull[sa], (i / SA) & 1, kWaitLimit, abort_flag);
+      for (int i = 0; i < nk && ok; i += C::kBatch) {
+        const int n = min(C::kBatch, nk - i);
+        // the last tile of each group in the batch; earlier ones of a group are done before it
+        for (int j = max(i, i + n - kGroups); j < i + n && ok; ++j)
+          ok = wait_count(&ready[j % SL], static_cast<uint32_t>(kGW * (j / SL + 1)), abort_flag);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t xa = smem_u32(xring + sx * C::kX);
+        for (int j = i; j < i + n; ++j) {
+          const int s = j % SL;
+          const uint32_t xa = smem_u32(xring + s * C::kX);
 #pragma unroll
-        for (int rb = 0; rb < RB; ++rb) {
-          const uint32_t ta = tmem_base + kACol + 32u * (sa * RB + rb);
+          for (int rb = 0; rb < RB; ++rb) {
+            const uint32_t ta = tmem_base + kACol + 32u * (s * RB + rb);
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            // B (X): K-major, 8-row groups 1 KiB apart; +32 bytes per 16-wide k step
-            const uint64_t bdesc = smem_desc_sw128(xa + kk * 32, 16, 1024);
-            mma_f16_ts(tmem_base + rb * C::kAcc, ta + 8u * kk, bdesc, kIdesc, (i > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < BK / 16; ++kk) {
+              // B (X): K-major, 8-row groups 1 KiB apart; +32 bytes per 16-wide k step
+              const uint64_t bdesc = smem_desc_sw128(xa + kk * 32, 16, 1024);
+              mma_f16_ts(tmem_base + rb * C::kAcc, ta + 8u * kk, bdesc, kIdesc, (j > 0 || kk > 0) ? 1u : 0u);
+            }
           }
+          mma_commit(&consumed[s]);
         }
-        mma_commit(&xempty[sx]);
-        mma_commit(&aempty[sa]);
       }
       mma_commit(done);
       if (!ok) atomicOr(p.err, DEV_ERR_WAIT_TIMEOUT);
@@ -305,9 +330,9 @@ __global__ void __launch_bounds__(TsCfg<BT, RB>::kThreads, TsCfg<BT, RB>::kMinBl
     const uint32_t trow = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + kACol + 32u * rb;
     bool ok = true;
     for (int i = grp; i < nk && ok; i += kGroups) {
-      const int s = i % SW, sa = i % SA;
+      const int s = i % SW, sl = i % SL;
       ok = mbar_wait(&wfull[s], (i / SW) & 1, kWaitLimit, abort_flag) &&
-           mbar_wait(&aempty[sa], ((i / SA) & 1) ^ 1, kWaitLimit, abort_flag);
+           mbar_wait(&consumed[sl], ((i / SL) & 1) ^ 1, kWaitLimit, abort_flag);
       ok = __all_sync(0xffffffffu, ok);   // the warp-wide tcgen05.st below needs every lane
       if (!ok) break;
       tc_fence_after();
@@ -333,12 +358,15 @@ __global__ void __launch_bounds__(TsCfg<BT, RB>::kThreads, TsCfg<BT, RB>::kMinBl
           __syncwarp();
           if (lane == 0) mbar_arrive(&wempty[s]);   // this k tile's codes and pairs are in registers
         }
-        tmem_st_32x32b_x16(trow + 32u * RB * sa + 16u * h, a);
+        tmem_st_32x32b_x16(trow + 32u * RB * sl + 16u * h, a);
       }
+      // the X tile of this slot has landed too, then the slot is ready for the MMAs
+      ok = __all_sync(0xffffffffu, mbar_wait(&xfull[sl], (i / SL) & 1, kWaitLimit, abort_flag));
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&afull[sa]);
+      if (lane == 0) add_release_u32(&ready[sl], 1u);
+      if (!ok) break;
     }
   }
 

@@ -31,6 +31,9 @@ CASES = [
     (1, 1, 64, 1, 8, True, torch.float16),         # a single cached token
     (2, 2, 64, 37, 40, True, torch.float32),       # fp32 activations: CUDA-core kernel
     (2, 2, 128, 37, 40, False, torch.float16),     # uncompressed cache
+    (4, 2, 128, 333, 333, True, torch.float16),    # capacity not a multiple of 4: register-block kernel
+    (2, 3, 128, 70, 72, True, torch.float16),      # ragged last chunk of the shared-memory ring
+    (1, 2, 128, 1000, 1024, True, torch.float16),  # 16 token splits of 64, one ring chunk each
 ]
 
 
