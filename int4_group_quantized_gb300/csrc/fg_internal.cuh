@@ -45,6 +45,9 @@ enum KernelClass : int {
 constexpr int kProfilePhases = 4;
 void trace_begin(int cls, cudaStream_t st);
 void trace_end(int cls, cudaStream_t st);
+// A second kernel launched inside a Trace scope, timed as part of that
+// scope's launch (only the launch counter sees it).
+void trace_extra_launch();
 struct Trace {
   int cls;
   cudaStream_t st;

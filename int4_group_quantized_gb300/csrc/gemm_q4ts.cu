@@ -62,13 +62,6 @@ constexpr int kDqWarp0 = 4;            // dequantization warps start here
 constexpr int kGroups = 2;             // groups of dequantization warps, alternate k tiles
 constexpr uint32_t kWaitLimit = 1u << 24;
 
-// Split-K tickets: kSlices slices of one counter per 128-channel tile; each
-// launch takes the next slice, so launches in flight at the same time (up to
-// kSlices across all streams of a device) never share a counter.
-constexpr int kSlices = 64;
-constexpr int kSliceTiles = 1024;
-__device__ unsigned int g_tickets[kSlices * kSliceTiles];   // zero at load; reset by each tile's last CTA
-
 // ---- packing -------------------------------------------------------------------
 // The decode copy is one 4608-byte block per (128-channel tile nt, 64-k tile
 // kt), blocks in order nt-major, so a CTA streams one contiguous run of HBM
@@ -136,7 +129,6 @@ struct TsParams {
   int ldr;
   int relu;
   float* part;              // [splits][M][N] fp32 when splits > 1
-  unsigned int* tickets;    // [n_tiles] of this launch's slice
   unsigned int* err;
 };
 
@@ -171,7 +163,7 @@ struct TsCfg {
   static constexpr int kWStages = cmin(16, (kBudget - kSlots * kX) / kW);
   static constexpr int kXBytes = kSlots * kX;
   static constexpr int kWBytes = kWStages * kW;
-  static constexpr int kBarBytes = (2 * (kSlots + kWStages) + 2) * 8 + kSlots * 4 + 16;   // + done, red, counters
+  static constexpr int kBarBytes = (2 * (kSlots + kWStages) + 1) * 8 + kSlots * 4 + 16;   // + done, counters
   static constexpr int kTotal = 1024 + kXBytes + kWBytes + kBarBytes;
   static_assert(kSlots >= 2 && kWStages >= 2, "pipeline needs two stages");
   static_assert(kX % 1024 == 0, "X slots stay 1024-byte aligned");
@@ -211,11 +203,10 @@ __global__ void __launch_bounds__(TsCfg<BT, RB>::kThreads, TsCfg<BT, RB>::kMinBl
   uint64_t* consumed = xfull + SL;   // slot s read by its MMAs (X tile and TMEM A slot)
   uint64_t* wfull = consumed + SL;
   uint64_t* wempty = wfull + SW;
-  uint64_t* done = wempty + SW;      // done + 1: the reduction barrier of the split-K epilogue
-  uint32_t* ready = reinterpret_cast<uint32_t*>(done + 2);   // [SL] warps that finished slot s, cumulative
+  uint64_t* done = wempty + SW;
+  uint32_t* ready = reinterpret_cast<uint32_t*>(done + 1);   // [SL] warps that finished slot s, cumulative
   uint32_t* tmem_slot = ready + SL;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  volatile int* last_flag = abort_flag + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int split = blockIdx.x % p.splits;
@@ -414,10 +405,9 @@ __global__ void __launch_bounds__(TsCfg<BT, RB>::kThreads, TsCfg<BT, RB>::kMinBl
     return;
   }
 
-  // K splits.  Each split's partial, [M][NCH] fp32, goes to its own contiguous
-  // block of the workspace with one bulk copy from the drained rings; the
-  // tile's last CTA brings all blocks back the same way and sums them in
-  // split order.
+  // K splits: each split's partial, [M][NCH] fp32, goes to its own
+  // contiguous block of the workspace with one bulk copy from the drained
+  // rings; splitk_sum_kernel, the next launch, sums the blocks in split order.
   float* stage = reinterpret_cast<float*>(xring);   // the rings are free: every load and MMA is done
   const size_t blk = static_cast<size_t>(p.M) * NCH;   // floats per partial block
   float* myblk = p.part + (static_cast<size_t>(split) * p.n_tiles + nt) * blk;
@@ -442,91 +432,54 @@ __global__ void __launch_bounds__(TsCfg<BT, RB>::kThreads, TsCfg<BT, RB>::kMinBl
   if (threadIdx.x == 0) {
     bulk_store(myblk, stage, static_cast<uint32_t>(blk * 4));
     bulk_commit();
-    bulk_wait_all();
-    fence_proxy_async_global();
-    __threadfence();   // this split's partial before its ticket
-    *last_flag = atomicAdd(&p.tickets[nt], 1u) == static_cast<unsigned>(p.splits - 1);
+    bulk_wait_all();   // complete before the CTA (and its shared memory) goes away
   }
-  __syncthreads();
-  if (!*last_flag) return;
+}
 
-  // The tile's last CTA.  Rows are taken in chunks small enough that the
-  // rings hold at least three chunk slots; per chunk, rounds bring as many
-  // splits as the slots hold, slot 0 keeping the running sum (split order).
-  constexpr int kRing = C::kXBytes + C::kWBytes;
-  const int rc = min(p.M, kRing / (3 * NCH * 4));      // rows per chunk
-  const int slots = kRing / (rc * NCH * 4);              // >= 3
-  const size_t slot_f = static_cast<size_t>(rc) * NCH;   // floats per slot
-  uint64_t* red = done + 1;
-  if (threadIdx.x == 0) {
-    mbar_init(red, 1);
-    mbar_fence_init();
-    __threadfence();            // every split's partial is visible to this CTA
-    fence_proxy_async_global();
-  }
-  __syncthreads();
-  uint32_t phase = 0;
-  bool good = true;
-  for (int m0 = 0; m0 < p.M && good; m0 += rc) {
-    const int rows = min(rc, p.M - m0);
-    const uint32_t bytes = static_cast<uint32_t>(rows) * NCH * 4;
-    const int nf4 = rows * NCH / 4;
-    for (int s0 = 0; s0 < p.splits && good;) {
-      const int first = s0 == 0 ? 0 : 1;                 // later rounds keep slot 0
-      const int n = min(p.splits - s0, slots - first);
-      if (threadIdx.x == 0) {
-        mbar_expect_tx(red, bytes * n);
-        for (int j = 0; j < n; ++j)
-          bulk_load(stage + (first + j) * slot_f,
-                    p.part + (static_cast<size_t>(s0 + j) * p.n_tiles + nt) * blk + static_cast<size_t>(m0) * NCH,
-                    bytes, red);
-      }
-      good = __syncthreads_and(mbar_wait(red, phase, kWaitLimit, abort_flag) ? 1 : 0) != 0;   // uniform
-      phase ^= 1;
-      if (!good) {
-        if (threadIdx.x == 0) atomicOr(p.err, DEV_ERR_WAIT_TIMEOUT);
-        break;
-      }
-      for (int e = threadIdx.x; e < nf4; e += C::kThreads) {
-        float4 a4 = reinterpret_cast<const float4*>(stage)[e];
-        for (int j = 1; j < first + n; ++j) {
-          const float4 v = reinterpret_cast<const float4*>(stage + j * slot_f)[e];
-          a4.x += v.x;
-          a4.y += v.y;
-          a4.z += v.z;
-          a4.w += v.w;
-        }
-        reinterpret_cast<float4*>(stage)[e] = a4;
-      }
-      __syncthreads();   // slot 0 complete; the other slots may be refilled
-      s0 += n;
+// Y = epilogue(sum of the K splits' partial blocks in split order), over the
+// whole GPU.  Launched right after gemm_q4ts_kernel with programmatic stream
+// serialization: it may be scheduled early and waits for the partials.
+__global__ void __launch_bounds__(256) splitk_sum_kernel(const float* __restrict__ part, int splits, int M, int N,
+                                                         int nch, int n_tiles, const __half* __restrict__ R,
+                                                         int ldr, int relu, __half* __restrict__ Y, int ldy) {
+  griddep_launch();
+  griddep_wait();
+  const size_t blk = static_cast<size_t>(M) * nch;
+  const size_t sstride = static_cast<size_t>(n_tiles) * blk;
+  const int64_t total = static_cast<int64_t>(M) * N / 4;
+  for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < total;
+       e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t flat = 4 * e;
+    const int m = static_cast<int>(flat / N), n = static_cast<int>(flat % N);
+    const float* src = part + (static_cast<size_t>(n / nch) * M + m) * nch + n % nch;
+    float4 a4 = __ldcg(reinterpret_cast<const float4*>(src));
+#pragma unroll 4
+    for (int s = 1; s < splits; ++s) {
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(src + s * sstride));
+      a4.x += v.x;
+      a4.y += v.y;
+      a4.z += v.z;
+      a4.w += v.w;
     }
-    // Y = epilogue(sum) for these rows, 4 channels per thread and pass
-    for (int e = threadIdx.x; e < nf4 && good; e += C::kThreads) {
-      const int m = m0 + e / (NCH / 4), ch = n0 + 4 * (e % (NCH / 4));
-      float4 a4 = reinterpret_cast<const float4*>(stage)[e];
-      if (p.R) {
-        const uint2 rr = *reinterpret_cast<const uint2*>(p.R + static_cast<size_t>(m) * p.ldr + ch);
-        const float2 r01 = __half22float2(*reinterpret_cast<const __half2*>(&rr.x));
-        const float2 r23 = __half22float2(*reinterpret_cast<const __half2*>(&rr.y));
-        a4.x += r01.x;
-        a4.y += r01.y;
-        a4.z += r23.x;
-        a4.w += r23.y;
-      }
-      if (p.relu) {
-        a4.x = fmaxf(a4.x, 0.0f);
-        a4.y = fmaxf(a4.y, 0.0f);
-        a4.z = fmaxf(a4.z, 0.0f);
-        a4.w = fmaxf(a4.w, 0.0f);
-      }
-      const __half2 y01 = __floats2half2_rn(a4.x, a4.y), y23 = __floats2half2_rn(a4.z, a4.w);
-      *reinterpret_cast<uint2*>(p.Y + static_cast<size_t>(m) * p.ldy + ch) =
-          make_uint2(*reinterpret_cast<const uint32_t*>(&y01), *reinterpret_cast<const uint32_t*>(&y23));
+    if (R) {
+      const uint2 rr = *reinterpret_cast<const uint2*>(R + static_cast<size_t>(m) * ldr + n);
+      const float2 r01 = __half22float2(*reinterpret_cast<const __half2*>(&rr.x));
+      const float2 r23 = __half22float2(*reinterpret_cast<const __half2*>(&rr.y));
+      a4.x += r01.x;
+      a4.y += r01.y;
+      a4.z += r23.x;
+      a4.w += r23.y;
     }
-    __syncthreads();   // slot 0 is read before the next chunk refills it
+    if (relu) {
+      a4.x = fmaxf(a4.x, 0.0f);
+      a4.y = fmaxf(a4.y, 0.0f);
+      a4.z = fmaxf(a4.z, 0.0f);
+      a4.w = fmaxf(a4.w, 0.0f);
+    }
+    const __half2 y01 = __floats2half2_rn(a4.x, a4.y), y23 = __floats2half2_rn(a4.z, a4.w);
+    *reinterpret_cast<uint2*>(Y + static_cast<size_t>(m) * ldy + n) =
+        make_uint2(*reinterpret_cast<const uint32_t*>(&y01), *reinterpret_cast<const uint32_t*>(&y23));
   }
-  if (threadIdx.x == 0) p.tickets[nt] = 0;   // the slice is clean for its next launch
 }
 
 template <int BT, int RB>
@@ -554,7 +507,21 @@ fg_status launch_ts(TsParams& p, cudaStream_t st) {
   cfg.numAttrs = 1;
   if (cudaLaunchKernelEx(&cfg, gemm_q4ts_kernel<BT, RB>, p) != cudaSuccess)
     return check_launch("gemm_q4ts_kernel (launch)");
-  return check_launch("gemm_q4ts_kernel");
+  const fg_status s = check_launch("gemm_q4ts_kernel");
+  if (s != FG_OK || p.splits == 1) return s;
+  // the split sum over the whole GPU, programmatically after the product
+  const int64_t total = static_cast<int64_t>(p.M) * p.N / 4;
+  cudaLaunchConfig_t rc = {};
+  rc.gridDim = dim3(static_cast<unsigned>(std::min<int64_t>((total + 255) / 256, static_cast<int64_t>(num_sms()) * 8)));
+  rc.blockDim = dim3(256);
+  rc.stream = st;
+  rc.attrs = attr;
+  rc.numAttrs = 1;
+  trace_extra_launch();
+  if (cudaLaunchKernelEx(&rc, splitk_sum_kernel, static_cast<const float*>(p.part), p.splits, p.M, p.N, BNC * RB,
+                         p.n_tiles, p.R, p.ldr, p.relu, p.Y, p.ldy) != cudaSuccess)
+    return check_launch("splitk_sum_kernel (launch)");
+  return check_launch("splitk_sum_kernel");
 }
 
 int bt_for(int64_t M) { return M <= 32 ? 32 : (M <= 64 ? 64 : (M <= 128 ? 128 : 256)); }
@@ -563,19 +530,6 @@ int bt_for(int64_t M) { return M <= 32 ? 32 : (M <= 64 ? 64 : (M <= 128 ? 128 : 
 // beat one of 256 (the X tile is re-read twice as often, but the two CTAs'
 // pipelines overlap each other's stalls).
 int rb_for(const GemmArgs&) { return 1; }
-
-unsigned int* ticket_slice() {
-  static std::atomic<unsigned> next{0};
-  static unsigned int* base[64] = {nullptr};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  if (!base[dev]) {
-    void* a = nullptr;
-    if (cudaGetSymbolAddress(&a, g_tickets) != cudaSuccess) return nullptr;
-    base[dev] = static_cast<unsigned int*>(a);
-  }
-  return base[dev] + static_cast<size_t>(next.fetch_add(1) % kSlices) * kSliceTiles;
-}
 
 // Split count: K is cut so that the CTAs fill the GPU's slots (one per SM
 // with two row blocks, two per SM with one) with the fewest waves of per-CTA
@@ -610,7 +564,6 @@ size_t gemm_q4ts_workspace_bytes(int64_t M, int64_t N, int64_t K) {
 
 bool gemm_q4ts_supported(const GemmArgs& a) {
   if (a.dtype != FG_F16 || !a.quant || a.M < 1 || a.M > 256 || a.K % BK) return false;
-  if (a.N / BNC > kSliceTiles) return false;
   for (int i = 0; i < a.nseg; ++i) {
     const WSeg& s = a.seg[i];
     if (!s.packed || s.N % BNC || !aligned(s.packed, 16)) return false;
@@ -648,8 +601,6 @@ fg_status gemm_q4ts(const GemmArgs& a, void* ws, size_t ws_bytes, cudaStream_t s
     const size_t need = static_cast<size_t>(p.splits) * a.M * a.N * 4;
     if (!ws || ws_bytes < need) return fail(FG_ERR_WORKSPACE, "decode product needs %zu workspace bytes", need);
     p.part = static_cast<float*>(ws);
-    p.tickets = ticket_slice();
-    if (!p.tickets) return fail(FG_ERR_CUDA, "split-K tickets");
   }
   p.Y = static_cast<__half*>(a.Y);
   p.ldy = static_cast<int>(a.ldy);
