@@ -26,6 +26,7 @@
 
 #include "codec_dev.cuh"
 #include "fg_internal.cuh"
+#include "tc_ptx.cuh"
 
 namespace fg {
 namespace {
@@ -361,6 +362,12 @@ __global__ void __launch_bounds__(128) decode_attn_mma_kernel(const DecodeArgs a
   const int64_t t1 = min(len, t0 + a.tps);
   const int64_t slot0 = static_cast<int64_t>(bh) * a.cap;
 
+  // launched with programmatic stream serialization: the next kernel may be
+  // scheduled now; q, the new K/V and the cache are read after the previous
+  // kernel has completed
+  tc::griddep_launch();
+  tc::griddep_wait();
+
   // ---- Concat: quantize the new token's K and V into slot pos -----------------
   if (a.knew != nullptr && a.pos >= t0 && a.pos < t1) {
     if (warp == 0) append_token<D>(a, slot0, bi, h, lane);
@@ -442,6 +449,8 @@ __global__ void __launch_bounds__(128) decode_attn_mma_kernel(const DecodeArgs a
 template <int D>
 __global__ void decode_attn_combine_kernel(const float* __restrict__ part, int splits, int heads,
                                            __half* __restrict__ out, int64_t ldo) {
+  tc::griddep_launch();
+  tc::griddep_wait();
   const int bh = blockIdx.x, dim = threadIdx.x;
   const float* p = part + static_cast<int64_t>(bh) * splits * (D + 2);
   float M = -INFINITY;
@@ -498,9 +507,19 @@ fg_status launch_mma(const fg_kv& kv, const void* q, int64_t ldq, const void* kn
     if (!ws || ws_bytes < need) return fail(FG_ERR_WORKSPACE, "attention split partials need %zu bytes", need);
     a.part = static_cast<float*>(ws);
   }
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
   {
     Trace tr(KC_ATTN_DECODE, st);
-    decode_attn_mma_kernel<D><<<static_cast<unsigned>(bh * a.splits), 128, 0, st>>>(a);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(bh * a.splits));
+    cfg.blockDim = dim3(128);
+    cfg.stream = st;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, decode_attn_mma_kernel<D>, a) != cudaSuccess)
+      return check_launch("decode_attn_mma_kernel (launch)");
   }
   {
     const fg_status s = check_launch("decode_attn_mma_kernel");
@@ -508,8 +527,15 @@ fg_status launch_mma(const fg_kv& kv, const void* q, int64_t ldq, const void* kn
   }
   if (a.splits > 1) {
     Trace tr(KC_ATTN_COMBINE, st);
-    decode_attn_combine_kernel<D><<<static_cast<unsigned>(bh), D, 0, st>>>(a.part, a.splits, kv.heads,
-                                                                           a.out, ldo);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(bh));
+    cfg.blockDim = dim3(D);
+    cfg.stream = st;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, decode_attn_combine_kernel<D>, static_cast<const float*>(a.part), a.splits,
+                           static_cast<int>(kv.heads), a.out, ldo) != cudaSuccess)
+      return check_launch("decode_attn_combine_kernel (launch)");
     return check_launch("decode_attn_combine_kernel");
   }
   return FG_OK;

@@ -285,8 +285,8 @@ __global__ void __launch_bounds__(TsCfg<BT, RB>::kThreads, TsCfg<BT, RB>::kMinBl
   } else if (warp == 1) {
     if (lane == 0) {
       bool ok = true;
-      for (int i = 0; i < nk && ok; i += C::kBatch) {
-        const int n = min(C::kBatch, nk - i);
+      for (int i = 0; i < nk && ok;) {
+        const int n = min(i == 0 ? 1 : C::kBatch, nk - i);   // the first tile alone: start early
         // the last tile of each group in the batch; earlier ones of a group are done before it
         for (int j = max(i, i + n - kGroups); j < i + n && ok; ++j)
           ok = wait_count(&ready[j % SL], static_cast<uint32_t>(kGW * (j / SL + 1)), abort_flag);
@@ -307,6 +307,7 @@ __global__ void __launch_bounds__(TsCfg<BT, RB>::kThreads, TsCfg<BT, RB>::kMinBl
           }
           mma_commit(&consumed[s]);
         }
+        i += n;
       }
       mma_commit(done);
       if (!ok) atomicOr(p.err, DEV_ERR_WAIT_TIMEOUT);
