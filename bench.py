@@ -192,6 +192,25 @@ def oracle_decode_sample(w, budget_s: float = 20.0) -> dict:
             "seconds_per_layer_step": t}
 
 
+# ---------------------------------------------------------------------------------------
+# replicas (torchrun): every rank runs its own block, no collective on the data path
+# ---------------------------------------------------------------------------------------
+
+def max_over_ranks(values, world: int, device) -> list:
+    """Per-rank seconds -> their element-wise max over the ranks: the job's
+    clock is its slowest replica."""
+    if world <= 1:
+        return list(values)
+    t = torch.tensor(list(values), device=device, dtype=torch.float64)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_tokens(w, steps: int, world: int) -> int:
+    """Decode tokens the whole job produces: b*n per step on every rank."""
+    return w.b * w.n * steps * world
+
+
 def run_reference(args, w, rank, world):
     if rank != 0:
         return
@@ -291,10 +310,7 @@ def run_ours(args, w, rank, world, device):
     dec_total = sum(dec_ms) / 1e3
     tot_total = sum(tot_ms) / 1e3
     pre_total = sum(pre_ms) / 1e3
-    if world > 1:
-        t = torch.tensor([dec_total, tot_total, pre_total], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        dec_total, tot_total, pre_total = t.tolist()
+    dec_total, tot_total, pre_total = max_over_ranks([dec_total, tot_total, pre_total], world, dev)
     nonfinite = int((~torch.isfinite(outs)).sum().item())
 
     # end to end through the public API with host buffers: the prompt and each
@@ -317,17 +333,13 @@ def run_ours(args, w, rank, world, device):
         e[1].record(st)
         torch.cuda.synchronize()
         e2e_ms.append(e[0].elapsed_time(e[1]))
-    e2e_dec = sum(e2e_ms) / 1e3
-    if world > 1:
-        t = torch.tensor([e2e_dec], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_dec = t.item()
+    e2e_dec = max_over_ranks([sum(e2e_ms) / 1e3], world, dev)[0]
 
     if rank != 0:
         return
     pk = peaks()
     K = args.steps
-    tokens = w.b * w.n * K * world
+    tokens = job_tokens(w, K, world)
     value = tokens / dec_total
     # roofline of the decode phase's dominant kernel class
     mean_len = statistics.mean(w.s + t + 1 for t in range(w.n))
