@@ -113,38 +113,47 @@ __global__ void __launch_bounds__(256) kv_store_q4_kernel(const T* __restrict__ 
                                                           int64_t b, int64_t ntok, int64_t pos0,
                                                           int h1, int heads, int d, int64_t cap,
                                                           KVDst dst) {
+  // A warp takes whole token rows (one K or V row of h1 values): the row's
+  // indices are worked out once, then its 64-groups go 4 at a time, 8 lanes
+  // per group.  head_dim is 64 or 128, so heads and groups split by shifts.
   const int lane = threadIdx.x & 31;
   const int part = lane & 7;
-  const int gpr = h1 >> 6;  // groups per token row
-  const int64_t ngroups = 2 * b * ntok * gpr;
+  const int gpr = h1 >> 6;                    // groups per row
+  const int dshift = d == 128 ? 7 : 6;        // log2(head_dim)
+  const int gph = d >> 6;                     // groups per head
+  const int64_t rows = b * ntok;
   const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-  for (int64_t base = warp * 4; base < ngroups; base += nwarps * 4) {
-    int64_t g = base + (lane >> 3);
-    const bool valid = g < ngroups;
-    if (!valid) g = 0;
-    const int gi = static_cast<int>(g % gpr);
-    int64_t rest = g / gpr;
-    const int64_t row = rest % (b * ntok);  // bi * ntok + ti
-    const int which = static_cast<int>(rest / (b * ntok));
-    const int64_t bi = row / ntok, ti = row % ntok;
-    float v[8];
-    if (valid) {
-      load8((which ? vsrc : ksrc) + row * ld + gi * 64 + part * 8, v);
-    } else {
+  for (int64_t r = warp; r < 2 * rows; r += nwarps) {
+    const int which = r >= rows ? 1 : 0;
+    const int64_t row = r - which * rows;    // bi * ntok + ti
+    const int64_t bi = row / ntok, ti = row - bi * ntok;
+    const T* src = (which ? vsrc : ksrc) + row * ld;
+    const int64_t slot_base = bi * heads * cap + pos0 + ti;   // slot of head 0
+    uint32_t* codes = dst.codes[which];
+    float* mins = dst.mins[which];
+    float* scales = dst.scales[which];
+    for (int gi0 = 0; gi0 < gpr; gi0 += 4) {
+      const int gi = gi0 + (lane >> 3);
+      const bool valid = gi < gpr;
+      float v[8];
+      if (valid) {
+        load8(src + gi * 64 + part * 8, v);
+      } else {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] = 0.0f;
-    }
-    float mn, sc;
-    const uint32_t packed = quantize_group8(v, mn, sc);
-    if (valid) {
-      const int head = (gi * 64) / d;
-      const int wg = ((gi * 64) % d) >> 6;
-      const int64_t slot = (bi * heads + head) * cap + pos0 + ti;
-      dst.codes[which][(slot * (d >> 1) + wg * 32) / 4 + part] = packed;
-      if (part == 0) {
-        dst.mins[which][slot * (d >> 6) + wg] = mn;
-        dst.scales[which][slot * (d >> 6) + wg] = sc;
+        for (int i = 0; i < 8; ++i) v[i] = 0.0f;
+      }
+      float mn, sc;
+      const uint32_t packed = quantize_group8(v, mn, sc);
+      if (valid) {
+        const int head = (gi * 64) >> dshift;
+        const int wg = gi - head * gph;
+        const int64_t slot = slot_base + static_cast<int64_t>(head) * cap;
+        codes[(slot * (d >> 1) + wg * 32) / 4 + part] = packed;
+        if (part == 0) {
+          mins[slot * gph + wg] = mn;
+          scales[slot * gph + wg] = sc;
+        }
       }
     }
   }
@@ -221,8 +230,7 @@ fg_status kv_store(const fg_kv& kv, const void* ksrc, const void* vsrc, int64_t 
     dst.mins[1] = kv.v_mins;
     dst.scales[0] = kv.k_scales;
     dst.scales[1] = kv.v_scales;
-    const int64_t ngroups = 2 * b * ntok * (h1 / 64);
-    const int grid = grid_for(ngroups, 32);
+    const int grid = grid_for(2 * b * ntok, 8);   // a token row per warp, 8 warps per block
     Trace tr(KC_KV_STORE, st);
     if (kv.dtype == FG_F16)
       kv_store_q4_kernel<__half><<<grid, 256, 0, st>>>(
