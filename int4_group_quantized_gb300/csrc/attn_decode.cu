@@ -19,8 +19,8 @@
 // multiply-adds.
 //
 // One CTA (4 warps) per (sequence, head, token split).  Each warp walks its
-// tokens 16 at a time with an online softmax in base 2 (q is pre-scaled by
-// log2(e)/sqrt(d)); warps, then splits, are merged with the usual
+// tokens 16 at a time with an online softmax in base 2 (the fp32 scores are
+// scaled by log2(e)/sqrt(d)); warps, then splits, are merged with the usual
 // max/sum rescaling.
 #include <math.h>
 
@@ -142,6 +142,10 @@ __device__ __forceinline__ void process_block(WarpState<D>& W, int64_t tb, int64
       sc0 += ksc[0][g] * (d[0] - bias[g]) + kmn[0][g] * qsum[g];
       sc1 += ksc[1][g] * (d[2] - bias[g]) + kmn[1][g] * qsum[g];
     }
+    // log2(e)/sqrt(d): scores in base 2 for exp2
+    constexpr float kQs = static_cast<float>(1.4426950408889634074 * (D == 128 ? 0.088388347648318440550 : 0.125));
+    sc0 *= kQs;
+    sc1 *= kQs;
     if (!kval[0]) sc0 = -INFINITY;
     if (!kval[1]) sc1 = -INFINITY;
 
@@ -254,7 +258,8 @@ __device__ __forceinline__ void setup_q(WarpState<D>& W, const __half* qrow, int
   auto& bias = W.bias;
   auto& qsum = W.qsum;
   {
-    const float qscale = 1.4426950408889634f / sqrtf(static_cast<float>(D));
+    // q stays exact (it is fp16 already); log2(e)/sqrt(d) is applied to the
+    // fp32 scores instead, so no rounding of a scaled q enters them
 #pragma unroll
     for (int g = 0; g < NG; ++g) {
       float qv[16];
@@ -266,8 +271,8 @@ __device__ __forceinline__ void setup_q(WarpState<D>& W, const __half* qrow, int
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const float2 f = __half22float2(hh[i]);
-          qv[8 * c + 2 * i] = f.x * qscale;
-          qv[8 * c + 2 * i + 1] = f.y * qscale;
+          qv[8 * c + 2 * i] = f.x;
+          qv[8 * c + 2 * i + 1] = f.y;
         }
       }
       float bsum = 0.0f, qs = 0.0f;

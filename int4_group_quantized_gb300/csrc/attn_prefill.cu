@@ -8,7 +8,7 @@
 // chunk's K and V codes to fp16 in shared memory (fmaf(q, scale, min) in
 // fp32, rounded to fp16 -- the same values the codec's dequantization gives),
 // then every warp forms S = Q K^T with m16n8k16 MMAs (fp32 accumulate), keeps
-// a running max and sum in base 2 (Q is pre-scaled by log2(e)/sqrt(d)),
+// a running max and sum in base 2 (scores scaled by log2(e)/sqrt(d) in fp32),
 // re-uses the S accumulators as the A operand of P V, and rescales its output
 // accumulators when the max moves.  Chunks wholly above a warp's rows are
 // skipped; the diagonal chunk is masked.
@@ -82,10 +82,11 @@ __global__ void __launch_bounds__(128) prefill_attn_mma_kernel(const PrefillArgs
   const int64_t kend = min(q0 + QB, a.s);             // keys the CTA needs: 0..kend-1
   const int64_t slot0 = bh * a.cap;
 
-  // Q as A fragments, pre-scaled so that exp2 gives the softmax numerator
+  // Q as A fragments, exact (fp16 already); log2(e)/sqrt(d) is applied to
+  // the fp32 scores, so that no rounding of a scaled Q enters them
+  constexpr float kQs = static_cast<float>(1.4426950408889634074 * (D == 128 ? 0.088388347648318440550 : 0.125));
   uint32_t qa[NKS][4];
   {
-    const float qs = 1.4426950408889634f / sqrtf(static_cast<float>(D));
     const int64_t r0 = wr0 + g, r1 = wr0 + g + 8;
 #pragma unroll
     for (int kk = 0; kk < NKS; ++kk) {
@@ -95,7 +96,7 @@ __global__ void __launch_bounds__(128) prefill_attn_mma_kernel(const PrefillArgs
         const int c = 16 * kk + 2 * tig + 8 * (e >> 1);
         float2 f = make_float2(0.0f, 0.0f);
         if (r < a.s) f = __half22float2(*reinterpret_cast<const __half2*>(a.q + (bi * a.s + r) * a.ldq + h * D + c));
-        qa[kk][e] = pack_h2(f.x * qs, f.y * qs);
+        qa[kk][e] = pack_h2(f.x, f.y);
       }
     }
   }
@@ -142,6 +143,13 @@ __global__ void __launch_bounds__(128) prefill_attn_mma_kernel(const PrefillArgs
         mma16816(sacc[nt], qa[kk], r[0], r[1]);
         mma16816(sacc[nt + 1], qa[kk], r[2], r[3]);
       }
+    }
+#pragma unroll
+    for (int i = 0; i < KC / 8; ++i) {
+      sacc[i][0] *= kQs;
+      sacc[i][1] *= kQs;
+      sacc[i][2] *= kQs;
+      sacc[i][3] *= kQs;
     }
     // causal mask and sequence end (only where the chunk reaches them)
     if (kc + KC > wr0 || kc + KC > a.s) {

@@ -136,16 +136,68 @@ def test_opt125m_two_layer_chain(fg):
     _compare(w, y, outs, oracle_block(w, raw, True, x, tin, seqs), seqs, 1e-2)
 
 
-@pytest.mark.parametrize("name,layer", [("opt-125m", 0), ("opt-125m", 6), ("opt-125m", 11),
-                                        ("opt-6.7b", 0), ("opt-6.7b", 31)])
+LAYER_LOCAL = [("opt-125m", 0), ("opt-125m", 6), ("opt-125m", 11),
+               ("opt-6.7b", 0), ("opt-6.7b", 16), ("opt-6.7b", 31),
+               ("opt-30b", 0), ("opt-30b", 24), ("opt-30b", 47),
+               ("opt-175b", 0), ("opt-175b", 48), ("opt-175b", 95)]
+
+
+@pytest.mark.parametrize("name,layer", LAYER_LOCAL)
 def test_layer_local_full_block(fg, name, layer):
-    """One layer of a large shape at the full block size and prompt length,
-    with its own N(0,1) inputs (the stack overflows fp16 past a few layers
-    without normalisation, so parity is checked layer by layer)."""
+    """One layer of each shaped config (first, middle, last) with its own
+    N(0,1) inputs (the stack overflows fp16 past a few layers without
+    normalisation, so parity is checked layer by layer): at the config's
+    block size and prompt length, except 175B at b = 4."""
     w = synth.WORKLOADS[name]
+    b = 4 if name == "opt-175b" else w.b
     raw = [synth.layer_weights(w, layer, "cuda")]
-    x = synth.prompt(w, device="cuda", seed_offset=layer)
-    tin = synth.decode_inputs(w, n=w.n if w.h1 < 2048 else 4, device="cuda", seed_offset=layer)
-    y, outs, _ = run_gpu_block(fg, w, raw, True, x, tin)
-    seqs = [0, w.b - 1]
-    _compare(w, y, outs, oracle_block(w, raw, True, x, tin, seqs), seqs, 1e-2)
+    x = synth.prompt(w, b=b, device="cuda", seed_offset=layer)
+    tin = synth.decode_inputs(w, b=b, n=w.n if w.h1 < 2048 else 4, device="cuda", seed_offset=layer)
+    y, outs, kvs = run_gpu_block(fg, w, raw, True, x, tin)
+    seqs = [0, b - 1]
+    ref = oracle_block(w, raw, True, x, tin, seqs)
+    # the cache itself: the codec is bit-exact, so its codes differ only
+    # where a K/V row entered it one fp16 ulp apart (fp32 vs fp64 sums)
+    oc = ref[2][0]
+    for g_codes, o_codes in ((kvs[0].k_codes, oc.k_codes), (kvs[0].v_codes, oc.v_codes)):
+        assert np.mean(g_codes[seqs].cpu().numpy() != o_codes) <= 1e-3
+    if w.h1 < 7168:
+        _compare(w, y, outs, ref, seqs, 1e-2)
+    else:
+        # A K/V row computed with fp32 sums and rounded to fp16 sits one
+        # ulp away from the oracle's fp64-rounded row in a few % of its
+        # elements; through the codec that moves ~1% of the groups' (min,
+        # scale) by an ulp and flips ~1e-4 of the codes by a whole step.  At
+        # h1 >= 7168 a few prefill outputs in 1e4 cross 1e-2 from that alone
+        # (the codec-off case below meets 1e-2 on the max).  The decode
+        # products apply fp16-rounded (scale, min) (~1e-3 relative per
+        # weight), which the large attention scores of these unnormalised
+        # layers amplify: up to ~0.5% of decode outputs cross 1e-2 at 175B.
+        # Bars: 1e-2 for all but 2e-4 (prefill) / 1e-2 (decode) of the
+        # outputs, 3e-2 on the max.
+        _compare_flips(y, outs, ref, seqs, 1e-2, (2e-4, 1e-2), 3e-2)
+
+
+def _compare_flips(y, outs, ref, seqs, tol, frac, tol_max):
+    """frac: (prefill, decode) share of the outputs allowed above tol."""
+    ry, routs, _ = ref
+    pairs = [(y[seqs].cpu().numpy(), ry)] + [(outs[t][seqs].cpu().numpy(), routs[t]) for t in range(len(outs))]
+    for k, (got, want) in enumerate(pairs):
+        d = np.abs(np.asarray(got, dtype=np.float64) - want) / max(np.max(np.abs(want)), 1e-30)
+        assert np.max(d) <= tol_max, f"output {k}: max rel err {np.max(d)}"
+        f = frac[0] if k == 0 else frac[1]
+        assert np.mean(d > tol) <= f, f"output {k}: {np.mean(d > tol)} of the outputs above {tol}"
+
+
+@pytest.mark.parametrize("name,layer", [("opt-30b", 0), ("opt-175b", 0)])
+def test_layer_local_codec_off(fg, name, layer):
+    """The same layer with the codec off (fp16 weights and cache): the
+    arithmetic alone meets the 1e-2 bar on the max at the largest shapes."""
+    w = synth.WORKLOADS[name]
+    b = 4 if name == "opt-175b" else w.b
+    raw = [synth.layer_weights(w, layer, "cuda")]
+    x = synth.prompt(w, b=b, device="cuda", seed_offset=layer)
+    tin = synth.decode_inputs(w, b=b, n=2, device="cuda", seed_offset=layer)
+    y, outs, _ = run_gpu_block(fg, w, raw, False, x, tin)
+    seqs = [0, b - 1]
+    _compare(w, y, outs, oracle_block(w, raw, False, x, tin, seqs), seqs, 1e-2)
