@@ -161,15 +161,20 @@ fg_status fg_linear(const fg_wmat* w, fg_codec codec, fg_dtype dtype, const void
  * K*N/16 bytes: one 4608-byte block per (128-channel tile t, 64-k tile u),
  * block (t, u) at byte offset (t * K/64 + u) * 4608, so the k tiles of a
  * channel tile are one contiguous run:
- *   bytes 0..4095: codes; channel r of the tile in bytes r*32 .. r*32+31,
- *     its two 16-byte halves (k 0..31 of the tile, k 32..63) stored swapped
- *     when bit 2 of r is set; within each 32-bit word (8 consecutive k) the
- *     nibbles from the low end hold k0 k2 k4 k6 k1 k3 k5 k7, so one mask
- *     turns a word into fp16 pairs of consecutive k;
- *   bytes 4096..4607: for the tile's two 64-channel groups (lower first) and
- *     j = 0..31, fp16x2 (scale[2j], scale[2j+1]) then fp16x2 (min[2j],
- *     min[2j+1]) of the tile's k, each rounded to nearest -- the precision
- *     the decode products apply them in.
+ *   bytes 0..4095: codes, 16-byte units [q][g2][t] (q = 0..3, g2 = 0..1,
+ *     t = 0..31) at q*1024 + g2*512 + t*16; 32-bit word w of unit (q, g2, t)
+ *     holds channel 32q + t/4 + 8w of the tile at the tile's k pairs
+ *     j = 16*g2 + 4e + t%4, e = 0..3: nibble e (from the low end) is k = 2j,
+ *     nibble e+4 is k = 2j+1, so one mask turns a word into fp16 pairs of
+ *     consecutive k;
+ *   bytes 4096..4607: (scale, min) pairs, for the tile's two 64-channel
+ *     groups gl (lower first) 16-byte units at 4096 + gl*256 + (u*4 + c)*16,
+ *     u = 0..3, c = 0..3: fp16x2 (scale[2j], scale[2j+1]), fp16x2 (min[2j],
+ *     min[2j+1]) for j = 8u + c, then the same for j = 8u + 4 + c; each
+ *     rounded to nearest -- the precision the decode products apply them in.
+ *   (The order is the one in which the converting threads read them: thread
+ *   t of warp quarter q converts channels 32q + t/4 + 8w at the k pairs
+ *   4i + t%4, the register order of a 16x128b tensor-memory store.)
  * packed: device, 16-byte aligned, owned by the caller, then stored in
  * w->packed.  K a multiple of 64 and N of 128, else FG_ERR_SHAPE; null
  * arrays -> FG_ERR_ARG.  Asynchronous on `stream`. */

@@ -13,9 +13,9 @@
 //   * the accumulator is 128 TMEM lanes (channels) x BT columns (sequences).
 // Each weight byte crosses HBM once per step; the kernel is HBM-bound, so the
 // CTA is small enough for two per SM and splits K when the output has too
-// few 128-channel tiles to fill the GPU.  The split partials are summed in
-// the same launch by the last CTA of each tile (a counter per tile in the
-// workspace, zero on entry and reset to zero by that CTA).
+// few 128-channel tiles to fill the GPU.  The K splits of a tile form one
+// thread-block cluster and sum their partials over distributed shared memory
+// in the same launch.
 //
 // Warp roles (384 threads): warp 0 issues TMA, warp 1 owns TMEM and issues
 // the MMAs, warps 4..11 dequantize, warps 4..7 drain TMEM.  Every wait is

@@ -10,31 +10,30 @@
 //     packed codes and fp16 (scale, min) pairs (fg_pack_weight) into fp16
 //     weights in registers and store them with tcgen05.st: TMEM lane =
 //     channel, column = two consecutive k.  A warp reaches only its own
-//     32-lane quarter of TMEM (warp % 4); two groups of 4*RB warps take
-//     alternate k tiles, so two tiles are in conversion at any time.
+//     32-lane quarter of TMEM (warp % 4); two sets of 4*RB warps convert
+//     the two k tiles of a chunk side by side.
 //   * B = X tile [BT rows][64 k], K-major, 128-byte swizzle, by TMA, shared
 //     by the RB row blocks: the activations cross L2 once per 128*RB
 //     channels, which is what bounds this kernel at small RB.
 //   * D = RB accumulators of 128 lanes (channels) x BT columns (sequences).
 // Shared memory carries only what HBM delivers (codes, pairs) and X; the fp16
-// weights never touch it.  Stage i of the ring is one smem slot and RB
-// 32-column TMEM slots; one mbarrier per stage frees both (the MMA's commit
-// plus one arrival per warp of the converting group).
+// weights never touch it.
 //
 // K is split when there are too few channel tiles to fill the GPU: each
-// split writes its fp32 partial to the workspace, and the last CTA of a tile
-// to finish (a ticket counter per tile, library-owned and reset by that CTA)
-// sums the splits in index order and applies the epilogue.
+// split bulk-copies its fp32 partial into its own workspace block
+// [split][tile][M][128], and splitk_sum_kernel, launched next on the same
+// stream, sums the blocks in split order and applies the epilogue.
 //
 // The kernel is launched with programmatic stream serialization: the weight
 // tiles of the first stages are requested and converted before
 // griddepcontrol.wait, so they stream while the previous kernel finishes; X,
 // the residual, the workspace and Y are touched only after it.
 //
-// Warp roles (128 + 256*RB threads): warp 0 issues the copies, warp 1 owns
-// TMEM and issues the MMAs, warps 4.. dequantize, and the first 4*RB of them
-// drain TMEM.  Every wait is bounded and raises the device error word on
-// timeout.
+// Warp roles (128 + 256*RB threads): warp 0 issues the weight copies, warp 2
+// the X copies, warp 1 owns TMEM and issues the MMAs, warps 4.. dequantize,
+// and the first 4*RB of them drain TMEM.  Every mbarrier wait is bounded and
+// raises the device error word on timeout; the one named barrier is taken
+// the same number of times by all of its warps.
 #include <cudaTypedefs.h>
 #include <string.h>
 
@@ -59,21 +58,25 @@ using namespace q4;
 constexpr int BK = 64;
 constexpr int BNC = 128;               // channels per row block (the MMA's M)
 constexpr int kDqWarp0 = 4;            // dequantization warps start here
-constexpr int kGroups = 2;             // groups of dequantization warps, alternate k tiles
 constexpr uint32_t kWaitLimit = 1u << 24;
 
 // ---- packing -------------------------------------------------------------------
 // The decode copy is one 4608-byte block per (128-channel tile nt, 64-k tile
 // kt), blocks in order nt-major, so a CTA streams one contiguous run of HBM
-// and fetches a stage with one bulk copy:
-//   bytes 0..4095: codes, channel r of the tile in bytes r*32..r*32+31, its
-//     two 16-byte halves (k 0..31, k 32..63) swapped when bit 2 of r is set
-//     (the order in which eight lanes reading rows r..r+7 hit distinct shared
-//     memory banks); in each 32-bit word (8 consecutive k) nibble slot p
-//     (from the low end) holds k = 2*(p & 3) + (p >> 2), so slots (p, p+4)
-//     are the pair (2p, 2p+1);
-//   bytes 4096..4607: for the tile's two 64-channel groups gl and j = 0..31,
-//     fp16x2 (scale[2j], scale[2j+1]) then fp16x2 (min[2j], min[2j+1]).
+// and fetches a stage with one bulk copy.  Inside a block the data sit where
+// the thread that converts them reads them, for the 16x128b TMEM store shape
+// (warp quarter q writes TMEM lanes 32q..32q+31 with two stores of 16 lanes;
+// thread t of the warp holds lanes t/4, t/4+8, t/4+16, t/4+24 and the
+// 32-bit columns c = t%4, t%4+4, ..., i.e. the k pairs j = 4i + t%4, i = 0..7):
+//   bytes 0..4095: codes, [q][g2][t] 16-byte units (q = 0..3, g2 = 0..1,
+//     t = 0..31): word w of unit (q, g2, t) is channel 32q + t/4 + 8w, k pairs
+//     j = 16*g2 + 4e + t%4 for e = 0..3, nibble slot e (from the low end)
+//     holding k = 2j and slot e+4 holding k = 2j+1.  A warp's 128-bit loads
+//     are 512 contiguous bytes each.
+//   bytes 4096..4607: (scale, min) pairs, [gl][u][c4] 16-byte units for the
+//     tile's two 64-channel groups gl, u = 0..3, c4 = 0..3: fp16x2
+//     (scale[2j], scale[2j+1]), fp16x2 (min[2j], min[2j+1]) for j = 8u + c4,
+//     then the same for j = 8u + 4 + c4.
 constexpr int kTileCodes = BNC * BK / 2;             // 4096
 constexpr int kTilePairs = 2 * (BK / 2) * 8;         // 512
 constexpr int kTileBytes = kTileCodes + kTilePairs;  // 4608
@@ -84,20 +87,23 @@ __global__ void pack_codes_kernel(const uint8_t* __restrict__ codes, int64_t K, 
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < words;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int64_t n = i % N, rest = i / N;   // threads along n: coalesced reads of a code row
-    const int wq = static_cast<int>(rest % 4), c = static_cast<int>((rest / 4) % 2);
+    const int c4 = static_cast<int>(rest % 4), g2 = static_cast<int>((rest / 4) % 2);
     const int64_t kt = rest / 8;
-    const int64_t k0 = kt * BK + 32 * c + 8 * wq;
+    const int r = static_cast<int>(n % BNC);
+    const int q = r / 32, w = (r % 32) / 8, t = ((r % 8) << 2) | c4;
     uint32_t out = 0;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const uint32_t byte = codes[(k0 + j) * (N / 2) + n / 2];
-      const uint32_t q = (n & 1) ? (byte >> 4) : (byte & 15u);
-      out |= q << (4 * (((j & 1) << 2) | (j >> 1)));
+    for (int e = 0; e < 4; ++e) {
+      const int64_t k = kt * BK + 2 * (16 * g2 + 4 * e + c4);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t byte = codes[(k + h) * (N / 2) + n / 2];
+        const uint32_t c = (n & 1) ? (byte >> 4) : (byte & 15u);
+        out |= c << (4 * (e + 4 * h));
+      }
     }
-    const int64_t nt = n / BNC;
-    const int r = static_cast<int>(n % BNC);
-    uint8_t* tile = packed + (nt * KT + kt) * kTileBytes;
-    *reinterpret_cast<uint32_t*>(tile + r * 32 + 16 * (c ^ ((r >> 2) & 1)) + 4 * wq) = out;
+    uint8_t* tile = packed + ((n / BNC) * KT + kt) * kTileBytes;
+    *reinterpret_cast<uint32_t*>(tile + q * 1024 + g2 * 512 + t * 16 + w * 4) = out;
   }
 }
 
@@ -109,9 +115,11 @@ __global__ void pack_pairs_kernel(const float* __restrict__ mins, const float* _
     const int64_t g = i % G, jj = i / G;     // jj = global k pair; threads along g: coalesced reads
     const __half2 s2 = __floats2half2_rn(scales[(2 * jj) * G + g], scales[(2 * jj + 1) * G + g]);
     const __half2 m2 = __floats2half2_rn(mins[(2 * jj) * G + g], mins[(2 * jj + 1) * G + g]);
-    const int64_t kt = jj / (BK / 2), j = jj % (BK / 2);
+    const int64_t kt = jj / (BK / 2);
+    const int j = static_cast<int>(jj % (BK / 2));
+    const int u = j / 8, hi = (j / 4) % 2, c4 = j % 4;
     uint8_t* tile = packed + ((g / 2) * KT + kt) * kTileBytes;
-    *reinterpret_cast<uint2*>(tile + kTileCodes + ((g % 2) * (BK / 2) + j) * 8) =
+    *reinterpret_cast<uint2*>(tile + kTileCodes + (g % 2) * 256 + (u * 4 + c4) * 16 + hi * 8) =
         make_uint2(*reinterpret_cast<const uint32_t*>(&s2), *reinterpret_cast<const uint32_t*>(&m2));
   }
 }
@@ -135,77 +143,71 @@ struct TsParams {
 constexpr int cmin(int a, int b) { return a < b ? a : b; }
 constexpr int cmax(int a, int b) { return a > b ? a : b; }
 
-// Rings, each released by the stage that last needs it: weights (released
-// once the dequantization warps hold them in registers; deep, to cover HBM
-// latency) and slots (an X tile in shared memory plus its TMEM A slot, both
-// released by the commit of the MMAs that read them).
+// The main loop runs in lockstep chunks of kT k tiles.  The dequantization
+// warps (kT sets of 4*RB, one k tile of the chunk each) convert chunk c into
+// TMEM buffer c % kBufs and meet the MMA warp at one hardware named barrier;
+// the MMA warp then issues chunk c's MMAs while the dequantization warps
+// convert chunk c+1.  One barrier per chunk replaces a handoff per k tile:
+// on this GPU every synchronisation the issuing thread takes (an mbarrier
+// wait, an acquire load) costs a few hundred cycles, about the MMA time of a
+// whole k tile at N = 64.  Every warp that takes the named barrier runs the
+// same number of chunks and leaves the loop only at its end, so the barrier
+// always completes; a failed (bounded) wait skips the work, not the barrier.
 //
-// The issuing thread synchronises rarely: any acquire-ordered check it makes
-// (an mbarrier wait, an acquire load) stalls it behind its MMAs in flight
-// (~250 cycles each on this GPU, against ~50 cycles per 128x64x16 MMA).  So
-// the dequantization warps also wait for the X tile, then publish "slot
-// ready" with a release add on a per-slot counter, and the issuing thread
-// checks readiness once per batch of kBatch k tiles (the last tile of each
-// group: a group finishes its tiles in order).
+// Rings around it, each released by the stage that last needs it: weights
+// (a chunk's packed blocks, one bulk copy per row block; released once every
+// dequantization warp holds its codes in registers), X (a chunk's tiles) and
+// the TMEM buffers (both released by the commit of the MMAs that read them).
 template <int BT, int RB>
 struct TsCfg {
-  static constexpr int kThreads = 128 + kGroups * 4 * RB * 32;   // warps 0..3, then the dequant groups
-  static constexpr int kGroupWarps = 4 * RB;
+  static constexpr int kT = 2;                        // k tiles per chunk
+  static constexpr int kGroupWarps = 4 * RB;          // warps converting one k tile (all row blocks)
+  static constexpr int kDqWarps = kT * kGroupWarps;
+  static constexpr int kThreads = 128 + kDqWarps * 32;   // warps 0..3, then the dequantization warps
+  static constexpr int kBarThreads = 32 + kDqWarps * 32; // the MMA warp and the dequantization warps
   static constexpr int kX = BT * BK * 2;              // X tile, K-major, 128-byte swizzle
-  static constexpr int kW = RB * kTileBytes;          // the weights of one k tile: RB packed blocks
+  static constexpr int kXStage = kT * kX;
+  static constexpr int kWStage = kT * RB * kTileBytes;   // a chunk's packed blocks, [rb][t]
   static constexpr int kAcc = BT < 32 ? 32 : BT;      // accumulator columns per row block
+  static constexpr int kBufCols = 32 * RB * kT;       // TMEM columns of one A buffer
   static constexpr uint32_t kTmemCols = (RB == 1 && BT <= 128) ? 256 : 512;
   static constexpr int kMinBlocks = kTmemCols == 256 ? 2 : 1;
   static constexpr int kBudget = kMinBlocks == 2 ? 104 * 1024 : 204 * 1024;
-  static constexpr int kSlots = cmin(cmin((static_cast<int>(kTmemCols) - RB * kAcc) / (32 * RB),
-                                          cmax(2, (kBudget / 2) / kX)), 8);
-  static constexpr int kBatch = cmax(1, cmin(4, kSlots - 2));
-  static constexpr int kWStages = cmin(16, (kBudget - kSlots * kX) / kW);
-  static constexpr int kXBytes = kSlots * kX;
-  static constexpr int kWBytes = kWStages * kW;
-  static constexpr int kBarBytes = (2 * (kSlots + kWStages) + 1) * 8 + kSlots * 4 + 16;   // + done, counters
+  // TMEM A buffers; X stage b goes with buffer b
+  static constexpr int kBufs = cmin(cmin(4, (static_cast<int>(kTmemCols) - RB * kAcc) / kBufCols),
+                                    cmax(2, (kBudget * 5 / 8) / kXStage));
+  static constexpr int kWStages = cmin(8, (kBudget - kBufs * kXStage) / kWStage);
+  static constexpr int kXBytes = kBufs * kXStage;
+  static constexpr int kWBytes = kWStages * kWStage;
+  static constexpr int kBarBytes = (2 * (kBufs + kWStages) + 1) * 8 + 16;   // + done, TMEM slot, flag
   static constexpr int kTotal = 1024 + kXBytes + kWBytes + kBarBytes;
-  static_assert(kSlots >= 2 && kWStages >= 2, "pipeline needs two stages");
-  static_assert(kX % 1024 == 0, "X slots stay 1024-byte aligned");
+  static_assert(kBufs >= 2 && kWStages >= 2, "pipeline needs two stages");
+  static_assert(kX % 1024 == 0, "X tiles stay 1024-byte aligned");
+  static_assert(kXBytes + kWBytes >= BT * RB * BNC * 4, "a split partial is staged in the drained rings");
 };
 
-__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
-  return v;
-}
-__device__ __forceinline__ void add_release_u32(uint32_t* p, uint32_t v) {
-  asm volatile("red.release.cta.shared::cta.add.u32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
-}
-// Waits until *p >= target (acquire), bounded like the mbarrier waits.
-__device__ __forceinline__ bool wait_count(const uint32_t* p, uint32_t target, volatile int* abort) {
-  for (uint32_t i = 0; i < kWaitLimit; ++i) {
-    if (static_cast<int32_t>(ld_acquire_u32(p) - target) >= 0) return true;
-    if ((i & 1023u) == 1023u && *abort) return false;
-  }
-  *abort = 1;
-  return false;
-}
+constexpr uint32_t kChunkBarrier = 1;   // named barrier id (0 is __syncthreads)
 
 template <int BT, int RB>
 __global__ void __launch_bounds__(TsCfg<BT, RB>::kThreads, TsCfg<BT, RB>::kMinBlocks)
     gemm_q4ts_kernel(const __grid_constant__ TsParams p) {
   using C = TsCfg<BT, RB>;
-  constexpr int SL = C::kSlots, SW = C::kWStages;
-  constexpr int kGW = C::kGroupWarps;
+  constexpr int KT = C::kT, NB = C::kBufs, SW = C::kWStages;
   constexpr uint32_t kIdesc = idesc_f16(128, BT, 0, 0);   // A (TMEM) and B (X) K-major
-  constexpr uint32_t kACol = RB * C::kAcc;                // TMEM A slots follow the accumulators
+  constexpr uint32_t kACol = RB * C::kAcc;                // TMEM A buffers follow the accumulators
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* xring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* wring = xring + C::kXBytes;
+  // xfull[b]: X stage b has landed, and it was requested only once the MMAs
+  // that last read X stage b and TMEM buffer b had completed, so it also
+  // means "buffer b is free"
   uint64_t* xfull = reinterpret_cast<uint64_t*>(wring + C::kWBytes);
-  uint64_t* consumed = xfull + SL;   // slot s read by its MMAs (X tile and TMEM A slot)
-  uint64_t* wfull = consumed + SL;
-  uint64_t* wempty = wfull + SW;
-  uint64_t* done = wempty + SW;
-  uint32_t* ready = reinterpret_cast<uint32_t*>(done + 1);   // [SL] warps that finished slot s, cumulative
-  uint32_t* tmem_slot = ready + SL;
+  uint64_t* wfull = xfull + NB;
+  uint64_t* wempty = wfull + SW;     // one arrival per dequantization warp
+  uint64_t* bufdone = wempty + SW;   // TMEM A buffer read by its MMAs
+  uint64_t* done = bufdone + NB;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -218,19 +220,17 @@ __global__ void __launch_bounds__(TsCfg<BT, RB>::kThreads, TsCfg<BT, RB>::kMinBl
   const int kt0 = split * p.ktiles_per_split;
   const int kt1 = min(kt0 + p.ktiles_per_split, p.K / BK);
   const int nk = kt1 - kt0;
+  const int nch = (nk + KT - 1) / KT;
 
   griddep_launch();   // a dependent grid waits for this one before it reads Y
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < SL; ++i) {
-      mbar_init(&xfull[i], 1);
-      mbar_init(&consumed[i], 1);    // the MMA commit
-      ready[i] = 0;
-    }
+    for (int i = 0; i < NB; ++i) mbar_init(&xfull[i], 1);
     for (int i = 0; i < SW; ++i) {
       mbar_init(&wfull[i], 1);
-      mbar_init(&wempty[i], kGW);    // one arrival per warp of the converting group
+      mbar_init(&wempty[i], C::kDqWarps);
     }
+    for (int i = 0; i < NB; ++i) mbar_init(&bufdone[i], 1);   // the MMA commit
     mbar_init(done, 1);
     *abort_flag = 0;
     mbar_fence_init();
@@ -249,19 +249,20 @@ __global__ void __launch_bounds__(TsCfg<BT, RB>::kThreads, TsCfg<BT, RB>::kMinBl
       const size_t run = static_cast<size_t>(p.K / BK) * kTileBytes;
       const uint8_t* wsrc = p.wp[seg] + static_cast<size_t>(nl / BNC) * run + static_cast<size_t>(kt0) * kTileBytes;
       int issued = 0;
-      for (int i = 0; i < nk; ++i) {
-        const int s = i % SW;
-        if (!mbar_wait(&wempty[s], ((i / SW) & 1) ^ 1, kWaitLimit, abort_flag)) break;
-        mbar_expect_tx(&wfull[s], C::kW);
+      for (int c = 0; c < nch; ++c) {
+        const int s = c % SW;
+        const uint32_t bytes = static_cast<uint32_t>(min(KT, nk - KT * c) * kTileBytes);
+        if (!mbar_wait(&wempty[s], ((c / SW) & 1) ^ 1, kWaitLimit, abort_flag)) break;
+        mbar_expect_tx(&wfull[s], bytes * RB);
 #pragma unroll
         for (int rb = 0; rb < RB; ++rb)
-          bulk_load(wring + s * C::kW + rb * kTileBytes, wsrc + rb * run + static_cast<size_t>(i) * kTileBytes,
-                    kTileBytes, &wfull[s]);
+          bulk_load(wring + s * C::kWStage + rb * KT * kTileBytes,
+                    wsrc + rb * run + static_cast<size_t>(KT * c) * kTileBytes, bytes, &wfull[s]);
         ++issued;
       }
-      for (int i = max(0, issued - SW); i < issued; ++i) {   // nothing in flight at exit
+      for (int c = max(0, issued - SW); c < issued; ++c) {   // nothing in flight at exit
         volatile int dummy = 0;
-        mbar_wait(&wfull[i % SW], (i / SW) & 1, kWaitLimit, &dummy);
+        mbar_wait(&wfull[c % SW], (c / SW) & 1, kWaitLimit, &dummy);
       }
       if (*abort_flag) atomicOr(p.err, DEV_ERR_WAIT_TIMEOUT);
     }
@@ -269,96 +270,121 @@ __global__ void __launch_bounds__(TsCfg<BT, RB>::kThreads, TsCfg<BT, RB>::kMinBl
     if (lane == 0) {
       griddep_wait();   // X comes from the previous kernel
       int issued = 0;
-      for (int i = 0; i < nk; ++i) {
-        const int s = i % SL;
-        if (!mbar_wait(&consumed[s], ((i / SL) & 1) ^ 1, kWaitLimit, abort_flag)) break;
-        mbar_expect_tx(&xfull[s], C::kX);
-        tma_load_2d(xring + s * C::kX, &p.mapX, (kt0 + i) * BK, 0, &xfull[s]);
+      for (int c = 0; c < nch; ++c) {
+        const int s = c % NB, n = min(KT, nk - KT * c);
+        // the MMAs of chunk c - NB (stage and buffer s) have completed
+        if (!mbar_wait(&bufdone[s], ((c / NB) & 1) ^ 1, kWaitLimit, abort_flag)) break;
+        mbar_expect_tx(&xfull[s], n * C::kX);
+        for (int t = 0; t < n; ++t)
+          tma_load_2d(xring + s * C::kXStage + t * C::kX, &p.mapX, (kt0 + KT * c + t) * BK, 0, &xfull[s]);
         ++issued;
       }
-      for (int i = max(0, issued - SL); i < issued; ++i) {
+      for (int c = max(0, issued - NB); c < issued; ++c) {
         volatile int dummy = 0;
-        mbar_wait(&xfull[i % SL], (i / SL) & 1, kWaitLimit, &dummy);
+        mbar_wait(&xfull[c % NB], (c / NB) & 1, kWaitLimit, &dummy);
       }
       if (*abort_flag) atomicOr(p.err, DEV_ERR_WAIT_TIMEOUT);
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      bool ok = true;
-      for (int i = 0; i < nk && ok;) {
-        const int n = min(i == 0 ? 1 : C::kBatch, nk - i);   // the first tile alone: start early
-        // the last tile of each group in the batch; earlier ones of a group are done before it
-        for (int j = max(i, i + n - kGroups); j < i + n && ok; ++j)
-          ok = wait_count(&ready[j % SL], static_cast<uint32_t>(kGW * (j / SL + 1)), abort_flag);
-        if (!ok) break;
+    // every lane takes the barrier; lane 0 issues
+    for (int c = 0; c < nch; ++c) {
+      const int n = min(KT, nk - KT * c);
+      named_bar_sync(kChunkBarrier, C::kBarThreads);   // chunk c is in TMEM and its X tiles have landed
+      if (lane == 0) {
         tc_fence_after();
-        for (int j = i; j < i + n; ++j) {
-          const int s = j % SL;
-          const uint32_t xa = smem_u32(xring + s * C::kX);
+        const int b = c % NB;
+        if (!*abort_flag) {
+          for (int t = 0; t < n; ++t) {
+            const uint32_t xa = smem_u32(xring + b * C::kXStage + t * C::kX);
 #pragma unroll
-          for (int rb = 0; rb < RB; ++rb) {
-            const uint32_t ta = tmem_base + kACol + 32u * (s * RB + rb);
+            for (int rb = 0; rb < RB; ++rb) {
+              const uint32_t ta = tmem_base + kACol + b * C::kBufCols + 32u * (t * RB + rb);
 #pragma unroll
-            for (int kk = 0; kk < BK / 16; ++kk) {
-              // B (X): K-major, 8-row groups 1 KiB apart; +32 bytes per 16-wide k step
-              const uint64_t bdesc = smem_desc_sw128(xa + kk * 32, 16, 1024);
-              mma_f16_ts(tmem_base + rb * C::kAcc, ta + 8u * kk, bdesc, kIdesc, (j > 0 || kk > 0) ? 1u : 0u);
+              for (int kk = 0; kk < BK / 16; ++kk) {
+                // B (X): K-major, 8-row groups 1 KiB apart; +32 bytes per 16-wide k step
+                const uint64_t bdesc = smem_desc_sw128(xa + kk * 32, 16, 1024);
+                mma_f16_ts(tmem_base + rb * C::kAcc, ta + 8u * kk, bdesc, kIdesc, (c > 0 || t > 0 || kk > 0) ? 1u : 0u);
+              }
             }
           }
-          mma_commit(&consumed[s]);
         }
-        i += n;
+        mma_commit(&bufdone[b]);   // frees X stage b and TMEM buffer b
       }
+      __syncwarp();
+    }
+    if (lane == 0) {
       mma_commit(done);
-      if (!ok) atomicOr(p.err, DEV_ERR_WAIT_TIMEOUT);
+      if (*abort_flag) atomicOr(p.err, DEV_ERR_WAIT_TIMEOUT);
     }
   } else if (warp >= kDqWarp0) {
     const int d = warp - kDqWarp0;
-    const int grp = d / kGW;                    // takes tiles i with i % kGroups == grp
+    const int tile = d / C::kGroupWarps;        // the k tile of each chunk this warp converts
     const int rb = (d / 4) % RB;                // row block
     const int q = warp & 3;                     // TMEM lane quarter of this warp
-    const int r = 32 * q + lane;                // channel in the row block = TMEM lane
-    const int sw = ((r >> 2) & 1) << 4;         // halves swapped in rows with bit 2 set
-    const uint32_t trow = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + kACol + 32u * rb;
-    bool ok = true;
-    for (int i = grp; i < nk && ok; i += kGroups) {
-      const int s = i % SW, sl = i % SL;
-      ok = mbar_wait(&wfull[s], (i / SW) & 1, kWaitLimit, abort_flag) &&
-           mbar_wait(&consumed[sl], ((i / SL) & 1) ^ 1, kWaitLimit, abort_flag);
-      ok = __all_sync(0xffffffffu, ok);   // the warp-wide tcgen05.st below needs every lane
-      if (!ok) break;
-      tc_fence_after();
-      const uint8_t* st = wring + s * C::kW + rb * kTileBytes;
-      const uint4 c0 = *reinterpret_cast<const uint4*>(st + r * 32 + (0 ^ sw));    // k 0..31
-      const uint4 c1 = *reinterpret_cast<const uint4*>(st + r * 32 + (16 ^ sw));   // k 32..63
-      const uint4* pr = reinterpret_cast<const uint4*>(st + kTileCodes + (q >> 1) * 256);   // this group's pairs
+    const int c4 = lane & 3;                    // this thread's columns: c4, c4+4, ... (k pairs 4i + c4)
+    const uint32_t trow = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + kACol + 32u * (tile * RB + rb);
+    // Software-pipelined by one chunk: the stores of chunk c are issued, then
+    // chunk c+1 is loaded and converted in registers while they complete, and
+    // only then does the warp wait for them and take the barrier.  a[0..15]
+    // are TMEM lanes 32q + (0..15), a[16..31] lanes 32q + (16..31), each in the
+    // 16x128b register order: a[16h + 2i + w] is channel 32q + 16h + lane/4 + 8w,
+    // column 4i + c4.
+    uint32_t a[32];
+    // Waits for the weight stage of chunk c (false when the wait gave up).
+    auto wait_w = [&](int c) -> bool {
+      return __all_sync(0xffffffffu, mbar_wait(&wfull[c % SW], (c / SW) & 1, kWaitLimit, abort_flag));
+    };
+    // Loads and converts this warp's tile of chunk c (its stage has landed)
+    // into a[] and releases the weight stage.
+    auto convert = [&](int c) {
+      const int s = c % SW;
+      if (tile < min(KT, nk - KT * c)) {
+        const uint8_t* st = wring + s * C::kWStage + (rb * KT + tile) * kTileBytes;
+        // codes of channels 32q + lane/4 + 8w (w = 0..3): k pairs 4i + c4 for i = 0..3, then i = 4..7
+        const uint4 w0 = *reinterpret_cast<const uint4*>(st + q * 1024 + lane * 16);
+        const uint4 w1 = *reinterpret_cast<const uint4*>(st + q * 1024 + 512 + lane * 16);
+        // this 64-channel group's (scale, min) pairs for k pairs 4i + c4: unit u holds i = 2u, 2u+1
+        const uint4* pr = reinterpret_cast<const uint4*>(st + kTileCodes + (q >> 1) * 256) + c4;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {   // columns 16h .. 16h+15 (k 32h .. 32h+31)
-        const uint4 c = h ? c1 : c0;
-        const uint32_t words[4] = {c.x, c.y, c.z, c.w};
-        uint32_t a[16];
+        for (int u = 0; u < 4; ++u) {
+          const uint4 pv = pr[4 * u];
+          const uint4 cw = u < 2 ? w0 : w1;
+          const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
 #pragma unroll
-        for (int wd = 0; wd < 4; ++wd) {
-          const uint4 m01 = pr[8 * h + 2 * wd], m23 = pr[8 * h + 2 * wd + 1];   // (scale, min), 4 columns
-          const uint32_t x = words[wd], y = x >> 8;
-          a[4 * wd + 0] = hfma2_u(hfma2_u(lop_mask_or(x, 0x000F000Fu, kMagic), kOne, kNegMagic), m01.x, m01.y);
-          a[4 * wd + 1] = hfma2_u(hfma2_u(lop_mask_or(x, 0x00F000F0u, kMagic), kSixteenth, kNeg64), m01.z, m01.w);
-          a[4 * wd + 2] = hfma2_u(hfma2_u(lop_mask_or(y, 0x000F000Fu, kMagic), kOne, kNegMagic), m23.x, m23.y);
-          a[4 * wd + 3] = hfma2_u(hfma2_u(lop_mask_or(y, 0x00F000F0u, kMagic), kSixteenth, kNeg64), m23.z, m23.w);
+          for (int hi = 0; hi < 2; ++hi) {
+            const int i = 2 * u + hi, e = i & 3;   // column 4i + c4: nibble slots e and e+4
+            const uint32_t s2 = hi ? pv.z : pv.x, m2 = hi ? pv.w : pv.y;
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+              const uint32_t x = e >= 2 ? words[w] >> 8 : words[w];
+              a[16 * (w >> 1) + 2 * i + (w & 1)] =
+                  (e & 1) ? hfma2_u(hfma2_u(lop_mask_or(x, 0x00F000F0u, kMagic), kSixteenth, kNeg64), s2, m2)
+                          : hfma2_u(hfma2_u(lop_mask_or(x, 0x000F000Fu, kMagic), kOne, kNegMagic), s2, m2);
+            }
+          }
         }
-        if (h == 1) {
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&wempty[s]);   // this k tile's codes and pairs are in registers
-        }
-        tmem_st_32x32b_x16(trow + 32u * RB * sl + 16u * h, a);
       }
-      // the X tile of this slot has landed too, then the slot is ready for the MMAs
-      ok = __all_sync(0xffffffffu, mbar_wait(&xfull[sl], (i / SL) & 1, kWaitLimit, abort_flag));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&wempty[s]);   // this warp's codes and pairs are in registers
+    };
+    bool ok = nch > 0 && wait_w(0);
+    if (ok) convert(0);
+    for (int c = 0; c < nch; ++c) {
+      const int b = c % NB;
+      // X stage b holds chunk c (so TMEM buffer b is free too), and the next
+      // chunk's weights have landed: the two waits of the chunk, back to back.
+      // The warp-wide tcgen05.st below needs every lane.
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&xfull[b], (c / NB) & 1, kWaitLimit, abort_flag)) &&
+                   (c + 1 >= nch || wait_w(c + 1));
+      if (ok && tile < min(KT, nk - KT * c)) {
+        tc_fence_after();
+        tmem_st_16x128b_x8(trow + b * C::kBufCols, a);
+        tmem_st_16x128b_x8(trow + (16u << 16) + b * C::kBufCols, a + 16);
+      }
+      if (ok && c + 1 < nch) convert(c + 1);
       tmem_st_wait();
       tc_fence_before();
-      __syncwarp();
-      if (lane == 0) add_release_u32(&ready[sl], 1u);
-      if (!ok) break;
+      named_bar_sync(kChunkBarrier, C::kBarThreads);
     }
   }
 

@@ -167,6 +167,18 @@ __device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_
       "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
 }
+// 16 lanes x 32 consecutive 32-bit columns from 16 registers per thread:
+// register 2i of thread t goes to lane (taddr.lane + t/4), column
+// (taddr.col + 4i + t%4); register 2i+1 to lane (taddr.lane + t/4 + 8), same
+// column.  taddr.lane is the warp's lane quarter base, or that base + 16.
+__device__ __forceinline__ void tmem_st_16x128b_x8(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x128b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+      "%12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
 __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -190,6 +202,15 @@ __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wa
 // serialization) be scheduled once every CTA of this grid has issued this.
 __device__ __forceinline__ void griddep_launch() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---- named barriers --------------------------------------------------------------
+// CTA barrier `id` (1..15; 0 is __syncthreads) over `threads` threads, a
+// multiple of 32, whole warps.  Orders the memory accesses of the arriving
+// threads before those after it.  Every participant must reach it the same
+// number of times.
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
 // ---- descriptors ---------------------------------------------------------------

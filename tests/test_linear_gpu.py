@@ -93,9 +93,11 @@ def test_linear_repeatable(fg, packed):
 def test_pack_layout(fg):
     """fg_pack_weight's layout as its declaration states it, rebuilt here in
     numpy from the [K][N/2] codes and [K][N/64] (min, scale): 4608-byte
-    blocks per (128-channel tile, 64-k tile); channel r's 32 code bytes with
-    halves swapped when bit 2 of r is set, nibbles k0 k2 k4 k6 k1 k3 k5 k7
-    per word; then per (group, k pair) fp16 (scale, scale') and (min, min')."""
+    blocks per (128-channel tile, 64-k tile).  Codes in 16-byte units
+    [q][g2][t]: word w is channel 32q + t/4 + 8w, k pairs j = 16 g2 + 4e + t%4
+    with k = 2j in nibble slot e and k = 2j+1 in slot e+4.  Then per group
+    16-byte units [u][c4]: fp16 (scale, scale') and (min, min') for the k
+    pairs j = 8u + c4 and 8u + 4 + c4."""
     K, N = 192, 384
     w16 = synth.normal((K, N), 5, synth.WEIGHT_STD, torch.float16, "cuda")
     W = fg.QuantWeight.from_dense(w16, True, pack=True)
@@ -104,29 +106,33 @@ def test_pack_layout(fg):
     nib = np.empty((K, N), dtype=np.uint32)
     nib[:, 0::2] = codes & 15
     nib[:, 1::2] = codes >> 4
-    slot_of_j = [0, 4, 1, 5, 2, 6, 3, 7]
-    words = np.zeros((N, K // 8), dtype=np.uint32)           # channel n, k = 8w..8w+7
-    for j in range(8):
-        words |= nib[j::8, :].T << np.uint32(4 * slot_of_j[j])
     sc = W.scales.cpu().numpy().astype(np.float16)    # [K][N/64], rounded to nearest even
     mn = W.mins.cpu().numpy().astype(np.float16)
     packed = W.packed.cpu().numpy()
     assert packed.size == K * N // 2 + K * N // 16
     blocks = packed.reshape(N // 128, K // 64, 4608)
+    lane = np.arange(32)
     for t in range(N // 128):
         for u in range(K // 64):
             blk = blocks[t, u]
-            cw = blk[:4096].view(np.uint32).reshape(128, 2, 4)
-            for r in range(128):
-                sw = (r >> 2) & 1
-                for c in range(2):
-                    want = words[128 * t + r, 8 * u + 4 * c: 8 * u + 4 * c + 4]
-                    assert np.array_equal(cw[r, c ^ sw], want), (t, u, r, c)
-            pr = blk[4096:].view(np.float16).reshape(2, 32, 4)
+            cw = blk[:4096].view(np.uint32).reshape(4, 2, 32, 4)
+            for q in range(4):
+                for g2 in range(2):
+                    for w in range(4):
+                        n = 128 * t + 32 * q + lane // 4 + 8 * w           # per lane
+                        want = np.zeros(32, dtype=np.uint32)
+                        for e in range(4):
+                            k = 64 * u + 2 * (16 * g2 + 4 * e + lane % 4)
+                            want |= nib[k, n] << np.uint32(4 * e)
+                            want |= nib[k + 1, n] << np.uint32(4 * (e + 4))
+                        assert np.array_equal(cw[q, g2, :, w], want), (t, u, q, g2, w)
+            pr = blk[4096:].view(np.uint16).reshape(2, 4, 4, 2, 4)   # [gl][u][c4][hi][s, s', m, m']
             for gl in range(2):
                 g = 2 * t + gl
-                ks = slice(64 * u, 64 * u + 64)
-                assert np.array_equal(pr[gl, :, 0].view(np.uint16), sc[ks, g][0::2].view(np.uint16))
-                assert np.array_equal(pr[gl, :, 1].view(np.uint16), sc[ks, g][1::2].view(np.uint16))
-                assert np.array_equal(pr[gl, :, 2].view(np.uint16), mn[ks, g][0::2].view(np.uint16))
-                assert np.array_equal(pr[gl, :, 3].view(np.uint16), mn[ks, g][1::2].view(np.uint16))
+                for uu in range(4):
+                    for c4 in range(4):
+                        for hi in range(2):
+                            k = 64 * u + 2 * (8 * uu + 4 * hi + c4)
+                            got = pr[gl, uu, c4, hi]
+                            want = np.array([sc[k, g], sc[k + 1, g], mn[k, g], mn[k + 1, g]]).view(np.uint16)
+                            assert np.array_equal(got, want), (t, u, gl, uu, c4, hi)
