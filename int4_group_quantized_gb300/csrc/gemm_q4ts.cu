@@ -59,6 +59,9 @@ constexpr int BK = 64;
 constexpr int BNC = 128;               // channels per row block (the MMA's M)
 constexpr int kDqWarp0 = 4;            // dequantization warps start here
 constexpr uint32_t kWaitLimit = 1u << 24;
+// The copy producers run stages ahead and usually find their ring full; they
+// poll with this pause so that they leave the issue slots to the converters.
+constexpr uint32_t kProducerSleepNs = 100;
 
 // ---- packing -------------------------------------------------------------------
 // The decode copy is one 4608-byte block per (128-channel tile nt, 64-k tile
@@ -164,7 +167,8 @@ struct TsCfg {
   static constexpr int kGroupWarps = 4 * RB;          // warps converting one k tile (all row blocks)
   static constexpr int kDqWarps = kT * kGroupWarps;
   static constexpr int kThreads = 128 + kDqWarps * 32;   // warps 0..3, then the dequantization warps
-  static constexpr int kBarThreads = 32 + kDqWarps * 32; // the MMA warp and the dequantization warps
+  static constexpr int kBarThreads = 64 + kDqWarps * 32;   // MMA warp, sync warp, dequantization warps
+  static constexpr int kStartThreads = 32 + kDqWarps * 32; // sync warp, dequantization warps
   static constexpr int kX = BT * BK * 2;              // X tile, K-major, 128-byte swizzle
   static constexpr int kXStage = kT * kX;
   static constexpr int kWStage = kT * RB * kTileBytes;   // a chunk's packed blocks, [rb][t]
@@ -186,7 +190,9 @@ struct TsCfg {
   static_assert(kXBytes + kWBytes >= BT * RB * BNC * 4, "a split partial is staged in the drained rings");
 };
 
-constexpr uint32_t kChunkBarrier = 1;   // named barrier id (0 is __syncthreads)
+constexpr uint32_t kChunkBarrier = 1;   // named barrier ids (0 is __syncthreads)
+constexpr uint32_t kStartBarrier = 2;
+constexpr int kSyncWarp = 3;
 
 template <int BT, int RB>
 __global__ void __launch_bounds__(TsCfg<BT, RB>::kThreads, TsCfg<BT, RB>::kMinBlocks)
@@ -228,7 +234,7 @@ __global__ void __launch_bounds__(TsCfg<BT, RB>::kThreads, TsCfg<BT, RB>::kMinBl
     for (int i = 0; i < NB; ++i) mbar_init(&xfull[i], 1);
     for (int i = 0; i < SW; ++i) {
       mbar_init(&wfull[i], 1);
-      mbar_init(&wempty[i], C::kDqWarps);
+      mbar_init(&wempty[i], 1);        // the sync warp, once every warp has converted the stage
     }
     for (int i = 0; i < NB; ++i) mbar_init(&bufdone[i], 1);   // the MMA commit
     mbar_init(done, 1);
@@ -252,7 +258,7 @@ __global__ void __launch_bounds__(TsCfg<BT, RB>::kThreads, TsCfg<BT, RB>::kMinBl
       for (int c = 0; c < nch; ++c) {
         const int s = c % SW;
         const uint32_t bytes = static_cast<uint32_t>(min(KT, nk - KT * c) * kTileBytes);
-        if (!mbar_wait(&wempty[s], ((c / SW) & 1) ^ 1, kWaitLimit, abort_flag)) break;
+        if (!mbar_wait_sleep(&wempty[s], ((c / SW) & 1) ^ 1, kWaitLimit, abort_flag, kProducerSleepNs)) break;
         mbar_expect_tx(&wfull[s], bytes * RB);
 #pragma unroll
         for (int rb = 0; rb < RB; ++rb)
@@ -273,7 +279,7 @@ __global__ void __launch_bounds__(TsCfg<BT, RB>::kThreads, TsCfg<BT, RB>::kMinBl
       for (int c = 0; c < nch; ++c) {
         const int s = c % NB, n = min(KT, nk - KT * c);
         // the MMAs of chunk c - NB (stage and buffer s) have completed
-        if (!mbar_wait(&bufdone[s], ((c / NB) & 1) ^ 1, kWaitLimit, abort_flag)) break;
+        if (!mbar_wait_sleep(&bufdone[s], ((c / NB) & 1) ^ 1, kWaitLimit, abort_flag, kProducerSleepNs)) break;
         mbar_expect_tx(&xfull[s], n * C::kX);
         for (int t = 0; t < n; ++t)
           tma_load_2d(xring + s * C::kXStage + t * C::kX, &p.mapX, (kt0 + KT * c + t) * BK, 0, &xfull[s]);
@@ -316,6 +322,27 @@ __global__ void __launch_bounds__(TsCfg<BT, RB>::kThreads, TsCfg<BT, RB>::kMinBl
       mma_commit(done);
       if (*abort_flag) atomicOr(p.err, DEV_ERR_WAIT_TIMEOUT);
     }
+  } else if (warp == kSyncWarp) {
+    // Waits, on behalf of the warps that take the chunk barrier, for what the
+    // next chunk needs, so that the dequantization warps touch no mbarrier:
+    // before chunk barrier c, X stage of chunk c+1 (its TMEM buffer free too)
+    // and the weights of chunk c+2; after it, releases the weight stages that
+    // have been converted by then.
+    bool ok = nch > 0 && mbar_wait(&wfull[0], 0, kWaitLimit, abort_flag) &&
+              (nch < 2 || mbar_wait(&wfull[1 % SW], (1 / SW) & 1, kWaitLimit, abort_flag)) &&
+              mbar_wait(&xfull[0], 0, kWaitLimit, abort_flag);
+    named_bar_sync(kStartBarrier, C::kStartThreads);
+    for (int c = 0; c < nch; ++c) {
+      if (ok && c + 1 < nch) ok = mbar_wait(&xfull[(c + 1) % NB], ((c + 1) / NB) & 1, kWaitLimit, abort_flag);
+      if (ok && c + 2 < nch) ok = mbar_wait(&wfull[(c + 2) % SW], ((c + 2) / SW) & 1, kWaitLimit, abort_flag);
+      __syncwarp();
+      named_bar_sync(kChunkBarrier, C::kBarThreads);
+      // chunks up to c+1 are converted now
+      if (lane == 0) {
+        if (c == 0) mbar_arrive(&wempty[0]);
+        if (c + 1 < nch) mbar_arrive(&wempty[(c + 1) % SW]);
+      }
+    }
   } else if (warp >= kDqWarp0) {
     const int d = warp - kDqWarp0;
     const int tile = d / C::kGroupWarps;        // the k tile of each chunk this warp converts
@@ -330,58 +357,60 @@ __global__ void __launch_bounds__(TsCfg<BT, RB>::kThreads, TsCfg<BT, RB>::kMinBl
     // 16x128b register order: a[16h + 2i + w] is channel 32q + 16h + lane/4 + 8w,
     // column 4i + c4.
     uint32_t a[32];
-    // Waits for the weight stage of chunk c (false when the wait gave up).
-    auto wait_w = [&](int c) -> bool {
-      return __all_sync(0xffffffffu, mbar_wait(&wfull[c % SW], (c / SW) & 1, kWaitLimit, abort_flag));
+    // This warp's tile of chunk c, loaded from its weight stage (landed):
+    // codes of channels 32q + lane/4 + 8w (w = 0..3) at k pairs 4i + c4, i =
+    // 0..3 in w0 and 4..7 in w1; this 64-channel group's (scale, min) pairs
+    // for those k pairs, unit u holding i = 2u and 2u+1.
+    uint4 w0, w1, pv[4];
+    auto load = [&](int c) {
+      const uint8_t* st = wring + (c % SW) * C::kWStage + (rb * KT + tile) * kTileBytes;
+      w0 = *reinterpret_cast<const uint4*>(st + q * 1024 + lane * 16);
+      w1 = *reinterpret_cast<const uint4*>(st + q * 1024 + 512 + lane * 16);
+      const uint4* pr = reinterpret_cast<const uint4*>(st + kTileCodes + (q >> 1) * 256) + c4;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) pv[u] = pr[4 * u];
     };
-    // Loads and converts this warp's tile of chunk c (its stage has landed)
-    // into a[] and releases the weight stage.
-    auto convert = [&](int c) {
-      const int s = c % SW;
-      if (tile < min(KT, nk - KT * c)) {
-        const uint8_t* st = wring + s * C::kWStage + (rb * KT + tile) * kTileBytes;
-        // codes of channels 32q + lane/4 + 8w (w = 0..3): k pairs 4i + c4 for i = 0..3, then i = 4..7
-        const uint4 w0 = *reinterpret_cast<const uint4*>(st + q * 1024 + lane * 16);
-        const uint4 w1 = *reinterpret_cast<const uint4*>(st + q * 1024 + 512 + lane * 16);
-        // this 64-channel group's (scale, min) pairs for k pairs 4i + c4: unit u holds i = 2u, 2u+1
-        const uint4* pr = reinterpret_cast<const uint4*>(st + kTileCodes + (q >> 1) * 256) + c4;
+    // Converts what load() fetched into a[].
+    auto convert = [&]() {
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const uint4 pv = pr[4 * u];
-          const uint4 cw = u < 2 ? w0 : w1;
-          const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+      for (int u = 0; u < 4; ++u) {
+        const uint4 cw = u < 2 ? w0 : w1;
+        const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
 #pragma unroll
-          for (int hi = 0; hi < 2; ++hi) {
-            const int i = 2 * u + hi, e = i & 3;   // column 4i + c4: nibble slots e and e+4
-            const uint32_t s2 = hi ? pv.z : pv.x, m2 = hi ? pv.w : pv.y;
+        for (int hi = 0; hi < 2; ++hi) {
+          const int i = 2 * u + hi, e = i & 3;   // column 4i + c4: nibble slots e and e+4
+          const uint32_t s2 = hi ? pv[u].z : pv[u].x, m2 = hi ? pv[u].w : pv[u].y;
 #pragma unroll
-            for (int w = 0; w < 4; ++w) {
-              const uint32_t x = e >= 2 ? words[w] >> 8 : words[w];
-              a[16 * (w >> 1) + 2 * i + (w & 1)] =
-                  (e & 1) ? hfma2_u(hfma2_u(lop_mask_or(x, 0x00F000F0u, kMagic), kSixteenth, kNeg64), s2, m2)
-                          : hfma2_u(hfma2_u(lop_mask_or(x, 0x000F000Fu, kMagic), kOne, kNegMagic), s2, m2);
-            }
+          for (int w = 0; w < 4; ++w) {
+            const uint32_t x = e >= 2 ? words[w] >> 8 : words[w];
+            a[16 * (w >> 1) + 2 * i + (w & 1)] =
+                (e & 1) ? hfma2_u(hfma2_u(lop_mask_or(x, 0x00F000F0u, kMagic), kSixteenth, kNeg64), s2, m2)
+                        : hfma2_u(hfma2_u(lop_mask_or(x, 0x000F000Fu, kMagic), kOne, kNegMagic), s2, m2);
           }
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&wempty[s]);   // this warp's codes and pairs are in registers
     };
-    bool ok = nch > 0 && wait_w(0);
-    if (ok) convert(0);
+    auto mine = [&](int c) { return tile < min(KT, nk - KT * c); };   // a ragged last chunk has one tile
+    // The sync warp has seen the weights of chunks 0 and 1 land and X stage 0
+    // fill before this barrier, and before chunk barrier c those of chunk c+2
+    // and X stage c+1 (which also means TMEM buffer (c+1) % NB is free).
+    named_bar_sync(kStartBarrier, C::kStartThreads);
+    if (nch > 0 && mine(0)) {
+      load(0);
+      convert();
+    }
     for (int c = 0; c < nch; ++c) {
       const int b = c % NB;
-      // X stage b holds chunk c (so TMEM buffer b is free too), and the next
-      // chunk's weights have landed: the two waits of the chunk, back to back.
-      // The warp-wide tcgen05.st below needs every lane.
-      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&xfull[b], (c / NB) & 1, kWaitLimit, abort_flag)) &&
-                   (c + 1 >= nch || wait_w(c + 1));
-      if (ok && tile < min(KT, nk - KT * c)) {
+      // chunk c+1's loads go out before chunk c's stores: a load queued
+      // behind a tensor-memory store waits for it
+      const bool next = c + 1 < nch && mine(c + 1);
+      if (next) load(c + 1);
+      if (mine(c)) {
         tc_fence_after();
         tmem_st_16x128b_x8(trow + b * C::kBufCols, a);
         tmem_st_16x128b_x8(trow + (16u << 16) + b * C::kBufCols, a + 16);
       }
-      if (ok && c + 1 < nch) convert(c + 1);
+      if (next) convert();
       tmem_st_wait();
       tc_fence_before();
       named_bar_sync(kChunkBarrier, C::kBarThreads);
@@ -459,7 +488,7 @@ __global__ void __launch_bounds__(TsCfg<BT, RB>::kThreads, TsCfg<BT, RB>::kMinBl
   if (threadIdx.x == 0) {
     bulk_store(myblk, stage, static_cast<uint32_t>(blk * 4));
     bulk_commit();
-    bulk_wait_all();   // complete before the CTA (and its shared memory) goes away
+    bulk_wait_read_all();   // the source is read before the CTA (and its shared memory) goes away
   }
 }
 
