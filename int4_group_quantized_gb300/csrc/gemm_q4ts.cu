@@ -59,6 +59,7 @@ constexpr int BK = 64;
 constexpr int BNC = 128;               // channels per row block (the MMA's M)
 constexpr int kDqWarp0 = 4;            // dequantization warps start here
 constexpr uint32_t kWaitLimit = 1u << 24;
+constexpr int kMaxSplits = 16;         // K splits of a decode product (splits_for)
 // The copy producers run stages ahead and usually find their ring full; they
 // poll with this pause so that they leave the issue slots to the converters.
 constexpr uint32_t kProducerSleepNs = 100;
@@ -495,6 +496,7 @@ __global__ void __launch_bounds__(TsCfg<BT, RB>::kThreads, TsCfg<BT, RB>::kMinBl
 // Y = epilogue(sum of the K splits' partial blocks in split order), over the
 // whole GPU.  Launched right after gemm_q4ts_kernel with programmatic stream
 // serialization: it may be scheduled early and waits for the partials.
+template <int MAXS>
 __global__ void __launch_bounds__(256) splitk_sum_kernel(const float* __restrict__ part, int splits, int M, int N,
                                                          int nch, int n_tiles, const __half* __restrict__ R,
                                                          int ldr, int relu, __half* __restrict__ Y, int ldy) {
@@ -508,15 +510,21 @@ __global__ void __launch_bounds__(256) splitk_sum_kernel(const float* __restrict
     const int64_t flat = 4 * e;
     const int m = static_cast<int>(flat / N), n = static_cast<int>(flat % N);
     const float* src = part + (static_cast<size_t>(n / nch) * M + m) * nch + n % nch;
-    float4 a4 = __ldcg(reinterpret_cast<const float4*>(src));
-#pragma unroll 4
-    for (int s = 1; s < splits; ++s) {
-      const float4 v = __ldcg(reinterpret_cast<const float4*>(src + s * sstride));
-      a4.x += v.x;
-      a4.y += v.y;
-      a4.z += v.z;
-      a4.w += v.w;
-    }
+    // every split's load in flight at once (latency, not bandwidth, bounds
+    // this kernel), then the sum in split order
+    float4 v[MAXS];
+#pragma unroll
+    for (int s = 0; s < MAXS; ++s)
+      if (s < splits) v[s] = __ldcg(reinterpret_cast<const float4*>(src + s * sstride));
+    float4 a4 = v[0];
+#pragma unroll
+    for (int s = 1; s < MAXS; ++s)
+      if (s < splits) {
+        a4.x += v[s].x;
+        a4.y += v[s].y;
+        a4.z += v[s].z;
+        a4.w += v[s].w;
+      }
     if (R) {
       const uint2 rr = *reinterpret_cast<const uint2*>(R + static_cast<size_t>(m) * ldr + n);
       const float2 r01 = __half22float2(*reinterpret_cast<const __half2*>(&rr.x));
@@ -574,8 +582,13 @@ fg_status launch_ts(TsParams& p, cudaStream_t st) {
   rc.attrs = attr;
   rc.numAttrs = 1;
   trace_extra_launch();
-  if (cudaLaunchKernelEx(&rc, splitk_sum_kernel, static_cast<const float*>(p.part), p.splits, p.M, p.N, BNC * RB,
-                         p.n_tiles, p.R, p.ldr, p.relu, p.Y, p.ldy) != cudaSuccess)
+  // the kernel holds every split's load in registers: the smallest bucket
+  // that fits, so that few splits keep few registers
+  auto sum = p.splits <= 2 ? splitk_sum_kernel<2>
+             : p.splits <= 4 ? splitk_sum_kernel<4>
+             : p.splits <= 8 ? splitk_sum_kernel<8> : splitk_sum_kernel<kMaxSplits>;
+  if (cudaLaunchKernelEx(&rc, sum, static_cast<const float*>(p.part), p.splits, p.M, p.N, BNC * RB, p.n_tiles, p.R,
+                         p.ldr, p.relu, p.Y, p.ldy) != cudaSuccess)
     return check_launch("splitk_sum_kernel (launch)");
   return check_launch("splitk_sum_kernel");
 }
@@ -596,7 +609,7 @@ int splits_for(int64_t M, int64_t N, int64_t K, int rb) {
   const int64_t slots = (rb == 1 && M <= 128 ? 2 : 1) * static_cast<int64_t>(num_sms());
   int64_t best = 1;
   double best_cost = 1e30;
-  for (int64_t s = 1; s <= 16 && s <= ktiles / 2; ++s) {
+  for (int64_t s = 1; s <= kMaxSplits && s <= ktiles / 2; ++s) {
     const int64_t waves = (tiles * s + slots - 1) / slots;
     const double cost = static_cast<double>(waves) * ((ktiles + s - 1) / s) + (s > 1 ? 2.0 + 0.5 * s : 0.0);
     if (cost < best_cost) {
