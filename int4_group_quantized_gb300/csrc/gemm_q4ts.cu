@@ -30,10 +30,11 @@
 // the residual, the workspace and Y are touched only after it.
 //
 // Warp roles (128 + 256*RB threads): warp 0 issues the weight copies, warp 2
-// the X copies, warp 1 owns TMEM and issues the MMAs, warps 4.. dequantize,
-// and the first 4*RB of them drain TMEM.  Every mbarrier wait is bounded and
-// raises the device error word on timeout; the one named barrier is taken
-// the same number of times by all of its warps.
+// the X copies, warp 1 owns TMEM and issues the MMAs, warp 3 (the sync warp)
+// waits on the copies' mbarriers for the converting warps, warps 4..
+// dequantize, and the first 4*RB of them drain TMEM.  Every mbarrier wait is
+// bounded and raises the device error word on timeout; each named barrier is
+// taken the same number of times by all of its warps.
 #include <cudaTypedefs.h>
 #include <string.h>
 
