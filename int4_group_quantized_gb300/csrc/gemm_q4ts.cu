@@ -179,15 +179,17 @@ struct TsCfg {
   static constexpr uint32_t kTmemCols = (RB == 1 && BT <= 128) ? 256 : 512;
   static constexpr int kMinBlocks = kTmemCols == 256 ? 2 : 1;
   static constexpr int kBudget = kMinBlocks == 2 ? 104 * 1024 : 204 * 1024;
-  // TMEM A buffers; X stage b goes with buffer b
-  static constexpr int kBufs = cmin(cmin(4, (static_cast<int>(kTmemCols) - RB * kAcc) / kBufCols),
-                                    cmax(2, (kBudget * 5 / 8) / kXStage));
-  static constexpr int kWStages = cmin(8, (kBudget - kBufs * kXStage) / kWStage);
-  static constexpr int kXBytes = kBufs * kXStage;
+  // TMEM A buffers, and X stages (no more than the buffers: every parity
+  // wait on a buffer's commit barrier then sees its phase before the next)
+  static constexpr int kBufs = cmin(4, (static_cast<int>(kTmemCols) - RB * kAcc) / kBufCols);
+  static constexpr int kXStages = cmax(2, cmin(kBufs, (kBudget * 5 / 8) / kXStage));
+  static constexpr int kWStages = cmin(8, (kBudget - kXStages * kXStage) / kWStage);
+  static constexpr int kXBytes = kXStages * kXStage;
   static constexpr int kWBytes = kWStages * kWStage;
-  static constexpr int kBarBytes = (2 * (kBufs + kWStages) + 1) * 8 + 16;   // + done, TMEM slot, flag
+  static constexpr int kBarBytes = (kXStages + 2 * kWStages + kBufs + 1) * 8 + 16;   // + done, TMEM slot, flag
   static constexpr int kTotal = 1024 + kXBytes + kWBytes + kBarBytes;
   static_assert(kBufs >= 2 && kWStages >= 2, "pipeline needs two stages");
+  static_assert(kXStages <= kBufs, "X stages are freed by buffer commits");
   static_assert(kX % 1024 == 0, "X tiles stay 1024-byte aligned");
   static_assert(kXBytes + kWBytes >= BT * RB * BNC * 4, "a split partial is staged in the drained rings");
 };
@@ -200,18 +202,17 @@ template <int BT, int RB>
 __global__ void __launch_bounds__(TsCfg<BT, RB>::kThreads, TsCfg<BT, RB>::kMinBlocks)
     gemm_q4ts_kernel(const __grid_constant__ TsParams p) {
   using C = TsCfg<BT, RB>;
-  constexpr int KT = C::kT, NB = C::kBufs, SW = C::kWStages;
+  constexpr int KT = C::kT, NB = C::kBufs, SX = C::kXStages, SW = C::kWStages;
   constexpr uint32_t kIdesc = idesc_f16(128, BT, 0, 0);   // A (TMEM) and B (X) K-major
   constexpr uint32_t kACol = RB * C::kAcc;                // TMEM A buffers follow the accumulators
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* xring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* wring = xring + C::kXBytes;
-  // xfull[b]: X stage b has landed, and it was requested only once the MMAs
-  // that last read X stage b and TMEM buffer b had completed, so it also
-  // means "buffer b is free"
+  // xfull[x]: X stage x has landed (chunk c uses stage c % SX); it is
+  // requested once the MMAs of chunk c - SX, the last to read it, completed
   uint64_t* xfull = reinterpret_cast<uint64_t*>(wring + C::kWBytes);
-  uint64_t* wfull = xfull + NB;
+  uint64_t* wfull = xfull + SX;
   uint64_t* wempty = wfull + SW;     // one arrival per dequantization warp
   uint64_t* bufdone = wempty + SW;   // TMEM A buffer read by its MMAs
   uint64_t* done = bufdone + NB;
@@ -233,7 +234,7 @@ __global__ void __launch_bounds__(TsCfg<BT, RB>::kThreads, TsCfg<BT, RB>::kMinBl
   griddep_launch();   // a dependent grid waits for this one before it reads Y
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < NB; ++i) mbar_init(&xfull[i], 1);
+    for (int i = 0; i < SX; ++i) mbar_init(&xfull[i], 1);
     for (int i = 0; i < SW; ++i) {
       mbar_init(&wfull[i], 1);
       mbar_init(&wempty[i], 1);        // the sync warp, once every warp has converted the stage
@@ -279,17 +280,19 @@ __global__ void __launch_bounds__(TsCfg<BT, RB>::kThreads, TsCfg<BT, RB>::kMinBl
       griddep_wait();   // X comes from the previous kernel
       int issued = 0;
       for (int c = 0; c < nch; ++c) {
-        const int s = c % NB, n = min(KT, nk - KT * c);
-        // the MMAs of chunk c - NB (stage and buffer s) have completed
-        if (!mbar_wait_sleep(&bufdone[s], ((c / NB) & 1) ^ 1, kWaitLimit, abort_flag, kProducerSleepNs)) break;
+        const int s = c % SX, n = min(KT, nk - KT * c);
+        // the MMAs of chunk c - SX, the last to read stage s, have completed
+        if (c >= SX && !mbar_wait_sleep(&bufdone[(c - SX) % NB], ((c - SX) / NB) & 1, kWaitLimit, abort_flag,
+                                        kProducerSleepNs))
+          break;
         mbar_expect_tx(&xfull[s], n * C::kX);
         for (int t = 0; t < n; ++t)
           tma_load_2d(xring + s * C::kXStage + t * C::kX, &p.mapX, (kt0 + KT * c + t) * BK, 0, &xfull[s]);
         ++issued;
       }
-      for (int c = max(0, issued - NB); c < issued; ++c) {
+      for (int c = max(0, issued - SX); c < issued; ++c) {
         volatile int dummy = 0;
-        mbar_wait(&xfull[c % NB], (c / NB) & 1, kWaitLimit, &dummy);
+        mbar_wait(&xfull[c % SX], (c / SX) & 1, kWaitLimit, &dummy);
       }
       if (*abort_flag) atomicOr(p.err, DEV_ERR_WAIT_TIMEOUT);
     }
@@ -303,7 +306,7 @@ __global__ void __launch_bounds__(TsCfg<BT, RB>::kThreads, TsCfg<BT, RB>::kMinBl
         const int b = c % NB;
         if (!*abort_flag) {
           for (int t = 0; t < n; ++t) {
-            const uint32_t xa = smem_u32(xring + b * C::kXStage + t * C::kX);
+            const uint32_t xa = smem_u32(xring + (c % SX) * C::kXStage + t * C::kX);
 #pragma unroll
             for (int rb = 0; rb < RB; ++rb) {
               const uint32_t ta = tmem_base + kACol + b * C::kBufCols + 32u * (t * RB + rb);
@@ -325,17 +328,19 @@ __global__ void __launch_bounds__(TsCfg<BT, RB>::kThreads, TsCfg<BT, RB>::kMinBl
       if (*abort_flag) atomicOr(p.err, DEV_ERR_WAIT_TIMEOUT);
     }
   } else if (warp == kSyncWarp) {
-    // Waits, on behalf of the warps that take the chunk barrier, for what the
-    // next chunk needs, so that the dequantization warps touch no mbarrier:
-    // before chunk barrier c, X stage of chunk c+1 (its TMEM buffer free too)
-    // and the weights of chunk c+2; after it, releases the weight stages that
-    // have been converted by then.
+    // Waits, on behalf of the warps that take the chunk barrier, for what
+    // comes after it, so that the dequantization warps touch no mbarrier:
+    // before chunk barrier c, chunk c's X tiles (for the MMA warp), TMEM
+    // buffer (c+1) % NB free (the MMAs of chunk c+1-NB done) and the weights
+    // of chunk c+2 (for the converting warps); after it, releases the weight
+    // stages that have been converted by then.
     bool ok = nch > 0 && mbar_wait(&wfull[0], 0, kWaitLimit, abort_flag) &&
-              (nch < 2 || mbar_wait(&wfull[1 % SW], (1 / SW) & 1, kWaitLimit, abort_flag)) &&
-              mbar_wait(&xfull[0], 0, kWaitLimit, abort_flag);
+              (nch < 2 || mbar_wait(&wfull[1 % SW], (1 / SW) & 1, kWaitLimit, abort_flag));
     named_bar_sync(kStartBarrier, C::kStartThreads);
     for (int c = 0; c < nch; ++c) {
-      if (ok && c + 1 < nch) ok = mbar_wait(&xfull[(c + 1) % NB], ((c + 1) / NB) & 1, kWaitLimit, abort_flag);
+      if (ok) ok = mbar_wait(&xfull[c % SX], (c / SX) & 1, kWaitLimit, abort_flag);
+      if (ok && c + 1 < nch && c + 1 >= NB)
+        ok = mbar_wait(&bufdone[(c + 1) % NB], ((c + 1 - NB) / NB) & 1, kWaitLimit, abort_flag);
       if (ok && c + 2 < nch) ok = mbar_wait(&wfull[(c + 2) % SW], ((c + 2) / SW) & 1, kWaitLimit, abort_flag);
       __syncwarp();
       named_bar_sync(kChunkBarrier, C::kBarThreads);
@@ -393,9 +398,9 @@ __global__ void __launch_bounds__(TsCfg<BT, RB>::kThreads, TsCfg<BT, RB>::kMinBl
       }
     };
     auto mine = [&](int c) { return tile < min(KT, nk - KT * c); };   // a ragged last chunk has one tile
-    // The sync warp has seen the weights of chunks 0 and 1 land and X stage 0
-    // fill before this barrier, and before chunk barrier c those of chunk c+2
-    // and X stage c+1 (which also means TMEM buffer (c+1) % NB is free).
+    // The sync warp has seen the weights of chunks 0 and 1 land before this
+    // barrier, and before chunk barrier c those of chunk c+2 and TMEM buffer
+    // (c+1) % NB free.
     named_bar_sync(kStartBarrier, C::kStartThreads);
     if (nch > 0 && mine(0)) {
       load(0);
