@@ -40,6 +40,10 @@ CASES = [
     (33, 2048, 1536, True, True, False, torch.float16),       # ragged 64-row block
     (64, 64, 1024, True, False, False, torch.float16),        # a single k tile
     (130, 4096, 256, True, False, True, torch.float16),       # two tiles, eight K splits
+    # odd k-tile counts: splits whose last two-tile chunk holds one tile
+    (64, 960, 512, True, False, True, torch.float16),         # 15 k tiles, 64-row block
+    (96, 1088, 768, True, True, False, torch.float16),        # 17 k tiles, 128-row block
+    (256, 960, 384, True, False, True, torch.float16),        # 15 k tiles, 256-row block
 ]
 
 # quantized fp16 products with at most 256 rows run on the packed-weight
