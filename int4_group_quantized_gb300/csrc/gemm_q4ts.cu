@@ -159,6 +159,12 @@ constexpr int cmax(int a, int b) { return a > b ? a : b; }
 // same number of chunks and leaves the loop only at its end, so the barrier
 // always completes; a failed (bounded) wait skips the work, not the barrier.
 //
+// The dequantization warps touch no mbarrier: a sync warp takes every wait
+// on their behalf before each chunk barrier (the chunk's X tiles, the next
+// TMEM buffer free, the weights two chunks ahead) and releases the weight
+// stages they have converted after it.  They are software-pipelined by one
+// chunk: chunk c+1 is loaded and converted while chunk c's stores complete.
+//
 // Rings around it, each released by the stage that last needs it: weights
 // (a chunk's packed blocks, one bulk copy per row block; released once every
 // dequantization warp holds its codes in registers), X (a chunk's tiles) and
