@@ -157,11 +157,9 @@ __device__ __forceinline__ void process_block(WarpState<D>& W, int64_t tb, int64
     const float new_m = fmaxf(run_m, m);
     const float alpha = exp2f(run_m - new_m);
     const float p0 = exp2f(sc0 - new_m), p1 = exp2f(sc1 - new_m);
-    float l = p0 + p1;
-    l += __shfl_xor_sync(0xffffffffu, l, 4);
-    l += __shfl_xor_sync(0xffffffffu, l, 8);
-    l += __shfl_xor_sync(0xffffffffu, l, 16);
-    run_l = run_l * alpha + l;
+    // run_l, ps and cmn are kept per lane (this lane's tokens; alpha is the
+    // same in every lane) and reduced across the warp once, after the last block
+    run_l = run_l * alpha + (p0 + p1);
     run_m = new_m;
 
     // value weights p*scale per group, as B fragments for tokens
@@ -177,15 +175,8 @@ __device__ __forceinline__ void process_block(WarpState<D>& W, int64_t tb, int64
       vb[g][0] = pack_h2(a0, a1);
       vb[g][1] = pack_h2(a8, a9);
       const float2 u = unpack_h2(vb[g][0]), v = unpack_h2(vb[g][1]);
-      float s = u.x + u.y + v.x + v.y;   // the fp16 weights the MMA multiplies
-      s += __shfl_xor_sync(0xffffffffu, s, 1);
-      s += __shfl_xor_sync(0xffffffffu, s, 2);
-      ps[g] = ps[g] * alpha + s;
-      float c = p0 * vmn[0][g] + p1 * vmn[1][g];
-      c += __shfl_xor_sync(0xffffffffu, c, 4);
-      c += __shfl_xor_sync(0xffffffffu, c, 8);
-      c += __shfl_xor_sync(0xffffffffu, c, 16);
-      cmn[g] = cmn[g] * alpha + c;
+      ps[g] = ps[g] * alpha + (u.x + u.y + v.x + v.y);   // the fp16 weights the MMA multiplies
+      cmn[g] = cmn[g] * alpha + (p0 * vmn[0][g] + p1 * vmn[1][g]);
     }
 
     // O^T[dim] += sum_t V^T[dim][t] * (p scale)[t]; tile i covers dims
@@ -447,6 +438,19 @@ __global__ void __launch_bounds__(128) decode_attn_mma_kernel(const DecodeArgs a
     process(blk + 1, buf1);
   }
 
+  // the per-lane sums over this warp's tokens: run_l and cmn over the rows gq
+  // (lanes 4 apart), ps over the token pairs of tig (lanes 1 apart)
+  W.run_l += __shfl_xor_sync(0xffffffffu, W.run_l, 4);
+  W.run_l += __shfl_xor_sync(0xffffffffu, W.run_l, 8);
+  W.run_l += __shfl_xor_sync(0xffffffffu, W.run_l, 16);
+#pragma unroll
+  for (int g = 0; g < NG; ++g) {
+    W.ps[g] += __shfl_xor_sync(0xffffffffu, W.ps[g], 1);
+    W.ps[g] += __shfl_xor_sync(0xffffffffu, W.ps[g], 2);
+    W.cmn[g] += __shfl_xor_sync(0xffffffffu, W.cmn[g], 4);
+    W.cmn[g] += __shfl_xor_sync(0xffffffffu, W.cmn[g], 8);
+    W.cmn[g] += __shfl_xor_sync(0xffffffffu, W.cmn[g], 16);
+  }
   merge_warps<D>(W, red_m, red_l, red_o, a, bi, h, bh, sp, warp, lane, gq, tig);
 }
 
