@@ -42,7 +42,9 @@ import synth  # noqa: E402
 
 METRIC = "decode tokens/s (OPT-6.7B shape, int4 W+KV); achieved HBM GB/s vs ~8 TB/s"
 Q4 = 0.5 + 8.0 / 64.0   # bytes per element: 4-bit code + fp32 (min, scale) per 64
-Q4_PACKED = 0.5 + 4.0 / 64.0   # the decode copy of a weight: 4-bit code + fp16 (scale, min) per 64
+# bytes per weight of each decode-copy format (fg_pack_weight): the default
+# carries the stored fp32 pairs, the opt-in one fp16 pairs
+PACK_BYTES = {0: Q4, 1: 0.5 + 4.0 / 64.0}
 
 
 def peaks() -> dict:
@@ -117,13 +119,14 @@ class ClockSampler:
 # algorithmic work (FlexGen notes "背景知识" memory formulas, "附录 A.3" compute terms)
 # ---------------------------------------------------------------------------------------
 
-def decode_product_bytes(w, b) -> float:
+def decode_product_bytes(w, b, pack_format: int = 0) -> float:
     """One decode step of one layer, all four products: every 4-bit weight
     once for the whole block, in the form the decode products read it (the
-    packed copy: 4-bit codes + one fp16 (scale, min) pair per group, Q4_PACKED
-    bytes per weight), plus fp16 activations in, out and residual."""
+    decode copy, PACK_BYTES per weight), plus the fp16 activations they read
+    and write: t in and Q|K|V out; attention output and residual t in, t_Out
+    out; t_Out in, hidden out; hidden and residual t_Out in, t^{i+1} out."""
     h1, h2 = w.h1, w.h2
-    weights = (4 * h1 * h1 + 2 * h1 * h2) * Q4_PACKED
+    weights = (4 * h1 * h1 + 2 * h1 * h2) * PACK_BYTES[pack_format]
     act = 2 * b * ((h1 + 3 * h1) + (h1 + h1 + h1) + (h1 + h2) + (h2 + h1 + h1))
     return weights + act
 
@@ -133,8 +136,10 @@ def decode_product_flops(w, b) -> float:
 
 
 def decode_attn_bytes(w, b, length) -> float:
-    """Read K and V of `length` tokens (4-bit), read q, write the output."""
-    return 2 * b * w.h1 * length * Q4 + 2 * b * w.h1 * 2
+    """The append and attention launch: read K and V of `length` tokens
+    (4-bit, the new one included), write the appended K/V row once, read q
+    and the new K/V rows (fp16), write the output (fp16)."""
+    return 2 * b * w.h1 * length * Q4 + 2 * b * w.h1 * Q4 + 2 * b * w.h1 * 4
 
 
 def prefill_product_flops(w, b, s) -> float:
@@ -145,8 +150,8 @@ def prefill_attn_flops(w, b, s) -> float:
     return 4.0 * b * w.h1 * (s * (s + 1) / 2)
 
 
-def decode_step_bytes(w, b, length) -> float:
-    return decode_product_bytes(w, b) + decode_attn_bytes(w, b, length) + 2 * b * w.h1 * Q4
+def decode_step_bytes(w, b, length, pack_format: int = 0) -> float:
+    return decode_product_bytes(w, b, pack_format) + decode_attn_bytes(w, b, length)
 
 
 # ---------------------------------------------------------------------------------------
@@ -189,7 +194,7 @@ def oracle_decode_sample(w, budget_s: float = 20.0) -> dict:
             "sample": (f"one decode step of one {w.name} layer for all b={w.b} sequences at cache length "
                        f"{length}, weight dequantization included, median of {len(times)}; scaled to "
                        f"l={w.l} layers"),
-            "seconds_per_layer_step": t}
+            "seconds_per_layer_step": t, "samples": len(times)}
 
 
 # ---------------------------------------------------------------------------------------
@@ -217,7 +222,13 @@ def run_reference(args, w, rank, world):
     res = oracle_decode_sample(w)
     line = {"impl": "reference", "metric": METRIC, "value": res["value"], "unit": "tokens/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": res["seconds_per_layer_step"] * w.l * w.n * 1e3, "higher_is_better": True,
+            # not run end to end: the oracle's time for one sampled layer-step,
+            # scaled to the l layers and n decode steps of one bench step
+            "ms_per_step": res["seconds_per_layer_step"] * w.l * w.n * 1e3,
+            "ms_per_step_kind": "scaled from the sample: seconds_per_layer_step * l * n",
+            "sampled_work": {"layer_steps": res["samples"], "seconds_per_layer_step": res["seconds_per_layer_step"],
+                             "b": w.b, "cache_length": w.s + w.n // 2},
+            "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": w.name, "l": w.l, "h1": w.h1, "h2": w.h2, "heads": w.heads, "b": w.b,
                        "s": w.s, "n": w.n},
@@ -313,27 +324,40 @@ def run_ours(args, w, rank, world, device):
     dec_total, tot_total, pre_total = max_over_ranks([dec_total, tot_total, pre_total], world, dev)
     nonfinite = int((~torch.isfinite(outs)).sum().item())
 
-    # end to end through the public API with host buffers: the prompt and each
-    # step's embedding come from pinned host memory, each step's output goes back
+    # end to end through the public API with host buffers: the prompt comes from
+    # pinned host memory before the decode phase (outside the timed region, like
+    # the prefill); inside it, each step's embedding is copied in from pinned
+    # host memory and each step's output copied back
     x_h = x.cpu().pin_memory()
     tin_h = tin.cpu().pin_memory()
     out_h = torch.empty(outs.shape, dtype=outs.dtype, pin_memory=True)
     x_d = torch.empty_like(x)
     t_d = torch.empty_like(tin[0])
     e2e_ms = []
+    h2d_step = d2h_step = 0
     for k in range(args.steps):
         e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
         x_d.copy_(x_h, non_blocking=True)
         fg.fg_prefill_block(blk, x_d, y, ws, st)
         e[0].record(st)
+        h2d_step = d2h_step = 0
         for t in range(w.n):
             t_d.copy_(tin_h[t], non_blocking=True)
+            h2d_step += t_d.numel() * t_d.element_size()
             fg.fg_decode_block_step(blk, t_d, w.s + t, outs[t], ws, st)
             out_h[t].copy_(outs[t], non_blocking=True)
+            d2h_step += outs[t].numel() * outs[t].element_size()
         e[1].record(st)
         torch.cuda.synchronize()
         e2e_ms.append(e[0].elapsed_time(e[1]))
     e2e_dec = max_over_ranks([sum(e2e_ms) / 1e3], world, dev)[0]
+
+    # the same decode layer-steps on finite data: one layer of the stack, its
+    # cache filled by its own prefill of a fresh N(0, 1) prompt, and a fresh
+    # N(0, 1) input at every step (the chained stack above overflows fp16 after
+    # a few layers: the page's layer has no normalisation); per-kernel device
+    # time per layer-step, beside the chained run's
+    finite = finite_layer_steps(fg, w, layers[w.l // 2], dev, st, args.steps)
 
     if rank != 0:
         return
@@ -406,12 +430,44 @@ def run_ours(args, w, rank, world, device):
         "gpu_launches": int(n_launch), "nonfinite_decode_outputs": nonfinite,
         "cpu_baseline": cpu and {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample", "threads")},
         "e2e": {"value": w.b * w.n * K * world / e2e_dec, "unit": "tokens/s",
-                "h2d_bytes_per_step": x.numel() * x.element_size() + tin.numel() * tin.element_size(),
-                "d2h_bytes_per_step": outs.numel() * outs.element_size(),
-                "definition": "decode phase with per-step host->device input and device->host output copies"},
+                "h2d_bytes_per_step": h2d_step, "d2h_bytes_per_step": d2h_step,
+                "definition": ("decode phase through fg_decode_block_step with every step's embedding copied in "
+                               "from pinned host memory and its output copied back, inside the timed region; "
+                               "the prompt copy and the prefill run before it")},
+        "finite_data_check": {
+            "chained_us_per_layer_step": {k.split(":", 1)[1]: round(v[1] / (w.l * w.n * K) * 1e3, 2)
+                                          for k, v in ((f"decode:{a}", b) for a, b in dec_prof.items())},
+            "finite_us_per_layer_step": finite},
         "clocks": clocks, "wall_s_timed": t_wall,
     }
     print(json.dumps(line), flush=True)
+
+
+def finite_layer_steps(fg, w, L, dev, st, steps: int) -> dict:
+    """Per-kernel device microseconds per decode layer-step of one layer on
+    finite data (see run_ours)."""
+    dt = synth.torch_dtype(w.act)
+    kv = fg.KVCache(w.b, w.heads, w.head_dim, w.s + w.n, True, dt, dev)
+    x = synth.prompt(w, device=dev, seed_offset=101)
+    y = torch.empty_like(x)
+    ws = fg.workspace(max(fg.fg_prefill_workspace_bytes(L, w.b, w.s),
+                          fg.fg_decode_workspace_bytes(L, w.b, w.s + w.n)), dev)
+    tin = synth.decode_inputs(w, device=dev, seed_offset=102)
+    out = torch.empty_like(tin[0])
+    total = {}
+    for k in range(max(1, steps)):
+        fg.fg_prefill_layer(L, x, kv, y, ws, st)
+        torch.cuda.synchronize()
+        fg.fg_profile_start(w.n * 16 + 64)
+        fg.fg_profile_phase(1)
+        for t in range(w.n):
+            fg.fg_decode_step(L, tin[t], w.s + t, kv, out, ws, st)
+        torch.cuda.synchronize()
+        prof = fg.fg_profile_stop().get(1, {})
+        assert torch.isfinite(out).all(), "finite-data decode produced a non-finite output"
+        for name, (cnt, ms) in prof.items():
+            total[name] = total.get(name, 0.0) + ms
+    return {name: round(ms / (w.n * max(1, steps)) * 1e3, 2) for name, ms in total.items()}
 
 
 CASES = ("linear-qkv", "linear-o", "linear-fc1", "linear-fc2", "prefill-linear-fc1", "attn-decode",
@@ -438,7 +494,7 @@ def run_case(args, w, device):
             N *= 3
         prefill = name.startswith("prefill")
         M = min(w.b * w.s, 8192) if prefill else w.b      # a few GB at most on the device
-        per = K * N * (2 if prefill else 0.5625)
+        per = K * N * (2 if prefill else Q4)
         copies = 1 if prefill else max(2, min(32, int(-(-l2 // per))))
         Ws = []
         for c in range(copies):

@@ -70,8 +70,9 @@ typedef enum { FG_CODEC_NONE = 0, FG_CODEC_Q4G64 = 1 } fg_codec; /* storage     
  * mins and scales [K][N/64] -- each group is 64 consecutive output channels
  * at one input index ([S5]: "along the output-channel dimension").  With
  * FG_CODEC_NONE: dense [K][N] in the layer's activation dtype.  Device.
- * packed (optional, may be NULL): the decode copy written by fg_pack_weight;
- * fp16 products of up to 256 rows read it instead of codes/mins/scales. */
+ * packed (optional, may be NULL): the decode copy written by fg_pack_weight
+ * in format packed_format (an fg_pack_format); fp16 products of up to 256
+ * rows read it instead of codes/mins/scales. */
 typedef struct {
   const uint8_t* codes;
   const float* mins;
@@ -79,7 +80,21 @@ typedef struct {
   const void* dense;
   int64_t K, N;
   const uint8_t* packed;
+  int32_t packed_format;
 } fg_wmat;
+
+/* Formats of the decode copy of a Q4G64 weight (fg_pack_weight).
+ *   FG_PACK_EXACT (default): the stored fp32 (min, scale) of every group, so
+ *     a decode product restores each weight as fp16(fmaf(q, scale, min)),
+ *     exactly the value fg_dequant_g64 writes ([S5] "converted back to FP16
+ *     before compute"); 0.625 bytes per weight, like the stored form.
+ *   FG_PACK_F16META (opt-in, approximate): (scale, min) rounded to fp16 and
+ *     applied in fp16, w~ = fp16(q * fp16(scale) + fp16(min)) with one
+ *     rounding; 0.5625 bytes per weight (10% fewer bytes to read).  Bound:
+ *     |w~ - x| <= scale/2 + 15 * ulp16(scale)/2 + ulp16(min)/2 + ulp16(w~)/2
+ *     + the fp32 codec's own rounding, for finite groups whose scale and
+ *     min are normal fp16 numbers. */
+typedef enum { FG_PACK_EXACT = 0, FG_PACK_F16META = 1 } fg_pack_format;
 
 /* One transformer layer ([BG]): w_Q, w_K, w_V, w_O in R^{h1 x h1},
  * w_1 in R^{h1 x h2}, w_2 in R^{h2 x h1}; `heads` attention heads of
@@ -157,29 +172,34 @@ fg_status fg_linear(const fg_wmat* w, fg_codec codec, fg_dtype dtype, const void
                     cudaStream_t stream);
 
 /* The decode copy of a Q4G64 weight ([S5] storage; [BG] x . w with one
- * weight read for the whole block), fg_pack_weight_bytes(K, N) = K*N/2 +
- * K*N/16 bytes: one 4608-byte block per (128-channel tile t, 64-k tile u),
- * block (t, u) at byte offset (t * K/64 + u) * 4608, so the k tiles of a
- * channel tile are one contiguous run:
+ * weight read for the whole block) in `format` (fg_pack_format):
+ * fg_pack_weight_bytes(K, N, format) = (K/64) * (N/128) blocks of B bytes,
+ * B = 5120 (FG_PACK_EXACT) or 4608 (FG_PACK_F16META): one block per
+ * (128-channel tile t, 64-k tile u), block (t, u) at byte offset
+ * (t * K/64 + u) * B, so the k tiles of a channel tile are one contiguous run:
  *   bytes 0..4095: codes, 16-byte units [q][g2][t] (q = 0..3, g2 = 0..1,
  *     t = 0..31) at q*1024 + g2*512 + t*16; 32-bit word w of unit (q, g2, t)
  *     holds channel 32q + t/4 + 8w of the tile at the tile's k pairs
  *     j = 16*g2 + 4e + t%4, e = 0..3: nibble e (from the low end) is k = 2j,
  *     nibble e+4 is k = 2j+1, so one mask turns a word into fp16 pairs of
  *     consecutive k;
- *   bytes 4096..4607: (scale, min) pairs, for the tile's two 64-channel
- *     groups gl (lower first) 16-byte units at 4096 + gl*256 + (u*4 + c)*16,
- *     u = 0..3, c = 0..3: fp16x2 (scale[2j], scale[2j+1]), fp16x2 (min[2j],
- *     min[2j+1]) for j = 8u + c, then the same for j = 8u + 4 + c; each
- *     rounded to nearest -- the precision the decode products apply them in.
+ *   FG_PACK_EXACT, bytes 4096..5119: for the tile's two 64-channel groups gl
+ *     (lower first) and its k pairs j = 0..31, the 16-byte unit at
+ *     4096 + gl*512 + j*16 holds fp32 (scale[2j], scale[2j+1], min[2j],
+ *     min[2j+1]) as stored;
+ *   FG_PACK_F16META, bytes 4096..4607: for the groups gl, 16-byte units at
+ *     4096 + gl*256 + (u*4 + c)*16, u = 0..3, c = 0..3: fp16x2 (scale[2j],
+ *     scale[2j+1]), fp16x2 (min[2j], min[2j+1]) for j = 8u + c, then the same
+ *     for j = 8u + 4 + c; each rounded to nearest even.
  *   (The order is the one in which the converting threads read them: thread
  *   t of warp quarter q converts channels 32q + t/4 + 8w at the k pairs
  *   4i + t%4, the register order of a 16x128b tensor-memory store.)
  * packed: device, 16-byte aligned, owned by the caller, then stored in
- * w->packed.  K a multiple of 64 and N of 128, else FG_ERR_SHAPE; null
- * arrays -> FG_ERR_ARG.  Asynchronous on `stream`. */
-size_t fg_pack_weight_bytes(int64_t K, int64_t N);
-fg_status fg_pack_weight(const fg_wmat* w, uint8_t* packed, cudaStream_t stream);
+ * w->packed with w->packed_format = format.  K a multiple of 64 and N of
+ * 128, else FG_ERR_SHAPE; null arrays or an unknown format -> FG_ERR_ARG
+ * (fg_pack_weight_bytes returns 0 for those).  Asynchronous on `stream`. */
+size_t fg_pack_weight_bytes(int64_t K, int64_t N, int32_t format);
+fg_status fg_pack_weight(const fg_wmat* w, int32_t format, uint8_t* packed, cudaStream_t stream);
 
 /* [BG] decode attention alone: for every sequence and head,
  * Softmax(q K^T / sqrt(head_dim)) V over cache slots 0..pos of kv (nothing
@@ -204,11 +224,19 @@ fg_status fg_decode_attention(const fg_kv* kv, const void* q, int64_t ldq, int64
  * GPU that loads the library holds until the process exits.  Caches whose
  * fg_decode_attention_workspace_bytes exceeds 1 MiB are rejected with
  * FG_ERR_WORKSPACE (the split rule needs at most ~0.9 MB, so none is
- * today).  The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress, with that device current); make that first call
- * before any stream capture.  Calls share the array, so calls whose kernels
- * overlap on the GPU (concurrent streams) race; nothing in the array needs
- * to start at zero.  Allocates nothing, on the device or the host. */
+ * today).  Argument errors are reported before any CUDA call, as for
+ * fg_decode_attention.  The first call on a device looks up the array's
+ * device address (cudaGetSymbolAddress, with that device current) and caches
+ * it until the process exits; make that first call before any stream
+ * capture and before any region where allocations are forbidden (under lazy
+ * module loading it is also the call that loads this code, and the array,
+ * onto the device).  After a device reset (or a destroyed primary context)
+ * the cached address is stale: do not call this entry point again in that
+ * process.  Calls share the array, so calls whose kernels overlap on the GPU
+ * (concurrent streams) race; nothing in the array needs to start at zero.
+ * Calls no allocating routine, on the device or the host (the array is part
+ * of the library's device code; under lazy module loading the driver places
+ * it on the device when the first call loads that code). */
 fg_status fg_decode_attention_noalloc(const fg_kv* kv, const void* q, int64_t ldq, int64_t pos,
                                       void* out, int64_t ldo, cudaStream_t stream);
 
@@ -257,6 +285,18 @@ fg_status fg_decode_block_step(const fg_layer* layers, int32_t l, const void* t,
 /* Synchronize `stream`, then report (and clear) the device error word that
  * kernels raise when a bounded wait runs out: FG_ERR_DEVICE_TIMEOUT, or
  * FG_ERR_CUDA if the synchronization itself failed. */
+#define FG_WAIT_LIMIT_DEFAULT (1u << 24)
+
+/* Failure handling: the number of polls every bounded wait of the library's
+ * kernels makes (on copies landing, on other warps' stages) before it gives
+ * up, sets the device error word and lets its CTA leave -- after the CTA's
+ * own copies and tensor-core operations in flight have completed and its
+ * tensor memory is freed -- so that a lost dependency ends in
+ * FG_ERR_DEVICE_TIMEOUT from fg_sync_status instead of a hang.  Process-wide,
+ * read at each launch; 0 makes every such wait give up at once (outputs are
+ * then undefined).  Returns the previous value; FG_WAIT_LIMIT_DEFAULT is the
+ * initial one. */
+uint32_t fg_set_wait_limit(uint32_t polls);
 fg_status fg_sync_status(cudaStream_t stream);
 
 /* Human-readable name of a status, and the detail message of the most recent

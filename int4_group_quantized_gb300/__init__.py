@@ -31,6 +31,7 @@ STATUS = {0: "FG_OK", 1: "FG_ERR_ARG", 2: "FG_ERR_SHAPE", 3: "FG_ERR_ALIGN", 4: 
           5: "FG_ERR_WORKSPACE", 6: "FG_ERR_CUDA", 7: "FG_ERR_DEVICE_TIMEOUT", 8: "FG_ERR_UNSUPPORTED"}
 FG_F16, FG_F32 = 0, 1
 FG_CODEC_NONE, FG_CODEC_Q4G64 = 0, 1
+FG_PACK_EXACT, FG_PACK_F16META = 0, 1
 GROUP = 64
 
 
@@ -44,7 +45,7 @@ class FGError(RuntimeError):
 class fg_wmat(ctypes.Structure):
     _fields_ = [("codes", ctypes.c_void_p), ("mins", ctypes.c_void_p), ("scales", ctypes.c_void_p),
                 ("dense", ctypes.c_void_p), ("K", ctypes.c_int64), ("N", ctypes.c_int64),
-                ("packed", ctypes.c_void_p)]
+                ("packed", ctypes.c_void_p), ("packed_format", ctypes.c_int32)]
 
 
 class fg_layer(ctypes.Structure):
@@ -103,8 +104,8 @@ _sig("fg_profile_phase", _INT, ctypes.c_int32)
 _sig("fg_profile_query", _INT, ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(ctypes.c_int64),
      ctypes.POINTER(ctypes.c_double))
 _sig("fg_launch_count", ctypes.c_uint64)
-_sig("fg_pack_weight_bytes", _SZ, _I64, _I64)
-_sig("fg_pack_weight", _INT, ctypes.POINTER(fg_wmat), _P, _P)
+_sig("fg_pack_weight_bytes", _SZ, _I64, _I64, ctypes.c_int32)
+_sig("fg_pack_weight", _INT, ctypes.POINTER(fg_wmat), ctypes.c_int32, _P, _P)
 
 lib = _lib
 
@@ -172,33 +173,37 @@ class QuantWeight:
     """w in R^{K x N} (x . w) as stored: Q4G64 (codes/mins/scales, grouped
     along N = the output channel) or dense."""
 
-    def __init__(self, K, N, codes=None, mins=None, scales=None, dense=None, packed=None):
+    def __init__(self, K, N, codes=None, mins=None, scales=None, dense=None, packed=None,
+                 packed_format=FG_PACK_EXACT):
         self.K, self.N = int(K), int(N)
         self.codes, self.mins, self.scales, self.dense = codes, mins, scales, dense
         self.packed = packed
+        self.packed_format = int(packed_format)
 
     @staticmethod
-    def from_dense(w: torch.Tensor, quantize_it: bool = True, stream=None, pack: bool | None = None) -> "QuantWeight":
+    def from_dense(w: torch.Tensor, quantize_it: bool = True, stream=None, pack: bool | None = None,
+                   pack_format: int = FG_PACK_EXACT) -> "QuantWeight":
         """pack (default: fp16 weights with N a multiple of 128) adds the
-        decode copy the decode products read (fg_pack_weight)."""
+        decode copy the decode products read (fg_pack_weight), in pack_format."""
         K, N = w.shape
         if not quantize_it:
             return QuantWeight(K, N, dense=w.contiguous())
         codes, mins, scales = quantize(w.contiguous(), stream)
         q = QuantWeight(K, N, codes, mins, scales)
         if pack if pack is not None else (w.dtype == torch.float16 and N % 128 == 0):
-            q.pack(stream)
+            q.pack(stream, pack_format)
         return q
 
-    def pack(self, stream=None) -> "QuantWeight":
-        self.packed = torch.empty(fg_pack_weight_bytes(self.K, self.N), dtype=torch.uint8,
+    def pack(self, stream=None, fmt: int = FG_PACK_EXACT) -> "QuantWeight":
+        self.packed = torch.empty(fg_pack_weight_bytes(self.K, self.N, fmt), dtype=torch.uint8,
                                   device=self.codes.device)
-        fg_pack_weight(self, self.packed, stream)
+        fg_pack_weight(self, fmt, self.packed, stream)
+        self.packed_format = int(fmt)
         return self
 
     def struct(self) -> fg_wmat:
         return fg_wmat(_ptr(self.codes), _ptr(self.mins), _ptr(self.scales), _ptr(self.dense), self.K,
-                       self.N, _ptr(self.packed))
+                       self.N, _ptr(self.packed), self.packed_format)
 
     def nbytes(self) -> int:
         """Bytes of the stored format (the packed copy is counted apart: packed_nbytes)."""
@@ -209,14 +214,14 @@ class QuantWeight:
         return 0 if self.packed is None else self.packed.numel()
 
 
-def fg_pack_weight_bytes(K: int, N: int) -> int:
-    return int(_lib.fg_pack_weight_bytes(K, N))
+def fg_pack_weight_bytes(K: int, N: int, fmt: int = FG_PACK_EXACT) -> int:
+    return int(_lib.fg_pack_weight_bytes(K, N, fmt))
 
 
-def fg_pack_weight(w: "QuantWeight", packed: torch.Tensor, stream=None) -> None:
+def fg_pack_weight(w: "QuantWeight", fmt: int, packed: torch.Tensor, stream=None) -> None:
     s = w.struct()
     s.packed = None
-    _check(_lib.fg_pack_weight(ctypes.byref(s), _ptr(packed), _stream(stream)), "fg_pack_weight")
+    _check(_lib.fg_pack_weight(ctypes.byref(s), int(fmt), _ptr(packed), _stream(stream)), "fg_pack_weight")
 
 
 class Layer:
@@ -232,9 +237,10 @@ class Layer:
                            FG_F16 if dtype == torch.float16 else FG_F32)
 
     @staticmethod
-    def from_dense(ws: dict, heads: int, quantized: bool = True, stream=None) -> "Layer":
+    def from_dense(ws: dict, heads: int, quantized: bool = True, stream=None,
+                   pack_format: int = FG_PACK_EXACT) -> "Layer":
         h1, h2 = ws["w1"].shape
-        q = {m: QuantWeight.from_dense(ws[m], quantized, stream) for m in Layer.MATS}
+        q = {m: QuantWeight.from_dense(ws[m], quantized, stream, pack_format=pack_format) for m in Layer.MATS}
         return Layer(q, h1, h2, heads, quantized, ws["wq"].dtype)
 
     @property
@@ -373,6 +379,15 @@ def fg_profile_stop(phases: int = 4) -> dict:
                 out.setdefault(p, {})[_lib.fg_profile_kernel_name(i).decode()] = (n.value, ms.value)
     _check(st, "fg_profile_stop")
     return out
+
+
+_sig("fg_set_wait_limit", ctypes.c_uint32, ctypes.c_uint32)
+FG_WAIT_LIMIT_DEFAULT = 1 << 24
+
+
+def fg_set_wait_limit(polls: int) -> int:
+    """Polls of every bounded device wait (process-wide); returns the previous value."""
+    return int(_lib.fg_set_wait_limit(int(polls)))
 
 
 def fg_launch_count() -> int:

@@ -585,15 +585,21 @@ fg_status decode_attention(const fg_kv& kv, const void* q, int64_t ldq, const vo
 // caller allocates.  This entry point uses instead a fixed array compiled
 // into the library, which every GPU that loads libfg.so holds until the
 // process exits.  Its device address is looked up once per device (with
-// that device current) by the first call on that device; make that first
-// call before any stream capture.  Every call shares the array: calls whose
-// kernels overlap on the GPU race on it.  Nothing in it needs to start at
-// zero (each split writes its partial before the merge reads it).
+// that device current) by the first call on that device and then cached
+// for the life of the process; make that first call before any stream
+// capture and before any region in which allocations are forbidden (with
+// lazy module loading, that first call is also what loads this code onto
+// the device).  A device reset or a destroyed primary context invalidates
+// the cached address.  Every call shares the array: calls whose kernels
+// overlap on the GPU race on it.  Nothing in it needs to start at zero
+// (each split writes its partial before the merge reads it).
 // ---------------------------------------------------------------------------
 #include <mutex>
 
-// The split rule above asks for at most ~0.9 MB (b*H*splits*(d+2)*4 bytes,
-// largest near b*H = 888/2 with head_dim 128), so 1 MiB covers every cache.
+// The split rule above asks for b*H*splits*(d+2)*4 bytes.  Splits happen only
+// while b*H < 888; with head_dim 128 the largest need is at b*H = 887 with two
+// splits, 1774*130*4 = 922,480 bytes (head_dim 64: less), so 1 MiB covers
+// every cache (a host-side sweep in the tests checks it).
 static constexpr size_t kNoAllocScratchBytes = size_t(1) << 20;   // 1 MiB
 static __device__ __align__(256) unsigned char g_decode_attn_scratch[kNoAllocScratchBytes];
 
@@ -615,13 +621,16 @@ static fg_status noalloc_scratch(void** ptr) {
 
 extern "C" fg_status fg_decode_attention_noalloc(const fg_kv* kv, const void* q, int64_t ldq, int64_t pos,
                                                  void* out, int64_t ldo, cudaStream_t stream) {
-  if (!kv) return fg::fail(FG_ERR_ARG, "null kv");
+  // every host-side check first, so that bad arguments never reach a CUDA call
+  const fg_status c = fg::check_decode_attention(kv, q, ldq, pos, out, ldo);
+  if (c != FG_OK) return c;
   const size_t need = fg_decode_attention_workspace_bytes(kv);
   if (need > kNoAllocScratchBytes)
     return fg::fail(FG_ERR_WORKSPACE,
                     "this cache needs %zu bytes of split scratch; the built-in array holds %zu "
                     "(use fg_decode_attention with a caller workspace)",
                     need, kNoAllocScratchBytes);
+  if (kv->b == 0) return FG_OK;
   void* scratch = nullptr;
   const fg_status s = noalloc_scratch(&scratch);
   if (s != FG_OK) return s;

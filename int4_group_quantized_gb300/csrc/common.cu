@@ -29,6 +29,9 @@ fg_status check_launch(const char* what) {
 
 static constexpr int kMaxDevices = 64;
 
+static std::atomic<uint32_t> g_wait_limit{FG_WAIT_LIMIT_DEFAULT};
+uint32_t wait_limit() { return g_wait_limit.load(std::memory_order_relaxed); }
+
 int num_sms() {
   static int cache[kMaxDevices] = {0};
   int dev = 0;
@@ -58,7 +61,7 @@ unsigned int* device_error_word() {
 // ---- launch tracing ----------------------------------------------------------
 namespace {
 const char* const kClassNames[KC_COUNT] = {
-    "quantize_g64", "dequant_g64", "kv_store_q4", "gemm_simt", "gemm_tc_q4",
+    "quantize_g64", "dequant_g64", "kv_store_q4", "gemm_simt", "gemm_tc",
     "gemm_splitk_reduce", "attn_decode", "attn_decode_combine", "attn_prefill", "gemm_q4_decode",
     "pack_weight"};
 
@@ -213,6 +216,8 @@ const char* fg_status_str(fg_status s) {
 const char* fg_last_error(void) { return fg::g_detail; }
 
 const char* fg_version(void) { return "fg 0.1 sm_103a"; }
+
+uint32_t fg_set_wait_limit(uint32_t polls) { return fg::g_wait_limit.exchange(polls); }
 
 fg_status fg_sync_status(cudaStream_t stream) {
   cudaError_t e = cudaStreamSynchronize(stream);

@@ -23,6 +23,12 @@ int num_sms();
 unsigned int* device_error_word();
 
 enum DeviceError : unsigned int { DEV_ERR_WAIT_TIMEOUT = 1u };
+// Polls a bounded wait makes before it gives up (fg_set_wait_limit), passed
+// to every kernel that waits.  Waits for work that is already in flight (a
+// copy issued, an MMA committed) use kDrainLimit instead: a CTA never leaves
+// with its own copies or MMAs outstanding.
+uint32_t wait_limit();
+constexpr uint32_t kDrainLimit = 1u << 26;
 
 // ---- launch tracing ----------------------------------------------------------
 // Every kernel launch is bracketed by a Trace; while fg_profile_start() is
@@ -61,7 +67,8 @@ struct Trace {
 // multiple of 64 and its columns start at `n0` in the output.
 struct WSeg {
   const uint8_t* codes;
-  const uint8_t* packed;   // channel-major codes + fp16 (scale, min) pairs (fg_pack_weight) or null
+  const uint8_t* packed;   // the decode copy (fg_pack_weight) or null
+  int packed_format;       // fg_pack_format of `packed`
   const float* mins;
   const float* scales;
   const void* dense;
@@ -87,17 +94,10 @@ struct GemmArgs {
 
 // CUDA-core product (any M, fp16 or fp32).
 fg_status gemm_simt(const GemmArgs& a, cudaStream_t st);
-// Tensor-core product (fp16, M >= 64); Q4 segments are dequantized in shared
-// memory, dense segments are loaded by TMA.
+// Tensor-core product on dense fp16 weights (M >= 64), operands by TMA.
 bool gemm_tc_supported(const GemmArgs& a);
 fg_status gemm_tc(const GemmArgs& a, void* ws, size_t ws_bytes, cudaStream_t st);
-size_t gemm_tc_workspace_bytes(int64_t M, int64_t N, int64_t K, bool q4);
-// Decode product on 4-bit weights for M <= 256 rows (weights as the MMA's
-// M operand; K splits of a tile reduced through distributed shared memory
-// inside a thread-block cluster, so no global scratch).
-bool gemm_q4dec_supported(const GemmArgs& a);
-fg_status gemm_q4dec(const GemmArgs& a, cudaStream_t st);
-int gemm_q4dec_splits(int64_t M, int64_t N, int64_t K);
+size_t gemm_tc_workspace_bytes(int64_t M, int64_t N, int64_t K);
 // Decode product on channel-major packed 4-bit weights for M <= 256 rows:
 // the weights are dequantized straight into tensor memory (the MMA's A
 // operand), so shared memory carries only codes, (min, scale) and X.
@@ -105,14 +105,23 @@ int gemm_q4dec_splits(int64_t M, int64_t N, int64_t K);
 bool gemm_q4ts_supported(const GemmArgs& a);
 fg_status gemm_q4ts(const GemmArgs& a, void* ws, size_t ws_bytes, cudaStream_t st);
 size_t gemm_q4ts_workspace_bytes(int64_t M, int64_t N, int64_t K);
-// The packed copy of a [K][N] 4-bit weight read by gemm_q4ts (fg_pack_weight).
+// The decode copy of a [K][N] 4-bit weight read by gemm_q4ts (fg_pack_weight),
+// in fg_pack_format `format`, and its size.
 fg_status pack_weight(const uint8_t* codes, const float* mins, const float* scales, int64_t K, int64_t N,
-                      uint8_t* packed, cudaStream_t st);
+                      int format, uint8_t* packed, cudaStream_t st);
+size_t pack_weight_bytes(int64_t K, int64_t N, int format);
 
-// Y = epilogue(X . W); chooses the kernel for the shape.  `ws` (ws_bytes >=
-// gemm_workspace_bytes) holds split-K partial sums where a kernel needs them.
+// Y = epilogue(X . W); chooses the kernel for the operands:
+//   fp16, 4-bit weights with their decode copy, M <= 256: gemm_q4ts;
+//   fp16, 4-bit weights without it, M >= 64: the weight converted back to
+//     fp16 into the workspace, then gemm_tc;
+//   fp16, dense weights, M >= 64: gemm_tc;
+//   everything else (fp32, fewer than 64 rows without a decode copy): gemm_simt.
+// `ws` (ws_bytes >= gemm_workspace_bytes) holds split-K partial sums and the
+// converted weight where a path needs them; `packed` says whether every
+// weight segment carries its decode copy.
 fg_status gemm(const GemmArgs& a, void* ws, size_t ws_bytes, cudaStream_t st);
-size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, fg_dtype dt, int quant);
+size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, fg_dtype dt, int quant, bool packed);
 
 // ---- KV cache --------------------------------------------------------------
 // Store K/V rows of `T` tokens per sequence at slots pos0..pos0+T-1.  The
@@ -122,6 +131,9 @@ fg_status kv_store(const fg_kv& kv, const void* ksrc, const void* vsrc, int64_t 
                    int64_t T, int64_t pos0, cudaStream_t st);
 
 // ---- attention -------------------------------------------------------------
+// Host-side argument checks of fg_decode_attention (no CUDA call).
+fg_status check_decode_attention(const fg_kv* kv, const void* q, int64_t ldq, int64_t pos, const void* out,
+                                 int64_t ldo);
 // Decode: one query per (sequence, head) at slot pos over slots 0..pos.
 // q: [b][ldq] (head h at columns h*d..), out: [b][ldo].  When knew/vnew are
 // given ([b][ldnew] rows), the new token's K/V are first written to slot pos

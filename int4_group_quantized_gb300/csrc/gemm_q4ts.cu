@@ -7,8 +7,11 @@
 // owns RB row blocks of 128 output channels (RB = 2: one CTA per SM with all
 // 512 TMEM columns; RB = 1: two CTAs per SM):
 //   * A = 128 channels x 64 k per row block.  Dequantization warps turn the
-//     packed codes and fp16 (scale, min) pairs (fg_pack_weight) into fp16
-//     weights in registers and store them with tcgen05.st: TMEM lane =
+//     packed codes and (scale, min) pairs of the decode copy (fg_pack_weight)
+//     into fp16 weights in registers and store them with tcgen05.st: with the
+//     stored fp32 pairs each weight is fp16(fmaf(q, scale, min)), exactly the
+//     value the format's dequantization gives; with the opt-in fp16 pairs it
+//     is fp16(q * scale' + min') in one fp16 FMA.  TMEM lane =
 //     channel, column = two consecutive k.  A warp reaches only its own
 //     32-lane quarter of TMEM (warp % 4); two sets of 4*RB warps convert
 //     the two k tiles of a chunk side by side.
@@ -59,34 +62,38 @@ using namespace q4;
 constexpr int BK = 64;
 constexpr int BNC = 128;               // channels per row block (the MMA's M)
 constexpr int kDqWarp0 = 4;            // dequantization warps start here
-constexpr uint32_t kWaitLimit = 1u << 24;
 constexpr int kMaxSplits = 16;         // K splits of a decode product (splits_for)
 // The copy producers run stages ahead and usually find their ring full; they
 // poll with this pause so that they leave the issue slots to the converters.
 constexpr uint32_t kProducerSleepNs = 100;
 
 // ---- packing -------------------------------------------------------------------
-// The decode copy is one 4608-byte block per (128-channel tile nt, 64-k tile
-// kt), blocks in order nt-major, so a CTA streams one contiguous run of HBM
-// and fetches a stage with one bulk copy.  Inside a block the data sit where
-// the thread that converts them reads them, for the 16x128b TMEM store shape
-// (warp quarter q writes TMEM lanes 32q..32q+31 with two stores of 16 lanes;
-// thread t of the warp holds lanes t/4, t/4+8, t/4+16, t/4+24 and the
-// 32-bit columns c = t%4, t%4+4, ..., i.e. the k pairs j = 4i + t%4, i = 0..7):
+// The decode copy is one block per (128-channel tile nt, 64-k tile kt), blocks
+// in order nt-major, so a CTA streams one contiguous run of HBM and fetches a
+// stage with one bulk copy.  Inside a block the data sit where the thread
+// that converts them reads them, for the 16x128b TMEM store shape (warp
+// quarter q writes TMEM lanes 32q..32q+31 with two stores of 16 lanes; thread
+// t of the warp holds lanes t/4, t/4+8, t/4+16, t/4+24 and the 32-bit columns
+// c = t%4, t%4+4, ..., i.e. the k pairs j = 4i + t%4, i = 0..7):
 //   bytes 0..4095: codes, [q][g2][t] 16-byte units (q = 0..3, g2 = 0..1,
 //     t = 0..31): word w of unit (q, g2, t) is channel 32q + t/4 + 8w, k pairs
 //     j = 16*g2 + 4e + t%4 for e = 0..3, nibble slot e (from the low end)
 //     holding k = 2j and slot e+4 holding k = 2j+1.  A warp's 128-bit loads
 //     are 512 contiguous bytes each.
-//   bytes 4096..4607: (scale, min) pairs, [gl][u][c4] 16-byte units for the
-//     tile's two 64-channel groups gl, u = 0..3, c4 = 0..3: fp16x2
-//     (scale[2j], scale[2j+1]), fp16x2 (min[2j], min[2j+1]) for j = 8u + c4,
-//     then the same for j = 8u + 4 + c4.
+//   then the (scale, min) pairs of the tile's two 64-channel groups gl:
+//   * FG_PACK_EXACT (1024 bytes): the 16-byte unit gl*512 + j*16 holds fp32
+//     (scale[2j], scale[2j+1], min[2j], min[2j+1]) as stored; a warp's load
+//     of unit j = 4i + t%4 touches 4 distinct units (64 contiguous bytes);
+//   * FG_PACK_F16META (512 bytes): [gl][u][c4] 16-byte units, u = 0..3,
+//     c4 = 0..3: fp16x2 (scale[2j], scale[2j+1]), fp16x2 (min[2j],
+//     min[2j+1]) for j = 8u + c4, then the same for j = 8u + 4 + c4.
 constexpr int kTileCodes = BNC * BK / 2;             // 4096
-constexpr int kTilePairs = 2 * (BK / 2) * 8;         // 512
-constexpr int kTileBytes = kTileCodes + kTilePairs;  // 4608
 
-__global__ void pack_codes_kernel(const uint8_t* __restrict__ codes, int64_t K, int64_t N,
+__host__ __device__ constexpr int tile_bytes(int fmt) {
+  return kTileCodes + (fmt == FG_PACK_EXACT ? 2 * (BK / 2) * 16 : 2 * (BK / 2) * 8);   // 5120 or 4608
+}
+
+__global__ void pack_codes_kernel(const uint8_t* __restrict__ codes, int64_t K, int64_t N, int tb,
                                   uint8_t* __restrict__ packed) {
   const int64_t words = N * (K / 8), KT = K / BK;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < words;
@@ -107,13 +114,15 @@ __global__ void pack_codes_kernel(const uint8_t* __restrict__ codes, int64_t K, 
         out |= c << (4 * (e + 4 * h));
       }
     }
-    uint8_t* tile = packed + ((n / BNC) * KT + kt) * kTileBytes;
+    uint8_t* tile = packed + ((n / BNC) * KT + kt) * tb;
     *reinterpret_cast<uint32_t*>(tile + q * 1024 + g2 * 512 + t * 16 + w * 4) = out;
   }
 }
 
-__global__ void pack_pairs_kernel(const float* __restrict__ mins, const float* __restrict__ scales, int64_t K,
-                                  int64_t N, uint8_t* __restrict__ packed) {
+// FG_PACK_F16META pairs: (scale, min) rounded to fp16, nearest even.
+__global__ void pack_pairs_f16_kernel(const float* __restrict__ mins, const float* __restrict__ scales, int64_t K,
+                                      int64_t N, uint8_t* __restrict__ packed) {
+  constexpr int tb = tile_bytes(FG_PACK_F16META);
   const int64_t G = N / 64, total = G * (K / 2), KT = K / BK;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -123,9 +132,26 @@ __global__ void pack_pairs_kernel(const float* __restrict__ mins, const float* _
     const int64_t kt = jj / (BK / 2);
     const int j = static_cast<int>(jj % (BK / 2));
     const int u = j / 8, hi = (j / 4) % 2, c4 = j % 4;
-    uint8_t* tile = packed + ((g / 2) * KT + kt) * kTileBytes;
+    uint8_t* tile = packed + ((g / 2) * KT + kt) * tb;
     *reinterpret_cast<uint2*>(tile + kTileCodes + (g % 2) * 256 + (u * 4 + c4) * 16 + hi * 8) =
         make_uint2(*reinterpret_cast<const uint32_t*>(&s2), *reinterpret_cast<const uint32_t*>(&m2));
+  }
+}
+
+// FG_PACK_EXACT pairs: the stored fp32 values, regrouped per k pair.
+__global__ void pack_pairs_f32_kernel(const float* __restrict__ mins, const float* __restrict__ scales, int64_t K,
+                                      int64_t N, uint8_t* __restrict__ packed) {
+  constexpr int tb = tile_bytes(FG_PACK_EXACT);
+  const int64_t G = N / 64, total = G * (K / 2), KT = K / BK;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t g = i % G, jj = i / G;
+    const float4 v = make_float4(scales[(2 * jj) * G + g], scales[(2 * jj + 1) * G + g], mins[(2 * jj) * G + g],
+                                 mins[(2 * jj + 1) * G + g]);
+    const int64_t kt = jj / (BK / 2);
+    const int j = static_cast<int>(jj % (BK / 2));
+    uint8_t* tile = packed + ((g / 2) * KT + kt) * tb;
+    *reinterpret_cast<float4*>(tile + kTileCodes + (g % 2) * 512 + j * 16) = v;
   }
 }
 
@@ -143,6 +169,7 @@ struct TsParams {
   int relu;
   float* part;              // [splits][M][N] fp32 when splits > 1
   unsigned int* err;
+  uint32_t wait_limit;      // polls of a bounded wait (fg_set_wait_limit)
 };
 
 constexpr int cmin(int a, int b) { return a < b ? a : b; }
@@ -169,8 +196,9 @@ constexpr int cmax(int a, int b) { return a > b ? a : b; }
 // (a chunk's packed blocks, one bulk copy per row block; released once every
 // dequantization warp holds its codes in registers), X (a chunk's tiles) and
 // the TMEM buffers (both released by the commit of the MMAs that read them).
-template <int BT, int RB>
+template <int BT, int RB, int FMT>
 struct TsCfg {
+  static constexpr int kTileBytes = tile_bytes(FMT);
   static constexpr int kT = 2;                        // k tiles per chunk
   static constexpr int kGroupWarps = 4 * RB;          // warps converting one k tile (all row blocks)
   static constexpr int kDqWarps = kT * kGroupWarps;
@@ -204,10 +232,11 @@ constexpr uint32_t kChunkBarrier = 1;   // named barrier ids (0 is __syncthreads
 constexpr uint32_t kStartBarrier = 2;
 constexpr int kSyncWarp = 3;
 
-template <int BT, int RB>
-__global__ void __launch_bounds__(TsCfg<BT, RB>::kThreads, TsCfg<BT, RB>::kMinBlocks)
+template <int BT, int RB, int FMT>
+__global__ void __launch_bounds__(TsCfg<BT, RB, FMT>::kThreads, TsCfg<BT, RB, FMT>::kMinBlocks)
     gemm_q4ts_kernel(const __grid_constant__ TsParams p) {
-  using C = TsCfg<BT, RB>;
+  using C = TsCfg<BT, RB, FMT>;
+  constexpr int kTileBytes = C::kTileBytes;
   constexpr int KT = C::kT, NB = C::kBufs, SX = C::kXStages, SW = C::kWStages;
   constexpr uint32_t kIdesc = idesc_f16(128, BT, 0, 0);   // A (TMEM) and B (X) K-major
   constexpr uint32_t kACol = RB * C::kAcc;                // TMEM A buffers follow the accumulators
@@ -267,7 +296,7 @@ __global__ void __launch_bounds__(TsCfg<BT, RB>::kThreads, TsCfg<BT, RB>::kMinBl
       for (int c = 0; c < nch; ++c) {
         const int s = c % SW;
         const uint32_t bytes = static_cast<uint32_t>(min(KT, nk - KT * c) * kTileBytes);
-        if (!mbar_wait_sleep(&wempty[s], ((c / SW) & 1) ^ 1, kWaitLimit, abort_flag, kProducerSleepNs)) break;
+        if (!mbar_wait_sleep(&wempty[s], ((c / SW) & 1) ^ 1, p.wait_limit, abort_flag, kProducerSleepNs)) break;
         mbar_expect_tx(&wfull[s], bytes * RB);
 #pragma unroll
         for (int rb = 0; rb < RB; ++rb)
@@ -277,7 +306,7 @@ __global__ void __launch_bounds__(TsCfg<BT, RB>::kThreads, TsCfg<BT, RB>::kMinBl
       }
       for (int c = max(0, issued - SW); c < issued; ++c) {   // nothing in flight at exit
         volatile int dummy = 0;
-        mbar_wait(&wfull[c % SW], (c / SW) & 1, kWaitLimit, &dummy);
+        mbar_wait(&wfull[c % SW], (c / SW) & 1, kDrainLimit, &dummy);
       }
       if (*abort_flag) atomicOr(p.err, DEV_ERR_WAIT_TIMEOUT);
     }
@@ -288,7 +317,7 @@ __global__ void __launch_bounds__(TsCfg<BT, RB>::kThreads, TsCfg<BT, RB>::kMinBl
       for (int c = 0; c < nch; ++c) {
         const int s = c % SX, n = min(KT, nk - KT * c);
         // the MMAs of chunk c - SX, the last to read stage s, have completed
-        if (c >= SX && !mbar_wait_sleep(&bufdone[(c - SX) % NB], ((c - SX) / NB) & 1, kWaitLimit, abort_flag,
+        if (c >= SX && !mbar_wait_sleep(&bufdone[(c - SX) % NB], ((c - SX) / NB) & 1, p.wait_limit, abort_flag,
                                         kProducerSleepNs))
           break;
         mbar_expect_tx(&xfull[s], n * C::kX);
@@ -298,7 +327,7 @@ __global__ void __launch_bounds__(TsCfg<BT, RB>::kThreads, TsCfg<BT, RB>::kMinBl
       }
       for (int c = max(0, issued - SX); c < issued; ++c) {
         volatile int dummy = 0;
-        mbar_wait(&xfull[c % SX], (c / SX) & 1, kWaitLimit, &dummy);
+        mbar_wait(&xfull[c % SX], (c / SX) & 1, kDrainLimit, &dummy);
       }
       if (*abort_flag) atomicOr(p.err, DEV_ERR_WAIT_TIMEOUT);
     }
@@ -340,14 +369,14 @@ __global__ void __launch_bounds__(TsCfg<BT, RB>::kThreads, TsCfg<BT, RB>::kMinBl
     // buffer (c+1) % NB free (the MMAs of chunk c+1-NB done) and the weights
     // of chunk c+2 (for the converting warps); after it, releases the weight
     // stages that have been converted by then.
-    bool ok = nch > 0 && mbar_wait(&wfull[0], 0, kWaitLimit, abort_flag) &&
-              (nch < 2 || mbar_wait(&wfull[1 % SW], (1 / SW) & 1, kWaitLimit, abort_flag));
+    bool ok = nch > 0 && mbar_wait(&wfull[0], 0, p.wait_limit, abort_flag) &&
+              (nch < 2 || mbar_wait(&wfull[1 % SW], (1 / SW) & 1, p.wait_limit, abort_flag));
     named_bar_sync(kStartBarrier, C::kStartThreads);
     for (int c = 0; c < nch; ++c) {
-      if (ok) ok = mbar_wait(&xfull[c % SX], (c / SX) & 1, kWaitLimit, abort_flag);
+      if (ok) ok = mbar_wait(&xfull[c % SX], (c / SX) & 1, p.wait_limit, abort_flag);
       if (ok && c + 1 < nch && c + 1 >= NB)
-        ok = mbar_wait(&bufdone[(c + 1) % NB], ((c + 1 - NB) / NB) & 1, kWaitLimit, abort_flag);
-      if (ok && c + 2 < nch) ok = mbar_wait(&wfull[(c + 2) % SW], ((c + 2) / SW) & 1, kWaitLimit, abort_flag);
+        ok = mbar_wait(&bufdone[(c + 1) % NB], ((c + 1 - NB) / NB) & 1, p.wait_limit, abort_flag);
+      if (ok && c + 2 < nch) ok = mbar_wait(&wfull[(c + 2) % SW], ((c + 2) / SW) & 1, p.wait_limit, abort_flag);
       __syncwarp();
       named_bar_sync(kChunkBarrier, C::kBarThreads);
       // chunks up to c+1 are converted now
@@ -375,30 +404,56 @@ __global__ void __launch_bounds__(TsCfg<BT, RB>::kThreads, TsCfg<BT, RB>::kMinBl
     // 0..3 in w0 and 4..7 in w1; this 64-channel group's (scale, min) pairs
     // for those k pairs, unit u holding i = 2u and 2u+1.
     uint4 w0, w1, pv[4];
+    const uint8_t* cur = wring;   // the weight stage block load() read from
     auto load = [&](int c) {
-      const uint8_t* st = wring + (c % SW) * C::kWStage + (rb * KT + tile) * kTileBytes;
-      w0 = *reinterpret_cast<const uint4*>(st + q * 1024 + lane * 16);
-      w1 = *reinterpret_cast<const uint4*>(st + q * 1024 + 512 + lane * 16);
-      const uint4* pr = reinterpret_cast<const uint4*>(st + kTileCodes + (q >> 1) * 256) + c4;
+      cur = wring + (c % SW) * C::kWStage + (rb * KT + tile) * kTileBytes;
+      w0 = *reinterpret_cast<const uint4*>(cur + q * 1024 + lane * 16);
+      w1 = *reinterpret_cast<const uint4*>(cur + q * 1024 + 512 + lane * 16);
+      if (FMT == FG_PACK_F16META) {
+        const uint4* pr = reinterpret_cast<const uint4*>(cur + kTileCodes + (q >> 1) * 256) + c4;
 #pragma unroll
-      for (int u = 0; u < 4; ++u) pv[u] = pr[4 * u];
+        for (int u = 0; u < 4; ++u) pv[u] = pr[4 * u];
+      }
     };
     // Converts what load() fetched into a[].
     auto convert = [&]() {
+      if (FMT == FG_PACK_EXACT) {
+        // fp16(fmaf(q, scale, min)) with the stored fp32 pairs: the nibbles
+        // become exact fp16 (1024 + q or 1024 + 16q, one lop3 for both k of
+        // a pair), exact fp32 q by one mixed-precision op each, then one
+        // paired fp32 FMA (each lane rounded once) and one rounding to fp16
+        const float4* pr = reinterpret_cast<const float4*>(cur + kTileCodes + (q >> 1) * 512) + c4;
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const uint4 cw = u < 2 ? w0 : w1;
-        const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
-#pragma unroll
-        for (int hi = 0; hi < 2; ++hi) {
-          const int i = 2 * u + hi, e = i & 3;   // column 4i + c4: nibble slots e and e+4
-          const uint32_t s2 = hi ? pv[u].z : pv[u].x, m2 = hi ? pv[u].w : pv[u].y;
+        for (int i = 0; i < 8; ++i) {
+          const float4 sm = pr[4 * i];   // (scale[2j], scale[2j+1], min[2j], min[2j+1]), j = 4i + c4
+          const uint4 cw = i < 4 ? w0 : w1;
+          const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+          const int e = i & 3;
 #pragma unroll
           for (int w = 0; w < 4; ++w) {
             const uint32_t x = e >= 2 ? words[w] >> 8 : words[w];
-            a[16 * (w >> 1) + 2 * i + (w & 1)] =
-                (e & 1) ? hfma2_u(hfma2_u(lop_mask_or(x, 0x00F000F0u, kMagic), kSixteenth, kNeg64), s2, m2)
-                        : hfma2_u(hfma2_u(lop_mask_or(x, 0x000F000Fu, kMagic), kOne, kNegMagic), s2, m2);
+            const uint32_t h = lop_mask_or(x, (e & 1) ? 0x00F000F0u : 0x000F000Fu, kMagic);
+            const float2 qq = (e & 1) ? nib16_pair_f32(h) : nib_pair_f32(h);
+            const float2 r = fma_f32x2(qq, make_float2(sm.x, sm.y), make_float2(sm.z, sm.w));
+            a[16 * (w >> 1) + 2 * i + (w & 1)] = cvt_f16x2(r);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint4 cw = u < 2 ? w0 : w1;
+          const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+          for (int hi = 0; hi < 2; ++hi) {
+            const int i = 2 * u + hi, e = i & 3;   // column 4i + c4: nibble slots e and e+4
+            const uint32_t s2 = hi ? pv[u].z : pv[u].x, m2 = hi ? pv[u].w : pv[u].y;
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+              const uint32_t x = e >= 2 ? words[w] >> 8 : words[w];
+              a[16 * (w >> 1) + 2 * i + (w & 1)] =
+                  (e & 1) ? hfma2_u(hfma2_u(lop_mask_or(x, 0x00F000F0u, kMagic), kSixteenth, kNeg64), s2, m2)
+                          : hfma2_u(hfma2_u(lop_mask_or(x, 0x000F000Fu, kMagic), kOne, kNegMagic), s2, m2);
+            }
           }
         }
       }
@@ -437,7 +492,13 @@ __global__ void __launch_bounds__(TsCfg<BT, RB>::kThreads, TsCfg<BT, RB>::kMinBl
   constexpr int NCH = RB * BNC;                 // channels of the tile
   bool ok = true;
   if (epi) {
-    ok = mbar_wait(done, 0, kWaitLimit, abort_flag);
+    ok = mbar_wait(done, 0, p.wait_limit, abort_flag);
+    if (!ok) {
+      // the MMA warp always commits `done`: wait for its MMAs to finish
+      // before touching or freeing the tensor memory they write
+      volatile int dummy = 0;
+      mbar_wait(done, 0, kDrainLimit, &dummy);
+    }
     tc_fence_after();
     ok = ok && !*abort_flag;
   }
@@ -558,14 +619,14 @@ __global__ void __launch_bounds__(256) splitk_sum_kernel(const float* __restrict
   }
 }
 
-template <int BT, int RB>
+template <int BT, int RB, int FMT>
 fg_status launch_ts(TsParams& p, cudaStream_t st) {
-  using C = TsCfg<BT, RB>;
+  using C = TsCfg<BT, RB, FMT>;
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    if (cudaFuncSetAttribute(gemm_q4ts_kernel<BT, RB>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kTotal) !=
+    if (cudaFuncSetAttribute(gemm_q4ts_kernel<BT, RB, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kTotal) !=
         cudaSuccess)
       return check_launch("gemm_q4ts smem attribute");
     attr_set[dev] = true;
@@ -581,7 +642,7 @@ fg_status launch_ts(TsParams& p, cudaStream_t st) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, gemm_q4ts_kernel<BT, RB>, p) != cudaSuccess)
+  if (cudaLaunchKernelEx(&cfg, gemm_q4ts_kernel<BT, RB, FMT>, p) != cudaSuccess)
     return check_launch("gemm_q4ts_kernel (launch)");
   const fg_status s = check_launch("gemm_q4ts_kernel");
   if (s != FG_OK || p.splits == 1) return s;
@@ -648,6 +709,8 @@ bool gemm_q4ts_supported(const GemmArgs& a) {
   for (int i = 0; i < a.nseg; ++i) {
     const WSeg& s = a.seg[i];
     if (!s.packed || s.N % BNC || !aligned(s.packed, 16)) return false;
+    if (s.packed_format != a.seg[0].packed_format) return false;
+    if (s.packed_format != FG_PACK_EXACT && s.packed_format != FG_PACK_F16META) return false;
   }
   if ((a.ldx * 2) % 16 || !aligned(a.X, 16)) return false;
   if (a.ldy % 4 || !aligned(a.Y, 8) || (a.R && (a.ldr % 4 || !aligned(a.R, 8)))) return false;
@@ -690,28 +753,45 @@ fg_status gemm_q4ts(const GemmArgs& a, void* ws, size_t ws_bytes, cudaStream_t s
   p.relu = a.relu;
   p.err = device_error_word();
   if (!p.err) return fail(FG_ERR_CUDA, "device error word");
+  p.wait_limit = wait_limit();
+  if (a.seg[0].packed_format == FG_PACK_F16META) {
+    switch (bt) {
+      case 32: return launch_ts<32, 1, FG_PACK_F16META>(p, st);
+      case 64: return launch_ts<64, 1, FG_PACK_F16META>(p, st);
+      case 128: return launch_ts<128, 1, FG_PACK_F16META>(p, st);
+      default: return launch_ts<256, 1, FG_PACK_F16META>(p, st);
+    }
+  }
   switch (bt) {
-    case 32: return launch_ts<32, 1>(p, st);
-    case 64: return launch_ts<64, 1>(p, st);
-    case 128: return launch_ts<128, 1>(p, st);
-    default: return launch_ts<256, 1>(p, st);
+    case 32: return launch_ts<32, 1, FG_PACK_EXACT>(p, st);
+    case 64: return launch_ts<64, 1, FG_PACK_EXACT>(p, st);
+    case 128: return launch_ts<128, 1, FG_PACK_EXACT>(p, st);
+    default: return launch_ts<256, 1, FG_PACK_EXACT>(p, st);
   }
 }
 
 fg_status pack_weight(const uint8_t* codes, const float* mins, const float* scales, int64_t K, int64_t N,
-                      uint8_t* packed, cudaStream_t st) {
+                      int format, uint8_t* packed, cudaStream_t st) {
   if (K == 0 || N == 0) return FG_OK;
   Trace tr(KC_PACK, st);
   constexpr int kT = 256;
   const int64_t cap = static_cast<int64_t>(num_sms()) * 16;
   const int64_t words = N * (K / 8), pairs = (N / 64) * (K / 2);
   pack_codes_kernel<<<static_cast<unsigned>(std::min<int64_t>((words + kT - 1) / kT, cap)), kT, 0, st>>>(
-      codes, K, N, packed);
+      codes, K, N, tile_bytes(format), packed);
   const fg_status sc = check_launch("pack_codes_kernel");
   if (sc != FG_OK) return sc;
-  pack_pairs_kernel<<<static_cast<unsigned>(std::min<int64_t>((pairs + kT - 1) / kT, cap)), kT, 0, st>>>(
-      mins, scales, K, N, packed);
+  trace_extra_launch();
+  const unsigned grid = static_cast<unsigned>(std::min<int64_t>((pairs + kT - 1) / kT, cap));
+  if (format == FG_PACK_F16META)
+    pack_pairs_f16_kernel<<<grid, kT, 0, st>>>(mins, scales, K, N, packed);
+  else
+    pack_pairs_f32_kernel<<<grid, kT, 0, st>>>(mins, scales, K, N, packed);
   return check_launch("pack_pairs_kernel");
+}
+
+size_t pack_weight_bytes(int64_t K, int64_t N, int format) {
+  return static_cast<size_t>(K / BK) * static_cast<size_t>(N / BNC) * tile_bytes(format);
 }
 
 }  // namespace fg

@@ -6,25 +6,20 @@
 // 4-bit groups of 64 along the output channel and converted back to FP16
 // before compute.
 //
-// Two ways to feed the weight operand B ([K][N] row-major, i.e. MN-major):
-//   * Q4 (decode, a block of b >= 64 sequences): TMA brings the 4-bit codes
-//     and the (min, scale) pairs of a 64 x BN tile; six "dequant" warps turn
-//     them into fp16 in the 128-byte-swizzled MN-major layout the MMA reads,
-//     so each weight byte crosses HBM once per step for the whole block;
-//   * dense (prefill, b*s rows): the layer's weights were dequantized to fp16
-//     once, and TMA loads B tiles directly.
-// A = X tiles [128 rows][64 k] (K-major, 128-byte swizzle) come by TMA; rows
+// The weight operand B is fp16 [K][N] row-major (MN-major): for the prefill
+// products (b*s rows) the layer's 4-bit weights were converted back to fp16
+// once per layer, and every tile of them then feeds many rows.  A = X tiles
+// [128 rows][64 k] (K-major, 128-byte swizzle) and B tiles come by TMA; rows
 // past M are zero-filled by the TMA unit.
 //
 // Warp roles (256 threads): warp 0 issues TMA; warp 1 owns TMEM and one of
-// its lanes issues the MMAs; warps 2..7 dequantize (Q4); warps 4..7 drain the
-// accumulator in the epilogue.  Every wait is bounded: on timeout the CTA
-// raises the library's device error word and leaves.
+// its lanes issues the MMAs; warps 4..7 drain the accumulator in the
+// epilogue.  Every wait is bounded: on timeout the CTA raises the library's
+// device error word and leaves.
 #include <cudaTypedefs.h>
 #include <string.h>
 
 #include "fg_internal.cuh"
-#include "q4_dev.cuh"
 #include "tc_ptx.cuh"
 
 namespace fg {
@@ -33,19 +28,13 @@ namespace {
 using namespace tc;
 
 constexpr int BK = 64;             // k per pipeline stage (one 128-byte swizzle row of fp16)
-constexpr int kDenseThreads = 256;
-constexpr int kQ4Threads = 384;
-constexpr int kDequantWarp0 = 4;   // Q4: warps 4..11 dequantize
-constexpr int kDequantThreads = kQ4Threads - 32 * kDequantWarp0;
+constexpr int kThreads = 256;
 constexpr int kEpiWarp0 = 4;       // warps 4..7 drain TMEM
-__host__ __device__ constexpr int cta_threads(bool q4) { return q4 ? kQ4Threads : kDenseThreads; }
-constexpr uint32_t kWaitLimit = 1u << 24;
+constexpr int BN = 256;            // columns of a CTA tile
 
 struct TcParams {
   CUtensorMap mapA;
-  CUtensorMap mapB[3];      // dense: fp16 W [K][N_seg], box {64, 64}; q4: codes [K][N_seg/2], box {BN/2, 64}
-  CUtensorMap mapMin[3];    // q4: mins [K][N_seg/64], box {BN/64, 64}
-  CUtensorMap mapScale[3];
+  CUtensorMap mapB[3];      // fp16 W [K][N_seg], box {64, 64}
   int seg_n0[4];            // segment column offsets, seg_n0[nseg] = N
   int nseg;
   int M, N, K;
@@ -58,35 +47,27 @@ struct TcParams {
   int relu;
   float* partial;           // splits > 1: [splits][M][N]
   unsigned int* err;
+  uint32_t wait_limit;      // polls of a bounded wait (fg_set_wait_limit)
 };
 
-template <int MT, int BN, bool Q4>
+template <int MT>
 struct Smem {
   static constexpr int kA = MT * 128 * BK * 2;           // bytes of A per stage
   static constexpr int kB = BK * BN * 2;                 // fp16 B tile
-  static constexpr int kCodes = BK * BN / 2;
-  // (min, scale) tiles always span 256 columns (4 floats = 16 bytes per row)
-  // so every TMA box and coordinate stays 16-byte aligned; BN = 128 uses half.
-  static constexpr int kMeta = BK * 4 * 4;
-  static constexpr int kTx = Q4 ? (kA + kCodes + 2 * kMeta) : (kA + kB);   // TMA bytes per stage
+  static constexpr int kTx = kA + kB;                    // TMA bytes per stage
   static constexpr int kStage = (kTx + 1023) / 1024 * 1024;
-  static constexpr int kNB = 2;                          // dequantized B buffers (Q4)
   static constexpr int kBudget = 220 * 1024;
-  static constexpr int kStages = (kBudget - (Q4 ? kNB * kB : 0)) / kStage > 8
-                                     ? 8
-                                     : (kBudget - (Q4 ? kNB * kB : 0)) / kStage;
-  static constexpr int kTotal = 1024 /*align slack*/ + kStages * kStage + (Q4 ? kNB * kB : 0) + 256;
+  static constexpr int kStages = kBudget / kStage > 8 ? 8 : kBudget / kStage;
+  static constexpr int kTotal = 1024 /*align slack*/ + kStages * kStage + 256;
   static_assert(kStages >= 2, "pipeline needs two stages");
   static_assert(kA % 1024 == 0 && kB % 1024 == 0, "swizzle atoms need 1 KiB alignment");
 };
 
 __device__ __forceinline__ void raise(const TcParams& p) { atomicOr(p.err, DEV_ERR_WAIT_TIMEOUT); }
 
-using namespace q4;
-
-template <int MT, int BN, bool Q4>
-__global__ void __launch_bounds__(cta_threads(Q4), 1) gemm_tc_kernel(const __grid_constant__ TcParams p) {
-  using S = Smem<MT, BN, Q4>;
+template <int MT>
+__global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ TcParams p) {
+  using S = Smem<MT>;
   constexpr int STAGES = S::kStages;
   constexpr uint32_t kTmemCols = MT * BN;   // 128, 256 or 512
   constexpr uint32_t kIdesc = idesc_f16(128, BN, 0, 1);
@@ -94,13 +75,10 @@ __global__ void __launch_bounds__(cta_threads(Q4), 1) gemm_tc_kernel(const __gri
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stage_base = smem;
-  uint8_t* bbuf_base = smem + STAGES * S::kStage;
-  uint8_t* tail = bbuf_base + (Q4 ? S::kNB * S::kB : 0);
+  uint8_t* tail = smem + STAGES * S::kStage;
   uint64_t* full = reinterpret_cast<uint64_t*>(tail);
   uint64_t* empty = full + STAGES;
-  uint64_t* bfull = empty + STAGES;
-  uint64_t* bempty = bfull + S::kNB;
-  uint64_t* done = bempty + S::kNB;
+  uint64_t* done = empty + STAGES;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -133,11 +111,7 @@ __global__ void __launch_bounds__(cta_threads(Q4), 1) gemm_tc_kernel(const __gri
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], Q4 ? 1 + kDequantThreads / 32 : 1);   // MMA commit + one per dequant warp
-    }
-    for (int i = 0; i < S::kNB; ++i) {
-      mbar_init(&bfull[i], kDequantThreads / 32);
-      mbar_init(&bempty[i], 1);
+      mbar_init(&empty[i], 1);   // the MMA commit
     }
     mbar_init(done, 1);
     *abort_flag = 0;
@@ -147,10 +121,6 @@ __global__ void __launch_bounds__(cta_threads(Q4), 1) gemm_tc_kernel(const __gri
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&p.mapA);
     tma_prefetch_desc(&p.mapB[seg]);
-    if (Q4) {
-      tma_prefetch_desc(&p.mapMin[seg]);
-      tma_prefetch_desc(&p.mapScale[seg]);
-    }
   }
   tc_fence_before();
   __syncthreads();
@@ -163,26 +133,19 @@ __global__ void __launch_bounds__(cta_threads(Q4), 1) gemm_tc_kernel(const __gri
       int issued = 0;
       for (int i = 0; i < nk; ++i) {
         const int s = i % STAGES;
-        if (!mbar_wait(&empty[s], ((i / STAGES) & 1) ^ 1, kWaitLimit, abort_flag)) break;
+        if (!mbar_wait(&empty[s], ((i / STAGES) & 1) ^ 1, p.wait_limit, abort_flag)) break;
         uint8_t* st = stage_base + s * S::kStage;
         const int k0 = (kt0 + i) * BK;
         mbar_expect_tx(&full[s], S::kTx);
         for (int mt = 0; mt < MT; ++mt) tma_load_2d(st + mt * 128 * BK * 2, &p.mapA, k0, m0 + mt * 128, &full[s]);
-        if (Q4) {
-          uint8_t* codes = st + S::kA;
-          tma_load_2d(codes, &p.mapB[seg], nl / 2, k0, &full[s]);
-          tma_load_2d(codes + S::kCodes, &p.mapMin[seg], (nl / 256) * 4, k0, &full[s]);
-          tma_load_2d(codes + S::kCodes + S::kMeta, &p.mapScale[seg], (nl / 256) * 4, k0, &full[s]);
-        } else {
-          for (int j = 0; j < BN / 64; ++j)
-            tma_load_2d(st + S::kA + j * (BK * 128), &p.mapB[seg], nl + 64 * j, k0, &full[s]);
-        }
+        for (int j = 0; j < BN / 64; ++j)
+          tma_load_2d(st + S::kA + j * (BK * 128), &p.mapB[seg], nl + 64 * j, k0, &full[s]);
         ++issued;
       }
       // never leave with copies in flight: wait for the stages still owed
       for (int i = max(0, issued - STAGES); i < issued; ++i) {
         volatile int dummy = 0;
-        mbar_wait(&full[i % STAGES], (i / STAGES) & 1, kWaitLimit, &dummy);
+        mbar_wait(&full[i % STAGES], (i / STAGES) & 1, kDrainLimit, &dummy);
       }
       if (*abort_flag) raise(p);
     }
@@ -192,13 +155,11 @@ __global__ void __launch_bounds__(cta_threads(Q4), 1) gemm_tc_kernel(const __gri
       bool ok = true;
       for (int i = 0; i < nk && ok; ++i) {
         const int s = i % STAGES;
-        const int j = i % S::kNB;
-        ok = mbar_wait(&full[s], (i / STAGES) & 1, kWaitLimit, abort_flag);
-        if (ok && Q4) ok = mbar_wait(&bfull[j], (i / S::kNB) & 1, kWaitLimit, abort_flag);
+        ok = mbar_wait(&full[s], (i / STAGES) & 1, p.wait_limit, abort_flag);
         if (!ok) break;
         tc_fence_after();
         const uint8_t* a = stage_base + s * S::kStage;
-        const uint8_t* b = Q4 ? (bbuf_base + j * S::kB) : (a + S::kA);
+        const uint8_t* b = a + S::kA;
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk) {
           // B: MN-major, 128-byte swizzle; 64-column blocks 8 KiB apart
@@ -213,58 +174,21 @@ __global__ void __launch_bounds__(cta_threads(Q4), 1) gemm_tc_kernel(const __gri
           }
         }
         mma_commit(&empty[s]);
-        if (Q4) mma_commit(&bempty[j]);
       }
       mma_commit(done);
       if (!ok) raise(p);
-    }
-  } else if (Q4 && warp >= kDequantWarp0) {
-    // ---- dequantization warps ---------------------------------------------------
-    const int t = threadIdx.x - 32 * kDequantWarp0;
-    bool ok = true;
-    for (int i = 0; i < nk && ok; ++i) {
-      const int s = i % STAGES;
-      const int j = i % S::kNB;
-      ok = mbar_wait(&full[s], (i / STAGES) & 1, kWaitLimit, abort_flag) &&
-           mbar_wait(&bempty[j], ((i / S::kNB) & 1) ^ 1, kWaitLimit, abort_flag);
-      if (!ok) break;
-      const uint8_t* st = stage_base + s * S::kStage;
-      const uint2* codes = reinterpret_cast<const uint2*>(st + S::kA);
-      const float* mins = reinterpret_cast<const float*>(st + S::kA + S::kCodes);
-      const float* scales = mins + BK * 4;
-      const int g0 = (nl & 255) >> 6;   // first group of this tile inside the 256-column meta tile
-      uint8_t* b = bbuf_base + j * S::kB;
-      // unit = 16 consecutive channels of one input row (one 64-bit code
-      // word, one (min, scale) pair) -> two swizzled 16-byte chunks
-      constexpr int kUnits = BK * BN / 16;
-      static_assert(kUnits % kDequantThreads == 0, "units split evenly over the dequant threads");
-#pragma unroll
-      for (int it = 0; it < kUnits / kDequantThreads; ++it) {
-        const int u = t + it * kDequantThreads;
-        const int k = u / (BN / 16);
-        const int n = (u % (BN / 16)) * 16;
-        const int gi = k * 4 + g0 + n / 64;
-        const uint32_t s2 = bcast_h2(scales[gi]), m2 = bcast_h2(mins[gi]);
-        const uint2 c = codes[k * (BN / 16) + n / 16];
-        const uint4 v0 = dequant8(c.x, s2, m2);
-        const uint4 v1 = dequant8(c.y, s2, m2);
-        const int chunk = (n & 63) >> 3;
-        uint8_t* row = b + (n >> 6) * (BK * 128) + k * 128;
-        *reinterpret_cast<uint4*>(row + ((chunk ^ (k & 7)) << 4)) = v0;
-        *reinterpret_cast<uint4*>(row + (((chunk + 1) ^ (k & 7)) << 4)) = v1;
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&bfull[j]);
-        mbar_arrive(&empty[s]);
-      }
     }
   }
 
   // ---- epilogue ---------------------------------------------------------------------
   if (warp >= kEpiWarp0) {
-    const bool ok = mbar_wait(done, 0, kWaitLimit, abort_flag);
+    const bool ok = mbar_wait(done, 0, p.wait_limit, abort_flag);
+    if (!ok) {
+      // the MMA thread always commits `done`: wait for its MMAs to finish
+      // before the tensor memory they write is freed
+      volatile int dummy = 0;
+      mbar_wait(done, 0, kDrainLimit, &dummy);
+    }
     tc_fence_after();
     if (ok && !*abort_flag) {
       const int q = warp - kEpiWarp0;   // TMEM lanes 32q .. 32q+31
@@ -276,23 +200,6 @@ __global__ void __launch_bounds__(cta_threads(Q4), 1) gemm_tc_kernel(const __gri
           tmem_ld_wait();
           if (m >= p.M) continue;
           const int n = n0 + c0;
-          if (Q4) {
-            // accumulator column order inside each 8-chunk is channel
-            // (0,4,1,5,2,6,3,7): put it back
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              const uint32_t c[8] = {r[8 * v], r[8 * v + 1], r[8 * v + 2], r[8 * v + 3],
-                                     r[8 * v + 4], r[8 * v + 5], r[8 * v + 6], r[8 * v + 7]};
-              r[8 * v + 0] = c[0];
-              r[8 * v + 1] = c[2];
-              r[8 * v + 2] = c[4];
-              r[8 * v + 3] = c[6];
-              r[8 * v + 4] = c[1];
-              r[8 * v + 5] = c[3];
-              r[8 * v + 6] = c[5];
-              r[8 * v + 7] = c[7];
-            }
-          }
           if (p.splits > 1) {
             float4* dst = reinterpret_cast<float4*>(p.partial + (static_cast<size_t>(split) * p.M + m) * p.N + n);
 #pragma unroll
@@ -413,21 +320,21 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int MT, int BN, bool Q4>
+template <int MT>
 fg_status launch(TcParams& p, cudaStream_t st) {
-  using S = Smem<MT, BN, Q4>;
+  using S = Smem<MT>;
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    if (cudaFuncSetAttribute(gemm_tc_kernel<MT, BN, Q4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(gemm_tc_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              S::kTotal) != cudaSuccess)
       return check_launch("gemm_tc smem attribute");
     attr_set[dev] = true;
   }
   const int grid = p.m_tiles * p.n_tiles * p.splits;
   Trace tr(KC_GEMM_TC, st);
-  gemm_tc_kernel<MT, BN, Q4><<<grid, cta_threads(Q4), S::kTotal, st>>>(p);
+  gemm_tc_kernel<MT><<<grid, kThreads, S::kTotal, st>>>(p);
   return check_launch("gemm_tc_kernel");
 }
 
@@ -438,15 +345,13 @@ bool tc_make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint6
   return make_map(m, dt, base, inner, outer, row_bytes, box_inner, box_outer, sw);
 }
 
-// Column tile of the tensor-core path, and the split-K factor it uses for a
-// product (fixed by the shape only, so workspace sizes do not depend on the
-// device).
-static int tc_bn(int64_t M, bool q4) { return (q4 && M <= 128) ? 128 : 256; }
-static int tc_mt(int64_t M, bool q4) { return (M > 128) ? 2 : 1; }
+// Row tiles per CTA, and the split-K factor of a product (fixed by the shape
+// only, so workspace sizes do not depend on the device).
+static int tc_mt(int64_t M) { return (M > 128) ? 2 : 1; }
 
-int gemm_tc_splits(int64_t M, int64_t N, int64_t K, bool q4) {
-  const int bn = tc_bn(M, q4), mt = tc_mt(M, q4);
-  const int64_t tiles = ((M + 128 * mt - 1) / (128 * mt)) * (N / bn);
+int gemm_tc_splits(int64_t M, int64_t N, int64_t K) {
+  const int mt = tc_mt(M);
+  const int64_t tiles = ((M + 128 * mt - 1) / (128 * mt)) * (N / BN);
   const int64_t ktiles = K / BK;
   constexpr int64_t kTarget = 148;
   int64_t s = (kTarget + tiles - 1) / tiles;
@@ -459,27 +364,23 @@ int gemm_tc_splits(int64_t M, int64_t N, int64_t K, bool q4) {
 }
 
 bool gemm_tc_supported(const GemmArgs& a) {
-  if (a.dtype != FG_F16) return false;
+  if (a.dtype != FG_F16 || a.quant) return false;
   if (a.M < 64) return false;
   if (a.K % BK) return false;
-  const int bn = tc_bn(a.M, a.quant);
-  for (int i = 0; i < a.nseg; ++i) {
-    if (a.seg[i].N % bn) return false;
-    if (a.quant && ((a.seg[i].N / 64) * 4) % 16) return false;   // TMA row stride of the meta arrays
-  }
+  for (int i = 0; i < a.nseg; ++i)
+    if (a.seg[i].N % BN || !a.seg[i].dense) return false;
   if ((a.ldx * 2) % 16 || (a.ldy * 2) % 16 || (a.R && (a.ldr * 2) % 16)) return false;
   if (a.M > (1 << 30) || a.N > (1 << 30) || a.K > (1 << 30)) return false;
   return encode_fn() != nullptr;
 }
 
-size_t gemm_tc_workspace_bytes(int64_t M, int64_t N, int64_t K, bool q4) {
-  const int s = gemm_tc_splits(M, N, K, q4);
+size_t gemm_tc_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  const int s = gemm_tc_splits(M, N, K);
   return s > 1 ? static_cast<size_t>(s) * M * N * sizeof(float) : 0;
 }
 
 fg_status gemm_tc(const GemmArgs& a, void* ws, size_t ws_bytes, cudaStream_t st) {
-  const bool q4 = a.quant != 0;
-  const int bn = tc_bn(a.M, q4), mt = tc_mt(a.M, q4);
+  const int mt = tc_mt(a.M);
   TcParams p;
   memset(&p, 0, sizeof(p));
   p.M = static_cast<int>(a.M);
@@ -492,27 +393,17 @@ fg_status gemm_tc(const GemmArgs& a, void* ws, size_t ws_bytes, cudaStream_t st)
   for (int i = 0; i < a.nseg; ++i) {
     const WSeg& s = a.seg[i];
     p.seg_n0[i] = static_cast<int>(s.n0);
-    bool ok;
-    if (q4) {
-      ok = make_map(&p.mapB[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, s.codes, s.N / 2, a.K, s.N / 2, bn / 2, BK,
-                    CU_TENSOR_MAP_SWIZZLE_NONE) &&
-           make_map(&p.mapMin[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, s.mins, s.N / 64, a.K, (s.N / 64) * 4,
-                    4, BK, CU_TENSOR_MAP_SWIZZLE_NONE) &&
-           make_map(&p.mapScale[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, s.scales, s.N / 64, a.K,
-                    (s.N / 64) * 4, 4, BK, CU_TENSOR_MAP_SWIZZLE_NONE);
-    } else {
-      ok = make_map(&p.mapB[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, s.dense, s.N, a.K, s.N * 2, 64, BK,
-                    CU_TENSOR_MAP_SWIZZLE_128B);
-    }
+    const bool ok = make_map(&p.mapB[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, s.dense, s.N, a.K, s.N * 2, 64, BK,
+                             CU_TENSOR_MAP_SWIZZLE_128B);
     if (!ok) return fail(FG_ERR_CUDA, "tensor map for weight segment %d", i);
   }
   p.seg_n0[a.nseg] = static_cast<int>(a.N);
   p.m_tiles = static_cast<int>((a.M + 128 * mt - 1) / (128 * mt));
-  p.n_tiles = static_cast<int>(a.N / bn);
+  p.n_tiles = static_cast<int>(a.N / BN);
   {
     // no split may be empty: derive the count back from the per-split length
     const int ktiles = static_cast<int>(a.K / BK);
-    const int want = gemm_tc_splits(a.M, a.N, a.K, q4);
+    const int want = gemm_tc_splits(a.M, a.N, a.K);
     p.ktiles_per_split = (ktiles + want - 1) / want;
     p.splits = (ktiles + p.ktiles_per_split - 1) / p.ktiles_per_split;
   }
@@ -524,18 +415,13 @@ fg_status gemm_tc(const GemmArgs& a, void* ws, size_t ws_bytes, cudaStream_t st)
   p.relu = a.relu;
   p.err = device_error_word();
   if (!p.err) return fail(FG_ERR_CUDA, "device error word");
+  p.wait_limit = wait_limit();
   if (p.splits > 1) {
     const size_t need = static_cast<size_t>(p.splits) * a.M * a.N * sizeof(float);
     if (!ws || ws_bytes < need) return fail(FG_ERR_WORKSPACE, "split-K partials need %zu bytes", need);
     p.partial = static_cast<float*>(ws);
   }
-  fg_status s;
-  if (q4) {
-    if (mt == 1) s = bn == 128 ? launch<1, 128, true>(p, st) : launch<1, 256, true>(p, st);
-    else s = launch<2, 256, true>(p, st);
-  } else {
-    s = mt == 1 ? launch<1, 256, false>(p, st) : launch<2, 256, false>(p, st);
-  }
+  const fg_status s = mt == 1 ? launch<1>(p, st) : launch<2>(p, st);
   if (s != FG_OK || p.splits == 1) return s;
   const int64_t n8 = a.M * a.N / 8;
   int grid = static_cast<int>((n8 + 255) / 256);

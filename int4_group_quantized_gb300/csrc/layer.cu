@@ -20,6 +20,8 @@ fg_status check_wmat(const fg_wmat& w, int64_t K, int64_t N, fg_codec codec, con
     if (!aligned(w.codes, 16) || !aligned(w.mins, 4) || !aligned(w.scales, 4))
       return fail(FG_ERR_ALIGN, "%s: codes need 16-byte alignment", name);
     if (w.packed && !aligned(w.packed, 16)) return fail(FG_ERR_ALIGN, "%s: packed copy needs 16-byte alignment", name);
+    if (w.packed && w.packed_format != FG_PACK_EXACT && w.packed_format != FG_PACK_F16META)
+      return fail(FG_ERR_ARG, "%s: unknown packed_format %d", name, w.packed_format);
   } else {
     if (!w.dense) return fail(FG_ERR_ARG, "%s: null dense weights", name);
     if (!aligned(w.dense, 16)) return fail(FG_ERR_ALIGN, "%s: dense weights need 16-byte alignment", name);
@@ -73,6 +75,7 @@ WSeg seg_of(const fg_wmat& w, int64_t n0) {
   WSeg s;
   s.codes = w.codes;
   s.packed = w.packed;
+  s.packed_format = w.packed_format;
   s.mins = w.mins;
   s.scales = w.scales;
   s.dense = w.dense;
@@ -120,11 +123,30 @@ size_t activations_bytes(const fg_layer& L, int64_t M) {
   return up(M * 3 * L.h1 * e) + up(M * L.h1 * e) * 2 + up(M * L.h2 * e);
 }
 
-// Prefill with fp16 activations runs its products on the tensor cores from
-// fp16 weights: the layer's six 4-bit matrices are dequantized once into the
-// workspace (each weight then feeds all b*s rows).
-bool prefill_dequantizes(const fg_layer& L, int64_t M) {
-  return L.dtype == FG_F16 && L.codec == FG_CODEC_Q4G64 && M >= 128;
+// Prefill with fp16 activations runs its products from fp16 weights: the
+// layer's six 4-bit matrices are dequantized once into the workspace (each
+// weight then feeds all b*s rows).
+bool prefill_dequantizes(const fg_layer& L, int64_t) {
+  return L.dtype == FG_F16 && L.codec == FG_CODEC_Q4G64;
+}
+
+// fp16 decode products on 4-bit weights read the decode copy of every
+// matrix (fg_pack_weight): one launch per product, the weights converted in
+// registers.  A layer without it is rejected rather than run on a slower path.
+bool decode_needs_copies(const fg_layer& L) { return L.dtype == FG_F16 && L.codec == FG_CODEC_Q4G64; }
+
+fg_status check_decode_copies(const fg_layer& L) {
+  if (!decode_needs_copies(L)) return FG_OK;
+  const fg_wmat* m[6] = {&L.wq, &L.wk, &L.wv, &L.wo, &L.w1, &L.w2};
+  const char* names[6] = {"w_Q", "w_K", "w_V", "w_O", "w_1", "w_2"};
+  for (int i = 0; i < 6; ++i) {
+    if (!m[i]->packed)
+      return fail(FG_ERR_ARG, "%s has no decode copy: fp16 decode needs fg_pack_weight on every matrix", names[i]);
+    if (m[i]->packed_format != L.wq.packed_format)
+      return fail(FG_ERR_ARG, "%s: the decode copies of a layer must share one format", names[i]);
+  }
+  if (L.h1 % 128 || L.h2 % 128) return fail(FG_ERR_SHAPE, "fp16 decode needs h1 and h2 multiples of 128");
+  return FG_OK;
 }
 size_t w16_bytes(const fg_layer& L) {
   return up(L.h1 * L.h1 * 2) * 4 + up(L.h1 * L.h2 * 2) * 2;
@@ -132,17 +154,18 @@ size_t w16_bytes(const fg_layer& L) {
 
 size_t scratch_bytes(const fg_layer& L, int64_t M, int64_t capacity, bool decode) {
   int quant = L.codec == FG_CODEC_Q4G64;
+  const bool packed = decode && decode_needs_copies(L);
   size_t w16 = 0;
   if (!decode && prefill_dequantizes(L, M)) {
     w16 = w16_bytes(L);
     quant = 0;
   }
-  size_t s = gemm_workspace_bytes(M, 3 * L.h1, L.h1, L.dtype, quant);
-  size_t t = gemm_workspace_bytes(M, L.h1, L.h1, L.dtype, quant);
+  size_t s = gemm_workspace_bytes(M, 3 * L.h1, L.h1, L.dtype, quant, packed);
+  size_t t = gemm_workspace_bytes(M, L.h1, L.h1, L.dtype, quant, packed);
   s = t > s ? t : s;
-  t = gemm_workspace_bytes(M, L.h2, L.h1, L.dtype, quant);
+  t = gemm_workspace_bytes(M, L.h2, L.h1, L.dtype, quant, packed);
   s = t > s ? t : s;
-  t = gemm_workspace_bytes(M, L.h1, L.h2, L.dtype, quant);
+  t = gemm_workspace_bytes(M, L.h1, L.h2, L.dtype, quant, packed);
   s = t > s ? t : s;
   if (decode) {
     t = decode_attention_workspace_bytes(M, L.heads, static_cast<int32_t>(L.h1 / L.heads), capacity);
@@ -238,15 +261,34 @@ fg_status check_act(const void* p, const char* name) {
 
 fg_status gemm(const GemmArgs& a, void* ws, size_t ws_bytes, cudaStream_t st) {
   if (gemm_q4ts_supported(a)) return gemm_q4ts(a, ws, ws_bytes, st);
-  if (gemm_q4dec_supported(a)) return gemm_q4dec(a, st);
+  if (a.dtype == FG_F16 && a.M >= 64 && a.quant) {
+    // converted back to fp16 once into the workspace, then the dense product
+    GemmArgs d = a;
+    char* w = static_cast<char*>(ws);
+    size_t used = 0;
+    for (int i = 0; i < a.nseg; ++i) {
+      const size_t bytes = up(static_cast<size_t>(a.K) * a.seg[i].N * 2);
+      if (!ws || used + bytes > ws_bytes) return fail(FG_ERR_WORKSPACE, "workspace too small for the fp16 weight");
+      FG_TRY(dequant_rows(a.seg[i].codes, a.seg[i].mins, a.seg[i].scales, a.K, a.seg[i].N, w + used, FG_F16, st));
+      d.seg[i].dense = w + used;
+      d.seg[i].codes = nullptr;
+      d.seg[i].packed = nullptr;
+      used += bytes;
+    }
+    d.quant = 0;
+    if (gemm_tc_supported(d)) return gemm_tc(d, w + used, ws_bytes - used, st);
+    return gemm_simt(d, st);
+  }
   if (gemm_tc_supported(a)) return gemm_tc(a, ws, ws_bytes, st);
   return gemm_simt(a, st);
 }
 
-size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, fg_dtype dt, int quant) {
-  if (dt == FG_F16 && quant && M >= 1 && M <= 256) return gemm_q4ts_workspace_bytes(M, N, K);
-  if (dt != FG_F16 || M < 64 || (quant && M <= 256)) return 0;
-  return gemm_tc_workspace_bytes(M, N, K, quant != 0);
+size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, fg_dtype dt, int quant, bool packed) {
+  if (dt != FG_F16 || M <= 0) return 0;
+  if (quant && packed && M <= 256) return gemm_q4ts_workspace_bytes(M, N, K);
+  if (M < 64) return 0;
+  const size_t tc = gemm_tc_workspace_bytes(M, N, K);
+  return quant ? up(static_cast<size_t>(K) * N * 2) + 3 * kAlign + tc : tc;
 }
 
 }  // namespace fg
@@ -261,7 +303,7 @@ size_t fg_prefill_workspace_bytes(const fg_layer* L, int64_t b, int64_t s) {
 }
 
 size_t fg_decode_workspace_bytes(const fg_layer* L, int64_t b, int64_t capacity) {
-  if (check_layer(L) != FG_OK || b < 0 || capacity < 0) return 0;
+  if (check_layer(L) != FG_OK || check_decode_copies(*L) != FG_OK || b < 0 || capacity < 0) return 0;
   return activations_bytes(*L, b) + scratch_bytes(*L, b, capacity, true);
 }
 
@@ -277,7 +319,9 @@ size_t fg_decode_block_workspace_bytes(const fg_layer* L, int64_t b, int64_t cap
 
 size_t fg_linear_workspace_bytes(int64_t M, int64_t K, int64_t N, fg_codec codec, fg_dtype dtype) {
   if (M < 0 || K <= 0 || N <= 0) return 0;
-  return gemm_workspace_bytes(M, N, K, dtype, codec == FG_CODEC_Q4G64);
+  const int q = codec == FG_CODEC_Q4G64;
+  const size_t a = gemm_workspace_bytes(M, N, K, dtype, q, true), b = gemm_workspace_bytes(M, N, K, dtype, q, false);
+  return a > b ? a : b;
 }
 
 fg_status fg_linear(const fg_wmat* w, fg_codec codec, fg_dtype dtype, const void* x, int64_t M,
@@ -304,19 +348,20 @@ fg_status fg_linear(const fg_wmat* w, fg_codec codec, fg_dtype dtype, const void
   return gemm(a, ws, ws_bytes, stream);
 }
 
-size_t fg_pack_weight_bytes(int64_t K, int64_t N) {
-  if (K <= 0 || N <= 0) return 0;
-  const size_t kn = static_cast<size_t>(K) * static_cast<size_t>(N);
-  return kn / 2 + kn / 16;
+size_t fg_pack_weight_bytes(int64_t K, int64_t N, int32_t format) {
+  if (K <= 0 || N <= 0 || K % 64 || N % 128) return 0;
+  if (format != FG_PACK_EXACT && format != FG_PACK_F16META) return 0;
+  return pack_weight_bytes(K, N, format);
 }
 
-fg_status fg_pack_weight(const fg_wmat* w, uint8_t* packed, cudaStream_t stream) {
+fg_status fg_pack_weight(const fg_wmat* w, int32_t format, uint8_t* packed, cudaStream_t stream) {
   if (!w || !w->codes || !w->mins || !w->scales || !packed) return fail(FG_ERR_ARG, "null weight arrays or packed buffer");
+  if (format != FG_PACK_EXACT && format != FG_PACK_F16META) return fail(FG_ERR_ARG, "unknown pack format %d", format);
   if (w->K <= 0 || w->N <= 0) return fail(FG_ERR_ARG, "sizes");
   if (w->K % 64 || w->N % 128) return fail(FG_ERR_SHAPE, "K must be a multiple of 64 and N of 128");
   if (!aligned(w->codes, 16) || !aligned(packed, 16) || !aligned(w->mins, 4) || !aligned(w->scales, 4))
     return fail(FG_ERR_ALIGN, "codes and the packed buffer need 16-byte alignment");
-  return pack_weight(w->codes, w->mins, w->scales, w->K, w->N, packed, stream);
+  return pack_weight(w->codes, w->mins, w->scales, w->K, w->N, format, packed, stream);
 }
 
 size_t fg_decode_attention_workspace_bytes(const fg_kv* kv) {
@@ -325,8 +370,11 @@ size_t fg_decode_attention_workspace_bytes(const fg_kv* kv) {
   return decode_attention_workspace_bytes(kv->b, kv->heads, kv->head_dim, kv->capacity);
 }
 
-fg_status fg_decode_attention(const fg_kv* kv, const void* q, int64_t ldq, int64_t pos, void* out,
-                              int64_t ldo, void* ws, size_t ws_bytes, cudaStream_t stream) {
+}  // extern "C"
+
+namespace fg {
+fg_status check_decode_attention(const fg_kv* kv, const void* q, int64_t ldq, int64_t pos, const void* out,
+                                 int64_t ldo) {
   if (!kv) return fail(FG_ERR_ARG, "null kv");
   if (kv->heads <= 0 || kv->head_dim <= 0 || kv->b < 0) return fail(FG_ERR_ARG, "kv sizes");
   if (kv->head_dim != 64 && kv->head_dim != 128)
@@ -338,7 +386,16 @@ fg_status fg_decode_attention(const fg_kv* kv, const void* q, int64_t ldq, int64
   if (ldq < h1 || ldo < h1 || ldq % 8 || ldo % 8) return fail(FG_ERR_SHAPE, "ldq/ldo must be >= h1 and multiples of 8");
   if (kv->b == 0) return FG_OK;
   FG_TRY(check_act(q, "q"));
-  FG_TRY(check_act(out, "out"));
+  return check_act(out, "out");
+}
+}  // namespace fg
+
+extern "C" {
+
+fg_status fg_decode_attention(const fg_kv* kv, const void* q, int64_t ldq, int64_t pos, void* out,
+                              int64_t ldo, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  FG_TRY(check_decode_attention(kv, q, ldq, pos, out, ldo));
+  if (kv->b == 0) return FG_OK;
   const size_t need = fg_decode_attention_workspace_bytes(kv);
   if (need && (!ws || ws_bytes < need)) return fail(FG_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes, need);
   if (need && !aligned(ws, 16)) return fail(FG_ERR_ALIGN, "workspace needs 16-byte alignment");
@@ -379,6 +436,7 @@ fg_status fg_prefill_layer(const fg_layer* L, const void* x, int64_t b, int64_t 
 fg_status fg_decode_step(const fg_layer* L, const void* t, int64_t b, int64_t pos, const fg_kv* kv,
                          void* y, void* ws, size_t ws_bytes, cudaStream_t stream) {
   FG_TRY(check_layer(L));
+  FG_TRY(check_decode_copies(*L));
   if (b < 0) return fail(FG_ERR_ARG, "negative size");
   FG_TRY(check_kv(kv, b, L->heads, L->h1 / L->heads, L->codec, L->dtype));
   if (pos < 0 || pos >= kv->capacity)
@@ -434,6 +492,7 @@ fg_status fg_decode_block_step(const fg_layer* layers, int32_t l, const void* t,
   if (!layers || !kvs || l <= 0) return fail(FG_ERR_ARG, "layers/kvs/l");
   for (int32_t i = 0; i < l; ++i) {
     FG_TRY(check_layer(&layers[i]));
+    FG_TRY(check_decode_copies(layers[i]));
     if (layers[i].h1 != layers[0].h1 || layers[i].h2 != layers[0].h2 || layers[i].dtype != layers[0].dtype)
       return fail(FG_ERR_SHAPE, "layers differ in h1/h2/dtype");
     FG_TRY(check_kv(&kvs[i], b, layers[i].heads, layers[i].h1 / layers[i].heads, layers[i].codec,

@@ -30,6 +30,42 @@ constexpr uint32_t kOne = 0x3C003C00u;        // fp16 (1, 1)
 constexpr uint32_t kSixteenth = 0x2C002C00u;  // fp16 (1/16, 1/16)
 constexpr uint32_t kNeg64 = 0xD400D400u;      // fp16 (-64, -64)
 
+// fp16x2 h = (1024 + q0, 1024 + q1), q0, q1 in 0..15 -> exact fp32 (q0, q1),
+// one mixed-precision add per half.
+__device__ __forceinline__ float2 nib_pair_f32(uint32_t h) {
+  float lo, hi;
+  asm("{ .reg .f16 a, b; mov.b32 {a, b}, %2; add.rn.f32.f16 %0, a, %3; add.rn.f32.f16 %1, b, %3; }"
+      : "=f"(lo), "=f"(hi)
+      : "r"(h), "f"(-1024.0f));
+  return make_float2(lo, hi);
+}
+// fp16x2 h = (1024 + 16 q0, 1024 + 16 q1) -> exact fp32 (q0, q1): h/16 - 64
+// in one mixed-precision fma per half (both steps exact).
+__device__ __forceinline__ float2 nib16_pair_f32(uint32_t h) {
+  float lo, hi;
+  asm("{ .reg .f16 a, b, c; mov.b32 {a, b}, %2; mov.b16 c, 0x2C00; fma.rn.f32.f16 %0, a, c, %3; "
+      "fma.rn.f32.f16 %1, b, c, %3; }"
+      : "=f"(lo), "=f"(hi)
+      : "r"(h), "f"(-64.0f));
+  return make_float2(lo, hi);
+}
+// Two IEEE fp32 fmas (each rounded once, round to nearest even) in one
+// paired instruction: (a.x * b.x + c.x, a.y * b.y + c.y).
+__device__ __forceinline__ float2 fma_f32x2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{ .reg .b64 ra, rb, rc, rd; mov.b64 ra, {%2, %3}; mov.b64 rb, {%4, %5}; mov.b64 rc, {%6, %7};\n"
+      "fma.rn.f32x2 rd, ra, rb, rc; mov.b64 {%0, %1}, rd; }"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+// fp16x2 (round to nearest even) of (v.x, v.y): v.x in the lower half.
+__device__ __forceinline__ uint32_t cvt_f16x2(float2 v) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(v.y), "f"(v.x));
+  return r;
+}
+
 // 8 codes (one 32-bit word: consecutive output channels n..n+7 of one input
 // row, one 64-group) -> 8 fp16 weights q*scale + min (s2, m2: scale and min
 // broadcast to both fp16 halves).  A lop3 with the fp16 exponent of 1024

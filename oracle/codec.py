@@ -10,7 +10,7 @@ g = 64, weights grouped along the output channel, KV along the hidden
 dimension, storage in the quantized form and conversion back to FP16
 before compute.
 
-Readings of what the page leaves open (each one is stated in the design doc):
+Readings of what the page leaves open:
   * arithmetic is IEEE fp32, each operation rounded to nearest-even in the
     literal order ((x - mn) / r) * 15, no fused multiply-add;
   * "round" is round-half-to-even;
@@ -133,6 +133,23 @@ def dequant_g64(codes: np.ndarray, mins: np.ndarray, scales: np.ndarray,
     xh = fma_f32(qg, scales[..., None].astype(_F32), mins[..., None].astype(_F32))
     xh = xh.reshape(q.shape)
     return xh.astype(out_dtype)
+
+
+def dequant_g64_f16meta(codes: np.ndarray, mins: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """The opt-in fp16-metadata reading of "converted back to FP16": the
+    group's scale and min are first rounded to fp16 (nearest even), then
+    q * scale16 + min16 is formed exactly and rounded once to fp16.  (The
+    exact value needs at most 44 significant bits -- a 4-bit integer times an
+    11-bit fp16 significand, plus an fp16, all within fp16's exponent range
+    -- so fp64 holds it exactly and numpy's fp64 -> fp16 cast is the single
+    rounding.)  Returns float16 [..., C]."""
+    q = unpack_codes(codes).astype(np.float64)
+    qg = _group_view(q)
+    s16 = np.asarray(scales, dtype=_F32).astype(np.float16).astype(np.float64)
+    m16 = np.asarray(mins, dtype=_F32).astype(np.float16).astype(np.float64)
+    with np.errstate(all="ignore"):
+        exact = qg * s16[..., None] + m16[..., None]
+    return exact.reshape(q.shape).astype(np.float16)
 
 
 def round_trip(x: np.ndarray, out_dtype=None) -> np.ndarray:

@@ -17,7 +17,7 @@ Inference of Large Language Models with a Single GPU"), section
 and section "5. 近似方法": weights and the KV cache are stored in the 4-bit
 group format and converted back to FP16 before compute.
 
-Readings (each stated in the design doc):
+Readings:
   * the prefill softmax is causal (generation; it also makes a decode step
     equal to the last row of a prefill over the extended sequence);
   * with H heads the score scale is 1/sqrt(h1/H) per head; H = 1 is the

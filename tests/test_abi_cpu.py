@@ -54,9 +54,9 @@ def test_codec_argument_errors(fg):
     assert L.fg_dequant_g64(p, p, p, 1, 100, p, 0, None) == 2
 
 
-def _layer(fg, h1=128, h2=256, heads=2, codec=1, dtype=0):
+def _layer(fg, h1=128, h2=256, heads=2, codec=1, dtype=0, packed=True):
     P = 4096
-    wm = lambda K, N: fg.fg_wmat(P, P, P, P, K, N)
+    wm = lambda K, N: fg.fg_wmat(P, P, P, P, K, N, P if packed else None, 0)
     return fg.fg_layer(wm(h1, h1), wm(h1, h1), wm(h1, h1), wm(h1, h1), wm(h1, h2), wm(h2, h1),
                        h1, h2, heads, codec, dtype)
 
@@ -99,6 +99,61 @@ def test_layer_argument_errors(fg):
     # misaligned activation
     assert L.fg_decode_step(ctypes.byref(lay), ctypes.c_void_p(4098), 2, 3, ctypes.byref(kv), P, P, ws,
                             None) == 3
+    # fp16 4-bit decode without the decode copy of every matrix
+    bare = _layer(fg, packed=False)
+    assert L.fg_decode_step(ctypes.byref(bare), P, 2, 3, ctypes.byref(kv), P, P, ws, None) == 1
+    assert b"decode copy" in L.fg_last_error()
+    assert L.fg_decode_workspace_bytes(ctypes.byref(bare), 2, 16) == 0
+    # decode copies in two formats, or an unknown format
+    mixed = _layer(fg)
+    mixed.w1.packed_format = 1
+    assert L.fg_decode_step(ctypes.byref(mixed), P, 2, 3, ctypes.byref(kv), P, P, ws, None) == 1
+    mixed.w1.packed_format = 7
+    assert L.fg_decode_step(ctypes.byref(mixed), P, 2, 3, ctypes.byref(kv), P, P, ws, None) == 1
+    # fp32 layers need no decode copy
+    f32 = _layer(fg, dtype=1, packed=False)
+    assert fg.lib.fg_decode_workspace_bytes(ctypes.byref(f32), 2, 16) > 0
+
+
+def test_pack_weight_sizes_and_errors(fg):
+    L = fg.lib
+    assert L.fg_pack_weight_bytes(4096, 12288, 0) == 4096 * 12288 * 5 // 8        # 0.625 B per weight
+    assert L.fg_pack_weight_bytes(4096, 12288, 1) == 4096 * 12288 * 9 // 16       # 0.5625 B per weight
+    assert L.fg_pack_weight_bytes(4096, 12288, 2) == 0
+    assert L.fg_pack_weight_bytes(4096, 4160, 0) == 0                               # N % 128
+    P = 4096
+    w = fg.fg_wmat(P, P, P, None, 256, 512, None, 0)
+    assert L.fg_pack_weight(ctypes.byref(w), 2, ctypes.c_void_p(P), None) == 1
+    assert L.fg_pack_weight(ctypes.byref(w), 0, None, None) == 1
+    w.N = 320
+    assert L.fg_pack_weight(ctypes.byref(w), 0, ctypes.c_void_p(P), None) == 2
+
+
+def test_noalloc_attention_host_errors(fg):
+    """fg_decode_attention_noalloc rejects bad arguments on the host, before
+    any CUDA call (these need no GPU)."""
+    L = fg.lib
+    P = ctypes.c_void_p(4096)
+    assert L.fg_decode_attention_noalloc(None, P, 256, 3, P, 256, None) == 1           # FG_ERR_ARG
+    bad = _kv(fg, heads=2, d=96)
+    assert L.fg_decode_attention_noalloc(ctypes.byref(bad), P, 192, 3, P, 192, None) == 8   # head_dim
+    kv = _kv(fg, cap=16, heads=2, d=64)
+    assert L.fg_decode_attention_noalloc(ctypes.byref(kv), P, 128, 16, P, 128, None) == 4   # pos
+    assert L.fg_decode_attention_noalloc(ctypes.byref(kv), P, 100, 3, P, 128, None) == 2    # ldq
+
+
+def test_noalloc_scratch_bound_covers_every_cache(fg):
+    """The built-in split scratch (1 MiB) holds what the split rule asks for,
+    for every block size and cache capacity up to 4096 with head_dim 64 and
+    128 (fg_decode_attention_workspace_bytes is pure host code)."""
+    L = fg.lib
+    worst = 0
+    for d in (64, 128):
+        for bh in range(1, 4097):
+            for cap in (1, 2, 16, 100, 513, 544, 1024, 2048, 4096):
+                kv = _kv(fg, b=bh, cap=cap, heads=1, d=d)
+                worst = max(worst, L.fg_decode_attention_workspace_bytes(ctypes.byref(kv)))
+    assert 0 < worst <= 1 << 20
 
 
 def test_workspace_sizes_grow_with_tokens(fg):
@@ -107,3 +162,8 @@ def test_workspace_sizes_grow_with_tokens(fg):
     b = fg.lib.fg_prefill_workspace_bytes(ctypes.byref(lay), 2, 16)
     assert 0 < a < b
     assert fg.lib.fg_prefill_block_workspace_bytes(ctypes.byref(lay), 2, 8) > a
+
+
+def test_wait_limit_setting(fg):
+    assert fg.fg_set_wait_limit(1000) == fg.FG_WAIT_LIMIT_DEFAULT
+    assert fg.fg_set_wait_limit(fg.FG_WAIT_LIMIT_DEFAULT) == 1000

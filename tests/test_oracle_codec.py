@@ -250,3 +250,78 @@ def test_all_nan_group_and_shape_errors():
     assert np.isnan(mins[0, 0]) and np.isnan(scales[0, 0]) and np.all(codes == 0)
     with pytest.raises(ValueError):
         codec.quantize_g64(np.zeros((2, 65), np.float32))
+
+
+# ---- the opt-in fp16-metadata reading (the decode copy's FG_PACK_F16META) --------
+
+def _all_f16_finite():
+    v = np.arange(65536, dtype=np.uint32).astype(np.uint16).view(np.float16)
+    v = np.unique(v[np.isfinite(v)].astype(np.float64))
+    return v
+
+
+_F16 = None
+
+
+def _round_f16(x: Fraction) -> float:
+    """Nearest fp16 to the exact rational x, ties to even significand, found
+    by bisection in the sorted table of every finite fp16 value (no fp16
+    arithmetic involved)."""
+    global _F16
+    if _F16 is None:
+        _F16 = _all_f16_finite()
+    import bisect
+    i = bisect.bisect_left(_F16.tolist(), float(x))
+    cands = [_F16[j] for j in (i - 1, i, i + 1) if 0 <= j < len(_F16)]
+    best = min(cands, key=lambda c: (abs(Fraction(float(c)) - x),
+                                     int(np.float16(c).view(np.uint16)) & 1))
+    return float(best)
+
+
+def test_f16meta_matches_exact_rational_rounding():
+    """Every element: round_f16(q * round_f16(scale) + round_f16(min)) with
+    exact rationals and a table-search rounding."""
+    rng = np.random.default_rng(21)
+    x = np.concatenate([rng.standard_normal((2, 128)) * 0.02, rng.standard_normal((2, 128)) * 3.0,
+                        rng.standard_normal((2, 128)) * 900.0]).astype(np.float16)
+    codes, mins, scales = codec.quantize_g64(x)
+    got = codec.dequant_g64_f16meta(codes, mins, scales)
+    assert got.dtype == np.float16
+    q = codec.unpack_codes(codes)
+    for r in range(x.shape[0]):
+        for g in range(x.shape[1] // 64):
+            s16 = Fraction(_round_f16(Fraction(float(scales[r, g]))))
+            m16 = Fraction(_round_f16(Fraction(float(mins[r, g]))))
+            for c in range(64 * g, 64 * g + 64):
+                want = _round_f16(int(q[r, c]) * s16 + m16)
+                assert float(got[r, c]) == want, (r, c)
+
+
+def test_f16meta_error_bound():
+    """|x - w~| <= scale/2 + 15 ulp16(scale)/2 + ulp16(min)/2 + ulp16(w~)/2,
+    plus the fp32 codec's own slack, for finite groups whose scale and min are
+    normal fp16 numbers."""
+    rng = np.random.default_rng(22)
+    for std in (0.02, 1.0, 100.0):
+        x = (rng.standard_normal((8, 512)) * std).astype(np.float16)
+        codes, mins, scales = codec.quantize_g64(x)
+        w = codec.dequant_g64_f16meta(codes, mins, scales).astype(np.float64).reshape(8, 8, 64)
+        g = x.astype(np.float64).reshape(8, 8, 64)
+        mag = np.maximum(np.abs(g.min(-1)), np.abs(g.max(-1)))
+        ulp16 = lambda v: np.spacing(np.abs(np.asarray(v)).astype(np.float16)).astype(np.float64)
+        bound = (scales / 2 + 15 * ulp16(scales) / 2 + ulp16(mins) / 2
+                 + 4 * np.spacing(mag.astype(np.float32)))[..., None] + ulp16(w) / 2
+        assert np.all(np.abs(g - w) <= bound)
+
+
+def test_f16meta_equals_format_of_record_when_meta_is_fp16():
+    """A group whose min, scale and every q*scale + min are exact fp16 values:
+    both readings give the same fp16 weights."""
+    j = np.arange(64)
+    x = (1.0 + (j % 16) / 8.0).astype(np.float16)[None, :]   # min 1, max 2.875, scale 1/8
+    codes, mins, scales = codec.quantize_g64(x)
+    assert float(scales[0, 0]) == 0.125 and float(mins[0, 0]) == 1.0
+    a = codec.dequant_g64_f16meta(codes, mins, scales)
+    b = codec.dequant_g64(codes, mins, scales, np.float16)
+    assert np.array_equal(a.view(np.uint16), b.view(np.uint16))
+    assert np.array_equal(a, x)

@@ -185,3 +185,110 @@ def test_weights_grouped_along_output_channel():
             rt = w[k, 64 * g:64 * g + 64]
             step = (seg.max() - seg.min()) / 15
             assert np.max(np.abs(seg - rt)) <= step / 2 + 1e-3
+
+
+# ---- the remaining formulas, each against the sizes of the oracle's own tensors --------
+
+def _small():
+    return dict(h1=128, h2=512, b=3, H=2, s=5, n=4, l=2)
+
+
+def test_activation_bytes_is_one_fp16_hidden_state():
+    c = _small()
+    bls = c["b"] * c["s"]
+    x = np.zeros((c["b"], c["s"], c["h1"]), np.float16)
+    assert formulas.activation_bytes_fp16(bls, c["h1"]) == x.nbytes
+
+
+def test_zigzag_peak_mem_is_weights_plus_activation_plus_kv():
+    """Appendix A.2's zig-zag peak: the fp16 weights of all l layers, one fp16
+    hidden state of the block, and the fp16 KV cache of every layer grown to
+    s + n tokens -- summed from the oracle's own tensors."""
+    c = _small()
+    h1, h2, b, s, n, l, H = c["h1"], c["h2"], c["b"], c["s"], c["n"], c["l"], c["H"]
+    raws = [_tiny_weights(h1, h2, 40 + i, False, "f16")[0] for i in range(l)]
+    w_bytes = sum(a.nbytes for r in raws for a in r.values())
+    act = np.zeros((b, h1), np.float16).nbytes
+    caches = [layer.KVCache(b, H, h1 // H, s + n, False, "f16") for _ in range(l)]
+    kv = sum(2 * (cc.k_val.size + cc.v_val.size) for cc in caches)   # fp16 storage: 2 bytes a value
+    assert formulas.zigzag_peak_mem(w_bytes, h1, b, l, s, n) == w_bytes + act + kv
+
+
+def test_causal_prefill_flops_count_the_visible_pairs():
+    c = _small()
+    h1, h2, b = c["h1"], c["h2"], c["b"]
+    for s in (1, 2, 7, 64):
+        visible = int(np.sum(np.arange(s)[None, :] <= np.arange(s)[:, None]))
+        dense = formulas.prefill_flops_layer(b, s, h1, h2)
+        causal = formulas.prefill_flops_layer(b, s, h1, h2, causal=True)
+        # 2 products (scores and values) x 2 flops per multiply-add x h1 per pair
+        assert dense - causal == 4 * b * h1 * (s * s - visible)
+        if s == 1:
+            assert dense == causal
+
+
+def test_decode_flops_are_the_decode_layer_products():
+    """2 flops per multiply-add of every product decode_layer performs, from
+    the shapes of the oracle's weights and cache."""
+    c = _small()
+    h1, h2, b, H, length = c["h1"], c["h2"], c["b"], c["H"], 9
+    raw, w = _tiny_weights(h1, h2, 41, True, "f16")
+    macs = sum(b * m.shape[0] * m.shape[1] for m in (w.wq, w.wk, w.wv, w.wo, w.w1, w.w2))
+    cache = layer.KVCache(b, H, h1 // H, length, True, "f16")
+    d = cache.head_dim
+    macs += 2 * b * H * length * d          # q . K^T over `length` slots, then p . V
+    assert formulas.decode_flops_layer(b, h1, h2, length) == 2 * macs
+
+
+def test_decode_bytes_are_the_tensors_a_step_touches():
+    """Stored 4-bit weights, the KV slots read and the one written, and the
+    fp16 activations of one decode step, from the oracle's own arrays."""
+    c = _small()
+    h1, h2, b, H, length = c["h1"], c["h2"], c["b"], c["H"], 9
+    raw, _ = _tiny_weights(h1, h2, 42, False, "f16")
+    wbytes = 0
+    for m in raw.values():
+        cd, mn, sc = codec.quantize_g64(m)
+        wbytes += cd.nbytes + mn.nbytes + sc.nbytes
+    cache = layer.KVCache(b, H, h1 // H, length, True, "f16")
+    arrs = (cache.k_codes, cache.v_codes, cache.k_mins, cache.k_scales, cache.v_mins, cache.v_scales)
+    kv_read = sum(a[:, :, :length].nbytes for a in arrs)
+    kv_write = sum(a[:, :, :1].nbytes for a in arrs)
+    f16 = lambda *shape: np.zeros(shape, np.float16).nbytes
+    act = (f16(b, h1) + f16(b, 3 * h1)                      # t in, Q|K|V out
+           + f16(b, h1) * 3 + f16(b, h1)                    # q, new K, new V in; attention out
+           + f16(b, h1) * 2 + f16(b, h1)                    # attention out, residual t in; t_Out out
+           + f16(b, h1) + f16(b, h2)                        # t_Out in, hidden out
+           + f16(b, h2) + f16(b, h1) + f16(b, h1))          # hidden, residual t_Out in; t^{i+1} out
+    assert formulas.decode_bytes_layer_q4(b, h1, h2, length) == wbytes + kv_read + kv_write + act
+
+
+def test_generation_throughput_counts_block_tokens():
+    """b n / t: the tokens run_block generates (one per sequence per step)
+    over the time."""
+    h1, h2, H = 64, 128, 1
+    raw, w = _tiny_weights(h1, h2, 43, False)
+    rng = np.random.default_rng(44)
+    b, s, n = 3, 4, 5
+    _, outs, _ = layer.run_block(rng.standard_normal((b, s, h1)), rng.standard_normal((n, b, h1)), [w], H,
+                                 False, "f32")
+    tokens = sum(o.shape[0] for o in outs)
+    assert formulas.generation_throughput(b, n, 2.5) == tokens / 2.5
+
+
+def test_bench_byte_counts_equal_the_oracle_formula():
+    """bench.py's roofline numerator (its own restatement, since the timed
+    path may not import the oracle) equals the oracle's formula; with the
+    fp16-metadata decode copy it differs by exactly the weights' smaller
+    pairs."""
+    import bench
+    import synth
+    for name in ("opt-125m", "opt-6.7b", "opt-30b", "opt-175b"):
+        w = synth.WORKLOADS[name]
+        for length in (w.s + 1, w.s + w.n):
+            want = formulas.decode_bytes_layer_q4(w.b, w.h1, w.h2, length)
+            assert bench.decode_step_bytes(w, w.b, length, 0) == pytest.approx(want, rel=1e-12)
+            diff = formulas.layer_weight_elems(w.h1, w.h2) * (8.0 - 4.0) / 64.0
+            assert bench.decode_step_bytes(w, w.b, length, 1) == pytest.approx(want - diff, rel=1e-12)
+        assert bench.decode_product_flops(w, w.b) + 4.0 * w.b * w.h1 * (w.s + 1) == \
+            formulas.decode_flops_layer(w.b, w.h1, w.h2, w.s + 1)
