@@ -142,8 +142,22 @@ LAYER_LOCAL = [("opt-125m", 0), ("opt-125m", 6), ("opt-125m", 11),
                ("opt-175b", 0), ("opt-175b", 48), ("opt-175b", 95)]
 
 
+def _record(record_property, y, outs, ref, seqs, tol=1e-2):
+    """Max relative error and share of outputs above tol, prefill and decode
+    (kept in the junit report)."""
+    ry, routs, _ = ref
+    scale = lambda want: max(np.max(np.abs(want)), 1e-30)
+    d0 = np.abs(y[seqs].cpu().numpy().astype(np.float64) - ry) / scale(ry)
+    dd = [np.abs(outs[t][seqs].cpu().numpy().astype(np.float64) - routs[t]) / scale(routs[t])
+          for t in range(len(outs))]
+    record_property("prefill_max", float(d0.max()))
+    record_property("prefill_frac_above", float(np.mean(d0 > tol)))
+    record_property("decode_max", float(max(d.max() for d in dd)))
+    record_property("decode_frac_above", float(max(np.mean(d > tol) for d in dd)))
+
+
 @pytest.mark.parametrize("name,layer", LAYER_LOCAL)
-def test_layer_local_full_block(fg, name, layer):
+def test_layer_local_full_block(fg, name, layer, record_property):
     """One layer of each shaped config (first, middle, last) with its own
     N(0,1) inputs (the stack overflows fp16 past a few layers without
     normalisation, so parity is checked layer by layer): at the config's
@@ -159,6 +173,7 @@ def test_layer_local_full_block(fg, name, layer):
     # the cache itself: the codec is bit-exact, so its codes differ only
     # where a K/V row entered it one fp16 ulp apart (fp32 vs fp64 sums)
     oc = ref[2][0]
+    _record(record_property, y, outs, ref, seqs)
     for g_codes, o_codes in ((kvs[0].k_codes, oc.k_codes), (kvs[0].v_codes, oc.v_codes)):
         assert np.mean(g_codes[seqs].cpu().numpy() != o_codes) <= 1e-3
     if w.h1 < 7168:
