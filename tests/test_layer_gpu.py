@@ -182,15 +182,19 @@ def test_layer_local_full_block(fg, name, layer, record_property):
         # A K/V row computed with fp32 sums and rounded to fp16 sits one
         # ulp away from the oracle's fp64-rounded row in a few % of its
         # elements; through the codec that moves ~1% of the groups' (min,
-        # scale) by an ulp and flips ~1e-4 of the codes by a whole step.  At
-        # h1 >= 7168 a few prefill outputs in 1e4 cross 1e-2 from that alone
-        # (the codec-off case below meets 1e-2 on the max).  The decode
-        # products apply fp16-rounded (scale, min) (~1e-3 relative per
-        # weight), which the large attention scores of these unnormalised
-        # layers amplify: up to ~0.5% of decode outputs cross 1e-2 at 175B.
-        # Bars: 1e-2 for all but 2e-4 (prefill) / 1e-2 (decode) of the
-        # outputs, 3e-2 on the max.
-        _compare_flips(y, outs, ref, seqs, 1e-2, (2e-4, 1e-2), 3e-2)
+        # scale) by an ulp and flips ~1e-4 of the codes by a whole step.  The
+        # large attention scores of these unnormalised layers amplify a
+        # flipped code: at h1 >= 7168 a few prefill outputs in 1e4 cross
+        # 1e-2, and at h1 = 12288 up to ~0.4% of the decode outputs (the
+        # codec-off case below meets 1e-2 on the max, and the weights
+        # themselves are bit-exact, test_linear_gpu.py).  Bars: decode 1e-2
+        # on the max up to h1 = 7168; beyond, and for prefill, 1e-2 for all
+        # but 2e-4 (prefill) / 1e-2 (decode) of the outputs, 3e-2 on the max.
+        _compare_flips(y, outs, ref, seqs, 1e-2, (2e-4, 1e-2 if w.h1 > 7168 else 0.0), 3e-2)
+        if w.h1 <= 7168:
+            for t in range(len(outs)):
+                e = rel_err(outs[t][seqs].cpu().numpy(), ref[1][t])
+                assert e <= 1e-2, f"decode step {t} rel err {e}"
 
 
 def _compare_flips(y, outs, ref, seqs, tol, frac, tol_max):
