@@ -1,0 +1,613 @@
+// Decode products of one layer-step in one persistent launch (FlexGen notes,
+// "4. 卸载策略": zig-zag block, one read of a layer's weights serves every
+// sequence of the block; "背景知识": the decode products t w_Q|w_K|w_V,
+// t_Out = (..) w_O + t, relu(t_Out w_1), (..) w_2 + t_Out; "5. 近似方法":
+// weights stored in 4-bit groups of 64 along the output channel, converted
+// back to FP16 before compute).
+//
+// A chain is up to four products run back to back in one grid of one CTA per
+// SM, each product's X either an input of the launch or the output of the
+// product before it (e.g. w_O, w_1, w_2 of layer i and w_Q|w_K|w_V of layer
+// i+1).  Each product's work -- (128-channel tile, 128-k chunk) units, tile
+// major -- is cut into equal contiguous ranges, one per CTA ("stream-K"), so
+// every CTA streams the same share of every weight and there is no wave
+// quantisation and no separate split-sum launch.  A CTA's range covers the
+// end of one tile, whole tiles, and the start of another: each piece is
+// summed in a tensor-memory accumulator; a tile covered by one CTA gets its
+// epilogue at once, otherwise every contributor writes its fp32 partial to
+// its own workspace slot and the last to arrive (a per-tile counter) sums
+// all of them in contributor order -- deterministic whoever is last --
+// applies the epilogue and publishes the tile with a release flag.  The next
+// product's X chunk k is exactly tile k of the product before it; the CTA
+// that needs it waits on that flag (acquire, bounded) before its TMA load.
+// Weights never wait: the weight copies of the next product stream while the
+// current one finishes.
+//
+// Inside a CTA (512 threads, 512 TMEM columns): warp 0 issues the weight
+// copies (one 2-block bulk copy per chunk), warp 1 owns TMEM and issues the
+// MMAs, warp 2 issues the X copies (after the flags), warp 3 takes every
+// mbarrier wait for the converting warps, warps 4..11 convert weights into
+// TMEM (two 64-k tiles of a chunk side by side, the BlockConverter register
+// order), warps 12..15 drain the accumulators and run the epilogues and
+// fixups.  The main loop is the lockstep chunk loop of the decode products:
+// converting warps, sync warp and MMA warp meet at one named barrier per
+// chunk.  Two accumulators alternate between the pieces of the range, so an
+// epilogue overlaps the next piece's MMAs.
+//
+// Every wait is bounded (fg_set_wait_limit): a wait that gives up raises the
+// device error word and makes its role skip work, never a barrier; before the
+// CTA leaves, its copies and MMAs in flight have completed and its tensor
+// memory is freed.  Named barriers: the chunk barrier is taken once per chunk
+// by the MMA, sync and 8 converting warps; the start barrier once by the
+// sync and converting warps; the epilogue barrier the same number of times
+// per piece by the 4 epilogue warps (the branch between its counts is
+// decided once and broadcast through shared memory).
+#include <cudaTypedefs.h>
+#include <string.h>
+
+#include <algorithm>
+
+#include "fg_internal.cuh"
+#include "q4_convert.cuh"
+#include "q4_dev.cuh"
+#include "tc_ptx.cuh"
+
+namespace fg {
+
+bool tc_make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+                 uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw);
+
+namespace {
+
+using namespace tc;
+
+constexpr int BK = 64;                 // k per block / MMA tile
+constexpr int BNC = 128;               // channels per tile (the MMA's M)
+constexpr int CK = 128;                // k per chunk: two blocks
+constexpr int kThreads = 512;
+constexpr int kConvWarp0 = 4;
+constexpr int kEpiWarp0 = 12;
+constexpr int kSyncWarp = 3;
+constexpr uint32_t kChunkBar = 1, kStartBar = 2, kEpiBar = 3;
+constexpr uint32_t kProducerSleepNs = 100;
+constexpr uint32_t kFlagSleepNs = 64;
+
+struct ChainProduct {
+  const uint8_t* wp[3];     // decode copy of each weight segment
+  int seg_n0[4];            // segment column offsets, seg_n0[nseg] = N
+  int nseg;
+  int N, K;
+  __half* Y;
+  int ldy;
+  const __half* R;          // residual [M][ldr] or null
+  int ldr;
+  int r_prod;               // product of this chain that wrote R, or -1
+  int relu;
+  int x_prod;               // product of this chain that writes X, or -1 (an input)
+  unsigned* ready;          // [N/128] tile published (1) -- zero before the launch
+  unsigned* cnt;            // [N/128] contributors arrived -- zero before the launch
+  float* part;              // [N/128 + G - 1][M][128] fp32 partial slots
+};
+
+struct ChainParams {
+  CUtensorMap mapX[kMaxChain];
+  ChainProduct pr[kMaxChain];
+  int np;
+  int M;
+  int G;                    // CTAs
+  unsigned* err;
+  uint32_t wait_limit;
+};
+
+// ---- the partition (identical on the host: chain_owner) -------------------------
+// CTA c owns units [U c / G, U (c+1) / G) of a product with U units; unit u
+// belongs to CTA floor(((u + 1) G - 1) / U).
+__device__ __forceinline__ void cta_range(int64_t U, int c, int G, int64_t& u0, int64_t& u1) {
+  u0 = U * c / G;
+  u1 = U * (c + 1) / G;
+}
+__device__ __forceinline__ int owner(int64_t u, int64_t U, int G) {
+  return static_cast<int>(((u + 1) * G - 1) / U);
+}
+
+__device__ __forceinline__ uint32_t ld_acquire(const unsigned* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release(unsigned* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Waits until *flag != 0 (acquire), polling at most `limit` times.
+__device__ __forceinline__ bool wait_flag(const unsigned* flag, uint32_t limit, volatile int* abort) {
+  for (uint32_t i = 0; i < limit; ++i) {
+    if (ld_acquire(flag) != 0) return true;
+    if ((i & 255u) == 255u && *abort) return false;
+    __nanosleep(kFlagSleepNs);
+  }
+  *abort = 1;
+  return false;
+}
+
+constexpr int chain_min(int a, int b) { return a < b ? a : b; }
+
+template <int BT, int FMT>
+struct ChainCfg {
+  static constexpr int kBB = q4::block_bytes(FMT);   // one 128 x 64 weight block
+  static constexpr int kWStage = 2 * kBB;            // a chunk's two blocks
+  static constexpr int kXT = BT * BK * 2;            // one X tile, K-major, 128-byte swizzle
+  static constexpr int kXStage = 2 * kXT;
+  static constexpr int kAcc = BT < 32 ? 32 : BT;     // accumulator columns
+  static constexpr int kACol = 2 * kAcc;             // A buffers follow the two accumulators
+  static constexpr int kBufs = (512 - kACol) / 64;   // A buffers of 64 columns (a chunk)
+  static constexpr int kXStages = 4;
+  static constexpr int kSmemBudget = 200 * 1024;
+  static constexpr int kWStages = chain_min(16, (kSmemBudget - kXStages * kXStage) / kWStage);
+  static constexpr int kXBytes = kXStages * kXStage;
+  static constexpr int kWBytes = kWStages * kWStage;
+  static constexpr int kBarBytes = (kXStages + 2 * kWStages + kBufs + 4) * 8 + 16;
+  static constexpr int kTotal = 1024 + kXBytes + kWBytes + kBarBytes;
+  static_assert(kBufs >= 3 && kWStages >= 3, "pipeline depth");
+  static_assert(kXStages <= kBufs, "X stages are freed by buffer commits");
+  static_assert(kXT % 1024 == 0, "X tiles stay 1024-byte aligned");
+};
+
+// Walks a CTA's chunks of every product of the chain in order.
+struct Walk {
+  int p;                 // product
+  int64_t u, u1;         // current unit and end of this product's range
+  int cpt;               // chunks per tile of product p
+  __device__ __forceinline__ void settle(const ChainParams& P, int cta) {
+    while (p < P.np && u >= u1) {
+      ++p;
+      if (p < P.np) {
+        const ChainProduct& q = P.pr[p];
+        cpt = q.K / CK;
+        cta_range(static_cast<int64_t>(q.N / BNC) * cpt, cta, P.G, u, u1);
+      }
+    }
+  }
+  __device__ __forceinline__ void start(const ChainParams& P, int cta) {
+    p = -1;
+    u = u1 = 0;
+    settle(P, cta);
+  }
+  __device__ __forceinline__ void next(const ChainParams& P, int cta) {
+    ++u;
+    settle(P, cta);
+  }
+  __device__ __forceinline__ int tile() const { return static_cast<int>(u / cpt); }
+  __device__ __forceinline__ int kc() const { return static_cast<int>(u % cpt); }
+  __device__ __forceinline__ bool first_of_piece(int64_t u0) const { return u == u0 || kc() == 0; }
+};
+
+__device__ __forceinline__ int64_t total_chunks(const ChainParams& P, int cta) {
+  int64_t n = 0;
+  for (int p = 0; p < P.np; ++p) {
+    int64_t u0, u1;
+    cta_range(static_cast<int64_t>(P.pr[p].N / BNC) * (P.pr[p].K / CK), cta, P.G, u0, u1);
+    n += u1 - u0;
+  }
+  return n;
+}
+
+template <int BT, int FMT>
+__global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constant__ ChainParams P) {
+  using C = ChainCfg<BT, FMT>;
+  constexpr int NB = C::kBufs, SX = C::kXStages, SW = C::kWStages;
+  constexpr uint32_t kIdesc = idesc_f16(128, BT, 0, 0);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* xring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* wring = xring + C::kXBytes;
+  uint64_t* xfull = reinterpret_cast<uint64_t*>(wring + C::kWBytes);
+  uint64_t* wfull = xfull + SX;
+  uint64_t* wempty = wfull + SW;
+  uint64_t* bufdone = wempty + SW;     // MMAs of the chunk in TMEM buffer b completed
+  uint64_t* accfull = bufdone + NB;    // [2] the piece in accumulator a is summed
+  uint64_t* accempty = accfull + 2;    // [2] accumulator a drained by the epilogue warps
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accempty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* epi_last = abort_flag + 1;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int cta = blockIdx.x;
+  const int64_t nch = total_chunks(P, cta);
+
+  griddep_launch();
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < SX; ++i) mbar_init(&xfull[i], 1);
+    for (int i = 0; i < SW; ++i) {
+      mbar_init(&wfull[i], 1);
+      mbar_init(&wempty[i], 1);
+    }
+    for (int i = 0; i < NB; ++i) mbar_init(&bufdone[i], 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&accfull[i], 1);
+      mbar_init(&accempty[i], 4);   // one arrival per epilogue warp
+    }
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, 512);
+  if (warp == 2 && lane == 0)
+    for (int p = 0; p < P.np; ++p) tma_prefetch_desc(&P.mapX[p]);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ---- weight copies: independent of every flag, so they run ahead ----------------
+    if (lane == 0) {
+      Walk w;
+      w.start(P, cta);
+      int64_t issued = 0;
+      for (int64_t g = 0; g < nch; ++g, w.next(P, cta)) {
+        const int s = static_cast<int>(g % SW);
+        if (!mbar_wait_sleep(&wempty[s], static_cast<uint32_t>((g / SW) & 1) ^ 1u, P.wait_limit, abort_flag,
+                             kProducerSleepNs))
+          break;
+        const ChainProduct& q = P.pr[w.p];
+        const int n0 = w.tile() * BNC;
+        int seg = 0;
+        while (seg + 1 < q.nseg && n0 >= q.seg_n0[seg + 1]) ++seg;
+        const size_t run = static_cast<size_t>(q.K / BK) * C::kBB;   // the k blocks of one tile
+        const uint8_t* src = q.wp[seg] + static_cast<size_t>((n0 - q.seg_n0[seg]) / BNC) * run +
+                             static_cast<size_t>(w.kc()) * C::kWStage;
+        mbar_expect_tx(&wfull[s], C::kWStage);
+        bulk_load(wring + s * C::kWStage, src, C::kWStage, &wfull[s]);
+        ++issued;
+      }
+      for (int64_t g = issued > SW ? issued - SW : 0; g < issued; ++g) {   // nothing in flight at exit
+        volatile int dummy = 0;
+        mbar_wait(&wfull[g % SW], static_cast<uint32_t>((g / SW) & 1), kDrainLimit, &dummy);
+      }
+      if (*abort_flag) atomicOr(P.err, DEV_ERR_WAIT_TIMEOUT);
+    }
+  } else if (warp == 2) {
+    // ---- X copies: chunk k of a product's X is tile k of the product before it -------
+    if (lane == 0) {
+      griddep_wait();   // inputs, flags and counters belong to the stream order from here on
+      Walk w;
+      w.start(P, cta);
+      int64_t issued = 0;
+      for (int64_t g = 0; g < nch; ++g, w.next(P, cta)) {
+        const int s = static_cast<int>(g % SX);
+        // the MMAs of chunk g - SX, the last to read stage s, have completed
+        if (g >= SX && !mbar_wait_sleep(&bufdone[(g - SX) % NB], static_cast<uint32_t>(((g - SX) / NB) & 1),
+                                        P.wait_limit, abort_flag, kProducerSleepNs))
+          break;
+        const ChainProduct& q = P.pr[w.p];
+        const int kc = w.kc();
+        if (q.x_prod >= 0) {
+          if (!wait_flag(P.pr[q.x_prod].ready + kc, P.wait_limit, abort_flag)) break;
+          fence_proxy_async_global();   // the acquired tile, to the TMA reads that follow
+        }
+        mbar_expect_tx(&xfull[s], C::kXStage);
+        for (int t = 0; t < 2; ++t)
+          tma_load_2d(xring + s * C::kXStage + t * C::kXT, &P.mapX[w.p], kc * CK + t * BK, 0, &xfull[s]);
+        ++issued;
+      }
+      for (int64_t g = issued > SX ? issued - SX : 0; g < issued; ++g) {
+        volatile int dummy = 0;
+        mbar_wait(&xfull[g % SX], static_cast<uint32_t>((g / SX) & 1), kDrainLimit, &dummy);
+      }
+      if (*abort_flag) atomicOr(P.err, DEV_ERR_WAIT_TIMEOUT);
+    }
+  } else if (warp == 1) {
+    // ---- MMAs: every lane takes the chunk barrier, lane 0 issues ---------------------
+    Walk w;
+    w.start(P, cta);
+    int64_t piece = -1, u0 = -1;
+    int pp = -1;
+    for (int64_t g = 0; g < nch; ++g, w.next(P, cta)) {
+      if (w.p != pp) {   // a new product: its range starts here
+        pp = w.p;
+        u0 = w.u;
+      }
+      const bool first = w.first_of_piece(u0);
+      const bool last = (w.u + 1 == w.u1) || (w.kc() + 1 == w.cpt);
+      if (first) ++piece;
+      named_bar_sync(kChunkBar, 64 + 8 * 32);   // chunk g is in TMEM, its X has landed, its accumulator is free
+      if (lane == 0) {
+        tc_fence_after();
+        const int b = static_cast<int>(g % NB);
+        const uint32_t acc = tmem_base + static_cast<uint32_t>(piece & 1) * C::kAcc;
+        if (!*abort_flag) {
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            const uint32_t xa = smem_u32(xring + (g % SX) * C::kXStage + t * C::kXT);
+            const uint32_t ta = tmem_base + C::kACol + b * 64 + 32u * t;
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk) {
+              const uint64_t bdesc = smem_desc_sw128(xa + kk * 32, 16, 1024);
+              mma_f16_ts(acc, ta + 8u * kk, bdesc, kIdesc, (first && t == 0 && kk == 0) ? 0u : 1u);
+            }
+          }
+        }
+        mma_commit(&bufdone[b]);
+        if (last) mma_commit(&accfull[piece & 1]);
+      }
+      __syncwarp();
+    }
+  } else if (warp == kSyncWarp) {
+    // ---- waits on behalf of the warps that take the chunk barrier ----------------------
+    // Before chunk barrier g: chunk g's X, TMEM buffer (g+1) % NB free (the MMAs
+    // of chunk g+1-NB done), the weights of chunk g+2 landed, and -- at the
+    // first chunk of piece k >= 2 -- its accumulator drained.  After it: the
+    // weight stages converted by then are released.
+    bool ok = nch == 0 || (mbar_wait(&wfull[0], 0, P.wait_limit, abort_flag) &&
+                           (nch < 2 || mbar_wait(&wfull[1 % SW], (1 / SW) & 1, P.wait_limit, abort_flag)));
+    named_bar_sync(kStartBar, 32 + 8 * 32);
+    Walk w;
+    w.start(P, cta);
+    int64_t piece = -1, u0 = -1;
+    int pp = -1;
+    for (int64_t g = 0; g < nch; ++g, w.next(P, cta)) {
+      if (w.p != pp) {
+        pp = w.p;
+        u0 = w.u;
+      }
+      if (w.first_of_piece(u0)) ++piece;
+      if (ok) ok = mbar_wait(&xfull[g % SX], static_cast<uint32_t>((g / SX) & 1), P.wait_limit, abort_flag);
+      if (ok && g + 1 < nch && g + 1 >= NB)
+        ok = mbar_wait(&bufdone[(g + 1) % NB], static_cast<uint32_t>(((g + 1 - NB) / NB) & 1), P.wait_limit,
+                       abort_flag);
+      if (ok && g + 2 < nch)
+        ok = mbar_wait(&wfull[(g + 2) % SW], static_cast<uint32_t>(((g + 2) / SW) & 1), P.wait_limit, abort_flag);
+      if (ok && w.first_of_piece(u0) && piece >= 2)
+        ok = mbar_wait(&accempty[piece & 1], static_cast<uint32_t>(((piece - 2) / 2) & 1), P.wait_limit,
+                       abort_flag);
+      __syncwarp();
+      named_bar_sync(kChunkBar, 64 + 8 * 32);
+      if (lane == 0) {
+        if (g == 0) mbar_arrive(&wempty[0]);
+        if (g + 1 < nch) mbar_arrive(&wempty[(g + 1) % SW]);
+      }
+    }
+  } else if (warp < kEpiWarp0) {
+    // ---- conversion of the weights into TMEM --------------------------------------------
+    const int d = warp - kConvWarp0;
+    const int t = d >> 2;                 // which block of the chunk
+    const int q = warp & 3;               // TMEM lane quarter
+    const uint32_t trow = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + C::kACol + 32u * t;
+    q4::BlockConverter<FMT> cv;
+    uint32_t a[32];
+    named_bar_sync(kStartBar, 32 + 8 * 32);
+    if (nch > 0) {
+      cv.load(wring + t * C::kBB, q, lane);
+      cv.convert(a, q, lane);
+    }
+    for (int64_t g = 0; g < nch; ++g) {
+      const bool next = g + 1 < nch;
+      // the next chunk's loads go out before this chunk's stores
+      if (next) cv.load(wring + ((g + 1) % SW) * C::kWStage + t * C::kBB, q, lane);
+      tc_fence_after();
+      const uint32_t dst = trow + static_cast<uint32_t>(g % NB) * 64;
+      tmem_st_16x128b_x8(dst, a);
+      tmem_st_16x128b_x8(dst + (16u << 16), a + 16);
+      if (next) cv.convert(a, q, lane);
+      tmem_st_wait();
+      tc_fence_before();
+      named_bar_sync(kChunkBar, 64 + 8 * 32);
+    }
+  } else {
+    // ---- epilogues: drain each piece, then the tile's output or its fixup ------------------
+    const int eq = warp & 3;              // TMEM lane quarter = 32 channels of the tile
+    const int tid = threadIdx.x - 32 * kEpiWarp0;
+    griddep_wait();
+    int64_t piece = -1;
+    for (int p = 0; p < P.np; ++p) {
+      const ChainProduct& q = P.pr[p];
+      const int cpt = q.K / CK;
+      const int64_t U = static_cast<int64_t>(q.N / BNC) * cpt;
+      int64_t u0, u1;
+      cta_range(U, cta, P.G, u0, u1);
+      for (int64_t u = u0; u < u1;) {
+        const int n = static_cast<int>(u / cpt);
+        const int64_t uend = std::min<int64_t>(u1, static_cast<int64_t>(n + 1) * cpt);
+        ++piece;
+        const int first = owner(static_cast<int64_t>(n) * cpt, U, P.G);
+        const int lastc = owner(static_cast<int64_t>(n + 1) * cpt - 1, U, P.G);
+        const int J = lastc - first + 1;
+        u = uend;
+
+        bool ok = mbar_wait(&accfull[piece & 1], static_cast<uint32_t>((piece / 2) & 1), P.wait_limit, abort_flag);
+        if (!ok) {
+          volatile int dummy = 0;   // the MMA warp always commits: let the MMAs finish first
+          mbar_wait(&accfull[piece & 1], static_cast<uint32_t>((piece / 2) & 1), kDrainLimit, &dummy);
+        }
+        tc_fence_after();
+        float v[BT];
+        {
+          const uint32_t ta = tmem_base + (static_cast<uint32_t>(32 * eq) << 16) + static_cast<uint32_t>(piece & 1) * C::kAcc;
+#pragma unroll
+          for (int c0 = 0; c0 < BT; c0 += 32) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(ta + c0, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[c0 + e] = __uint_as_float(r[e]);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&accempty[piece & 1]);
+        ok = ok && !*abort_flag;
+
+        const int ch = n * BNC + 32 * eq + lane;   // this thread's output channel
+        const int M = P.M;
+        bool publish = J == 1;
+        if (J > 1) {
+          float* mine = q.part + (static_cast<size_t>(n) + cta) * M * BNC + 32 * eq + lane;
+#pragma unroll
+          for (int m = 0; m < BT; ++m)
+            if (m < M) mine[m * BNC] = v[m];
+          __threadfence();
+          named_bar_sync(kEpiBar, 128);
+          if (tid == 0) *epi_last = atomicAdd(q.cnt + n, 1u) == static_cast<unsigned>(J - 1);
+          named_bar_sync(kEpiBar, 128);
+          publish = *epi_last != 0;
+          if (publish) {
+            __threadfence();
+            // every contributor's partial (this CTA's too, as written) in
+            // contributor order: the same sum whichever CTA arrives last
+#pragma unroll
+            for (int m = 0; m < BT; ++m) v[m] = 0.0f;
+#pragma unroll 1
+            for (int c = first; c <= lastc; ++c) {
+              const float* src = q.part + (static_cast<size_t>(n) + c) * M * BNC + 32 * eq + lane;
+#pragma unroll
+              for (int m = 0; m < BT; ++m)
+                if (m < M) v[m] += __ldcg(src + m * BNC);
+            }
+          }
+        }
+        if (publish) {
+          if (q.R && q.r_prod >= 0) ok = ok && wait_flag(P.pr[q.r_prod].ready + n, P.wait_limit, abort_flag);
+#pragma unroll
+          for (int m = 0; m < BT; ++m) {
+            if (m < M) {
+              float y = v[m];
+              if (q.R) y += __half2float(__ldcg(q.R + static_cast<size_t>(m) * q.ldr + ch));
+              if (q.relu) y = fmaxf(y, 0.0f);
+              if (ok) q.Y[static_cast<size_t>(m) * q.ldy + ch] = __float2half_rn(y);
+            }
+          }
+          __threadfence();
+          named_bar_sync(kEpiBar, 128);
+          if (tid == 0) {
+            if (J > 1) q.cnt[n] = 0;   // every contributor has arrived: ready for the next launch
+            st_release(q.ready + n, 1u);
+          }
+        }
+      }
+    }
+    if (tid == 0 && *abort_flag) atomicOr(P.err, DEV_ERR_WAIT_TIMEOUT);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 512);
+  }
+}
+
+template <int BT, int FMT>
+fg_status launch_chain(const ChainParams& P, cudaStream_t st, bool pdl) {
+  using C = ChainCfg<BT, FMT>;
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    if (cudaFuncSetAttribute(chain_kernel<BT, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kTotal) !=
+        cudaSuccess)
+      return check_launch("chain smem attribute");
+    attr_set[dev] = true;
+  }
+  Trace tr(KC_GEMM_Q4DEC, st);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(P.G));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::kTotal;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  if (cudaLaunchKernelEx(&cfg, chain_kernel<BT, FMT>, P) != cudaSuccess) return check_launch("chain_kernel (launch)");
+  return check_launch("chain_kernel");
+}
+
+}  // namespace
+
+int chain_owner(int64_t u, int64_t U, int G) { return static_cast<int>(((u + 1) * G - 1) / U); }
+
+int chain_ctas() { return std::min(num_sms(), kChainMaxCtas); }
+
+size_t chain_part_bytes(int64_t M, int64_t N) {
+  return static_cast<size_t>(N / BNC + kChainMaxCtas - 1) * static_cast<size_t>(M) * BNC * sizeof(float);
+}
+
+size_t chain_ctrl_bytes(int64_t N) { return static_cast<size_t>(N / BNC) * 2 * sizeof(unsigned); }
+
+bool chain_supported(const GemmArgs& a) {
+  if (a.dtype != FG_F16 || !a.quant || a.M < 1 || a.M > 64 || a.K % CK || a.N % BNC) return false;
+  for (int i = 0; i < a.nseg; ++i) {
+    const WSeg& s = a.seg[i];
+    if (!s.packed || s.N % BNC || !aligned(s.packed, 16) || s.packed_format != a.seg[0].packed_format) return false;
+    if (s.packed_format != FG_PACK_EXACT && s.packed_format != FG_PACK_F16META) return false;
+  }
+  if ((a.ldx * 2) % 16 || !aligned(a.X, 16)) return false;
+  if (a.ldy % 8 || !aligned(a.Y, 16) || (a.R && (a.ldr % 8 || !aligned(a.R, 16)))) return false;
+  return true;
+}
+
+fg_status chain_run(const ChainLink* links, int n, void* part_ws, size_t part_bytes, unsigned* ctrl,
+                    size_t ctrl_bytes, bool ctrl_zeroed, cudaStream_t st) {
+  if (n < 1 || n > kMaxChain) return fail(FG_ERR_ARG, "chain of %d products", n);
+  ChainParams P;
+  memset(&P, 0, sizeof(P));
+  P.np = n;
+  P.M = static_cast<int>(links[0].a.M);
+  P.G = chain_ctas();
+  P.err = device_error_word();
+  if (!P.err) return fail(FG_ERR_CUDA, "device error word");
+  P.wait_limit = wait_limit();
+  char* part = static_cast<char*>(part_ws);
+  size_t pused = 0, cused = 0;
+  const int fmt = links[0].a.seg[0].packed_format;
+  for (int i = 0; i < n; ++i) {
+    const GemmArgs& a = links[i].a;
+    if (!chain_supported(a) || a.M != P.M || a.seg[0].packed_format != fmt)
+      return fail(FG_ERR_ARG, "product %d cannot join the chain", i);
+    ChainProduct& q = P.pr[i];
+    if (!tc_make_map(&P.mapX[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.X, a.K, a.M, a.ldx * 2, BK,
+                     static_cast<uint32_t>(a.M <= 32 ? 32 : 64), CU_TENSOR_MAP_SWIZZLE_128B))
+      return fail(FG_ERR_CUDA, "tensor map for X of product %d", i);
+    for (int s = 0; s < a.nseg; ++s) {
+      q.wp[s] = a.seg[s].packed;
+      q.seg_n0[s] = static_cast<int>(a.seg[s].n0);
+    }
+    q.nseg = a.nseg;
+    q.seg_n0[a.nseg] = static_cast<int>(a.N);
+    q.N = static_cast<int>(a.N);
+    q.K = static_cast<int>(a.K);
+    q.Y = static_cast<__half*>(a.Y);
+    q.ldy = static_cast<int>(a.ldy);
+    q.R = static_cast<const __half*>(a.R);
+    q.ldr = static_cast<int>(a.ldr);
+    q.r_prod = links[i].r_prod;
+    q.relu = a.relu;
+    q.x_prod = links[i].x_prod;
+    if (q.x_prod >= i || q.r_prod >= i) return fail(FG_ERR_ARG, "a chain product reads a later product");
+    if (q.x_prod >= 0 && P.pr[q.x_prod].N != q.K) return fail(FG_ERR_SHAPE, "chain X width");
+    if (q.r_prod >= 0 && (!q.R || P.pr[q.r_prod].N != q.N)) return fail(FG_ERR_SHAPE, "chain residual width");
+    const size_t pb = chain_part_bytes(a.M, a.N), cb = chain_ctrl_bytes(a.N);
+    if (pused + pb > part_bytes || cused + cb > ctrl_bytes) return fail(FG_ERR_WORKSPACE, "chain workspace");
+    q.part = reinterpret_cast<float*>(part + pused);
+    q.ready = ctrl + cused / sizeof(unsigned);
+    q.cnt = q.ready + a.N / BNC;
+    pused += (pb + 255) / 256 * 256;
+    cused += cb;
+  }
+  if (!ctrl_zeroed) {
+    if (cudaMemsetAsync(ctrl, 0, cused, st) != cudaSuccess) return check_launch("chain control reset");
+  }
+  const bool pdl = ctrl_zeroed;   // after a memset the launch keeps the full stream order
+  if (fmt == FG_PACK_F16META)
+    return P.M <= 32 ? launch_chain<32, FG_PACK_F16META>(P, st, pdl) : launch_chain<64, FG_PACK_F16META>(P, st, pdl);
+  return P.M <= 32 ? launch_chain<32, FG_PACK_EXACT>(P, st, pdl) : launch_chain<64, FG_PACK_EXACT>(P, st, pdl);
+}
+
+size_t chain_workspace_bytes(const int64_t* N, int n, int64_t M) {
+  size_t b = 0;
+  for (int i = 0; i < n; ++i) b += (chain_part_bytes(M, N[i]) + 255) / 256 * 256;
+  return b;
+}
+
+}  // namespace fg

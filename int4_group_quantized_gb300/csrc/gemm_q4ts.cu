@@ -45,6 +45,7 @@
 #include <atomic>
 
 #include "fg_internal.cuh"
+#include "q4_convert.cuh"
 #include "q4_dev.cuh"
 #include "tc_ptx.cuh"
 
@@ -403,61 +404,11 @@ __global__ void __launch_bounds__(TsCfg<BT, RB, FMT>::kThreads, TsCfg<BT, RB, FM
     // codes of channels 32q + lane/4 + 8w (w = 0..3) at k pairs 4i + c4, i =
     // 0..3 in w0 and 4..7 in w1; this 64-channel group's (scale, min) pairs
     // for those k pairs, unit u holding i = 2u and 2u+1.
-    uint4 w0, w1, pv[4];
-    const uint8_t* cur = wring;   // the weight stage block load() read from
+    q4::BlockConverter<FMT> cv;
     auto load = [&](int c) {
-      cur = wring + (c % SW) * C::kWStage + (rb * KT + tile) * kTileBytes;
-      w0 = *reinterpret_cast<const uint4*>(cur + q * 1024 + lane * 16);
-      w1 = *reinterpret_cast<const uint4*>(cur + q * 1024 + 512 + lane * 16);
-      if (FMT == FG_PACK_F16META) {
-        const uint4* pr = reinterpret_cast<const uint4*>(cur + kTileCodes + (q >> 1) * 256) + c4;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) pv[u] = pr[4 * u];
-      }
+      cv.load(wring + (c % SW) * C::kWStage + (rb * KT + tile) * kTileBytes, q, lane);
     };
-    // Converts what load() fetched into a[].
-    auto convert = [&]() {
-      if (FMT == FG_PACK_EXACT) {
-        // fp16(fmaf(q, scale, min)) with the stored fp32 pairs: the nibbles
-        // become exact fp16 (1024 + q or 1024 + 16q, one lop3 for both k of
-        // a pair), exact fp32 q by one mixed-precision op each, then one
-        // paired fp32 FMA (each lane rounded once) and one rounding to fp16
-        const float4* pr = reinterpret_cast<const float4*>(cur + kTileCodes + (q >> 1) * 512) + c4;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float4 sm = pr[4 * i];   // (scale[2j], scale[2j+1], min[2j], min[2j+1]), j = 4i + c4
-          const uint4 cw = i < 4 ? w0 : w1;
-          const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
-          const int e = i & 3;
-#pragma unroll
-          for (int w = 0; w < 4; ++w) {
-            const uint32_t x = e >= 2 ? words[w] >> 8 : words[w];
-            const uint32_t h = lop_mask_or(x, (e & 1) ? 0x00F000F0u : 0x000F000Fu, kMagic);
-            const float2 qq = (e & 1) ? nib16_pair_f32(h) : nib_pair_f32(h);
-            const float2 r = fma_f32x2(qq, make_float2(sm.x, sm.y), make_float2(sm.z, sm.w));
-            a[16 * (w >> 1) + 2 * i + (w & 1)] = cvt_f16x2(r);
-          }
-        }
-      } else {
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const uint4 cw = u < 2 ? w0 : w1;
-          const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
-#pragma unroll
-          for (int hi = 0; hi < 2; ++hi) {
-            const int i = 2 * u + hi, e = i & 3;   // column 4i + c4: nibble slots e and e+4
-            const uint32_t s2 = hi ? pv[u].z : pv[u].x, m2 = hi ? pv[u].w : pv[u].y;
-#pragma unroll
-            for (int w = 0; w < 4; ++w) {
-              const uint32_t x = e >= 2 ? words[w] >> 8 : words[w];
-              a[16 * (w >> 1) + 2 * i + (w & 1)] =
-                  (e & 1) ? hfma2_u(hfma2_u(lop_mask_or(x, 0x00F000F0u, kMagic), kSixteenth, kNeg64), s2, m2)
-                          : hfma2_u(hfma2_u(lop_mask_or(x, 0x000F000Fu, kMagic), kOne, kNegMagic), s2, m2);
-            }
-          }
-        }
-      }
-    };
+    auto convert = [&]() { cv.convert(a, q, lane); };
     auto mine = [&](int c) { return tile < min(KT, nk - KT * c); };   // a ragged last chunk has one tile
     // The sync warp has seen the weights of chunks 0 and 1 land before this
     // barrier, and before chunk barrier c those of chunk c+2 and TMEM buffer
