@@ -109,6 +109,7 @@ __device__ __forceinline__ void cta_range(int64_t U, int c, int G, int64_t& u0, 
 __device__ __forceinline__ int owner(int64_t u, int64_t U, int G) {
   return static_cast<int>(((u + 1) * G - 1) / U);
 }
+__device__ __forceinline__ bool nonempty(int64_t U, int c, int G) { return U * (c + 1) / G > U * c / G; }
 
 __device__ __forceinline__ uint32_t ld_acquire(const unsigned* p) {
   uint32_t v;
@@ -409,9 +410,13 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
         const int n = static_cast<int>(u / cpt);
         const int64_t uend = std::min<int64_t>(u1, static_cast<int64_t>(n + 1) * cpt);
         ++piece;
+        // contributors: the CTAs from the owner of the tile's first unit to
+        // the owner of its last, less those with an empty range (fewer units
+        // than CTAs)
         const int first = owner(static_cast<int64_t>(n) * cpt, U, P.G);
         const int lastc = owner(static_cast<int64_t>(n + 1) * cpt - 1, U, P.G);
-        const int J = lastc - first + 1;
+        int J = 0;
+        for (int c = first; c <= lastc; ++c) J += nonempty(U, c, P.G);
         u = uend;
 
         bool ok = mbar_wait(&accfull[piece & 1], static_cast<uint32_t>((piece / 2) & 1), P.wait_limit, abort_flag);
@@ -458,6 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
             for (int m = 0; m < BT; ++m) v[m] = 0.0f;
 #pragma unroll 1
             for (int c = first; c <= lastc; ++c) {
+              if (!nonempty(U, c, P.G)) continue;
               const float* src = q.part + (static_cast<size_t>(n) + c) * M * BNC + 32 * eq + lane;
 #pragma unroll
               for (int m = 0; m < BT; ++m)
