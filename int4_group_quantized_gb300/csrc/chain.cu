@@ -71,6 +71,7 @@ constexpr int kSyncWarp = 3;
 constexpr uint32_t kChunkBar = 1, kStartBar = 2, kEpiBar = 3;
 constexpr uint32_t kProducerSleepNs = 100;
 constexpr uint32_t kFlagSleepNs = 64;
+constexpr uint32_t kEpiSleepNs = 200;
 
 struct ChainProduct {
   const uint8_t* wp[3];     // decode copy of each weight segment
@@ -419,11 +420,20 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
         for (int c = first; c <= lastc; ++c) J += nonempty(U, c, P.G);
         u = uend;
 
-        bool ok = mbar_wait(&accfull[piece & 1], static_cast<uint32_t>((piece / 2) & 1), P.wait_limit, abort_flag);
-        if (!ok) {
-          volatile int dummy = 0;   // the MMA warp always commits: let the MMAs finish first
-          mbar_wait(&accfull[piece & 1], static_cast<uint32_t>((piece / 2) & 1), kDrainLimit, &dummy);
+        // one lane polls, pausing between polls: these warps wait most of the
+        // time, and their polling would take shared-memory and issue slots
+        // from the converting warps
+        bool ok = true;
+        if (lane == 0) {
+          ok = mbar_wait_sleep(&accfull[piece & 1], static_cast<uint32_t>((piece / 2) & 1), P.wait_limit, abort_flag,
+                               kEpiSleepNs);
+          if (!ok) {
+            volatile int dummy = 0;   // the MMA warp always commits: let the MMAs finish first
+            mbar_wait(&accfull[piece & 1], static_cast<uint32_t>((piece / 2) & 1), kDrainLimit, &dummy);
+          }
         }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        __syncwarp();
         tc_fence_after();
         float v[BT];
         {
