@@ -102,15 +102,13 @@ struct ChainParams {
 
 // ---- the partition (identical on the host: chain_owner) -------------------------
 // CTA c owns units [U c / G, U (c+1) / G) of a product with U units; unit u
-// belongs to CTA floor(((u + 1) G - 1) / U).
-__device__ __forceinline__ void cta_range(int64_t U, int c, int G, int64_t& u0, int64_t& u1) {
+// belongs to CTA floor(((u + 1) G - 1) / U).  U G stays below 2^31 (U <= 2^16
+// units of 128 x 128 weights, G <= 256), so 32-bit arithmetic is exact.
+__device__ __forceinline__ void cta_range(int U, int c, int G, int& u0, int& u1) {
   u0 = U * c / G;
   u1 = U * (c + 1) / G;
 }
-__device__ __forceinline__ int owner(int64_t u, int64_t U, int G) {
-  return static_cast<int>(((u + 1) * G - 1) / U);
-}
-__device__ __forceinline__ bool nonempty(int64_t U, int c, int G) { return U * (c + 1) / G > U * c / G; }
+__device__ __forceinline__ int owner(int u, int U, int G) { return ((u + 1) * G - 1) / U; }
 
 __device__ __forceinline__ uint32_t ld_acquire(const unsigned* p) {
   uint32_t v;
@@ -154,18 +152,23 @@ struct ChainCfg {
   static_assert(kXT % 1024 == 0, "X tiles stay 1024-byte aligned");
 };
 
-// Walks a CTA's chunks of every product of the chain in order.
+// Walks a CTA's chunks of every product of the chain in order, keeping the
+// tile and chunk of the current unit (no division per chunk).
 struct Walk {
   int p;                 // product
-  int64_t u, u1;         // current unit and end of this product's range
+  int u, u0, u1;         // current unit, this product's range
   int cpt;               // chunks per tile of product p
+  int tile, kc;          // u = tile * cpt + kc
   __device__ __forceinline__ void settle(const ChainParams& P, int cta) {
     while (p < P.np && u >= u1) {
       ++p;
       if (p < P.np) {
         const ChainProduct& q = P.pr[p];
         cpt = q.K / CK;
-        cta_range(static_cast<int64_t>(q.N / BNC) * cpt, cta, P.G, u, u1);
+        cta_range((q.N / BNC) * cpt, cta, P.G, u0, u1);
+        u = u0;
+        tile = u0 / cpt;
+        kc = u0 - tile * cpt;
       }
     }
   }
@@ -176,18 +179,21 @@ struct Walk {
   }
   __device__ __forceinline__ void next(const ChainParams& P, int cta) {
     ++u;
+    if (++kc == cpt) {
+      kc = 0;
+      ++tile;
+    }
     settle(P, cta);
   }
-  __device__ __forceinline__ int tile() const { return static_cast<int>(u / cpt); }
-  __device__ __forceinline__ int kc() const { return static_cast<int>(u % cpt); }
-  __device__ __forceinline__ bool first_of_piece(int64_t u0) const { return u == u0 || kc() == 0; }
+  __device__ __forceinline__ bool first() const { return u == u0 || kc == 0; }
+  __device__ __forceinline__ bool last() const { return u + 1 == u1 || kc + 1 == cpt; }
 };
 
-__device__ __forceinline__ int64_t total_chunks(const ChainParams& P, int cta) {
-  int64_t n = 0;
+__device__ __forceinline__ int total_chunks(const ChainParams& P, int cta) {
+  int n = 0;
   for (int p = 0; p < P.np; ++p) {
-    int64_t u0, u1;
-    cta_range(static_cast<int64_t>(P.pr[p].N / BNC) * (P.pr[p].K / CK), cta, P.G, u0, u1);
+    int u0, u1;
+    cta_range((P.pr[p].N / BNC) * (P.pr[p].K / CK), cta, P.G, u0, u1);
     n += u1 - u0;
   }
   return n;
@@ -214,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cta = blockIdx.x;
-  const int64_t nch = total_chunks(P, cta);
+  const int nch = total_chunks(P, cta);
 
   griddep_launch();
 
@@ -245,44 +251,45 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
     if (lane == 0) {
       Walk w;
       w.start(P, cta);
-      int64_t issued = 0;
-      for (int64_t g = 0; g < nch; ++g, w.next(P, cta)) {
+      int issued = 0;
+      for (int g = 0; g < nch; ++g, w.next(P, cta)) {
         const int s = static_cast<int>(g % SW);
         if (!mbar_wait_sleep(&wempty[s], static_cast<uint32_t>((g / SW) & 1) ^ 1u, P.wait_limit, abort_flag,
                              kProducerSleepNs))
           break;
         const ChainProduct& q = P.pr[w.p];
-        const int n0 = w.tile() * BNC;
+        const int n0 = w.tile * BNC;
         int seg = 0;
         while (seg + 1 < q.nseg && n0 >= q.seg_n0[seg + 1]) ++seg;
         const size_t run = static_cast<size_t>(q.K / BK) * C::kBB;   // the k blocks of one tile
         const uint8_t* src = q.wp[seg] + static_cast<size_t>((n0 - q.seg_n0[seg]) / BNC) * run +
-                             static_cast<size_t>(w.kc()) * C::kWStage;
+                             static_cast<size_t>(w.kc) * C::kWStage;
         mbar_expect_tx(&wfull[s], C::kWStage);
         bulk_load(wring + s * C::kWStage, src, C::kWStage, &wfull[s]);
         ++issued;
       }
-      for (int64_t g = issued > SW ? issued - SW : 0; g < issued; ++g) {   // nothing in flight at exit
+      for (int g = issued > SW ? issued - SW : 0; g < issued; ++g) {   // nothing in flight at exit
         volatile int dummy = 0;
         mbar_wait(&wfull[g % SW], static_cast<uint32_t>((g / SW) & 1), kDrainLimit, &dummy);
       }
       if (*abort_flag) atomicOr(P.err, DEV_ERR_WAIT_TIMEOUT);
     }
+    __syncwarp();   // the warp reaches the CTA barrier below converged
   } else if (warp == 2) {
     // ---- X copies: chunk k of a product's X is tile k of the product before it -------
     if (lane == 0) {
       griddep_wait();   // inputs, flags and counters belong to the stream order from here on
       Walk w;
       w.start(P, cta);
-      int64_t issued = 0;
-      for (int64_t g = 0; g < nch; ++g, w.next(P, cta)) {
+      int issued = 0;
+      for (int g = 0; g < nch; ++g, w.next(P, cta)) {
         const int s = static_cast<int>(g % SX);
         // the MMAs of chunk g - SX, the last to read stage s, have completed
         if (g >= SX && !mbar_wait_sleep(&bufdone[(g - SX) % NB], static_cast<uint32_t>(((g - SX) / NB) & 1),
                                         P.wait_limit, abort_flag, kProducerSleepNs))
           break;
         const ChainProduct& q = P.pr[w.p];
-        const int kc = w.kc();
+        const int kc = w.kc;
         if (q.x_prod >= 0) {
           if (!wait_flag(P.pr[q.x_prod].ready + kc, P.wait_limit, abort_flag)) break;
           fence_proxy_async_global();   // the acquired tile, to the TMA reads that follow
@@ -292,25 +299,20 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
           tma_load_2d(xring + s * C::kXStage + t * C::kXT, &P.mapX[w.p], kc * CK + t * BK, 0, &xfull[s]);
         ++issued;
       }
-      for (int64_t g = issued > SX ? issued - SX : 0; g < issued; ++g) {
+      for (int g = issued > SX ? issued - SX : 0; g < issued; ++g) {
         volatile int dummy = 0;
         mbar_wait(&xfull[g % SX], static_cast<uint32_t>((g / SX) & 1), kDrainLimit, &dummy);
       }
       if (*abort_flag) atomicOr(P.err, DEV_ERR_WAIT_TIMEOUT);
     }
+    __syncwarp();
   } else if (warp == 1) {
     // ---- MMAs: every lane takes the chunk barrier, lane 0 issues ---------------------
     Walk w;
     w.start(P, cta);
-    int64_t piece = -1, u0 = -1;
-    int pp = -1;
-    for (int64_t g = 0; g < nch; ++g, w.next(P, cta)) {
-      if (w.p != pp) {   // a new product: its range starts here
-        pp = w.p;
-        u0 = w.u;
-      }
-      const bool first = w.first_of_piece(u0);
-      const bool last = (w.u + 1 == w.u1) || (w.kc() + 1 == w.cpt);
+    int piece = -1;
+    for (int g = 0; g < nch; ++g, w.next(P, cta)) {
+      const bool first = w.first(), last = w.last();
       if (first) ++piece;
       named_bar_sync(kChunkBar, 64 + 8 * 32);   // chunk g is in TMEM, its X has landed, its accumulator is free
       if (lane == 0) {
@@ -345,21 +347,17 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
     named_bar_sync(kStartBar, 32 + 8 * 32);
     Walk w;
     w.start(P, cta);
-    int64_t piece = -1, u0 = -1;
-    int pp = -1;
-    for (int64_t g = 0; g < nch; ++g, w.next(P, cta)) {
-      if (w.p != pp) {
-        pp = w.p;
-        u0 = w.u;
-      }
-      if (w.first_of_piece(u0)) ++piece;
+    int piece = -1;
+    for (int g = 0; g < nch; ++g, w.next(P, cta)) {
+      const bool first = w.first();
+      if (first) ++piece;
       if (ok) ok = mbar_wait(&xfull[g % SX], static_cast<uint32_t>((g / SX) & 1), P.wait_limit, abort_flag);
       if (ok && g + 1 < nch && g + 1 >= NB)
         ok = mbar_wait(&bufdone[(g + 1) % NB], static_cast<uint32_t>(((g + 1 - NB) / NB) & 1), P.wait_limit,
                        abort_flag);
       if (ok && g + 2 < nch)
         ok = mbar_wait(&wfull[(g + 2) % SW], static_cast<uint32_t>(((g + 2) / SW) & 1), P.wait_limit, abort_flag);
-      if (ok && w.first_of_piece(u0) && piece >= 2)
+      if (ok && first && piece >= 2)
         ok = mbar_wait(&accempty[piece & 1], static_cast<uint32_t>(((piece - 2) / 2) & 1), P.wait_limit,
                        abort_flag);
       __syncwarp();
@@ -382,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
       cv.load(wring + t * C::kBB, q, lane);
       cv.convert(a, q, lane);
     }
-    for (int64_t g = 0; g < nch; ++g) {
+    for (int g = 0; g < nch; ++g) {
       const bool next = g + 1 < nch;
       // the next chunk's loads go out before this chunk's stores
       if (next) cv.load(wring + ((g + 1) % SW) * C::kWStage + t * C::kBB, q, lane);
@@ -399,26 +397,26 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
     // ---- epilogues: drain each piece, then the tile's output or its fixup ------------------
     const int eq = warp & 3;              // TMEM lane quarter = 32 channels of the tile
     const int tid = threadIdx.x - 32 * kEpiWarp0;
+    const int M = P.M;
     griddep_wait();
-    int64_t piece = -1;
+    int piece = -1;
     for (int p = 0; p < P.np; ++p) {
       const ChainProduct& q = P.pr[p];
       const int cpt = q.K / CK;
-      const int64_t U = static_cast<int64_t>(q.N / BNC) * cpt;
-      int64_t u0, u1;
+      const int U = (q.N / BNC) * cpt;
+      int u0, u1;
       cta_range(U, cta, P.G, u0, u1);
-      for (int64_t u = u0; u < u1;) {
-        const int n = static_cast<int>(u / cpt);
-        const int64_t uend = std::min<int64_t>(u1, static_cast<int64_t>(n + 1) * cpt);
+      for (int u = u0; u < u1;) {
+        const int n = u / cpt;
+        u = min(u1, (n + 1) * cpt);
         ++piece;
-        // contributors: the CTAs from the owner of the tile's first unit to
-        // the owner of its last, less those with an empty range (fewer units
-        // than CTAs)
-        const int first = owner(static_cast<int64_t>(n) * cpt, U, P.G);
-        const int lastc = owner(static_cast<int64_t>(n + 1) * cpt - 1, U, P.G);
-        int J = 0;
-        for (int c = first; c <= lastc; ++c) J += nonempty(U, c, P.G);
-        u = uend;
+        // the tile's contributors, in order: with at least as many units as
+        // CTAs every CTA from the owner of the tile's first unit to the owner
+        // of its last; with fewer, every CTA holds at most one unit, and the
+        // contributors are the owners of the tile's units
+        const int first = owner(n * cpt, U, P.G);
+        const bool dense = U >= P.G;
+        const int J = dense ? owner((n + 1) * cpt - 1, U, P.G) - first + 1 : cpt;
 
         // one lane polls, pausing between polls: these warps wait most of the
         // time, and their polling would take shared-memory and issue slots
@@ -452,37 +450,11 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
         if (lane == 0) mbar_arrive(&accempty[piece & 1]);
         ok = ok && !*abort_flag;
 
-        const int ch = n * BNC + 32 * eq + lane;   // this thread's output channel
-        const int M = P.M;
-        bool publish = J == 1;
-        if (J > 1) {
-          float* mine = q.part + (static_cast<size_t>(n) + cta) * M * BNC + 32 * eq + lane;
-#pragma unroll
-          for (int m = 0; m < BT; ++m)
-            if (m < M) mine[m * BNC] = v[m];
-          __threadfence();
-          named_bar_sync(kEpiBar, 128);
-          if (tid == 0) *epi_last = atomicAdd(q.cnt + n, 1u) == static_cast<unsigned>(J - 1);
-          named_bar_sync(kEpiBar, 128);
-          publish = *epi_last != 0;
-          if (publish) {
-            __threadfence();
-            // every contributor's partial (this CTA's too, as written) in
-            // contributor order: the same sum whichever CTA arrives last
-#pragma unroll
-            for (int m = 0; m < BT; ++m) v[m] = 0.0f;
-#pragma unroll 1
-            for (int c = first; c <= lastc; ++c) {
-              if (!nonempty(U, c, P.G)) continue;
-              const float* src = q.part + (static_cast<size_t>(n) + c) * M * BNC + 32 * eq + lane;
-#pragma unroll
-              for (int m = 0; m < BT; ++m)
-                if (m < M) v[m] += __ldcg(src + m * BNC);
-            }
-          }
-        }
-        if (publish) {
+        if (J == 1) {
+          // the whole tile is this CTA's: epilogue from the accumulator
+          // (thread = channel n*128 + 32 eq + lane, rows m < M)
           if (q.R && q.r_prod >= 0) ok = ok && wait_flag(P.pr[q.r_prod].ready + n, P.wait_limit, abort_flag);
+          const int ch = n * BNC + 32 * eq + lane;
 #pragma unroll
           for (int m = 0; m < BT; ++m) {
             if (m < M) {
@@ -492,12 +464,85 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
               if (ok) q.Y[static_cast<size_t>(m) * q.ldy + ch] = __float2half_rn(y);
             }
           }
+        } else {
+          // this CTA's partial to its slot (n + cta), [M][128] fp32
+          float* mine = q.part + static_cast<size_t>(n + cta) * M * BNC + 32 * eq + lane;
+#pragma unroll
+          for (int m = 0; m < BT; ++m)
+            if (m < M) mine[m * BNC] = v[m];
           __threadfence();
           named_bar_sync(kEpiBar, 128);
-          if (tid == 0) {
-            if (J > 1) q.cnt[n] = 0;   // every contributor has arrived: ready for the next launch
-            st_release(q.ready + n, 1u);
+          if (tid == 0) *epi_last = atomicAdd(q.cnt + n, 1u) == static_cast<unsigned>(J - 1);
+          named_bar_sync(kEpiBar, 128);
+          if (*epi_last == 0) continue;   // the same for the four warps: no barrier below is skipped unevenly
+          __threadfence();
+          if (q.R && q.r_prod >= 0) ok = ok && wait_flag(P.pr[q.r_prod].ready + n, P.wait_limit, abort_flag);
+          // The last to arrive sums the J partials in contributor order (the
+          // same sum whichever CTA is last).  Thread tid takes channels
+          // 4 (tid % 32) .. +3 of rows m = tid / 32 + 4 i: 16-byte loads, each
+          // warp reading whole 512-byte rows; the rows go in two halves, the
+          // next contributor's loads in flight while the current one is added.
+          const int c4 = 4 * (tid & 31), m0 = tid >> 5;
+          constexpr int kRows = BT / 4;          // rows per thread
+          constexpr int kHalf = kRows / 2 > 0 ? kRows / 2 : 1;
+#pragma unroll 1
+          for (int h = 0; h < kRows; h += kHalf) {
+            float4 acc[kHalf], nxt[kHalf];
+            auto slot_of = [&](int k) {
+              const int c = dense ? first + k : owner(n * cpt + k, U, P.G);
+              return reinterpret_cast<const float4*>(q.part + static_cast<size_t>(n + c) * M * BNC + c4);
+            };
+            auto fetch = [&](float4 (&dst)[kHalf], const float4* src) {
+#pragma unroll
+              for (int i = 0; i < kHalf; ++i) {
+                const int m = m0 + 4 * (h + i);
+                dst[i] = m < M ? __ldcg(src + m * (BNC / 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+              }
+            };
+            fetch(acc, slot_of(0));
+#pragma unroll 1
+            for (int k = 1; k < J; ++k) {
+              fetch(nxt, slot_of(k));
+#pragma unroll
+              for (int i = 0; i < kHalf; ++i) {
+                acc[i].x += nxt[i].x;
+                acc[i].y += nxt[i].y;
+                acc[i].z += nxt[i].z;
+                acc[i].w += nxt[i].w;
+              }
+            }
+#pragma unroll
+            for (int i = 0; i < kHalf; ++i) {
+              const int m = m0 + 4 * (h + i);
+              if (m >= M) continue;
+              const int ch = n * BNC + c4;
+              float y[4] = {acc[i].x, acc[i].y, acc[i].z, acc[i].w};
+              if (q.R) {
+                const uint2 rr = __ldcg(reinterpret_cast<const uint2*>(q.R + static_cast<size_t>(m) * q.ldr + ch));
+                const float2 r01 = __half22float2(*reinterpret_cast<const __half2*>(&rr.x));
+                const float2 r23 = __half22float2(*reinterpret_cast<const __half2*>(&rr.y));
+                y[0] += r01.x;
+                y[1] += r01.y;
+                y[2] += r23.x;
+                y[3] += r23.y;
+              }
+              if (q.relu) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) y[e] = fmaxf(y[e], 0.0f);
+              }
+              const __half2 y01 = __floats2half2_rn(y[0], y[1]), y23 = __floats2half2_rn(y[2], y[3]);
+              if (ok)
+                *reinterpret_cast<uint2*>(q.Y + static_cast<size_t>(m) * q.ldy + ch) =
+                    make_uint2(*reinterpret_cast<const uint32_t*>(&y01), *reinterpret_cast<const uint32_t*>(&y23));
+            }
           }
+        }
+        // publish the tile
+        __threadfence();
+        named_bar_sync(kEpiBar, 128);
+        if (tid == 0) {
+          if (J > 1) q.cnt[n] = 0;   // every contributor has arrived: ready for the next launch
+          st_release(q.ready + n, 1u);
         }
       }
     }
@@ -543,6 +588,8 @@ fg_status launch_chain(const ChainParams& P, cudaStream_t st, bool pdl) {
 
 int chain_owner(int64_t u, int64_t U, int G) { return static_cast<int>(((u + 1) * G - 1) / U); }
 
+static_assert(kChainMaxCtas * 65536LL < (1LL << 31), "32-bit partition arithmetic");
+
 int chain_ctas() { return std::min(num_sms(), kChainMaxCtas); }
 
 size_t chain_part_bytes(int64_t M, int64_t N) {
@@ -553,6 +600,7 @@ size_t chain_ctrl_bytes(int64_t N) { return static_cast<size_t>(N / BNC) * 2 * s
 
 bool chain_supported(const GemmArgs& a) {
   if (a.dtype != FG_F16 || !a.quant || a.M < 1 || a.M > 64 || a.K % CK || a.N % BNC) return false;
+  if ((a.N / BNC) * (a.K / CK) > 65536) return false;   // the kernel's 32-bit partition arithmetic
   for (int i = 0; i < a.nseg; ++i) {
     const WSeg& s = a.seg[i];
     if (!s.packed || s.N % BNC || !aligned(s.packed, 16) || s.packed_format != a.seg[0].packed_format) return false;

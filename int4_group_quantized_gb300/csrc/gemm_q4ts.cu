@@ -311,6 +311,7 @@ __global__ void __launch_bounds__(TsCfg<BT, RB, FMT>::kThreads, TsCfg<BT, RB, FM
       }
       if (*abort_flag) atomicOr(p.err, DEV_ERR_WAIT_TIMEOUT);
     }
+    __syncwarp();   // the warp reaches the CTA barriers below converged
   } else if (warp == 2) {
     if (lane == 0) {
       griddep_wait();   // X comes from the previous kernel
@@ -332,6 +333,7 @@ __global__ void __launch_bounds__(TsCfg<BT, RB, FMT>::kThreads, TsCfg<BT, RB, FM
       }
       if (*abort_flag) atomicOr(p.err, DEV_ERR_WAIT_TIMEOUT);
     }
+    __syncwarp();
   } else if (warp == 1) {
     // every lane takes the barrier; lane 0 issues
     for (int c = 0; c < nch; ++c) {

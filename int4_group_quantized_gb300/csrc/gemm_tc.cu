@@ -149,6 +149,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
       }
       if (*abort_flag) raise(p);
     }
+    __syncwarp();   // the warp reaches the CTA barrier below converged
   } else if (warp == 1) {
     // ---- MMA issuer -------------------------------------------------------------
     if (lane == 0) {
@@ -178,6 +179,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
       mma_commit(done);
       if (!ok) raise(p);
     }
+    __syncwarp();
   }
 
   // ---- epilogue ---------------------------------------------------------------------
