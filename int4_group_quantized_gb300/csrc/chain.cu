@@ -118,6 +118,14 @@ __device__ __forceinline__ uint32_t ld_acquire(const unsigned* p) {
 __device__ __forceinline__ void st_release(unsigned* p, uint32_t v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
+// Returns the old value; acquire and release at GPU scope.  After a CTA
+// barrier, one thread's release orders every write the barrier's threads
+// made before it, and its acquire orders their reads after the next barrier.
+__device__ __forceinline__ uint32_t atom_add_acq_rel(unsigned* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
 // Waits until *flag != 0 (acquire), polling at most `limit` times.
 __device__ __forceinline__ bool wait_flag(const unsigned* flag, uint32_t limit, volatile int* abort) {
   for (uint32_t i = 0; i < limit; ++i) {
@@ -140,15 +148,17 @@ struct ChainCfg {
   static constexpr int kAcc = BT < 32 ? 32 : BT;     // accumulator columns
   static constexpr int kACol = 2 * kAcc;             // A buffers follow the two accumulators
   static constexpr int kBufs = (512 - kACol) / 64;   // A buffers of 64 columns (a chunk)
-  static constexpr int kXStages = 4;
-  static constexpr int kSmemBudget = 200 * 1024;
+  // X stages have their own release barriers (the MMA commit of the chunk
+  // that read them), so the X ring is as deep as the shared memory allows:
+  // an X tile comes from L2 with microseconds of latency under load
+  static constexpr int kXStages = BT <= 32 ? 8 : 7;
+  static constexpr int kSmemBudget = 212 * 1024;
   static constexpr int kWStages = chain_min(16, (kSmemBudget - kXStages * kXStage) / kWStage);
   static constexpr int kXBytes = kXStages * kXStage;
   static constexpr int kWBytes = kWStages * kWStage;
-  static constexpr int kBarBytes = (kXStages + 2 * kWStages + kBufs + 4) * 8 + 16;
+  static constexpr int kBarBytes = (2 * kXStages + 2 * kWStages + kBufs + 4) * 8 + 16;
   static constexpr int kTotal = 1024 + kXBytes + kWBytes + kBarBytes;
   static_assert(kBufs >= 3 && kWStages >= 3, "pipeline depth");
-  static_assert(kXStages <= kBufs, "X stages are freed by buffer commits");
   static_assert(kXT % 1024 == 0, "X tiles stay 1024-byte aligned");
 };
 
@@ -209,7 +219,8 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
   uint8_t* xring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* wring = xring + C::kXBytes;
   uint64_t* xfull = reinterpret_cast<uint64_t*>(wring + C::kWBytes);
-  uint64_t* wfull = xfull + SX;
+  uint64_t* xempty = xfull + SX;       // X stage read by its chunk's MMAs
+  uint64_t* wfull = xempty + SX;
   uint64_t* wempty = wfull + SW;
   uint64_t* bufdone = wempty + SW;     // MMAs of the chunk in TMEM buffer b completed
   uint64_t* accfull = bufdone + NB;    // [2] the piece in accumulator a is summed
@@ -225,7 +236,10 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
   griddep_launch();
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < SX; ++i) mbar_init(&xfull[i], 1);
+    for (int i = 0; i < SX; ++i) {
+      mbar_init(&xfull[i], 1);
+      mbar_init(&xempty[i], 1);        // the MMA commit
+    }
     for (int i = 0; i < SW; ++i) {
       mbar_init(&wfull[i], 1);
       mbar_init(&wempty[i], 1);
@@ -285,8 +299,8 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
       for (int g = 0; g < nch; ++g, w.next(P, cta)) {
         const int s = static_cast<int>(g % SX);
         // the MMAs of chunk g - SX, the last to read stage s, have completed
-        if (g >= SX && !mbar_wait_sleep(&bufdone[(g - SX) % NB], static_cast<uint32_t>(((g - SX) / NB) & 1),
-                                        P.wait_limit, abort_flag, kProducerSleepNs))
+        if (!mbar_wait_sleep(&xempty[s], static_cast<uint32_t>((g / SX) & 1) ^ 1u, P.wait_limit, abort_flag,
+                             kProducerSleepNs))
           break;
         const ChainProduct& q = P.pr[w.p];
         const int kc = w.kc;
@@ -332,6 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
           }
         }
         mma_commit(&bufdone[b]);
+        mma_commit(&xempty[g % SX]);
         if (last) mma_commit(&accfull[piece & 1]);
       }
       __syncwarp();
@@ -470,12 +485,10 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
 #pragma unroll
           for (int m = 0; m < BT; ++m)
             if (m < M) mine[m * BNC] = v[m];
-          __threadfence();
           named_bar_sync(kEpiBar, 128);
-          if (tid == 0) *epi_last = atomicAdd(q.cnt + n, 1u) == static_cast<unsigned>(J - 1);
+          if (tid == 0) *epi_last = atom_add_acq_rel(q.cnt + n, 1u) == static_cast<unsigned>(J - 1);
           named_bar_sync(kEpiBar, 128);
           if (*epi_last == 0) continue;   // the same for the four warps: no barrier below is skipped unevenly
-          __threadfence();
           if (q.R && q.r_prod >= 0) ok = ok && wait_flag(P.pr[q.r_prod].ready + n, P.wait_limit, abort_flag);
           // The last to arrive sums the J partials in contributor order (the
           // same sum whichever CTA is last).  Thread tid takes channels
@@ -487,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
           constexpr int kHalf = kRows / 2 > 0 ? kRows / 2 : 1;
 #pragma unroll 1
           for (int h = 0; h < kRows; h += kHalf) {
-            float4 acc[kHalf], nxt[kHalf];
+            float4 acc[kHalf], b0[kHalf], b1[kHalf];
             auto slot_of = [&](int k) {
               const int c = dense ? first + k : owner(n * cpt + k, U, P.G);
               return reinterpret_cast<const float4*>(q.part + static_cast<size_t>(n + c) * M * BNC + c4);
@@ -499,16 +512,26 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
                 dst[i] = m < M ? __ldcg(src + m * (BNC / 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
               }
             };
-            fetch(acc, slot_of(0));
-#pragma unroll 1
-            for (int k = 1; k < J; ++k) {
-              fetch(nxt, slot_of(k));
+            auto add = [&](const float4 (&src)[kHalf]) {
 #pragma unroll
               for (int i = 0; i < kHalf; ++i) {
-                acc[i].x += nxt[i].x;
-                acc[i].y += nxt[i].y;
-                acc[i].z += nxt[i].z;
-                acc[i].w += nxt[i].w;
+                acc[i].x += src[i].x;
+                acc[i].y += src[i].y;
+                acc[i].z += src[i].z;
+                acc[i].w += src[i].w;
+              }
+            };
+            // acc = p_0 + p_1 + ... + p_{J-1} in that order, two contributors'
+            // loads in flight ahead of the additions
+            fetch(acc, slot_of(0));
+            if (J > 1) fetch(b0, slot_of(1));
+#pragma unroll 1
+            for (int k = 1; k < J; k += 2) {
+              if (k + 1 < J) fetch(b1, slot_of(k + 1));
+              add(b0);
+              if (k + 1 < J) {
+                if (k + 2 < J) fetch(b0, slot_of(k + 2));
+                add(b1);
               }
             }
 #pragma unroll
@@ -537,8 +560,8 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
             }
           }
         }
-        // publish the tile
-        __threadfence();
+        // publish the tile: the release after the barrier orders every
+        // thread's stores of it
         named_bar_sync(kEpiBar, 128);
         if (tid == 0) {
           if (J > 1) q.cnt[n] = 0;   // every contributor has arrived: ready for the next launch
