@@ -30,15 +30,18 @@
 // TMEM (two 64-k tiles of a chunk side by side, the BlockConverter register
 // order), warps 12..15 drain the accumulators and run the epilogues and
 // fixups.  The main loop is the lockstep chunk loop of the decode products:
-// converting warps, sync warp and MMA warp meet at one named barrier per
-// chunk.  Two accumulators alternate between the pieces of the range, so an
-// epilogue overlaps the next piece's MMAs.
+// converting warps and sync warp meet at one named barrier per chunk, and the
+// sync warp then hands the chunk to the MMA warp through an mbarrier, so that
+// MMA issue never holds up the conversion.  Each piece is summed in two
+// accumulators (the chunk's two blocks), so consecutive MMAs are independent;
+// two accumulator pairs alternate between pieces, so an epilogue overlaps the
+// next piece's MMAs.
 //
 // Every wait is bounded (fg_set_wait_limit): a wait that gives up raises the
 // device error word and makes its role skip work, never a barrier; before the
 // CTA leaves, its copies and MMAs in flight have completed and its tensor
 // memory is freed.  Named barriers: the chunk barrier is taken once per chunk
-// by the MMA, sync and 8 converting warps; the start barrier once by the
+// by the sync and 8 converting warps; the start barrier once by the
 // sync and converting warps; the epilogue barrier the same number of times
 // per piece by the 4 epilogue warps (the branch between its counts is
 // decided once and broadcast through shared memory).
@@ -146,7 +149,9 @@ struct ChainCfg {
   static constexpr int kXT = BT * BK * 2;            // one X tile, K-major, 128-byte swizzle
   static constexpr int kXStage = 2 * kXT;
   static constexpr int kAcc = BT < 32 ? 32 : BT;     // accumulator columns
-  static constexpr int kACol = 2 * kAcc;             // A buffers follow the two accumulators
+  // two pieces in flight, each summed in two accumulators (the chunk's first
+  // and second block) so that consecutive MMAs do not depend on each other
+  static constexpr int kACol = 4 * kAcc;             // A buffers follow the accumulators
   static constexpr int kBufs = (512 - kACol) / 64;   // A buffers of 64 columns (a chunk)
   // X stages have their own release barriers (the MMA commit of the chunk
   // that read them), so the X ring is as deep as the shared memory allows:
@@ -156,7 +161,7 @@ struct ChainCfg {
   static constexpr int kWStages = chain_min(16, (kSmemBudget - kXStages * kXStage) / kWStage);
   static constexpr int kXBytes = kXStages * kXStage;
   static constexpr int kWBytes = kWStages * kWStage;
-  static constexpr int kBarBytes = (2 * kXStages + 2 * kWStages + kBufs + 4) * 8 + 16;
+  static constexpr int kBarBytes = (2 * kXStages + 2 * kWStages + 2 * kBufs + 4) * 8 + 16;
   static constexpr int kTotal = 1024 + kXBytes + kWBytes + kBarBytes;
   static_assert(kBufs >= 3 && kWStages >= 3, "pipeline depth");
   static_assert(kXT % 1024 == 0, "X tiles stay 1024-byte aligned");
@@ -223,7 +228,8 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
   uint64_t* wfull = xempty + SX;
   uint64_t* wempty = wfull + SW;
   uint64_t* bufdone = wempty + SW;     // MMAs of the chunk in TMEM buffer b completed
-  uint64_t* accfull = bufdone + NB;    // [2] the piece in accumulator a is summed
+  uint64_t* bufready = bufdone + NB;   // chunk in TMEM buffer b converted, its X landed, accumulators free
+  uint64_t* accfull = bufready + NB;   // [2] the piece in accumulator pair a is summed
   uint64_t* accempty = accfull + 2;    // [2] accumulator a drained by the epilogue warps
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accempty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -244,7 +250,10 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
       mbar_init(&wfull[i], 1);
       mbar_init(&wempty[i], 1);
     }
-    for (int i = 0; i < NB; ++i) mbar_init(&bufdone[i], 1);
+    for (int i = 0; i < NB; ++i) {
+      mbar_init(&bufdone[i], 1);
+      mbar_init(&bufready[i], 1);   // the sync warp, after the chunk barrier
+    }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&accfull[i], 1);
       mbar_init(&accempty[i], 4);   // one arrival per epilogue warp
@@ -321,27 +330,27 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ---- MMAs: every lane takes the chunk barrier, lane 0 issues ---------------------
-    Walk w;
-    w.start(P, cta);
-    int piece = -1;
-    for (int g = 0; g < nch; ++g, w.next(P, cta)) {
-      const bool first = w.first(), last = w.last();
-      if (first) ++piece;
-      named_bar_sync(kChunkBar, 64 + 8 * 32);   // chunk g is in TMEM, its X has landed, its accumulator is free
-      if (lane == 0) {
+    // ---- MMAs: lane 0 issues each chunk once the sync warp has handed it over ----------
+    if (lane == 0) {
+      Walk w;
+      w.start(P, cta);
+      int piece = -1;
+      for (int g = 0; g < nch; ++g, w.next(P, cta)) {
+        const bool first = w.first(), last = w.last();
+        if (first) ++piece;
+        const int b = g % NB;
+        const bool ok = mbar_wait(&bufready[b], static_cast<uint32_t>((g / NB) & 1), P.wait_limit, abort_flag);
         tc_fence_after();
-        const int b = static_cast<int>(g % NB);
-        const uint32_t acc = tmem_base + static_cast<uint32_t>(piece & 1) * C::kAcc;
-        if (!*abort_flag) {
+        const uint32_t acc = tmem_base + static_cast<uint32_t>(piece & 1) * 2 * C::kAcc;
+        if (ok && !*abort_flag) {
 #pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            const uint32_t xa = smem_u32(xring + (g % SX) * C::kXStage + t * C::kXT);
-            const uint32_t ta = tmem_base + C::kACol + b * 64 + 32u * t;
+          for (int kk = 0; kk < BK / 16; ++kk) {
 #pragma unroll
-            for (int kk = 0; kk < BK / 16; ++kk) {
+            for (int t = 0; t < 2; ++t) {   // the two blocks into their own accumulators, interleaved
+              const uint32_t xa = smem_u32(xring + (g % SX) * C::kXStage + t * C::kXT);
+              const uint32_t ta = tmem_base + C::kACol + b * 64 + 32u * t;
               const uint64_t bdesc = smem_desc_sw128(xa + kk * 32, 16, 1024);
-              mma_f16_ts(acc, ta + 8u * kk, bdesc, kIdesc, (first && t == 0 && kk == 0) ? 0u : 1u);
+              mma_f16_ts(acc + t * C::kAcc, ta + 8u * kk, bdesc, kIdesc, (first && kk == 0) ? 0u : 1u);
             }
           }
         }
@@ -349,8 +358,8 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
         mma_commit(&xempty[g % SX]);
         if (last) mma_commit(&accfull[piece & 1]);
       }
-      __syncwarp();
     }
+    __syncwarp();
   } else if (warp == kSyncWarp) {
     // ---- waits on behalf of the warps that take the chunk barrier ----------------------
     // Before chunk barrier g: chunk g's X, TMEM buffer (g+1) % NB free (the MMAs
@@ -376,8 +385,9 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
         ok = mbar_wait(&accempty[piece & 1], static_cast<uint32_t>(((piece - 2) / 2) & 1), P.wait_limit,
                        abort_flag);
       __syncwarp();
-      named_bar_sync(kChunkBar, 64 + 8 * 32);
+      named_bar_sync(kChunkBar, 32 + 8 * 32);
       if (lane == 0) {
+        mbar_arrive(&bufready[g % NB]);   // to the MMA warp
         if (g == 0) mbar_arrive(&wempty[0]);
         if (g + 1 < nch) mbar_arrive(&wempty[(g + 1) % SW]);
       }
@@ -388,25 +398,31 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
     const int t = d >> 2;                 // which block of the chunk
     const int q = warp & 3;               // TMEM lane quarter
     const uint32_t trow = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + C::kACol + 32u * t;
-    q4::BlockConverter<FMT> cv;
-    uint32_t a[32];
-    named_bar_sync(kStartBar, 32 + 8 * 32);
-    if (nch > 0) {
-      cv.load(wring + t * C::kBB, q, lane);
-      cv.convert(a, q, lane);
-    }
-    for (int g = 0; g < nch; ++g) {
+    q4::BlockConverter<FMT, true> cv;
+    // Two register buffers: chunk g+1 is converted into the other buffer
+    // while the tensor-memory stores of chunk g still read theirs.
+    uint32_t a0[32], a1[32];
+    auto step = [&](int g, uint32_t (&cur)[32], uint32_t (&nxt)[32]) {
       const bool next = g + 1 < nch;
       // the next chunk's loads go out before this chunk's stores
       if (next) cv.load(wring + ((g + 1) % SW) * C::kWStage + t * C::kBB, q, lane);
       tc_fence_after();
       const uint32_t dst = trow + static_cast<uint32_t>(g % NB) * 64;
-      tmem_st_16x128b_x8(dst, a);
-      tmem_st_16x128b_x8(dst + (16u << 16), a + 16);
-      if (next) cv.convert(a, q, lane);
+      tmem_st_16x128b_x8(dst, cur);
+      tmem_st_16x128b_x8(dst + (16u << 16), cur + 16);
+      if (next) cv.convert(nxt, q, lane);
       tmem_st_wait();
       tc_fence_before();
-      named_bar_sync(kChunkBar, 64 + 8 * 32);
+      named_bar_sync(kChunkBar, 32 + 8 * 32);
+    };
+    named_bar_sync(kStartBar, 32 + 8 * 32);
+    if (nch > 0) {
+      cv.load(wring + t * C::kBB, q, lane);
+      cv.convert(a0, q, lane);
+    }
+    for (int g = 0; g < nch; g += 2) {
+      step(g, a0, a1);
+      if (g + 1 < nch) step(g + 1, a1, a0);
     }
   } else {
     // ---- epilogues: drain each piece, then the tile's output or its fixup ------------------
@@ -450,14 +466,18 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
         tc_fence_after();
         float v[BT];
         {
-          const uint32_t ta = tmem_base + (static_cast<uint32_t>(32 * eq) << 16) + static_cast<uint32_t>(piece & 1) * C::kAcc;
+          // the piece's two accumulators, added (same order for every piece)
+          const uint32_t ta = tmem_base + (static_cast<uint32_t>(32 * eq) << 16) + static_cast<uint32_t>(piece & 1) * 2 * C::kAcc;
 #pragma unroll
-          for (int c0 = 0; c0 < BT; c0 += 32) {
-            uint32_t r[32];
-            tmem_ld_32x32b_x32(ta + c0, r);
-            tmem_ld_wait();
+          for (int h = 0; h < 2; ++h) {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) v[c0 + e] = __uint_as_float(r[e]);
+            for (int c0 = 0; c0 < BT; c0 += 32) {
+              uint32_t r[32];
+              tmem_ld_32x32b_x32(ta + h * C::kAcc + c0, r);
+              tmem_ld_wait();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) v[c0 + e] = h ? v[c0 + e] + __uint_as_float(r[e]) : __uint_as_float(r[e]);
+            }
           }
         }
         tc_fence_before();

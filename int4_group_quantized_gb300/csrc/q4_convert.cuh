@@ -24,17 +24,27 @@ __host__ __device__ constexpr int block_bytes(int fmt) {
   return kBlkCodes + (fmt == FG_PACK_EXACT ? 1024 : 512);   // 5120 or 4608
 }
 
-template <int FMT>
+// PRELOAD: load() also reads the fp32 pairs of FG_PACK_EXACT (32 more
+// registers), so that convert() issues no shared-memory load -- a load
+// issued after a tensor-memory store waits for that store.
+template <int FMT, bool PRELOAD = false>
 struct BlockConverter {
   uint4 w0, w1, pv[4];
+  float4 pf[PRELOAD ? 8 : 1];
   const uint8_t* blk;
 
   // Shared-memory loads of what this thread converts: its code words (the
-  // fp16 pairs too, for FG_PACK_F16META; the fp32 pairs are read by convert).
+  // fp16 pairs too, for FG_PACK_F16META; the fp32 pairs with PRELOAD, else
+  // convert reads them).
   __device__ __forceinline__ void load(const uint8_t* block, int q, int lane) {
     blk = block;
     w0 = *reinterpret_cast<const uint4*>(block + q * 1024 + lane * 16);
     w1 = *reinterpret_cast<const uint4*>(block + q * 1024 + 512 + lane * 16);
+    if (FMT == FG_PACK_EXACT && PRELOAD) {
+      const float4* pr = reinterpret_cast<const float4*>(block + kBlkCodes + (q >> 1) * 512) + (lane & 3);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) pf[PRELOAD ? i : 0] = pr[4 * i];
+    }
     if (FMT == FG_PACK_F16META) {
       const uint4* pr = reinterpret_cast<const uint4*>(block + kBlkCodes + (q >> 1) * 256) + (lane & 3);
 #pragma unroll
@@ -52,7 +62,7 @@ struct BlockConverter {
       const float4* pr = reinterpret_cast<const float4*>(blk + kBlkCodes + (q >> 1) * 512) + c4;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const float4 sm = pr[4 * i];   // (scale[2j], scale[2j+1], min[2j], min[2j+1]), j = 4i + c4
+        const float4 sm = PRELOAD ? pf[PRELOAD ? i : 0] : pr[4 * i];   // (scale[2j], scale[2j+1], min[2j], min[2j+1]), j = 4i + c4
         const uint4 cw = i < 4 ? w0 : w1;
         const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
         const int e = i & 3;
