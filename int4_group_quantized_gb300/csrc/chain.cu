@@ -23,28 +23,28 @@
 // Weights never wait: the weight copies of the next product stream while the
 // current one finishes.
 //
-// Inside a CTA (512 threads, 512 TMEM columns): warp 0 issues the weight
-// copies (one 2-block bulk copy per chunk), warp 1 owns TMEM and issues the
-// MMAs, warp 2 issues the X copies (after the flags), warp 3 takes every
-// mbarrier wait for the converting warps, warps 4..11 convert weights into
-// TMEM (two 64-k tiles of a chunk side by side, the BlockConverter register
-// order), warps 12..15 drain the accumulators and run the epilogues and
-// fixups.  The main loop is the lockstep chunk loop of the decode products:
-// converting warps and sync warp meet at one named barrier per chunk, and the
-// sync warp then hands the chunk to the MMA warp through an mbarrier, so that
-// MMA issue never holds up the conversion.  Each piece is summed in two
-// accumulators (the chunk's two blocks), so consecutive MMAs are independent;
-// two accumulator pairs alternate between pieces, so an epilogue overlaps the
-// next piece's MMAs.
+// Inside a CTA (768 threads, 512 TMEM columns): warp 0 issues the weight
+// copies (one 2-block bulk copy per chunk), warp 1 owns TMEM, warp 2 issues
+// the X copies (after the flags), warp 3 takes every mbarrier wait for the
+// converting warps, warps 4..19 convert weights into TMEM (two warps per
+// block and lane quarter, the HalfConverter register order), warps 20..23
+// drain the accumulators and run the epilogues and fixups.  The main loop is
+// a lockstep chunk loop: the converting warps and the sync warp meet at one
+// named barrier per chunk, and lane 0 of the first converting warp issues the
+// chunk's MMAs right after it (a separate MMA warp shares its scheduler with
+// the converting warps and is starved of issue slots).  Each piece is summed
+// in two accumulators (the chunk's two blocks), so consecutive MMAs are
+// independent; two accumulator pairs alternate between pieces, so an
+// epilogue overlaps the next piece's MMAs.
 //
 // Every wait is bounded (fg_set_wait_limit): a wait that gives up raises the
 // device error word and makes its role skip work, never a barrier; before the
 // CTA leaves, its copies and MMAs in flight have completed and its tensor
 // memory is freed.  Named barriers: the chunk barrier is taken once per chunk
-// by the sync and 8 converting warps; the start barrier once by the
-// sync and converting warps; the epilogue barrier the same number of times
-// per piece by the 4 epilogue warps (the branch between its counts is
-// decided once and broadcast through shared memory).
+// by the sync and 16 converting warps; the start barrier once by the same
+// warps; the epilogue barrier the same number of times per piece by the 4
+// epilogue warps (the branch between its counts is decided once and
+// broadcast through shared memory).
 #include <cudaTypedefs.h>
 #include <string.h>
 
@@ -67,9 +67,10 @@ using namespace tc;
 constexpr int BK = 64;                 // k per block / MMA tile
 constexpr int BNC = 128;               // channels per tile (the MMA's M)
 constexpr int CK = 128;                // k per chunk: two blocks
-constexpr int kThreads = 512;
-constexpr int kConvWarp0 = 4;
-constexpr int kEpiWarp0 = 12;
+constexpr int kThreads = 768;
+constexpr int kConvWarp0 = 4;                       // 16 converting warps
+constexpr int kEpiWarp0 = 20;                       // 4 epilogue warps
+constexpr int kBarThreads = 32 + 16 * 32;           // chunk and start barriers: sync warp + converters
 constexpr int kSyncWarp = 3;
 constexpr uint32_t kChunkBar = 1, kStartBar = 2, kEpiBar = 3;
 constexpr uint32_t kProducerSleepNs = 100;
@@ -161,7 +162,7 @@ struct ChainCfg {
   static constexpr int kWStages = chain_min(16, (kSmemBudget - kXStages * kXStage) / kWStage);
   static constexpr int kXBytes = kXStages * kXStage;
   static constexpr int kWBytes = kWStages * kWStage;
-  static constexpr int kBarBytes = (2 * kXStages + 2 * kWStages + 2 * kBufs + 4) * 8 + 16;
+  static constexpr int kBarBytes = (2 * kXStages + 2 * kWStages + kBufs + 4) * 8 + 16;
   static constexpr int kTotal = 1024 + kXBytes + kWBytes + kBarBytes;
   static_assert(kBufs >= 3 && kWStages >= 3, "pipeline depth");
   static_assert(kXT % 1024 == 0, "X tiles stay 1024-byte aligned");
@@ -228,9 +229,8 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
   uint64_t* wfull = xempty + SX;
   uint64_t* wempty = wfull + SW;
   uint64_t* bufdone = wempty + SW;     // MMAs of the chunk in TMEM buffer b completed
-  uint64_t* bufready = bufdone + NB;   // chunk in TMEM buffer b converted, its X landed, accumulators free
-  uint64_t* accfull = bufready + NB;   // [2] the piece in accumulator pair a is summed
-  uint64_t* accempty = accfull + 2;    // [2] accumulator a drained by the epilogue warps
+  uint64_t* accfull = bufdone + NB;    // [2] the piece in accumulator pair a is summed
+  uint64_t* accempty = accfull + 2;    // [2] accumulator pair a drained by the epilogue warps
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accempty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* epi_last = abort_flag + 1;
@@ -250,10 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
       mbar_init(&wfull[i], 1);
       mbar_init(&wempty[i], 1);
     }
-    for (int i = 0; i < NB; ++i) {
-      mbar_init(&bufdone[i], 1);
-      mbar_init(&bufready[i], 1);   // the sync warp, after the chunk barrier
-    }
+    for (int i = 0; i < NB; ++i) mbar_init(&bufdone[i], 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&accfull[i], 1);
       mbar_init(&accempty[i], 4);   // one arrival per epilogue warp
@@ -276,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
       w.start(P, cta);
       int issued = 0;
       for (int g = 0; g < nch; ++g, w.next(P, cta)) {
-        const int s = static_cast<int>(g % SW);
+        const int s = g % SW;
         if (!mbar_wait_sleep(&wempty[s], static_cast<uint32_t>((g / SW) & 1) ^ 1u, P.wait_limit, abort_flag,
                              kProducerSleepNs))
           break;
@@ -306,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
       w.start(P, cta);
       int issued = 0;
       for (int g = 0; g < nch; ++g, w.next(P, cta)) {
-        const int s = static_cast<int>(g % SX);
+        const int s = g % SX;
         // the MMAs of chunk g - SX, the last to read stage s, have completed
         if (!mbar_wait_sleep(&xempty[s], static_cast<uint32_t>((g / SX) & 1) ^ 1u, P.wait_limit, abort_flag,
                              kProducerSleepNs))
@@ -329,46 +326,15 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
       if (*abort_flag) atomicOr(P.err, DEV_ERR_WAIT_TIMEOUT);
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // ---- MMAs: lane 0 issues each chunk once the sync warp has handed it over ----------
-    if (lane == 0) {
-      Walk w;
-      w.start(P, cta);
-      int piece = -1;
-      for (int g = 0; g < nch; ++g, w.next(P, cta)) {
-        const bool first = w.first(), last = w.last();
-        if (first) ++piece;
-        const int b = g % NB;
-        const bool ok = mbar_wait(&bufready[b], static_cast<uint32_t>((g / NB) & 1), P.wait_limit, abort_flag);
-        tc_fence_after();
-        const uint32_t acc = tmem_base + static_cast<uint32_t>(piece & 1) * 2 * C::kAcc;
-        if (ok && !*abort_flag) {
-#pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-#pragma unroll
-            for (int t = 0; t < 2; ++t) {   // the two blocks into their own accumulators, interleaved
-              const uint32_t xa = smem_u32(xring + (g % SX) * C::kXStage + t * C::kXT);
-              const uint32_t ta = tmem_base + C::kACol + b * 64 + 32u * t;
-              const uint64_t bdesc = smem_desc_sw128(xa + kk * 32, 16, 1024);
-              mma_f16_ts(acc + t * C::kAcc, ta + 8u * kk, bdesc, kIdesc, (first && kk == 0) ? 0u : 1u);
-            }
-          }
-        }
-        mma_commit(&bufdone[b]);
-        mma_commit(&xempty[g % SX]);
-        if (last) mma_commit(&accfull[piece & 1]);
-      }
-    }
-    __syncwarp();
   } else if (warp == kSyncWarp) {
     // ---- waits on behalf of the warps that take the chunk barrier ----------------------
     // Before chunk barrier g: chunk g's X, TMEM buffer (g+1) % NB free (the MMAs
     // of chunk g+1-NB done), the weights of chunk g+2 landed, and -- at the
-    // first chunk of piece k >= 2 -- its accumulator drained.  After it: the
-    // weight stages converted by then are released.
+    // first chunk of piece k >= 2 -- its accumulator pair drained.  After it:
+    // the weight stages converted by then are released.
     bool ok = nch == 0 || (mbar_wait(&wfull[0], 0, P.wait_limit, abort_flag) &&
                            (nch < 2 || mbar_wait(&wfull[1 % SW], (1 / SW) & 1, P.wait_limit, abort_flag)));
-    named_bar_sync(kStartBar, 32 + 8 * 32);
+    named_bar_sync(kStartBar, kBarThreads);
     Walk w;
     w.start(P, cta);
     int piece = -1;
@@ -385,46 +351,81 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
         ok = mbar_wait(&accempty[piece & 1], static_cast<uint32_t>(((piece - 2) / 2) & 1), P.wait_limit,
                        abort_flag);
       __syncwarp();
-      named_bar_sync(kChunkBar, 32 + 8 * 32);
+      named_bar_sync(kChunkBar, kBarThreads);
       if (lane == 0) {
-        mbar_arrive(&bufready[g % NB]);   // to the MMA warp
         if (g == 0) mbar_arrive(&wempty[0]);
         if (g + 1 < nch) mbar_arrive(&wempty[(g + 1) % SW]);
       }
     }
-  } else if (warp < kEpiWarp0) {
-    // ---- conversion of the weights into TMEM --------------------------------------------
+  } else if (warp >= kConvWarp0 && warp < kEpiWarp0) {
+    // ---- conversion of the weights into TMEM, and the MMAs --------------------------------
+    // Warp d converts half h of block t of each chunk for TMEM lane quarter q.
+    // Lane 0 of the first converting warp also issues each chunk's MMAs, right
+    // after the chunk barrier: a warp of its own would be starved of issue
+    // slots by the converting warps sharing its scheduler.
     const int d = warp - kConvWarp0;
-    const int t = d >> 2;                 // which block of the chunk
-    const int q = warp & 3;               // TMEM lane quarter
-    const uint32_t trow = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + C::kACol + 32u * t;
-    q4::BlockConverter<FMT, true> cv;
-    // Two register buffers: chunk g+1 is converted into the other buffer
-    // while the tensor-memory stores of chunk g still read theirs.
-    uint32_t a0[32], a1[32];
-    auto step = [&](int g, uint32_t (&cur)[32], uint32_t (&nxt)[32]) {
+    const int t = d >> 3, h = (d >> 2) & 1, q = warp & 3;
+    const uint32_t trow = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + C::kACol + 32u * t + 16u * h;
+    const bool issuer = d == 0 && lane == 0;
+    Walk w;
+    w.start(P, cta);
+    int piece = -1;
+    // chunk g's MMAs: its blocks in TMEM buffer g % NB, its X in stage g % SX;
+    // the two blocks go to the two accumulators of the piece's pair, interleaved
+    auto issue = [&](int g) {
+      const bool first = w.first(), last = w.last();
+      if (first) ++piece;
+      tc_fence_after();
+      const int b = g % NB;
+      const uint32_t acc = tmem_base + static_cast<uint32_t>(piece & 1) * 2 * C::kAcc;
+      if (!*abort_flag) {
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk) {
+#pragma unroll
+          for (int tt = 0; tt < 2; ++tt) {
+            const uint32_t xa = smem_u32(xring + (g % SX) * C::kXStage + tt * C::kXT);
+            const uint32_t ta = tmem_base + C::kACol + b * 64 + 32u * tt;
+            mma_f16_ts(acc + tt * C::kAcc, ta + 8u * kk, smem_desc_sw128(xa + kk * 32, 16, 1024), kIdesc,
+                       (first && kk == 0) ? 0u : 1u);
+          }
+        }
+      }
+      mma_commit(&bufdone[b]);
+      mma_commit(&xempty[g % SX]);
+      if (last) mma_commit(&accfull[piece & 1]);
+      w.next(P, cta);
+    };
+    q4::HalfConverter<FMT> cv;
+    // two register buffers: chunk g+1 is converted into the other one while
+    // the tensor-memory stores of chunk g still read theirs
+    uint32_t a0[16], a1[16];
+    auto step = [&](int g, uint32_t (&cur)[16], uint32_t (&nxt)[16]) {
+      if (issuer && g > 0) issue(g - 1);
+      __syncwarp();
       const bool next = g + 1 < nch;
       // the next chunk's loads go out before this chunk's stores
-      if (next) cv.load(wring + ((g + 1) % SW) * C::kWStage + t * C::kBB, q, lane);
+      if (next) cv.load(wring + ((g + 1) % SW) * C::kWStage + t * C::kBB, q, lane, h);
       tc_fence_after();
       const uint32_t dst = trow + static_cast<uint32_t>(g % NB) * 64;
-      tmem_st_16x128b_x8(dst, cur);
-      tmem_st_16x128b_x8(dst + (16u << 16), cur + 16);
-      if (next) cv.convert(nxt, q, lane);
+      tmem_st_16x128b_x4(dst, cur);
+      tmem_st_16x128b_x4(dst + (16u << 16), cur + 8);
+      if (next) cv.convert(nxt);
       tmem_st_wait();
       tc_fence_before();
-      named_bar_sync(kChunkBar, 32 + 8 * 32);
+      named_bar_sync(kChunkBar, kBarThreads);
     };
-    named_bar_sync(kStartBar, 32 + 8 * 32);
+    named_bar_sync(kStartBar, kBarThreads);
     if (nch > 0) {
-      cv.load(wring + t * C::kBB, q, lane);
-      cv.convert(a0, q, lane);
+      cv.load(wring + t * C::kBB, q, lane, h);
+      cv.convert(a0);
     }
     for (int g = 0; g < nch; g += 2) {
       step(g, a0, a1);
       if (g + 1 < nch) step(g + 1, a1, a0);
     }
-  } else {
+    if (issuer && nch > 0) issue(nch - 1);
+    __syncwarp();
+  } else if (warp >= kEpiWarp0) {
     // ---- epilogues: drain each piece, then the tile's output or its fixup ------------------
     const int eq = warp & 3;              // TMEM lane quarter = 32 channels of the tile
     const int tid = threadIdx.x - 32 * kEpiWarp0;
@@ -449,62 +450,61 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
         const bool dense = U >= P.G;
         const int J = dense ? owner((n + 1) * cpt - 1, U, P.G) - first + 1 : cpt;
 
-        // one lane polls, pausing between polls: these warps wait most of the
-        // time, and their polling would take shared-memory and issue slots
-        // from the converting warps
+        // one lane polls, pausing between polls (these warps wait most of the time)
         bool ok = true;
         if (lane == 0) {
           ok = mbar_wait_sleep(&accfull[piece & 1], static_cast<uint32_t>((piece / 2) & 1), P.wait_limit, abort_flag,
                                kEpiSleepNs);
           if (!ok) {
-            volatile int dummy = 0;   // the MMA warp always commits: let the MMAs finish first
+            volatile int dummy = 0;   // the MMAs are always committed: let them finish first
             mbar_wait(&accfull[piece & 1], static_cast<uint32_t>((piece / 2) & 1), kDrainLimit, &dummy);
           }
         }
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         __syncwarp();
         tc_fence_after();
-        float v[BT];
-        {
-          // the piece's two accumulators, added (same order for every piece)
-          const uint32_t ta = tmem_base + (static_cast<uint32_t>(32 * eq) << 16) + static_cast<uint32_t>(piece & 1) * 2 * C::kAcc;
+        ok = ok && !*abort_flag;
+        if (J == 1 && q.R && q.r_prod >= 0) ok = ok && wait_flag(P.pr[q.r_prod].ready + n, P.wait_limit, abort_flag);
+        const int ch = n * BNC + 32 * eq + lane;   // this thread's channel (= TMEM lane)
+        float* mine = q.part + static_cast<size_t>(n + cta) * M * BNC + 32 * eq + lane;
+        const uint32_t ta = tmem_base + (static_cast<uint32_t>(32 * eq) << 16) + static_cast<uint32_t>(piece & 1) * 2 * C::kAcc;
+        // rows (sequences) 32 at a time: the pair's two accumulators added,
+        // then either the epilogue (the whole tile is this CTA's) or this
+        // CTA's partial to its slot (n + cta) of [M][128] fp32
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
+        for (int r0 = 0; r0 < BT; r0 += 32) {
+          float v[32];
 #pragma unroll
-            for (int c0 = 0; c0 < BT; c0 += 32) {
-              uint32_t r[32];
-              tmem_ld_32x32b_x32(ta + h * C::kAcc + c0, r);
+          for (int half = 0; half < 2; ++half) {
+#pragma unroll
+            for (int a = 0; a < 2; ++a) {
+              uint32_t r[16];
+              tmem_ld_32x32b_x16(ta + a * C::kAcc + r0 + 16 * half, r);
               tmem_ld_wait();
 #pragma unroll
-              for (int e = 0; e < 32; ++e) v[c0 + e] = h ? v[c0 + e] + __uint_as_float(r[e]) : __uint_as_float(r[e]);
+              for (int e = 0; e < 16; ++e) v[16 * half + e] = a ? v[16 * half + e] + __uint_as_float(r[e]) : __uint_as_float(r[e]);
             }
           }
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&accempty[piece & 1]);
-        ok = ok && !*abort_flag;
-
-        if (J == 1) {
-          // the whole tile is this CTA's: epilogue from the accumulator
-          // (thread = channel n*128 + 32 eq + lane, rows m < M)
-          if (q.R && q.r_prod >= 0) ok = ok && wait_flag(P.pr[q.r_prod].ready + n, P.wait_limit, abort_flag);
-          const int ch = n * BNC + 32 * eq + lane;
+          if (r0 + 32 >= BT) {   // the pair is drained
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&accempty[piece & 1]);
+          }
 #pragma unroll
-          for (int m = 0; m < BT; ++m) {
-            if (m < M) {
-              float y = v[m];
+          for (int e = 0; e < 32; ++e) {
+            const int m = r0 + e;
+            if (m >= M) continue;
+            if (J == 1) {
+              float y = v[e];
               if (q.R) y += __half2float(__ldcg(q.R + static_cast<size_t>(m) * q.ldr + ch));
               if (q.relu) y = fmaxf(y, 0.0f);
               if (ok) q.Y[static_cast<size_t>(m) * q.ldy + ch] = __float2half_rn(y);
+            } else {
+              mine[m * BNC] = v[e];
             }
           }
-        } else {
-          // this CTA's partial to its slot (n + cta), [M][128] fp32
-          float* mine = q.part + static_cast<size_t>(n + cta) * M * BNC + 32 * eq + lane;
-#pragma unroll
-          for (int m = 0; m < BT; ++m)
-            if (m < M) mine[m * BNC] = v[m];
+        }
+        if (J > 1) {
           named_bar_sync(kEpiBar, 128);
           if (tid == 0) *epi_last = atom_add_acq_rel(q.cnt + n, 1u) == static_cast<unsigned>(J - 1);
           named_bar_sync(kEpiBar, 128);
@@ -513,36 +513,34 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
           // The last to arrive sums the J partials in contributor order (the
           // same sum whichever CTA is last).  Thread tid takes channels
           // 4 (tid % 32) .. +3 of rows m = tid / 32 + 4 i: 16-byte loads, each
-          // warp reading whole 512-byte rows; the rows go in two halves, the
-          // next contributor's loads in flight while the current one is added.
+          // warp reading whole 512-byte rows, four rows at a time, the next
+          // contributor's loads in flight while the current one is added.
           const int c4 = 4 * (tid & 31), m0 = tid >> 5;
           constexpr int kRows = BT / 4;          // rows per thread
-          constexpr int kHalf = kRows / 2 > 0 ? kRows / 2 : 1;
+          constexpr int kGrp = 4;
 #pragma unroll 1
-          for (int h = 0; h < kRows; h += kHalf) {
-            float4 acc[kHalf], b0[kHalf], b1[kHalf];
+          for (int g0 = 0; g0 < kRows; g0 += kGrp) {
+            float4 acc[kGrp], b0[kGrp], b1[kGrp];
             auto slot_of = [&](int k) {
               const int c = dense ? first + k : owner(n * cpt + k, U, P.G);
               return reinterpret_cast<const float4*>(q.part + static_cast<size_t>(n + c) * M * BNC + c4);
             };
-            auto fetch = [&](float4 (&dst)[kHalf], const float4* src) {
+            auto fetch = [&](float4 (&dst)[kGrp], const float4* src) {
 #pragma unroll
-              for (int i = 0; i < kHalf; ++i) {
-                const int m = m0 + 4 * (h + i);
+              for (int i = 0; i < kGrp; ++i) {
+                const int m = m0 + 4 * (g0 + i);
                 dst[i] = m < M ? __ldcg(src + m * (BNC / 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
               }
             };
-            auto add = [&](const float4 (&src)[kHalf]) {
+            auto add = [&](const float4 (&src)[kGrp]) {
 #pragma unroll
-              for (int i = 0; i < kHalf; ++i) {
+              for (int i = 0; i < kGrp; ++i) {
                 acc[i].x += src[i].x;
                 acc[i].y += src[i].y;
                 acc[i].z += src[i].z;
                 acc[i].w += src[i].w;
               }
             };
-            // acc = p_0 + p_1 + ... + p_{J-1} in that order, two contributors'
-            // loads in flight ahead of the additions
             fetch(acc, slot_of(0));
             if (J > 1) fetch(b0, slot_of(1));
 #pragma unroll 1
@@ -555,13 +553,13 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
               }
             }
 #pragma unroll
-            for (int i = 0; i < kHalf; ++i) {
-              const int m = m0 + 4 * (h + i);
+            for (int i = 0; i < kGrp; ++i) {
+              const int m = m0 + 4 * (g0 + i);
               if (m >= M) continue;
-              const int ch = n * BNC + c4;
+              const int chq = n * BNC + c4;
               float y[4] = {acc[i].x, acc[i].y, acc[i].z, acc[i].w};
               if (q.R) {
-                const uint2 rr = __ldcg(reinterpret_cast<const uint2*>(q.R + static_cast<size_t>(m) * q.ldr + ch));
+                const uint2 rr = __ldcg(reinterpret_cast<const uint2*>(q.R + static_cast<size_t>(m) * q.ldr + chq));
                 const float2 r01 = __half22float2(*reinterpret_cast<const __half2*>(&rr.x));
                 const float2 r23 = __half22float2(*reinterpret_cast<const __half2*>(&rr.y));
                 y[0] += r01.x;
@@ -575,7 +573,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
               }
               const __half2 y01 = __floats2half2_rn(y[0], y[1]), y23 = __floats2half2_rn(y[2], y[3]);
               if (ok)
-                *reinterpret_cast<uint2*>(q.Y + static_cast<size_t>(m) * q.ldy + ch) =
+                *reinterpret_cast<uint2*>(q.Y + static_cast<size_t>(m) * q.ldy + chq) =
                     make_uint2(*reinterpret_cast<const uint32_t*>(&y01), *reinterpret_cast<const uint32_t*>(&y23));
             }
           }
