@@ -379,15 +379,19 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
       const int b = g % NB;
       const uint32_t acc = tmem_base + static_cast<uint32_t>(piece & 1) * 2 * C::kAcc;
       if (!*abort_flag) {
+        // few instructions per MMA: this thread shares its scheduler with
+        // three converting warps.  The B descriptors differ only in the
+        // start-address field (shared-memory offset / 16), which stays below
+        // 2^14, so one 64-bit add per MMA makes each from the stage's.
+        const uint64_t d0 = smem_desc_sw128(smem_u32(xring + (g % SX) * C::kXStage), 16, 1024);
+        const uint32_t ta = tmem_base + C::kACol + b * 64;
+        const uint32_t f = first ? 0u : 1u;
+        mma_f16_ts(acc, ta, d0, kIdesc, f);
+        mma_f16_ts(acc + C::kAcc, ta + 32u, d0 + (C::kXT >> 4), kIdesc, f);
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk) {
-#pragma unroll
-          for (int tt = 0; tt < 2; ++tt) {
-            const uint32_t xa = smem_u32(xring + (g % SX) * C::kXStage + tt * C::kXT);
-            const uint32_t ta = tmem_base + C::kACol + b * 64 + 32u * tt;
-            mma_f16_ts(acc + tt * C::kAcc, ta + 8u * kk, smem_desc_sw128(xa + kk * 32, 16, 1024), kIdesc,
-                       (first && kk == 0) ? 0u : 1u);
-          }
+        for (int kk = 1; kk < BK / 16; ++kk) {
+          mma_f16_ts(acc, ta + 8u * kk, d0 + ((kk * 32) >> 4), kIdesc, 1u);
+          mma_f16_ts(acc + C::kAcc, ta + 32u + 8u * kk, d0 + ((C::kXT + kk * 32) >> 4), kIdesc, 1u);
         }
       }
       mma_commit(&bufdone[b]);
