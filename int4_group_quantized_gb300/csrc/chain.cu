@@ -23,28 +23,27 @@
 // Weights never wait: the weight copies of the next product stream while the
 // current one finishes.
 //
-// Inside a CTA (768 threads, 512 TMEM columns): warp 0 issues the weight
-// copies (one 2-block bulk copy per chunk), warp 1 owns TMEM, warp 2 issues
-// the X copies (after the flags), warp 3 takes every mbarrier wait for the
-// converting warps, warps 4..19 convert weights into TMEM (two warps per
-// block and lane quarter, the HalfConverter register order), warps 20..23
-// drain the accumulators and run the epilogues and fixups.  The main loop is
-// a lockstep chunk loop: the converting warps and the sync warp meet at one
-// named barrier per chunk, and lane 0 of the first converting warp issues the
-// chunk's MMAs right after it (a separate MMA warp shares its scheduler with
-// the converting warps and is starved of issue slots).  Each piece is summed
-// in two accumulators (the chunk's two blocks), so consecutive MMAs are
-// independent; two accumulator pairs alternate between pieces, so an
-// epilogue overlaps the next piece's MMAs.
+// Inside a CTA (384 threads, 256 TMEM columns, two CTAs per SM whose
+// pipelines hide each other's stalls): warp 0 issues the weight copies (one
+// 2-block bulk copy per chunk), warp 2 the X copies (after the flags), warp 3
+// takes every mbarrier wait for the warps of the chunk barrier, warp 1 owns
+// TMEM and issues the MMAs, warps 4..11 convert weights into TMEM (one block
+// of the chunk per set of four, the BlockConverter register order).  The main
+// loop runs in lockstep chunks: converting warps, sync warp and MMA warp meet
+// at one named barrier per chunk, and the MMA warp issues the chunk's MMAs
+// right after it.  A piece is summed in one accumulator; when it ends, the
+// first four converting warps (one per TMEM lane quarter) drain it before the
+// next chunk barrier -- the next piece's first MMAs overwrite it -- and run
+// the piece's epilogue or its share of the tile's fixup.
 //
 // Every wait is bounded (fg_set_wait_limit): a wait that gives up raises the
 // device error word and makes its role skip work, never a barrier; before the
 // CTA leaves, its copies and MMAs in flight have completed and its tensor
 // memory is freed.  Named barriers: the chunk barrier is taken once per chunk
-// by the sync and 16 converting warps; the start barrier once by the same
-// warps; the epilogue barrier the same number of times per piece by the 4
-// epilogue warps (the branch between its counts is decided once and
-// broadcast through shared memory).
+// by the MMA, sync and 8 converting warps; the start barrier once by the sync
+// and converting warps; the epilogue barrier the same number of times per
+// piece by the 4 draining warps (the branch between its counts is decided
+// once and broadcast through shared memory).
 #include <cudaTypedefs.h>
 #include <string.h>
 
@@ -67,10 +66,11 @@ using namespace tc;
 constexpr int BK = 64;                 // k per block / MMA tile
 constexpr int BNC = 128;               // channels per tile (the MMA's M)
 constexpr int CK = 128;                // k per chunk: two blocks
-constexpr int kThreads = 768;
-constexpr int kConvWarp0 = 4;                       // 16 converting warps
-constexpr int kEpiWarp0 = 20;                       // 4 epilogue warps
-constexpr int kBarThreads = 32 + 16 * 32;           // chunk and start barriers: sync warp + converters
+constexpr int kThreads = 384;
+constexpr int kCtasPerSm = 2;
+constexpr int kConvWarp0 = 4;                       // 8 converting warps
+constexpr int kChunkThreads = 64 + 8 * 32;          // MMA warp, sync warp, converters
+constexpr int kStartThreads = 32 + 8 * 32;          // sync warp, converters
 constexpr int kSyncWarp = 3;
 constexpr uint32_t kChunkBar = 1, kStartBar = 2, kEpiBar = 3;
 constexpr uint32_t kProducerSleepNs = 100;
@@ -141,6 +141,20 @@ __device__ __forceinline__ bool wait_flag(const unsigned* flag, uint32_t limit, 
   return false;
 }
 
+// The piece of a CTA's range that ends at a chunk: tile n of product p,
+// this CTA's contributor slot and the tile's contributor count.
+struct Piece {
+  int p, n, first, J;
+  int dense;
+  int index;   // the piece's number in this CTA (parity of its accumulator phase)
+  int ended;   // the chunk that wrote this record ends the piece
+};
+
+// Drains the accumulator once the MMAs of the piece just ended are done and
+// runs its epilogue (J == 1) or writes this CTA's partial and, for the last
+// contributor to arrive, the tile's fixup; then publishes the tile.  Run by
+// the four warps of TMEM lane quarters q = 0..3 (tid = 0..127); a call of its
+// own, outside the converting loop's registers: it runs once per piece.
 constexpr int chain_min(int a, int b) { return a < b ? a : b; }
 
 template <int BT, int FMT>
@@ -150,19 +164,16 @@ struct ChainCfg {
   static constexpr int kXT = BT * BK * 2;            // one X tile, K-major, 128-byte swizzle
   static constexpr int kXStage = 2 * kXT;
   static constexpr int kAcc = BT < 32 ? 32 : BT;     // accumulator columns
-  // two pieces in flight, each summed in two accumulators (the chunk's first
-  // and second block) so that consecutive MMAs do not depend on each other
-  static constexpr int kACol = 4 * kAcc;             // A buffers follow the accumulators
-  static constexpr int kBufs = (512 - kACol) / 64;   // A buffers of 64 columns (a chunk)
+  static constexpr int kACol = kAcc;                 // A buffers follow the accumulator
+  static constexpr int kBufs = (256 - kACol) / 64;   // A buffers of 64 columns (a chunk)
   // X stages have their own release barriers (the MMA commit of the chunk
-  // that read them), so the X ring is as deep as the shared memory allows:
-  // an X tile comes from L2 with microseconds of latency under load
-  static constexpr int kXStages = BT <= 32 ? 8 : 7;
-  static constexpr int kSmemBudget = 212 * 1024;
-  static constexpr int kWStages = chain_min(16, (kSmemBudget - kXStages * kXStage) / kWStage);
+  // that read them), independent of the TMEM buffers
+  static constexpr int kXStages = BT <= 32 ? 4 : 3;
+  static constexpr int kSmemBudget = 108 * 1024;
+  static constexpr int kWStages = chain_min(8, (kSmemBudget - kXStages * kXStage) / kWStage);
   static constexpr int kXBytes = kXStages * kXStage;
   static constexpr int kWBytes = kWStages * kWStage;
-  static constexpr int kBarBytes = (2 * kXStages + 2 * kWStages + kBufs + 4) * 8 + 16;
+  static constexpr int kBarBytes = (2 * kXStages + 2 * kWStages + kBufs + 1) * 8 + 16 + 2 * sizeof(Piece);
   static constexpr int kTotal = 1024 + kXBytes + kWBytes + kBarBytes;
   static_assert(kBufs >= 3 && kWStages >= 3, "pipeline depth");
   static_assert(kXT % 1024 == 0, "X tiles stay 1024-byte aligned");
@@ -215,8 +226,135 @@ __device__ __forceinline__ int total_chunks(const ChainParams& P, int cta) {
   return n;
 }
 
+template <int BT>
+__device__ __forceinline__ void drain_piece(const ChainParams& P, const Piece pc, int q, int lane, int tid,
+                                         uint32_t tmem_base, int cta, uint64_t* accfull, volatile int* abort_flag,
+                                         volatile int* epi_last) {
+  const int M = P.M;
+    const ChainProduct& qp = P.pr[pc.p];
+    bool ok = true;
+    if (lane == 0) {
+      ok = mbar_wait_sleep(accfull, static_cast<uint32_t>(pc.index & 1), P.wait_limit, abort_flag, kEpiSleepNs);
+      if (!ok) {
+        volatile int dummy = 0;   // the MMAs are always committed: let them finish first
+        mbar_wait(accfull, static_cast<uint32_t>(pc.index & 1), kDrainLimit, &dummy);
+      }
+    }
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    __syncwarp();
+    tc_fence_after();
+    ok = ok && !*abort_flag;
+    griddep_wait();   // Y, R and the partial slots belong to the stream order
+    if (pc.J == 1 && qp.R && qp.r_prod >= 0) ok = ok && wait_flag(P.pr[qp.r_prod].ready + pc.n, P.wait_limit, abort_flag);
+    const int ch = pc.n * BNC + 32 * q + lane;   // this thread's channel (= TMEM lane)
+    float* mine = qp.part + static_cast<size_t>(pc.n + cta) * M * BNC + 32 * q + lane;
+    const uint32_t ta = tmem_base + (static_cast<uint32_t>(32 * q) << 16);
+#pragma unroll 1
+    for (int r0 = 0; r0 < BT; r0 += 16) {
+      uint32_t r[16];
+      tmem_ld_32x32b_x16(ta + r0, r);
+      tmem_ld_wait();
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const int m = r0 + e;
+        if (m >= M) continue;
+        const float v = __uint_as_float(r[e]);
+        if (pc.J == 1) {
+          float y = v;
+          if (qp.R) y += __half2float(__ldcg(qp.R + static_cast<size_t>(m) * qp.ldr + ch));
+          if (qp.relu) y = fmaxf(y, 0.0f);
+          if (ok) qp.Y[static_cast<size_t>(m) * qp.ldy + ch] = __float2half_rn(y);
+        } else {
+          mine[m * BNC] = v;
+        }
+      }
+    }
+    tc_fence_before();   // the accumulator reads, before the barrier after which it is overwritten
+    if (pc.J > 1) {
+      named_bar_sync(kEpiBar, 128);
+      if (tid == 0) *epi_last = atom_add_acq_rel(qp.cnt + pc.n, 1u) == static_cast<unsigned>(pc.J - 1);
+      named_bar_sync(kEpiBar, 128);
+      if (*epi_last == 0) return;   // the same for the four warps: no barrier below is skipped unevenly
+      if (qp.R && qp.r_prod >= 0) ok = ok && wait_flag(P.pr[qp.r_prod].ready + pc.n, P.wait_limit, abort_flag);
+      // The last to arrive sums the J partials in contributor order (the
+      // same sum whichever CTA is last).  Thread tid takes channels
+      // 4 (tid % 32) .. +3 of rows m = tid / 32 + 4 i: 16-byte loads, each
+      // warp reading whole 512-byte rows, two rows at a time, the next
+      // contributor's loads in flight while the current one is added.
+      const int c4 = 4 * (tid & 31), m0 = tid >> 5;
+      const int U = (qp.N / BNC) * (qp.K / CK), cpt = qp.K / CK;
+      constexpr int kRows = BT / 4;          // rows per thread
+      constexpr int kGrp = 2;
+#pragma unroll 1
+      for (int g0 = 0; g0 < kRows; g0 += kGrp) {
+        float4 acc[kGrp], b0[kGrp], b1[kGrp];
+        auto slot_of = [&](int k) {
+          const int c = pc.dense ? pc.first + k : owner(pc.n * cpt + k, U, P.G);
+          return reinterpret_cast<const float4*>(qp.part + static_cast<size_t>(pc.n + c) * M * BNC + c4);
+        };
+        auto fetch = [&](float4 (&dst)[kGrp], const float4* src) {
+#pragma unroll
+          for (int i = 0; i < kGrp; ++i) {
+            const int m = m0 + 4 * (g0 + i);
+            dst[i] = m < M ? __ldcg(src + m * (BNC / 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+        };
+        auto add = [&](const float4 (&src)[kGrp]) {
+#pragma unroll
+          for (int i = 0; i < kGrp; ++i) {
+            acc[i].x += src[i].x;
+            acc[i].y += src[i].y;
+            acc[i].z += src[i].z;
+            acc[i].w += src[i].w;
+          }
+        };
+        fetch(acc, slot_of(0));
+        fetch(b0, slot_of(1));
+#pragma unroll 1
+        for (int k = 1; k < pc.J; k += 2) {
+          if (k + 1 < pc.J) fetch(b1, slot_of(k + 1));
+          add(b0);
+          if (k + 1 < pc.J) {
+            if (k + 2 < pc.J) fetch(b0, slot_of(k + 2));
+            add(b1);
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < kGrp; ++i) {
+          const int m = m0 + 4 * (g0 + i);
+          if (m >= M) continue;
+          const int chq = pc.n * BNC + c4;
+          float y[4] = {acc[i].x, acc[i].y, acc[i].z, acc[i].w};
+          if (qp.R) {
+            const uint2 rr = __ldcg(reinterpret_cast<const uint2*>(qp.R + static_cast<size_t>(m) * qp.ldr + chq));
+            const float2 r01 = __half22float2(*reinterpret_cast<const __half2*>(&rr.x));
+            const float2 r23 = __half22float2(*reinterpret_cast<const __half2*>(&rr.y));
+            y[0] += r01.x;
+            y[1] += r01.y;
+            y[2] += r23.x;
+            y[3] += r23.y;
+          }
+          if (qp.relu) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) y[e] = fmaxf(y[e], 0.0f);
+          }
+          const __half2 y01 = __floats2half2_rn(y[0], y[1]), y23 = __floats2half2_rn(y[2], y[3]);
+          if (ok)
+            *reinterpret_cast<uint2*>(qp.Y + static_cast<size_t>(m) * qp.ldy + chq) =
+                make_uint2(*reinterpret_cast<const uint32_t*>(&y01), *reinterpret_cast<const uint32_t*>(&y23));
+        }
+      }
+    }
+    // publish the tile: the release after the barrier orders every thread's stores of it
+    named_bar_sync(kEpiBar, 128);
+    if (tid == 0) {
+      if (pc.J > 1) qp.cnt[pc.n] = 0;   // every contributor has arrived: ready for the next launch
+      st_release(qp.ready + pc.n, 1u);
+    }
+}
+
 template <int BT, int FMT>
-__global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constant__ ChainParams P) {
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) chain_kernel(const __grid_constant__ ChainParams P) {
   using C = ChainCfg<BT, FMT>;
   constexpr int NB = C::kBufs, SX = C::kXStages, SW = C::kWStages;
   constexpr uint32_t kIdesc = idesc_f16(128, BT, 0, 0);
@@ -229,11 +367,13 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
   uint64_t* wfull = xempty + SX;
   uint64_t* wempty = wfull + SW;
   uint64_t* bufdone = wempty + SW;     // MMAs of the chunk in TMEM buffer b completed
-  uint64_t* accfull = bufdone + NB;    // [2] the piece in accumulator pair a is summed
-  uint64_t* accempty = accfull + 2;    // [2] accumulator pair a drained by the epilogue warps
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accempty + 2);
+  uint64_t* accfull = bufdone + NB;    // the piece in the accumulator is summed (one phase per piece)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accfull + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* epi_last = abort_flag + 1;
+  // the piece record of chunk g, in slot g % 2: written by the MMA warp before
+  // chunk barrier g, read by the draining warps after it
+  Piece* pinfo = reinterpret_cast<Piece*>(reinterpret_cast<uint8_t*>(tmem_slot) + 16);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cta = blockIdx.x;
@@ -251,14 +391,11 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
       mbar_init(&wempty[i], 1);
     }
     for (int i = 0; i < NB; ++i) mbar_init(&bufdone[i], 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&accfull[i], 1);
-      mbar_init(&accempty[i], 4);   // one arrival per epilogue warp
-    }
+    mbar_init(accfull, 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
-  if (warp == 1) tmem_alloc(tmem_slot, 512);
+  if (warp == 1) tmem_alloc(tmem_slot, 256);
   if (warp == 2 && lane == 0)
     for (int p = 0; p < P.np; ++p) tma_prefetch_desc(&P.mapX[p]);
   tc_fence_before();
@@ -326,279 +463,128 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
       if (*abort_flag) atomicOr(P.err, DEV_ERR_WAIT_TIMEOUT);
     }
     __syncwarp();
-  } else if (warp == kSyncWarp) {
-    // ---- waits on behalf of the warps that take the chunk barrier ----------------------
-    // Before chunk barrier g: chunk g's X, TMEM buffer (g+1) % NB free (the MMAs
-    // of chunk g+1-NB done), the weights of chunk g+2 landed, and -- at the
-    // first chunk of piece k >= 2 -- its accumulator pair drained.  After it:
-    // the weight stages converted by then are released.
-    bool ok = nch == 0 || (mbar_wait(&wfull[0], 0, P.wait_limit, abort_flag) &&
-                           (nch < 2 || mbar_wait(&wfull[1 % SW], (1 / SW) & 1, P.wait_limit, abort_flag)));
-    named_bar_sync(kStartBar, kBarThreads);
+  } else if (warp == 1) {
+    // ---- MMAs: every lane takes the chunk barrier, lane 0 issues ---------------------
     Walk w;
     w.start(P, cta);
     int piece = -1;
+    Piece pc = {0, 0, 0, 0, 0, -1, 0};
     for (int g = 0; g < nch; ++g, w.next(P, cta)) {
-      const bool first = w.first();
-      if (first) ++piece;
+      const bool first = w.first(), last = w.last();
+      if (first) {
+        ++piece;
+        const ChainProduct& qp = P.pr[w.p];
+        const int cpt = qp.K / CK, U = (qp.N / BNC) * cpt;
+        pc.p = w.p;
+        pc.n = w.tile;
+        pc.first = owner(w.tile * cpt, U, P.G);
+        pc.dense = U >= P.G;
+        // the tile's contributors, in order: with at least as many units as
+        // CTAs every CTA from the owner of the tile's first unit to the owner
+        // of its last; with fewer, every CTA holds at most one unit, and the
+        // contributors are the owners of the tile's units
+        pc.J = pc.dense ? owner((w.tile + 1) * cpt - 1, U, P.G) - pc.first + 1 : cpt;
+        pc.index = piece;
+      }
+      pc.ended = last;
+      if (lane == 0) pinfo[g & 1] = pc;
+      named_bar_sync(kChunkBar, kChunkThreads);   // chunk g in TMEM, its X landed, the accumulator drained
+      if (lane == 0) {
+        tc_fence_after();
+        const int b = g % NB;
+        if (!*abort_flag) {
+          const uint64_t d0 = smem_desc_sw128(smem_u32(xring + (g % SX) * C::kXStage), 16, 1024);
+          const uint32_t ta = tmem_base + C::kACol + b * 64;
+#pragma unroll
+          for (int t = 0; t < 2; ++t)
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk)
+              mma_f16_ts(tmem_base, ta + 32u * t + 8u * kk, d0 + ((t * C::kXT + kk * 32) >> 4), kIdesc,
+                         (first && t == 0 && kk == 0) ? 0u : 1u);
+        }
+        mma_commit(&bufdone[b]);
+        mma_commit(&xempty[g % SX]);
+        if (last) mma_commit(accfull);
+      }
+      __syncwarp();
+    }
+  } else if (warp == kSyncWarp) {
+    // ---- waits on behalf of the warps that take the chunk barrier ----------------------
+    // Before chunk barrier g: chunk g's X, TMEM buffer (g+1) % NB free (the MMAs
+    // of chunk g+1-NB done) and the weights of chunk g+2 landed.  After it:
+    // the weight stages converted by then are released.
+    bool ok = nch == 0 || (mbar_wait(&wfull[0], 0, P.wait_limit, abort_flag) &&
+                           (nch < 2 || mbar_wait(&wfull[1 % SW], (1 / SW) & 1, P.wait_limit, abort_flag)));
+    named_bar_sync(kStartBar, kStartThreads);
+    for (int g = 0; g < nch; ++g) {
       if (ok) ok = mbar_wait(&xfull[g % SX], static_cast<uint32_t>((g / SX) & 1), P.wait_limit, abort_flag);
       if (ok && g + 1 < nch && g + 1 >= NB)
         ok = mbar_wait(&bufdone[(g + 1) % NB], static_cast<uint32_t>(((g + 1 - NB) / NB) & 1), P.wait_limit,
                        abort_flag);
       if (ok && g + 2 < nch)
         ok = mbar_wait(&wfull[(g + 2) % SW], static_cast<uint32_t>(((g + 2) / SW) & 1), P.wait_limit, abort_flag);
-      if (ok && first && piece >= 2)
-        ok = mbar_wait(&accempty[piece & 1], static_cast<uint32_t>(((piece - 2) / 2) & 1), P.wait_limit,
-                       abort_flag);
       __syncwarp();
-      named_bar_sync(kChunkBar, kBarThreads);
+      named_bar_sync(kChunkBar, kChunkThreads);
       if (lane == 0) {
         if (g == 0) mbar_arrive(&wempty[0]);
         if (g + 1 < nch) mbar_arrive(&wempty[(g + 1) % SW]);
       }
     }
-  } else if (warp >= kConvWarp0 && warp < kEpiWarp0) {
-    // ---- conversion of the weights into TMEM, and the MMAs --------------------------------
-    // Warp d converts half h of block t of each chunk for TMEM lane quarter q.
-    // Lane 0 of the first converting warp also issues each chunk's MMAs, right
-    // after the chunk barrier: a warp of its own would be starved of issue
-    // slots by the converting warps sharing its scheduler.
+  } else {
+    // ---- conversion of the weights into TMEM; the first four warps also drain -----------
     const int d = warp - kConvWarp0;
-    const int t = d >> 3, h = (d >> 2) & 1, q = warp & 3;
-    const uint32_t trow = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + C::kACol + 32u * t + 16u * h;
-    const bool issuer = d == 0 && lane == 0;
-    Walk w;
-    w.start(P, cta);
-    int piece = -1;
-    // chunk g's MMAs: its blocks in TMEM buffer g % NB, its X in stage g % SX;
-    // the two blocks go to the two accumulators of the piece's pair, interleaved
-    auto issue = [&](int g) {
-      const bool first = w.first(), last = w.last();
-      if (first) ++piece;
-      tc_fence_after();
-      const int b = g % NB;
-      const uint32_t acc = tmem_base + static_cast<uint32_t>(piece & 1) * 2 * C::kAcc;
-      if (!*abort_flag) {
-        // few instructions per MMA: this thread shares its scheduler with
-        // three converting warps.  The B descriptors differ only in the
-        // start-address field (shared-memory offset / 16), which stays below
-        // 2^14, so one 64-bit add per MMA makes each from the stage's.
-        const uint64_t d0 = smem_desc_sw128(smem_u32(xring + (g % SX) * C::kXStage), 16, 1024);
-        const uint32_t ta = tmem_base + C::kACol + b * 64;
-        const uint32_t f = first ? 0u : 1u;
-        mma_f16_ts(acc, ta, d0, kIdesc, f);
-        mma_f16_ts(acc + C::kAcc, ta + 32u, d0 + (C::kXT >> 4), kIdesc, f);
-#pragma unroll
-        for (int kk = 1; kk < BK / 16; ++kk) {
-          mma_f16_ts(acc, ta + 8u * kk, d0 + ((kk * 32) >> 4), kIdesc, 1u);
-          mma_f16_ts(acc + C::kAcc, ta + 32u + 8u * kk, d0 + ((C::kXT + kk * 32) >> 4), kIdesc, 1u);
-        }
-      }
-      mma_commit(&bufdone[b]);
-      mma_commit(&xempty[g % SX]);
-      if (last) mma_commit(&accfull[piece & 1]);
-      w.next(P, cta);
-    };
-    q4::HalfConverter<FMT> cv;
-    // two register buffers: chunk g+1 is converted into the other one while
-    // the tensor-memory stores of chunk g still read theirs
-    uint32_t a0[16], a1[16];
-    auto step = [&](int g, uint32_t (&cur)[16], uint32_t (&nxt)[16]) {
-      if (issuer && g > 0) issue(g - 1);
-      __syncwarp();
+    const int t = d >> 2;                 // which block of the chunk
+    const int q = warp & 3;               // TMEM lane quarter
+    const bool drains = d < 4;            // one warp per lane quarter
+    const int tid = threadIdx.x - 32 * kConvWarp0;   // 0..127 for the draining warps
+    const uint32_t trow = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + C::kACol + 32u * t;
+    const int M = P.M;
+    q4::BlockConverter<FMT> cv;
+    uint32_t a[32];
+
+    // Drains the accumulator once the MMAs of the piece just ended are done and
+    // runs its epilogue (J == 1) or writes this CTA's partial and, for the last
+    // contributor to arrive, the tile's fixup; then publishes the tile.
+    named_bar_sync(kStartBar, kStartThreads);
+    if (nch > 0) {
+      cv.load(wring + t * C::kBB, q, lane);
+      cv.convert(a, q, lane);
+    }
+    for (int g = 0; g < nch; ++g) {
       const bool next = g + 1 < nch;
-      // the next chunk's loads go out before this chunk's stores
-      if (next) cv.load(wring + ((g + 1) % SW) * C::kWStage + t * C::kBB, q, lane, h);
-      tc_fence_after();
       const uint32_t dst = trow + static_cast<uint32_t>(g % NB) * 64;
-      tmem_st_16x128b_x4(dst, cur);
-      tmem_st_16x128b_x4(dst + (16u << 16), cur + 8);
-      if (next) cv.convert(nxt);
+      // the record of chunk g-1 (written before chunk barrier g-1)
+      const bool ended = drains && g > 0 && pinfo[(g - 1) & 1].ended;
+      if (ended) {
+        // chunk g's MMAs come after this chunk's barrier: drain the piece that
+        // ended at chunk g-1 first (between the stores of chunk g and the
+        // loads of chunk g+1, where neither holds registers)
+        tc_fence_after();
+        tmem_st_16x128b_x8(dst, a);
+        tmem_st_16x128b_x8(dst + (16u << 16), a + 16);
+        drain_piece<BT>(P, pinfo[(g - 1) & 1], q, lane, tid, tmem_base, cta, accfull, abort_flag, epi_last);
+        if (next) cv.load(wring + ((g + 1) % SW) * C::kWStage + t * C::kBB, q, lane);
+      } else {
+        // the next chunk's loads go out before this chunk's stores
+        if (next) cv.load(wring + ((g + 1) % SW) * C::kWStage + t * C::kBB, q, lane);
+        tc_fence_after();
+        tmem_st_16x128b_x8(dst, a);
+        tmem_st_16x128b_x8(dst + (16u << 16), a + 16);
+      }
+      if (next) cv.convert(a, q, lane);
       tmem_st_wait();
       tc_fence_before();
-      named_bar_sync(kChunkBar, kBarThreads);
-    };
-    named_bar_sync(kStartBar, kBarThreads);
-    if (nch > 0) {
-      cv.load(wring + t * C::kBB, q, lane, h);
-      cv.convert(a0);
+      named_bar_sync(kChunkBar, kChunkThreads);
     }
-    for (int g = 0; g < nch; g += 2) {
-      step(g, a0, a1);
-      if (g + 1 < nch) step(g + 1, a1, a0);
-    }
-    if (issuer && nch > 0) issue(nch - 1);
-    __syncwarp();
-  } else if (warp >= kEpiWarp0) {
-    // ---- epilogues: drain each piece, then the tile's output or its fixup ------------------
-    const int eq = warp & 3;              // TMEM lane quarter = 32 channels of the tile
-    const int tid = threadIdx.x - 32 * kEpiWarp0;
-    const int M = P.M;
-    griddep_wait();
-    int piece = -1;
-    for (int p = 0; p < P.np; ++p) {
-      const ChainProduct& q = P.pr[p];
-      const int cpt = q.K / CK;
-      const int U = (q.N / BNC) * cpt;
-      int u0, u1;
-      cta_range(U, cta, P.G, u0, u1);
-      for (int u = u0; u < u1;) {
-        const int n = u / cpt;
-        u = min(u1, (n + 1) * cpt);
-        ++piece;
-        // the tile's contributors, in order: with at least as many units as
-        // CTAs every CTA from the owner of the tile's first unit to the owner
-        // of its last; with fewer, every CTA holds at most one unit, and the
-        // contributors are the owners of the tile's units
-        const int first = owner(n * cpt, U, P.G);
-        const bool dense = U >= P.G;
-        const int J = dense ? owner((n + 1) * cpt - 1, U, P.G) - first + 1 : cpt;
-
-        // one lane polls, pausing between polls (these warps wait most of the time)
-        bool ok = true;
-        if (lane == 0) {
-          ok = mbar_wait_sleep(&accfull[piece & 1], static_cast<uint32_t>((piece / 2) & 1), P.wait_limit, abort_flag,
-                               kEpiSleepNs);
-          if (!ok) {
-            volatile int dummy = 0;   // the MMAs are always committed: let them finish first
-            mbar_wait(&accfull[piece & 1], static_cast<uint32_t>((piece / 2) & 1), kDrainLimit, &dummy);
-          }
-        }
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        __syncwarp();
-        tc_fence_after();
-        ok = ok && !*abort_flag;
-        if (J == 1 && q.R && q.r_prod >= 0) ok = ok && wait_flag(P.pr[q.r_prod].ready + n, P.wait_limit, abort_flag);
-        const int ch = n * BNC + 32 * eq + lane;   // this thread's channel (= TMEM lane)
-        float* mine = q.part + static_cast<size_t>(n + cta) * M * BNC + 32 * eq + lane;
-        const uint32_t ta = tmem_base + (static_cast<uint32_t>(32 * eq) << 16) + static_cast<uint32_t>(piece & 1) * 2 * C::kAcc;
-        // rows (sequences) 32 at a time: the pair's two accumulators added,
-        // then either the epilogue (the whole tile is this CTA's) or this
-        // CTA's partial to its slot (n + cta) of [M][128] fp32
-#pragma unroll
-        for (int r0 = 0; r0 < BT; r0 += 32) {
-          float v[32];
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {
-#pragma unroll
-            for (int a = 0; a < 2; ++a) {
-              uint32_t r[16];
-              tmem_ld_32x32b_x16(ta + a * C::kAcc + r0 + 16 * half, r);
-              tmem_ld_wait();
-#pragma unroll
-              for (int e = 0; e < 16; ++e) v[16 * half + e] = a ? v[16 * half + e] + __uint_as_float(r[e]) : __uint_as_float(r[e]);
-            }
-          }
-          if (r0 + 32 >= BT) {   // the pair is drained
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&accempty[piece & 1]);
-          }
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int m = r0 + e;
-            if (m >= M) continue;
-            if (J == 1) {
-              float y = v[e];
-              if (q.R) y += __half2float(__ldcg(q.R + static_cast<size_t>(m) * q.ldr + ch));
-              if (q.relu) y = fmaxf(y, 0.0f);
-              if (ok) q.Y[static_cast<size_t>(m) * q.ldy + ch] = __float2half_rn(y);
-            } else {
-              mine[m * BNC] = v[e];
-            }
-          }
-        }
-        if (J > 1) {
-          named_bar_sync(kEpiBar, 128);
-          if (tid == 0) *epi_last = atom_add_acq_rel(q.cnt + n, 1u) == static_cast<unsigned>(J - 1);
-          named_bar_sync(kEpiBar, 128);
-          if (*epi_last == 0) continue;   // the same for the four warps: no barrier below is skipped unevenly
-          if (q.R && q.r_prod >= 0) ok = ok && wait_flag(P.pr[q.r_prod].ready + n, P.wait_limit, abort_flag);
-          // The last to arrive sums the J partials in contributor order (the
-          // same sum whichever CTA is last).  Thread tid takes channels
-          // 4 (tid % 32) .. +3 of rows m = tid / 32 + 4 i: 16-byte loads, each
-          // warp reading whole 512-byte rows, four rows at a time, the next
-          // contributor's loads in flight while the current one is added.
-          const int c4 = 4 * (tid & 31), m0 = tid >> 5;
-          constexpr int kRows = BT / 4;          // rows per thread
-          constexpr int kGrp = 4;
-#pragma unroll 1
-          for (int g0 = 0; g0 < kRows; g0 += kGrp) {
-            float4 acc[kGrp], b0[kGrp], b1[kGrp];
-            auto slot_of = [&](int k) {
-              const int c = dense ? first + k : owner(n * cpt + k, U, P.G);
-              return reinterpret_cast<const float4*>(q.part + static_cast<size_t>(n + c) * M * BNC + c4);
-            };
-            auto fetch = [&](float4 (&dst)[kGrp], const float4* src) {
-#pragma unroll
-              for (int i = 0; i < kGrp; ++i) {
-                const int m = m0 + 4 * (g0 + i);
-                dst[i] = m < M ? __ldcg(src + m * (BNC / 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
-              }
-            };
-            auto add = [&](const float4 (&src)[kGrp]) {
-#pragma unroll
-              for (int i = 0; i < kGrp; ++i) {
-                acc[i].x += src[i].x;
-                acc[i].y += src[i].y;
-                acc[i].z += src[i].z;
-                acc[i].w += src[i].w;
-              }
-            };
-            fetch(acc, slot_of(0));
-            if (J > 1) fetch(b0, slot_of(1));
-#pragma unroll 1
-            for (int k = 1; k < J; k += 2) {
-              if (k + 1 < J) fetch(b1, slot_of(k + 1));
-              add(b0);
-              if (k + 1 < J) {
-                if (k + 2 < J) fetch(b0, slot_of(k + 2));
-                add(b1);
-              }
-            }
-#pragma unroll
-            for (int i = 0; i < kGrp; ++i) {
-              const int m = m0 + 4 * (g0 + i);
-              if (m >= M) continue;
-              const int chq = n * BNC + c4;
-              float y[4] = {acc[i].x, acc[i].y, acc[i].z, acc[i].w};
-              if (q.R) {
-                const uint2 rr = __ldcg(reinterpret_cast<const uint2*>(q.R + static_cast<size_t>(m) * q.ldr + chq));
-                const float2 r01 = __half22float2(*reinterpret_cast<const __half2*>(&rr.x));
-                const float2 r23 = __half22float2(*reinterpret_cast<const __half2*>(&rr.y));
-                y[0] += r01.x;
-                y[1] += r01.y;
-                y[2] += r23.x;
-                y[3] += r23.y;
-              }
-              if (q.relu) {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) y[e] = fmaxf(y[e], 0.0f);
-              }
-              const __half2 y01 = __floats2half2_rn(y[0], y[1]), y23 = __floats2half2_rn(y[2], y[3]);
-              if (ok)
-                *reinterpret_cast<uint2*>(q.Y + static_cast<size_t>(m) * q.ldy + chq) =
-                    make_uint2(*reinterpret_cast<const uint32_t*>(&y01), *reinterpret_cast<const uint32_t*>(&y23));
-            }
-          }
-        }
-        // publish the tile: the release after the barrier orders every
-        // thread's stores of it
-        named_bar_sync(kEpiBar, 128);
-        if (tid == 0) {
-          if (J > 1) q.cnt[n] = 0;   // every contributor has arrived: ready for the next launch
-          st_release(q.ready + n, 1u);
-        }
-      }
-    }
-    if (tid == 0 && *abort_flag) atomicOr(P.err, DEV_ERR_WAIT_TIMEOUT);
+    if (drains && nch > 0)   // the last piece always ends at the last chunk
+      drain_piece<BT>(P, pinfo[(nch - 1) & 1], q, lane, tid, tmem_base, cta, accfull, abort_flag, epi_last);
   }
 
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, 512);
+    tmem_dealloc(tmem_base, 256);
   }
 }
 
@@ -635,7 +621,7 @@ int chain_owner(int64_t u, int64_t U, int G) { return static_cast<int>(((u + 1) 
 
 static_assert(kChainMaxCtas * 65536LL < (1LL << 31), "32-bit partition arithmetic");
 
-int chain_ctas() { return std::min(num_sms(), kChainMaxCtas); }
+int chain_ctas() { return std::min(kCtasPerSm * num_sms(), kChainMaxCtas); }
 
 size_t chain_part_bytes(int64_t M, int64_t N) {
   return static_cast<size_t>(N / BNC + kChainMaxCtas - 1) * static_cast<size_t>(M) * BNC * sizeof(float);

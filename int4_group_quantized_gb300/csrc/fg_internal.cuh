@@ -115,7 +115,7 @@ size_t gemm_q4ts_workspace_bytes(int64_t M, int64_t N, int64_t K);
 // zeroed them already (then the launch overlaps the previous kernel),
 // otherwise chain_run zeroes them first.
 constexpr int kMaxChain = 4;
-constexpr int kChainMaxCtas = 256;
+constexpr int kChainMaxCtas = 512;
 struct ChainLink {
   GemmArgs a;
   int x_prod;
