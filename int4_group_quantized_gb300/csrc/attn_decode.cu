@@ -51,8 +51,6 @@ struct DecodeArgs {
   int64_t cap;
   int splits;
   int tps;             // tokens per split (multiple of 16)
-  unsigned* zero;      // words to clear after the grid dependency (or null)
-  int64_t zero_words;
 };
 
 __device__ __forceinline__ uint32_t lop_mask_or(uint32_t x, uint32_t mask, uint32_t magic) {
@@ -365,10 +363,6 @@ __global__ void __launch_bounds__(128) decode_attn_mma_kernel(const DecodeArgs a
   // kernel has completed
   tc::griddep_launch();
   tc::griddep_wait();
-  if (a.zero)
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < a.zero_words;
-         i += static_cast<int64_t>(gridDim.x) * blockDim.x)
-      a.zero[i] = 0u;
 
   // ---- Concat: quantize the new token's K and V into slot pos -----------------
   if (a.knew != nullptr && a.pos >= t0 && a.pos < t1) {
@@ -494,10 +488,8 @@ int attn_splits(int64_t bh, int64_t len) {
 template <int D>
 fg_status launch_mma(const fg_kv& kv, const void* q, int64_t ldq, const void* knew, const void* vnew,
                      int64_t ldnew, int64_t b, int64_t pos, void* out, int64_t ldo, void* ws,
-                     size_t ws_bytes, cudaStream_t st, unsigned* zero, int64_t zero_words) {
+                     size_t ws_bytes, cudaStream_t st) {
   DecodeArgs a;
-  a.zero = zero;
-  a.zero_words = zero_words;
   a.kc = kv.k_codes;
   a.vc = kv.v_codes;
   a.kmin = kv.k_mins;
@@ -568,17 +560,14 @@ size_t decode_attention_workspace_bytes(int64_t b, int32_t heads, int32_t head_d
 
 fg_status decode_attention(const fg_kv& kv, const void* q, int64_t ldq, const void* knew,
                            const void* vnew, int64_t ldnew, int64_t b, int64_t pos, void* out,
-                           int64_t ldo, void* ws, size_t ws_bytes, cudaStream_t st, unsigned* zero,
-                           int64_t zero_words) {
+                           int64_t ldo, void* ws, size_t ws_bytes, cudaStream_t st) {
   if (b == 0) return FG_OK;
   if (kv.codec == FG_CODEC_Q4G64 && kv.dtype == FG_F16) {
     if (kv.head_dim == 128)
-      return launch_mma<128>(kv, q, ldq, knew, vnew, ldnew, b, pos, out, ldo, ws, ws_bytes, st, zero, zero_words);
+      return launch_mma<128>(kv, q, ldq, knew, vnew, ldnew, b, pos, out, ldo, ws, ws_bytes, st);
     if (kv.head_dim == 64)
-      return launch_mma<64>(kv, q, ldq, knew, vnew, ldnew, b, pos, out, ldo, ws, ws_bytes, st, zero, zero_words);
+      return launch_mma<64>(kv, q, ldq, knew, vnew, ldnew, b, pos, out, ldo, ws, ws_bytes, st);
   }
-  if (zero && zero_words > 0 && cudaMemsetAsync(zero, 0, zero_words * sizeof(unsigned), st) != cudaSuccess)
-    return check_launch("control words reset");
   // fp32 activations or an uncompressed cache: append, then CUDA-core attention
   if (knew) {
     fg_status s = kv_store(kv, knew, vnew, ldnew, b, 1, pos, st);

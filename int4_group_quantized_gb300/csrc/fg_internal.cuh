@@ -105,32 +105,6 @@ size_t gemm_tc_workspace_bytes(int64_t M, int64_t N, int64_t K);
 bool gemm_q4ts_supported(const GemmArgs& a);
 fg_status gemm_q4ts(const GemmArgs& a, void* ws, size_t ws_bytes, cudaStream_t st);
 size_t gemm_q4ts_workspace_bytes(int64_t M, int64_t N, int64_t K);
-// Decode products of a layer-step chained in one persistent launch (chain.cu):
-// up to kMaxChain products, each X an input (x_prod = -1) or the Y of an
-// earlier product of the chain, each residual an input (r_prod = -1) or an
-// earlier product's Y.  fp16, 4-bit weights with their decode copy, M <= 64.
-// Workspace: part_ws (chain_workspace_bytes) for the K-split partials, ctrl
-// (chain_ctrl_bytes per product, summed) for per-tile flags and counters,
-// which must be zero when the kernel starts: ctrl_zeroed says the stream has
-// zeroed them already (then the launch overlaps the previous kernel),
-// otherwise chain_run zeroes them first.
-constexpr int kMaxChain = 4;
-constexpr int kChainMaxCtas = 512;
-struct ChainLink {
-  GemmArgs a;
-  int x_prod;
-  int r_prod;
-};
-bool chain_supported(const GemmArgs& a);
-fg_status chain_run(const ChainLink* links, int n, void* part_ws, size_t part_bytes, unsigned* ctrl,
-                    size_t ctrl_bytes, bool ctrl_zeroed, cudaStream_t st);
-size_t chain_workspace_bytes(const int64_t* N, int n, int64_t M);
-size_t chain_ctrl_bytes(int64_t N);
-size_t chain_part_bytes(int64_t M, int64_t N);
-int chain_ctas();
-// The owner CTA of unit u of U units split over G CTAs (the kernel's partition).
-int chain_owner(int64_t u, int64_t U, int G);
-
 // The decode copy of a [K][N] 4-bit weight read by gemm_q4ts (fg_pack_weight),
 // in fg_pack_format `format`, and its size.
 fg_status pack_weight(const uint8_t* codes, const float* mins, const float* scales, int64_t K, int64_t N,
@@ -164,12 +138,9 @@ fg_status check_decode_attention(const fg_kv* kv, const void* q, int64_t ldq, in
 // q: [b][ldq] (head h at columns h*d..), out: [b][ldo].  When knew/vnew are
 // given ([b][ldnew] rows), the new token's K/V are first written to slot pos
 // (fused into the attention launch on the tensor-core path).
-// zero/zero_words (optional): words the launch sets to zero once the grids
-// before it have completed (the control words of the chain launched next).
 fg_status decode_attention(const fg_kv& kv, const void* q, int64_t ldq, const void* knew,
                            const void* vnew, int64_t ldnew, int64_t b, int64_t pos, void* out,
-                           int64_t ldo, void* ws, size_t ws_bytes, cudaStream_t st,
-                           unsigned* zero = nullptr, int64_t zero_words = 0);
+                           int64_t ldo, void* ws, size_t ws_bytes, cudaStream_t st);
 size_t decode_attention_workspace_bytes(int64_t b, int32_t heads, int32_t head_dim,
                                         int64_t capacity);
 fg_status decode_attention_simt(const fg_kv& kv, const void* q, int64_t ldq, int64_t b,

@@ -152,31 +152,7 @@ size_t w16_bytes(const fg_layer& L) {
   return up(L.h1 * L.h1 * 2) * 4 + up(L.h1 * L.h2 * 2) * 2;
 }
 
-// fp16 4-bit decode of a block of at most 64 sequences runs its products as
-// chains (chain.cu): [w_Q|w_K|w_V] of the first layer, then after each
-// layer's attention [w_O, w_1, w_2] and the next layer's [w_Q|w_K|w_V].
-bool decode_chained(const fg_layer& L, int64_t b) { return decode_needs_copies(L) && b >= 1 && b <= 64; }
-
-// Chain workspace of a decode step: the partial slots of the four products
-// and their control words (the largest chain: w_O, w_1, w_2, w_Q|w_K|w_V).
-struct ChainSpace {
-  size_t part, ctrl;
-};
-ChainSpace chain_space(const fg_layer& L, int64_t b) {
-  const int64_t N[4] = {L.h1, L.h2, L.h1, 3 * L.h1};
-  ChainSpace c;
-  c.part = chain_workspace_bytes(N, 4, b);
-  c.ctrl = 0;
-  for (int64_t n : N) c.ctrl += chain_ctrl_bytes(n);
-  return c;
-}
-
 size_t scratch_bytes(const fg_layer& L, int64_t M, int64_t capacity, bool decode) {
-  if (decode && decode_chained(L, M)) {
-    const ChainSpace c = chain_space(L, M);
-    return up(c.part) + up(c.ctrl) +
-           up(decode_attention_workspace_bytes(M, L.heads, static_cast<int32_t>(L.h1 / L.heads), capacity));
-  }
   int quant = L.codec == FG_CODEC_Q4G64;
   const bool packed = decode && decode_needs_copies(L);
   size_t w16 = 0;
@@ -257,45 +233,8 @@ fg_status run_prefill(const fg_layer& L, const void* x, int64_t b, int64_t s, co
   return FG_OK;
 }
 
-// One layer-step with chained products.  The layer's [w_Q|w_K|w_V] product
-// has already written B.qkv (by the previous chain, or by `first`).  If
-// `next` is given, the chain after attention also runs the next layer's
-// [w_Q|w_K|w_V] on this layer's output y, into B.qkv.
-fg_status run_decode_chained(const fg_layer& L, const void* t, int64_t b, int64_t pos, const fg_kv& kv,
-                             void* y, void* ws, const fg_layer* next, bool first, cudaStream_t st) {
-  const int64_t h1 = L.h1, h2 = L.h2;
-  Buffers B = carve(L, b, ws);
-  const ChainSpace cs = chain_space(L, b);
-  char* part = B.scratch;
-  unsigned* ctrl = reinterpret_cast<unsigned*>(B.scratch + up(cs.part));
-  char* attn_ws = B.scratch + up(cs.part) + up(cs.ctrl);
-  const size_t attn_bytes = decode_attention_workspace_bytes(b, L.heads, static_cast<int32_t>(h1 / L.heads), kv.capacity);
-  if (first) {
-    const fg_wmat qkv[3] = {L.wq, L.wk, L.wv};
-    const ChainLink link = {product(L, t, h1, b, qkv, 3, B.qkv, 3 * h1, nullptr, 0, 0), -1, -1};
-    FG_TRY(chain_run(&link, 1, part, cs.part, ctrl, cs.ctrl, false, st));
-  }
-  // Concat (t w_K, t w_V into slot pos), then Softmax(t_Q x_K^T / sqrt(d)) x_V;
-  // the launch also clears the control words of the chain that follows
-  const size_t e = dtype_bytes(L.dtype);
-  FG_TRY(decode_attention(kv, B.qkv, 3 * h1, B.qkv + h1 * e, B.qkv + 2 * h1 * e, 3 * h1, b, pos, B.att, h1,
-                          attn_ws, attn_bytes, st, ctrl, static_cast<int64_t>(cs.ctrl / sizeof(unsigned))));
-  ChainLink links[4];
-  links[0] = {product(L, B.att, h1, b, &L.wo, 1, B.xo, h1, t, h1, 0), -1, -1};        // t_Out = (..) w_O + t
-  links[1] = {product(L, B.xo, h1, b, &L.w1, 1, B.hid, h2, nullptr, 0, 1), 0, -1};    // relu(t_Out w_1)
-  links[2] = {product(L, B.hid, h2, b, &L.w2, 1, y, h1, B.xo, h1, 0), 1, 0};          // (..) w_2 + t_Out
-  int n = 3;
-  if (next) {
-    const fg_wmat qkv[3] = {next->wq, next->wk, next->wv};
-    links[3] = {product(*next, y, h1, b, qkv, 3, B.qkv, 3 * h1, nullptr, 0, 0), 2, -1};
-    n = 4;
-  }
-  return chain_run(links, n, part, cs.part, ctrl, cs.ctrl, true, st);
-}
-
 fg_status run_decode(const fg_layer& L, const void* t, int64_t b, int64_t pos, const fg_kv& kv,
                      void* y, void* ws, size_t scratch, cudaStream_t st) {
-  if (decode_chained(L, b)) return run_decode_chained(L, t, b, pos, kv, y, ws, nullptr, true, st);
   const int64_t h1 = L.h1, h2 = L.h2;
   Buffers B = carve(L, b, ws);
   const fg_wmat qkv[3] = {L.wq, L.wk, L.wv};
@@ -321,13 +260,6 @@ fg_status check_act(const void* p, const char* name) {
 }  // namespace
 
 fg_status gemm(const GemmArgs& a, void* ws, size_t ws_bytes, cudaStream_t st) {
-  if (chain_supported(a)) {
-    // a chain of one product
-    const size_t pb = chain_workspace_bytes(&a.N, 1, a.M), cb = chain_ctrl_bytes(a.N);
-    if (!ws || ws_bytes < pb + cb) return fail(FG_ERR_WORKSPACE, "decode product needs %zu workspace bytes", pb + cb);
-    const ChainLink link = {a, -1, -1};
-    return chain_run(&link, 1, ws, pb, reinterpret_cast<unsigned*>(static_cast<char*>(ws) + pb), cb, false, st);
-  }
   if (gemm_q4ts_supported(a)) return gemm_q4ts(a, ws, ws_bytes, st);
   if (a.dtype == FG_F16 && a.M >= 64 && a.quant) {
     // converted back to fp16 once into the workspace, then the dense product
@@ -353,7 +285,6 @@ fg_status gemm(const GemmArgs& a, void* ws, size_t ws_bytes, cudaStream_t st) {
 
 size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, fg_dtype dt, int quant, bool packed) {
   if (dt != FG_F16 || M <= 0) return 0;
-  if (quant && packed && M <= 64) return chain_workspace_bytes(&N, 1, M) + chain_ctrl_bytes(N);
   if (quant && packed && M <= 256) return gemm_q4ts_workspace_bytes(M, N, K);
   if (M < 64) return 0;
   const size_t tc = gemm_tc_workspace_bytes(M, N, K);
@@ -583,19 +514,10 @@ fg_status fg_decode_block_step(const fg_layer* layers, int32_t l, const void* t,
   if (!aligned(ws, kAlign)) return fail(FG_ERR_ALIGN, "workspace needs 256-byte alignment");
   char* ping[2] = {static_cast<char*>(ws) + up(layer_ws), static_cast<char*>(ws) + up(layer_ws) + act};
   const void* in = t;
-  bool chained = true;
-  for (int32_t i = 0; i < l; ++i) chained = chained && decode_chained(layers[i], b) && layers[i].h1 == layers[0].h1;
   for (int32_t i = 0; i < l; ++i) {
     void* out = (i == l - 1) ? y : ping[i & 1];
-    if (chained) {
-      // this layer's w_Q|w_K|w_V ran in the previous layer's chain (the first
-      // layer's runs alone); its chain runs the next layer's
-      FG_TRY(run_decode_chained(layers[i], in, b, pos, kvs[i], out, ws, i + 1 < l ? &layers[i + 1] : nullptr,
-                                i == 0, stream));
-    } else {
-      FG_TRY(run_decode(layers[i], in, b, pos, kvs[i], out, ws,
-                        scratch_bytes(layers[i], b, kvs[i].capacity, true), stream));
-    }
+    FG_TRY(run_decode(layers[i], in, b, pos, kvs[i], out, ws,
+                      scratch_bytes(layers[i], b, kvs[i].capacity, true), stream));
     in = out;
   }
   return FG_OK;

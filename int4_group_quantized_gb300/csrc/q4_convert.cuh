@@ -24,27 +24,17 @@ __host__ __device__ constexpr int block_bytes(int fmt) {
   return kBlkCodes + (fmt == FG_PACK_EXACT ? 1024 : 512);   // 5120 or 4608
 }
 
-// PRELOAD: load() also reads the fp32 pairs of FG_PACK_EXACT (32 more
-// registers), so that convert() issues no shared-memory load -- a load
-// issued after a tensor-memory store waits for that store.
-template <int FMT, bool PRELOAD = false>
+template <int FMT>
 struct BlockConverter {
   uint4 w0, w1, pv[4];
-  float4 pf[PRELOAD ? 8 : 1];
   const uint8_t* blk;
 
   // Shared-memory loads of what this thread converts: its code words (the
-  // fp16 pairs too, for FG_PACK_F16META; the fp32 pairs with PRELOAD, else
-  // convert reads them).
+  // fp16 pairs too, for FG_PACK_F16META; the fp32 pairs are read by convert).
   __device__ __forceinline__ void load(const uint8_t* block, int q, int lane) {
     blk = block;
     w0 = *reinterpret_cast<const uint4*>(block + q * 1024 + lane * 16);
     w1 = *reinterpret_cast<const uint4*>(block + q * 1024 + 512 + lane * 16);
-    if (FMT == FG_PACK_EXACT && PRELOAD) {
-      const float4* pr = reinterpret_cast<const float4*>(block + kBlkCodes + (q >> 1) * 512) + (lane & 3);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) pf[PRELOAD ? i : 0] = pr[4 * i];
-    }
     if (FMT == FG_PACK_F16META) {
       const uint4* pr = reinterpret_cast<const uint4*>(block + kBlkCodes + (q >> 1) * 256) + (lane & 3);
 #pragma unroll
@@ -62,7 +52,7 @@ struct BlockConverter {
       const float4* pr = reinterpret_cast<const float4*>(blk + kBlkCodes + (q >> 1) * 512) + c4;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const float4 sm = PRELOAD ? pf[PRELOAD ? i : 0] : pr[4 * i];   // (scale[2j], scale[2j+1], min[2j], min[2j+1]), j = 4i + c4
+        const float4 sm = pr[4 * i];   // (scale[2j], scale[2j+1], min[2j], min[2j+1]), j = 4i + c4
         const uint4 cw = i < 4 ? w0 : w1;
         const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
         const int e = i & 3;
@@ -93,54 +83,6 @@ struct BlockConverter {
                         : hfma2_u(hfma2_u(lop_mask_or(x, 0x000F000Fu, kMagic), kOne, kNegMagic), s2, m2);
           }
         }
-      }
-    }
-  }
-};
-
-// Half a block: the k pairs j = 4i + t%4 with i in [4h, 4h + 4) (16 of the
-// block's 32 TMEM columns), a[16] in the register order of two 16x128b.x4
-// tensor-memory stores (lanes 0..15, then 16..31 of the quarter).  Two warps
-// per lane quarter convert a block between them.
-template <int FMT>
-struct HalfConverter {
-  uint4 w, pv[2];
-  float4 pf[4];
-
-  __device__ __forceinline__ void load(const uint8_t* block, int q, int lane, int h) {
-    w = *reinterpret_cast<const uint4*>(block + q * 1024 + h * 512 + lane * 16);
-    if (FMT == FG_PACK_EXACT) {
-      const float4* pr = reinterpret_cast<const float4*>(block + kBlkCodes + (q >> 1) * 512) + (lane & 3);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) pf[i] = pr[4 * (4 * h + i)];
-    } else {
-      const uint4* pr = reinterpret_cast<const uint4*>(block + kBlkCodes + (q >> 1) * 256) + (lane & 3);
-#pragma unroll
-      for (int u = 0; u < 2; ++u) pv[u] = pr[4 * (2 * h + u)];
-    }
-  }
-
-  __device__ __forceinline__ void convert(uint32_t (&a)[16]) const {
-    const uint32_t words[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {   // i = the half's k-pair column 4i + t%4; nibble slots i and i+4
-      uint32_t s2 = 0, m2 = 0;
-      if (FMT == FG_PACK_F16META) {
-        s2 = (i & 1) ? pv[i >> 1].z : pv[i >> 1].x;
-        m2 = (i & 1) ? pv[i >> 1].w : pv[i >> 1].y;
-      }
-#pragma unroll
-      for (int ww = 0; ww < 4; ++ww) {
-        const uint32_t x = i >= 2 ? words[ww] >> 8 : words[ww];
-        const uint32_t hm = lop_mask_or(x, (i & 1) ? 0x00F000F0u : 0x000F000Fu, kMagic);
-        uint32_t r;
-        if (FMT == FG_PACK_EXACT) {
-          const float2 qq = (i & 1) ? nib16_pair_f32(hm) : nib_pair_f32(hm);
-          r = cvt_f16x2(fma_f32x2(qq, make_float2(pf[i].x, pf[i].y), make_float2(pf[i].z, pf[i].w)));
-        } else {
-          r = (i & 1) ? hfma2_u(hfma2_u(hm, kSixteenth, kNeg64), s2, m2) : hfma2_u(hfma2_u(hm, kOne, kNegMagic), s2, m2);
-        }
-        a[8 * (ww >> 1) + 2 * i + (ww & 1)] = r;
       }
     }
   }
