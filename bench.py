@@ -47,6 +47,40 @@ Q4 = 0.5 + 8.0 / 64.0   # bytes per element: 4-bit code + fp32 (min, scale) per 
 PACK_BYTES = {0: Q4, 1: 0.5 + 4.0 / 64.0}
 
 
+# DRAM traffic of the dominant decode kernel class from one ncu capture
+# (profiles/gemm_q4ts_qkv_opt-6.7b_b64.md): dram__bytes_read.sum +
+# dram__bytes_write.sum of x.[w_Q w_K w_V] (M = 64, K = 4096, N = 12288),
+# averaged over 4 launches, beside that launch's algorithmic bytes (weights as
+# stored + X read + Y written).  Valid only for the kernel sources it was
+# taken on (their hash); scaled to the class's average launch by algorithmic
+# bytes (the products differ only in size, and the capture reads each weight
+# byte once).
+TRAFFIC = {"gemm_q4_decode": {
+    "sources": ("int4_group_quantized_gb300/csrc/gemm_q4ts.cu", "int4_group_quantized_gb300/csrc/q4_convert.cuh",
+                "int4_group_quantized_gb300/csrc/q4_dev.cuh", "int4_group_quantized_gb300/csrc/tc_ptx.cuh"),
+    "sha256_16": ("c933a8f2578eb58b", "bdc48444633d6cb6", "360d7c9967f0a780", "9dc843e43182b935"),
+    "dram_bytes": 32036864.0,
+    "algorithmic_bytes": 4096 * 12288 * Q4 + 2 * 64 * (4096 + 3 * 4096),
+    "capture": "ncu, x.[w_Q w_K w_V] M=64 K=4096 N=12288, mean of 4 launches"}}
+
+
+def traffic_per_launch(kernel: str, algorithmic_per_launch: float):
+    """Measured DRAM bytes per launch of `kernel`, scaled from its capture,
+    or None when the capture does not match the current sources."""
+    import hashlib
+    t = TRAFFIC.get(kernel)
+    if t is None:
+        return None
+    for path, want in zip(t["sources"], t["sha256_16"]):
+        try:
+            got = hashlib.sha256(open(os.path.join(ROOT, path), "rb").read()).hexdigest()[:16]
+        except OSError:
+            return None
+        if got != want:
+            return None
+    return t["dram_bytes"] / t["algorithmic_bytes"] * algorithmic_per_launch
+
+
 def peaks() -> dict:
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -393,6 +427,10 @@ def run_ours(args, w, rank, world, device):
         roof.update({"launches": cnt, "avg_launch_us": ms / cnt * 1e3,
                      "algorithmic_per_launch": (byts if roof["unit"] == "GB/s" else flops) / cnt,
                      "peak_source": pk["source"] + (" sustained" if roof["unit"] == "TFLOP/s" else "")})
+        if roof["unit"] == "GB/s":
+            tr = traffic_per_launch(dom, byts / cnt)
+            roof["traffic"] = tr
+            roof["traffic_source"] = TRAFFIC[dom]["capture"] + ", scaled by algorithmic bytes" if tr else None
     roof_pre = None
     g_pre = {k: v for k, v in pre_prof.items() if k.startswith("gemm")}
     if g_pre:
