@@ -164,6 +164,48 @@ def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, q_pos: np.ndarray) ->
     return np.einsum("bhqk,bhkd->bqhd", p, v)
 
 
+
+def topk_keep(tokens: int, percent: int = 10) -> int:
+    """How many tokens the sparse approximation keeps: the top `percent` per
+    cent of `tokens`, rounded up, and at least one ("5. 近似方法", sparse
+    attention: the top 10% of the value cache).  Integer arithmetic, so that
+    e.g. 530 tokens keep 53, not the 54 a float ceil(0.1 * 530) gives."""
+    assert tokens >= 1 and 1 <= percent <= 100
+    return max(1, (tokens * percent + 99) // 100)
+
+
+def attention_topk(q: np.ndarray, k: np.ndarray, v: np.ndarray, keep: int):
+    """Top-K sparse decode attention ("5. 近似方法", sparse attention).
+
+    q: [b][H][d], one query per (sequence, head) at the newest slot;
+    k, v: [b][H][T][d], every one of the T cached tokens visible.
+    The page's steps, in its order:
+      1. the attention matrix: p = Softmax(q k^T / sqrt(d)) over all T tokens;
+      2. for each query, the indices of its `keep` largest entries (Top-K);
+      3. the other tokens are dropped, and only the selected rows of V are
+         read: out = sum over the selected i of p_i v_i.
+    Readings: the kept weights are the ones step 1 computed over all tokens
+    (the page drops tokens after the attention matrix exists, and says
+    nothing of renormalising); among equal scores the lower token index
+    ranks first; keep >= T keeps every token (dense attention).
+    Returns (out [b][H][d], idx [b][H][min(keep, T)] ascending)."""
+    b, H, T, d = k.shape
+    kk = min(keep, T)
+    scores = np.einsum("bhd,bhtd->bht", q, k) / np.sqrt(d)
+    mx = scores.max(axis=-1, keepdims=True)
+    p = np.exp(scores - mx)
+    p = p / p.sum(axis=-1, keepdims=True)
+    out = np.zeros((b, H, d))
+    idx = np.zeros((b, H, kk), np.int64)
+    for bi in range(b):
+        for h in range(H):
+            # descending score, ties by ascending index (lexsort: last key is primary)
+            order = np.lexsort((np.arange(T), -scores[bi, h]))
+            sel = np.sort(order[:kk])
+            idx[bi, h] = sel
+            out[bi, h] = p[bi, h, sel] @ v[bi, h, sel]
+    return out, idx
+
 def _relu(a: np.ndarray) -> np.ndarray:
     return np.maximum(a, 0.0)
 
