@@ -176,6 +176,13 @@ def decode_attn_bytes(w, b, length) -> float:
     return 2 * b * w.h1 * length * Q4 + 2 * b * w.h1 * Q4 + 2 * b * w.h1 * 4
 
 
+def topk_attn_bytes(w, length, keep) -> float:
+    """Top-K sparse attention alone (nothing appended): every K row of
+    `length` tokens, `keep` V rows per (sequence, head), q and the output
+    (fp16)."""
+    return w.b * w.h1 * length * Q4 + w.b * w.heads * min(keep, length) * w.head_dim * Q4 + 2 * w.b * w.h1 * 2
+
+
 def prefill_product_flops(w, b, s) -> float:
     return 2.0 * b * s * (4 * w.h1 * w.h1 + 2 * w.h1 * w.h2)
 
@@ -509,7 +516,7 @@ def finite_layer_steps(fg, w, L, dev, st, steps: int) -> dict:
 
 
 CASES = ("linear-qkv", "linear-o", "linear-fc1", "linear-fc2", "prefill-linear-fc1", "attn-decode",
-         "prefill-layer")
+         "attn-decode-topk", "prefill-layer")
 
 
 def run_case(args, w, device):
@@ -550,7 +557,7 @@ def run_case(args, w, device):
         y = torch.empty_like(x)
         ws = fg.workspace(max(fg.fg_prefill_workspace_bytes(L, w.b, w.s),
                               fg.fg_decode_workspace_bytes(L, w.b, w.s + w.n)), dev)
-        if name == "attn-decode":
+        if name.startswith("attn-decode"):
             kv_bytes = 2 * w.b * w.h1 * (w.s + w.n) * 0.625
             kvs = [fg.KVCache(w.b, w.heads, w.head_dim, w.s + w.n, True, dt, dev)
                    for _ in range(max(2, int(-(-l2 // kv_bytes))))]
@@ -559,11 +566,21 @@ def run_case(args, w, device):
             q = synth.normal((w.b, w.h1), 9, 1.0, dt, dev)
             out = torch.empty_like(q)
             pos = w.s + w.n // 2
-            calls = [lambda kv=kv: fg.fg_decode_attention(kv, q, pos, out) for kv in kvs]
+            if name == "attn-decode-topk":
+                keep = fg.topk_keep(pos + 1)
+                calls = [lambda kv=kv: fg.fg_decode_attention_topk(kv, q, pos, keep, out) for kv in kvs]
+                algo = topk_attn_bytes(w, pos + 1, keep)
+            else:
+                calls = [lambda kv=kv: fg.fg_decode_attention(kv, q, pos, out) for kv in kvs]
+                algo = 2 * w.b * w.h1 * (pos + 1) * Q4 + 2 * w.b * w.h1 * 2   # K, V; q and the output
         else:
             kv = fg.KVCache(w.b, w.heads, w.head_dim, w.s + w.n, True, dt, dev)
             calls = [lambda: fg.fg_prefill_layer(L, x, kv, y, ws)]
         shape = {"b": w.b, "s": w.s, "h1": w.h1, "heads": w.heads, "copies": len(calls)}
+        if name.startswith("attn-decode"):
+            shape.update({"len": pos + 1, "algorithmic_bytes": algo})
+            if name == "attn-decode-topk":
+                shape["keep"] = keep
     reps = max(1, 16 // len(calls)) * len(calls) if len(calls) < 16 else len(calls)
     side = torch.cuda.Stream(device=dev)
     side.wait_stream(torch.cuda.current_stream(dev))
@@ -586,8 +603,11 @@ def run_case(args, w, device):
     e1.record()
     e1.synchronize()
     fg.fg_sync_status()
-    print(json.dumps({"case": name, "workload": w.name, "shape": shape, "calls_per_replay": reps,
-                      "us_per_call": e0.elapsed_time(e1) / (args.steps * reps) * 1e3}), flush=True)
+    us = e0.elapsed_time(e1) / (args.steps * reps) * 1e3
+    rec = {"case": name, "workload": w.name, "shape": shape, "calls_per_replay": reps, "us_per_call": us}
+    if "algorithmic_bytes" in shape:
+        rec["achieved_gbs"] = shape["algorithmic_bytes"] / (us * 1e-6) / 1e9
+    print(json.dumps(rec), flush=True)
 
 
 def main():

@@ -214,6 +214,24 @@ size_t fg_decode_attention_workspace_bytes(const fg_kv* kv);
 fg_status fg_decode_attention(const fg_kv* kv, const void* q, int64_t ldq, int64_t pos, void* out,
                               int64_t ldo, void* ws, size_t ws_bytes, cudaStream_t stream);
 
+/* [S5] sparse attention ("4-bit-S"): decode attention that keeps, for each
+ * sequence and head, only the `keep` tokens of slots 0..pos with the largest
+ * scores q.k/sqrt(head_dim) and reads only their rows of V:
+ *   out = sum over the kept i of p_i v_i,  p = Softmax(q K^T / sqrt(d))
+ * over ALL pos+1 tokens (the kept weights are not renormalised).  Among equal
+ * scores the lower slot ranks first.  keep >= pos+1 keeps every token (dense
+ * attention); the page's setting keeps the top 10%, ceil((pos+1)/10).
+ * q, out, ldq, ldo as for fg_decode_attention; nothing is appended.
+ * idx: optional device int32 [kv->b][heads][min(keep, pos+1)], 4-byte
+ * aligned, receives the kept slots of each (sequence, head) in ascending
+ * order; NULL to skip.  Needs a 4-bit cache with fp16 activations and
+ * pos+1 <= 16384 (else FG_ERR_UNSUPPORTED); keep < 1 -> FG_ERR_ARG; pos
+ * outside [0, capacity) -> FG_ERR_CAPACITY.  No workspace.  Asynchronous on
+ * `stream`.  A cache holding NaN gives NaN outputs; which slots are then
+ * reported is unspecified. */
+fg_status fg_decode_attention_topk(const fg_kv* kv, const void* q, int64_t ldq, int64_t pos, int64_t keep,
+                                   void* out, int64_t ldo, int32_t* idx, cudaStream_t stream);
+
 /* fg_decode_attention for callers that cannot allocate device memory: code
  * embedded in a host application that owns the GPU memory pool and forbids
  * other allocations, or a latency-critical loop that cannot afford the

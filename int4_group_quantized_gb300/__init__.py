@@ -451,3 +451,25 @@ def fg_decode_attention_noalloc(kv: KVCache, q: torch.Tensor, pos: int, out: tor
                                             out.stride(0), _stream(stream)),
            "fg_decode_attention_noalloc")
 
+
+
+_sig("fg_decode_attention_topk", _INT, ctypes.POINTER(fg_kv), _P, _I64, _I64, _I64, _P, _I64, _P, _P)
+
+
+def fg_decode_attention_topk(kv: KVCache, q: torch.Tensor, pos: int, keep: int, out: torch.Tensor,
+                             idx: torch.Tensor | None = None, stream=None) -> None:
+    """Top-K sparse decode attention: per (sequence, head), only the `keep`
+    highest-scoring tokens of slots 0..pos, weighted by the softmax over all
+    of them.  idx (int32 [b][heads][min(keep, pos+1)]) receives the kept
+    slots in ascending order when given."""
+    if idx is not None and idx.dtype != torch.int32:
+        raise TypeError("idx must be int32")
+    _check(_lib.fg_decode_attention_topk(ctypes.byref(kv.struct), _ptr(q), q.stride(0), int(pos), int(keep),
+                                         _ptr(out), out.stride(0), _ptr(idx), _stream(stream)),
+           "fg_decode_attention_topk")
+
+
+def topk_keep(tokens: int, percent: int = 10) -> int:
+    """The page's sparse setting: the top `percent` per cent of the tokens,
+    rounded up, at least one."""
+    return max(1, (int(tokens) * int(percent) + 99) // 100)

@@ -63,7 +63,7 @@ namespace {
 const char* const kClassNames[KC_COUNT] = {
     "quantize_g64", "dequant_g64", "kv_store_q4", "gemm_simt", "gemm_tc",
     "gemm_splitk_reduce", "attn_decode", "attn_decode_combine", "attn_prefill", "gemm_q4_decode",
-    "pack_weight"};
+    "pack_weight", "attn_decode_topk"};
 
 // Launches of the same class that follow one another on a stream form one
 // timed run (one event pair): events between them would break the overlap

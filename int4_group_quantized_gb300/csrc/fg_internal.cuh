@@ -14,6 +14,13 @@ namespace fg {
 fg_status fail(fg_status s, const char* fmt, ...);
 // Maps cudaGetLastError() after a launch to FG_OK / FG_ERR_CUDA.
 fg_status check_launch(const char* what);
+// Return the status of `expr` when it is not FG_OK.
+#define FG_TRY(expr)                 \
+  do {                               \
+    fg_status _s = (expr);           \
+    if (_s != FG_OK) return _s;      \
+  } while (0)
+
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 inline size_t dtype_bytes(fg_dtype d) { return d == FG_F16 ? 2 : 4; }
 // Number of SMs of the current device (cached per device).
@@ -46,6 +53,7 @@ enum KernelClass : int {
   KC_ATTN_PREFILL,
   KC_GEMM_Q4DEC,
   KC_PACK,
+  KC_ATTN_TOPK,
   KC_COUNT
 };
 constexpr int kProfilePhases = 4;
@@ -145,6 +153,16 @@ size_t decode_attention_workspace_bytes(int64_t b, int32_t heads, int32_t head_d
                                         int64_t capacity);
 fg_status decode_attention_simt(const fg_kv& kv, const void* q, int64_t ldq, int64_t b,
                                 int64_t pos, void* out, int64_t ldo, cudaStream_t st);
+// Top-K sparse decode attention (one CTA per (sequence, head), no split):
+// the keep largest scores of each query, ties to the lower index, weighted
+// by the softmax over all tokens; knew/vnew as for decode_attention.  idx,
+// when given, receives the kept slots [b][heads][min(keep, pos+1)] in
+// ascending order.
+fg_status check_decode_attention_topk(const fg_kv* kv, const void* q, int64_t ldq, int64_t pos, int64_t keep,
+                                      const void* out, int64_t ldo, const int32_t* idx);
+fg_status decode_attention_topk(const fg_kv& kv, const void* q, int64_t ldq, const void* knew, const void* vnew,
+                                int64_t ldnew, int64_t pos, int64_t keep, void* out, int64_t ldo, int32_t* idx,
+                                cudaStream_t st);
 // Prefill: causal attention of s queries per sequence over slots 0..s-1.
 // q: [b*s][ldq]; out: [b*s][ldo].  Tensor cores for a 4-bit fp16 cache,
 // CUDA cores otherwise.

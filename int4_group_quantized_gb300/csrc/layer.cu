@@ -190,12 +190,6 @@ Buffers carve(const fg_layer& L, int64_t M, void* ws) {
   return B;
 }
 
-#define FG_TRY(expr)                 \
-  do {                               \
-    fg_status _s = (expr);           \
-    if (_s != FG_OK) return _s;      \
-  } while (0)
-
 fg_status run_prefill(const fg_layer& L, const void* x, int64_t b, int64_t s, const fg_kv& kv,
                       void* y, void* ws, size_t scratch, cudaStream_t st) {
   const int64_t M = b * s, h1 = L.h1, h2 = L.h2;

@@ -142,6 +142,29 @@ def test_noalloc_attention_host_errors(fg):
     assert L.fg_decode_attention_noalloc(ctypes.byref(kv), P, 100, 3, P, 128, None) == 2    # ldq
 
 
+def test_topk_attention_host_errors(fg):
+    """fg_decode_attention_topk rejects bad arguments on the host, before any
+    CUDA call (these need no GPU)."""
+    L = fg.lib
+    P = ctypes.c_void_p(4096)
+    kv = _kv(fg, cap=16, heads=2, d=64)
+    assert L.fg_decode_attention_topk(None, P, 128, 3, 2, P, 128, None, None) == 1             # null kv
+    assert L.fg_decode_attention_topk(ctypes.byref(kv), P, 128, 3, 0, P, 128, None, None) == 1  # keep < 1
+    assert L.fg_decode_attention_topk(ctypes.byref(kv), P, 128, 16, 2, P, 128, None, None) == 4  # pos
+    assert L.fg_decode_attention_topk(ctypes.byref(kv), P, 100, 3, 2, P, 128, None, None) == 2   # ldq
+    assert L.fg_decode_attention_topk(ctypes.byref(kv), P, 128, 3, 2, P, 128,
+                                      ctypes.c_void_p(4098), None) == 3                          # idx alignment
+    f32 = _kv(fg, cap=16, heads=2, d=64, dtype=1)
+    assert L.fg_decode_attention_topk(ctypes.byref(f32), P, 128, 3, 2, P, 128, None, None) == 8
+    dense = _kv(fg, cap=16, heads=2, d=64, codec=0)
+    assert L.fg_decode_attention_topk(ctypes.byref(dense), P, 128, 3, 2, P, 128, None, None) == 8
+    long = _kv(fg, cap=20000, heads=2, d=64)
+    assert L.fg_decode_attention_topk(ctypes.byref(long), P, 128, 16384, 2, P, 128, None, None) == 8
+    empty = _kv(fg, b=0, cap=16, heads=2, d=64)
+    assert L.fg_decode_attention_topk(ctypes.byref(empty), None, 128, 3, 2, None, 128, None, None) == 0
+    assert fg.topk_keep(528) == 53 and fg.topk_keep(530) == 53 and fg.topk_keep(1) == 1
+
+
 def test_noalloc_scratch_bound_covers_every_cache(fg):
     """The built-in split scratch (1 MiB) holds what the split rule asks for,
     for every block size and cache capacity up to 4096 with head_dim 64 and
