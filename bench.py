@@ -398,7 +398,7 @@ def run_ours(args, w, rank, world, device):
     # N(0, 1) input at every step (the chained stack above overflows fp16 after
     # a few layers: the page's layer has no normalisation); per-kernel device
     # time per layer-step, beside the chained run's
-    finite = finite_layer_steps(fg, w, layers[w.l // 2], dev, st, args.steps)
+    finite, topk = finite_layer_steps(fg, w, layers[w.l // 2], dev, st, args.steps)
 
     if rank != 0:
         return
@@ -483,6 +483,7 @@ def run_ours(args, w, rank, world, device):
             "chained_us_per_layer_step": {k.split(":", 1)[1]: round(v[1] / (w.l * w.n * K) * 1e3, 2)
                                           for k, v in ((f"decode:{a}", b) for a, b in dec_prof.items())},
             "finite_us_per_layer_step": finite},
+        "topk_attention_4bit_s": topk,
         "clocks": clocks, "wall_s_timed": t_wall,
     }
     print(json.dumps(line), flush=True)
@@ -512,7 +513,36 @@ def finite_layer_steps(fg, w, L, dev, st, steps: int) -> dict:
         assert torch.isfinite(out).all(), "finite-data decode produced a non-finite output"
         for name, (cnt, ms) in prof.items():
             total[name] = total.get(name, 0.0) + ms
-    return {name: round(ms / (w.n * max(1, steps)) * 1e3, 2) for name, ms in total.items()}
+    per_step = {name: round(ms / (w.n * max(1, steps)) * 1e3, 2) for name, ms in total.items()}
+    return per_step, topk_attention_timing(fg, w, kv, dev, st)
+
+
+def topk_attention_timing(fg, w, kv, dev, st, calls: int = 10) -> dict:
+    """Top-K sparse attention (the page's 4-bit-S setting, the top 10% of the
+    tokens) over a full finite cache of s + n tokens: device time per call,
+    L2 flushed before each call (the cache's K alone is below L2's size)."""
+    length = w.s + w.n
+    keep = fg.topk_keep(length)
+    q = synth.normal((w.b, w.h1), 5, 1.0, synth.torch_dtype(w.act), dev)
+    out = torch.empty_like(q)
+    flush = torch.empty(3 * 129 * 2 ** 20 // 4, dtype=torch.float32, device=dev)
+    ms = []
+    with torch.cuda.stream(st):
+        for k in range(calls + 3):
+            flush.fill_(float(k))
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            fg.fg_decode_attention_topk(kv, q, length - 1, keep, out, stream=st)
+            e1.record(st)
+            e1.synchronize()
+            if k >= 3:
+                ms.append(e0.elapsed_time(e1))
+    fg.fg_sync_status()
+    us = statistics.mean(ms) * 1e3
+    byts = topk_attn_bytes(w, length, keep)
+    return {"tokens": length, "keep": keep, "us_per_call": round(us, 2), "algorithmic_bytes": byts,
+            "achieved_gbs": round(byts / (us * 1e-6) / 1e9, 1),
+            "dense_bytes_same_cache": 2 * w.b * w.h1 * length * Q4 + 2 * w.b * w.h1 * 2}
 
 
 CASES = ("linear-qkv", "linear-o", "linear-fc1", "linear-fc2", "prefill-linear-fc1", "attn-decode",

@@ -33,6 +33,8 @@ struct DecodeArgs {
   int64_t cap;
   int splits;
   int tps;             // tokens per split (multiple of 16)
+  unsigned int* err;   // device error word (bounded waits of the staged kernels)
+  uint32_t wait_limit; // polls of a bounded wait
 };
 
 __device__ __forceinline__ uint32_t lop_mask_or(uint32_t x, uint32_t mask, uint32_t magic) {

@@ -3,7 +3,7 @@
 // each query keeps the indices of its Top-K tokens in the K cache, the other
 // tokens are dropped, and only those rows of the V cache are read).
 //
-// One CTA (8 warps) per (sequence, head), all tokens 0..pos visible:
+// One CTA (4 warps) per (sequence, head), all tokens 0..pos visible:
 //   1. scores.  Every K row is read, 16-token blocks per warp.  Unlike the
 //      dense kernel, each K value is first restored exactly as the format
 //      gives it, fp16(fmaf(c, scale, min)) ("converted back to FP16 before
@@ -38,10 +38,12 @@ namespace fg {
 namespace {
 
 using namespace attn;
+using namespace tc;
 
-constexpr int kTopkWarps = 8;
+constexpr int kTopkWarps = 4;
 constexpr int kTopkThreads = 32 * kTopkWarps;
 constexpr int64_t kTopkMaxLen = 16384;   // scores + list in shared memory: 8 bytes per token
+constexpr int kChunk = 128;              // tokens of K staged in shared memory at a time
 
 // q of one (sequence, head) as this lane's m16n8k16 B fragments, in the
 // order in which the K code words give their nibbles (the dense kernel's
@@ -134,17 +136,33 @@ __device__ __forceinline__ int block_excl_scan(int v, int* wsum, int& total) {
   return base + x - v;
 }
 
+// Shared memory of one CTA (dynamic): two staging buffers of kChunk tokens'
+// K codes and their (scale, min) pairs, then the scores of all tokens and
+// the list of kept tokens.
 template <int D>
-__global__ void __launch_bounds__(kTopkThreads) decode_attn_topk_kernel(const DecodeArgs a, int keep,
+struct TopkLayout {
+  static constexpr int NG = D / 64;
+  static constexpr int kCodes = kChunk * D / 2;          // bytes of one chunk's codes
+  static constexpr int kMeta = kChunk * NG * 2 * 4;      // its (scale, min) pairs
+  static constexpr int kBuf = kCodes + kMeta;
+  static constexpr int kFixed = 2 * kBuf + 16 * 2;       // + the two mbarriers
+  static size_t bytes(int64_t len, int64_t nsel) { return kFixed + static_cast<size_t>(len + nsel) * 4; }
+};
+
+template <int D>
+__global__ void __launch_bounds__(kTopkThreads, 8) decode_attn_topk_kernel(const DecodeArgs a, int keep,
                                                                          int32_t* __restrict__ idx_out) {
   constexpr int NG = D / 64;
-  constexpr int DPL = D / 32;   // value dims per lane
-  extern __shared__ float sc[];   // [len] base-2 scores, then int list[nsel]
+  using Lay = TopkLayout<D>;
+  extern __shared__ __align__(128) uint8_t dsm[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(dsm + 2 * Lay::kBuf);   // chunk buffer b has landed
+  float* sc = reinterpret_cast<float*>(dsm + Lay::kFixed);              // [len] base-2 scores
   __shared__ int hist[256];
   __shared__ int wsum[kTopkWarps];
   __shared__ float redf[kTopkWarps];
   __shared__ uint32_t sel_key;
   __shared__ int sel_need;
+  __shared__ int abort_flag;
   __shared__ float red_o[kTopkWarps][D];
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -156,6 +174,15 @@ __global__ void __launch_bounds__(kTopkThreads) decode_attn_topk_kernel(const De
   const int nsel = min(keep, len);
   const int64_t slot0 = static_cast<int64_t>(bh) * a.cap;
   int* list = reinterpret_cast<int*>(sc + len);
+  volatile int* abort = &abort_flag;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&full[0], 1);
+    mbar_init(&full[1], 1);
+    abort_flag = 0;
+    mbar_fence_init();
+  }
+  __syncthreads();
 
   tc::griddep_launch();
   tc::griddep_wait();
@@ -163,56 +190,95 @@ __global__ void __launch_bounds__(kTopkThreads) decode_attn_topk_kernel(const De
   if (a.knew != nullptr) {   // Concat first: the new token is one of the candidates
     if (warp == 0) append_token<D>(a, slot0, bi, h, lane);
     __syncthreads();
+    tc::fence_proxy_async_global();   // the appended codes, then the bulk copies that read them
   }
 
-  // ---- 1. scores of every token -------------------------------------------------
+  // ---- 1. scores of every token, K staged chunk by chunk ---------------------------
   uint32_t qb[NG][4][2];
   setup_q_plain<D>(qb, a.q + bi * a.ldq + h * D, tig);
+  const int nch = (len + kChunk - 1) / kChunk;
+  // chunk c into buffer c & 1: its codes by one bulk copy (thread 0), its
+  // (scale, min) pairs by 4-byte asynchronous copies (all threads, one group)
+  // Thread 0's record of the bulk copies: the last chunk it issued and the
+  // last it saw land; after a wait gives up, no chunk is issued and the ones
+  // in between are drained before the CTA leaves.
+  int issued = -1, landed = -1;
+  auto issue = [&](int c) {
+    const int t0 = c * kChunk, n = min(kChunk, len - t0);
+    uint8_t* buf = dsm + (c & 1) * Lay::kBuf;
+    const bool go = !*abort;
+    if (threadIdx.x == 0 && go) {
+      mbar_expect_tx(&full[c & 1], static_cast<uint32_t>(n * (D / 2)));
+      bulk_load(buf, a.kc + (slot0 + t0) * (D / 2), static_cast<uint32_t>(n * (D / 2)), &full[c & 1]);
+      issued = c;
+    }
+    float* meta = reinterpret_cast<float*>(buf + Lay::kCodes);   // [tok][g][scale, min]
+    if (go) {
+      for (int e = threadIdx.x; e < n * NG; e += kTopkThreads) {
+        const int64_t src = (slot0 + t0) * NG + e;
+        cp_async4(meta + 2 * e, a.kscale + src);
+        cp_async4(meta + 2 * e + 1, a.kmin + src);
+      }
+    }
+    cp_async_commit();   // one group per chunk in every thread, empty or not
+  };
+  issue(0);
   {
     constexpr float kQs = score_scale_log2<D>();
-    const int nblk = (len + 15) / 16;
-    uint2 kw[2][2][NG];
-    float ksc[2][2][NG], kmn[2][2][NG];
-    auto load = [&](int blk, int buf) {
+    for (int c = 0; c < nch; ++c) {
+      // buffer (c+1) & 1 was last read in chunk c-1, which ended with a CTA barrier
+      if (c + 1 < nch) {
+        issue(c + 1);
+        cp_async_wait<1>();   // this thread's copies of chunk c are done
+      } else {
+        cp_async_wait<0>();
+      }
+      // one thread waits for the codes (the others would spend issue slots
+      // polling); the CTA barrier then releases the rest
+      if (threadIdx.x == 0 && !*abort && mbar_wait(&full[c & 1], (c >> 1) & 1, a.wait_limit, abort)) landed = c;
+      __syncthreads();   // chunk c's codes have landed; every thread's pair copies are visible
+      const int t0 = c * kChunk, n = min(kChunk, len - t0);
+      const uint8_t* codes = dsm + (c & 1) * Lay::kBuf;
+      const float* meta = reinterpret_cast<const float*>(codes + Lay::kCodes);
+      if (!*abort) {
+        for (int blk = warp; blk * 16 < n; blk += kTopkWarps) {
+          uint2 kw[2][NG];
+          float ksc[2][NG], kmn[2][NG];
 #pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const int tok = blk * 16 + gq + 8 * r;
-        const int64_t slot = slot0 + tok;
+          for (int r = 0; r < 2; ++r) {
+            const int row = blk * 16 + gq + 8 * r;
 #pragma unroll
-        for (int g = 0; g < NG; ++g) {
-          if (tok < len) {
-            kw[buf][r][g] = __ldcs(reinterpret_cast<const uint2*>(a.kc + slot * (D / 2) + g * 32 + 8 * tig));
-            ksc[buf][r][g] = a.kscale[slot * NG + g];
-            kmn[buf][r][g] = a.kmin[slot * NG + g];
-          } else {
-            kw[buf][r][g] = make_uint2(0u, 0u);
-            ksc[buf][r][g] = kmn[buf][r][g] = 0.0f;
+            for (int g = 0; g < NG; ++g) {
+              const bool v = row < n;
+              kw[r][g] = v ? *reinterpret_cast<const uint2*>(codes + row * (D / 2) + g * 32 + 8 * tig)
+                           : make_uint2(0u, 0u);
+              ksc[r][g] = v ? meta[(row * NG + g) * 2] : 0.0f;
+              kmn[r][g] = v ? meta[(row * NG + g) * 2 + 1] : 0.0f;
+            }
+          }
+          float s0, s1;
+          block_scores_f16<NG>(qb, kw, ksc, kmn, s0, s1);
+          const int row = blk * 16 + gq;
+          if (tig == 0) {
+            if (row < n) sc[t0 + row] = s0 * kQs;
+            if (row + 8 < n) sc[t0 + row + 8] = s1 * kQs;
           }
         }
       }
-    };
-    auto score = [&](int blk, int buf) {
-      float s0, s1;
-      block_scores_f16<NG>(qb, kw[buf], ksc[buf], kmn[buf], s0, s1);
-      const int t0 = blk * 16 + gq;
-      if (tig == 0) {
-        if (t0 < len) sc[t0] = s0 * kQs;
-        if (t0 + 8 < len) sc[t0 + 8] = s1 * kQs;
-      }
-    };
-    // two buffers: the next block's loads are in flight while this one computes
-    int blk = warp;
-    if (blk < nblk) load(blk, 0);
-    for (; blk < nblk; blk += 2 * kTopkWarps) {
-      const int b1 = blk + kTopkWarps;
-      if (b1 < nblk) load(b1, 1);
-      score(blk, 0);
-      if (b1 >= nblk) break;
-      if (b1 + kTopkWarps < nblk) load(b1 + kTopkWarps, 0);
-      score(b1, 1);
+      __syncthreads();   // buffer c & 1 is free; the scores are visible
     }
   }
-  __syncthreads();
+  if (*abort) {
+    // a wait gave up: let every copy this CTA issued land before it leaves
+    // (the output of this call is not meaningful; the host reads the error)
+    if (threadIdx.x == 0) {
+      volatile int dummy = 0;
+      for (int c = landed + 1; c <= issued; ++c) mbar_wait(&full[c & 1], (c >> 1) & 1, kDrainLimit, &dummy);
+      atomicOr(a.err, DEV_ERR_WAIT_TIMEOUT);
+    }
+    cp_async_wait<0>();
+    return;
+  }
 
   // ---- 2. softmax over all tokens: max, then sum of exp2(s - max) -----------------
   float M, L;
@@ -244,7 +310,7 @@ __global__ void __launch_bounds__(kTopkThreads) decode_attn_topk_kernel(const De
     int need = nsel;
 #pragma unroll 1
     for (int shift = 24; shift >= 0; shift -= 8) {
-      hist[threadIdx.x] = 0;   // 256 threads, 256 bins
+      for (int i = threadIdx.x; i < 256; i += kTopkThreads) hist[i] = 0;
       __syncthreads();
       for (int i = threadIdx.x; i < len; i += kTopkThreads) {
         const uint32_t k = order_key(sc[i]);
@@ -309,30 +375,68 @@ __global__ void __launch_bounds__(kTopkThreads) decode_attn_topk_kernel(const De
   __syncthreads();
 
   // ---- 4. the listed V rows, weighted by their softmax probabilities ---------------
+  // A V row is D/8 code words of 8 dims; a warp covers kTpw = 256/D rows at
+  // a time (lane = slot * (D/8) + word).  Warp w takes list entries
+  // kTpw*w + slot, then kTpw*kTopkWarps further on, eight rows per lane per
+  // round with every load issued before any is used.  Each pair of dims is
+  // restored as fp16(fmaf(c, scale, min)) and accumulated in fp32 (paired
+  // FMA) in list order; the slots, then the warps, are summed in a fixed
+  // order.
   {
-    const int g = (lane * DPL) / 64;   // this lane's dims lane*DPL .. +DPL-1 lie in one group
-    float acc[DPL];
+    constexpr int kWords = D / 8;            // 32-bit code words per row
+    constexpr int kTpw = 32 / kWords;        // rows a warp covers at once
+    constexpr int kStep = kTpw * kTopkWarps;
+    const int slotl = lane / kWords, word = lane % kWords;
+    const int g = word / 8;                  // 64-group of this lane's dims
+    float2 acc[4];                           // dims (0,4) (1,5) (2,6) (3,7) of the word
 #pragma unroll
-    for (int u = 0; u < DPL; ++u) acc[u] = 0.0f;
-    for (int j = warp; j < nsel; j += kTopkWarps) {
-      const int t = list[j];
-      const int64_t slot = slot0 + t;
-      const float e = exp2f(sc[t] - M);
-      const float mn = a.vmin[slot * NG + g], s = a.vscale[slot * NG + g];
-      uint32_t codes;
-      if constexpr (D == 128)
-        codes = *reinterpret_cast<const uint16_t*>(a.vc + slot * (D / 2) + 2 * lane);
-      else
-        codes = a.vc[slot * (D / 2) + lane];
+    for (int u = 0; u < 4; ++u) acc[u] = make_float2(0.0f, 0.0f);
+    for (int j0 = warp * kTpw + slotl; j0 < nsel; j0 += 8 * kStep) {
+      uint32_t cw[8];
+      float mn[8], scl[8], e[8];
 #pragma unroll
-      for (int u = 0; u < DPL; ++u) {
-        const float c = static_cast<float>((codes >> (4 * u)) & 15u);   // even dim in the low nibble
-        const float v = __half2float(__float2half_rn(fmaf(c, s, mn)));
-        acc[u] = fmaf(e, v, acc[u]);
+      for (int r = 0; r < 8; ++r) {
+        const int j = j0 + r * kStep;
+        if (j < nsel) {
+          const int t = list[j];
+          const int64_t slot = slot0 + t;
+          cw[r] = *reinterpret_cast<const uint32_t*>(a.vc + slot * (D / 2) + 4 * word);
+          mn[r] = a.vmin[slot * NG + g];
+          scl[r] = a.vscale[slot * NG + g];
+          e[r] = exp2f(sc[t] - M);
+        } else {
+          cw[r] = 0u;
+          mn[r] = scl[r] = e[r] = 0.0f;
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        const float2 s2 = make_float2(scl[r], scl[r]), m2 = make_float2(mn[r], mn[r]);
+        const float2 e2 = make_float2(e[r], e[r]);
+        const uint32_t y = cw[r] >> 8;
+        const uint32_t h[4] = {restore_pair<false>(lop_mask_or(cw[r], kLoNib, kMagic), s2, m2),
+                               restore_pair<true>(lop_mask_or(cw[r], kHiNib, kMagic), s2, m2),
+                               restore_pair<false>(lop_mask_or(y, kLoNib, kMagic), s2, m2),
+                               restore_pair<true>(lop_mask_or(y, kHiNib, kMagic), s2, m2)};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) acc[u] = q4::fma_f32x2(e2, unpack_h2(h[u]), acc[u]);
       }
     }
+    // sum the row slots of the warp (lanes kWords apart), in slot order
 #pragma unroll
-    for (int u = 0; u < DPL; ++u) red_o[warp][lane * DPL + u] = acc[u];
+    for (int o = kWords; o < 32; o <<= 1)
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        acc[u].x += __shfl_xor_sync(0xffffffffu, acc[u].x, o);
+        acc[u].y += __shfl_xor_sync(0xffffffffu, acc[u].y, o);
+      }
+    if (slotl == 0) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        red_o[warp][8 * word + u] = acc[u].x;
+        red_o[warp][8 * word + u + 4] = acc[u].y;
+      }
+    }
   }
   __syncthreads();
   if (threadIdx.x < D) {
@@ -352,7 +456,7 @@ fg_status launch_topk(const fg_kv& kv, const void* q, int64_t ldq, const void* k
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
-  constexpr int kMaxDyn = static_cast<int>(2 * kTopkMaxLen * 4);
+  const int kMaxDyn = static_cast<int>(TopkLayout<D>::bytes(kTopkMaxLen, kTopkMaxLen));
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
     if (cudaFuncSetAttribute(decode_attn_topk_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDyn) !=
         cudaSuccess)
@@ -379,6 +483,9 @@ fg_status launch_topk(const fg_kv& kv, const void* q, int64_t ldq, const void* k
   a.splits = 1;
   a.tps = 0;
   a.part = nullptr;
+  a.err = device_error_word();
+  if (!a.err) return fail(FG_ERR_CUDA, "device error word");
+  a.wait_limit = wait_limit();
   const int64_t len = pos + 1, nsel = keep < len ? keep : len;
   cudaLaunchAttribute pdl[1];
   pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -387,7 +494,7 @@ fg_status launch_topk(const fg_kv& kv, const void* q, int64_t ldq, const void* k
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(kv.b * kv.heads));
   cfg.blockDim = dim3(kTopkThreads);
-  cfg.dynamicSmemBytes = static_cast<size_t>(len + nsel) * 4;
+  cfg.dynamicSmemBytes = TopkLayout<D>::bytes(len, nsel);
   cfg.stream = st;
   cfg.attrs = pdl;
   cfg.numAttrs = 1;
