@@ -188,9 +188,11 @@ __global__ void __launch_bounds__(kTopkThreads, 8) decode_attn_topk_kernel(const
   tc::griddep_wait();
 
   if (a.knew != nullptr) {   // Concat first: the new token is one of the candidates
-    if (warp == 0) append_token<D>(a, slot0, bi, h, lane);
+    if (warp == 0) {
+      append_token<D>(a, slot0, bi, h, lane);
+      tc::fence_proxy_async_global();   // the new row, then the bulk copies that read it
+    }
     __syncthreads();
-    tc::fence_proxy_async_global();   // the appended codes, then the bulk copies that read them
   }
 
   // ---- 1. scores of every token, K staged chunk by chunk ---------------------------

@@ -83,3 +83,4 @@ def test_topk_attention_wait_timeout_is_reported_and_recovers(fg):
     want, _ = olayer.attention_topk(q.cpu().numpy().astype(np.float64).reshape(b, H, d), oc.k_val, oc.v_val, keep)
     got = out.cpu().numpy().astype(np.float64).reshape(b, H, d)
     assert np.max(np.abs(got - want)) / np.max(np.abs(want)) <= 5e-3
+
