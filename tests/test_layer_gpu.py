@@ -68,12 +68,13 @@ def run_gpu_block(fg, w, layers_raw, quant, x, tin, per_layer_api=False):
     return y, outs, kvs
 
 
-def oracle_block(w, layers_raw, quant, x, tin, seqs):
+def oracle_block(w, layers_raw, quant, x, tin, seqs, with_weights=False):
     ow = [olayer.Weights.prepare({k: v.cpu().numpy() for k, v in r.items()}, quant, w.act)
           for r in layers_raw]
     xs = x[seqs].cpu().numpy().astype(np.float64)
     ts = tin[:, seqs].cpu().numpy().astype(np.float64)
-    return olayer.run_block(xs, ts, ow, w.heads, quant, w.act)
+    ref = olayer.run_block(xs, ts, ow, w.heads, quant, w.act)
+    return (ref, ow) if with_weights else ref
 
 
 def _compare(w, y, outs, ref, seqs, tol):
@@ -220,3 +221,71 @@ def test_layer_local_codec_off(fg, name, layer):
     y, outs, _ = run_gpu_block(fg, w, raw, False, x, tin)
     seqs = [0, b - 1]
     _compare(w, y, outs, oracle_block(w, raw, False, x, tin, seqs), seqs, 1e-2)
+
+
+def _gpu_cache_values(fg, kv, seq):
+    """The K/V values the GPU's cache restores for one sequence, [H][cap][d]
+    in fp64 (through fg_dequant_g64, bit-exact against the codec)."""
+    H, cap, half = kv.k_codes.shape[1], kv.k_codes.shape[2], kv.k_codes.shape[3]
+    vals = []
+    for codes, mins, scales in ((kv.k_codes, kv.k_mins, kv.k_scales), (kv.v_codes, kv.v_mins, kv.v_scales)):
+        out = torch.empty((H * cap, 2 * half), dtype=torch.float16, device=codes.device)
+        fg.fg_dequant_g64(codes[seq].reshape(H * cap, half), mins[seq].reshape(H * cap, -1),
+                          scales[seq].reshape(H * cap, -1), out)
+        vals.append(out.reshape(H, cap, 2 * half).cpu().numpy().astype(np.float64))
+    fg.fg_sync_status()
+    return vals
+
+
+def _layer_on_cache(wts, rows, qpos, kval, vval, heads):
+    """The layer's equations in fp64 for input rows at slots qpos, attending
+    over the given cache values (slots 0..qpos, causal): a diagnostic
+    recomputation local to this test, not the oracle."""
+    T, h1 = rows.shape
+    d = h1 // heads
+    q = torch.from_numpy(rows @ wts.wq).reshape(T, heads, d).transpose(0, 1)        # [H][T][d]
+    k = torch.from_numpy(kval[:, :qpos[-1] + 1])
+    v = torch.from_numpy(vval[:, :qpos[-1] + 1])
+    mask = torch.from_numpy(np.arange(k.shape[1])[None, :] <= np.asarray(qpos)[:, None])
+    att = torch.nn.functional.scaled_dot_product_attention(q, k, v, attn_mask=mask)
+    a = att.transpose(0, 1).reshape(T, h1).numpy() @ wts.wo + rows
+    return np.maximum(a @ wts.w1, 0.0) @ wts.w2 + a
+
+
+@pytest.mark.parametrize("name,layer", [("opt-30b", 0), ("opt-175b", 0)])
+def test_outputs_above_the_bar_come_from_flipped_kv_codes(fg, name, layer, record_property):
+    """Where the relaxed bars apply (30B prefill, 175B), the outputs beyond
+    1e-2 of the oracle are the work of the few K/V codes the GPU's fp32 sums
+    put one step away from the oracle's.  The layer's equations, evaluated
+    in fp64 in this test on the K/V values of the GPU's own cache (oracle
+    weights, same inputs), must meet the strict 1e-2 bar at every prefill and
+    decode output, and does with a wide margin (3e-3 asserted; ~1e-3
+    measured): with the flipped codes accounted for, nothing is left near
+    the bar.  (The test's recomputation reads GPU values; the oracle does
+    not.)"""
+    w = synth.WORKLOADS[name]
+    b = 4 if name == "opt-175b" else w.b
+    raw = [synth.layer_weights(w, layer, "cuda")]
+    x = synth.prompt(w, b=b, device="cuda", seed_offset=layer)
+    tin = synth.decode_inputs(w, b=b, n=4, device="cuda", seed_offset=layer)
+    y, outs, kvs = run_gpu_block(fg, w, raw, True, x, tin)
+    (ry, routs, rcaches), ows = oracle_block(w, raw, True, x, tin, [0], with_weights=True)
+    kval, vval = _gpu_cache_values(fg, kvs[0], 0)
+    flips = sum(int(np.sum(g[0].cpu().numpy() != o[0]))
+                for g, o in ((kvs[0].k_codes, rcaches[0].k_codes), (kvs[0].v_codes, rcaches[0].v_codes)))
+    record_property("flipped_code_bytes_seq0", flips)
+    s = x.shape[1]
+    got = [y[0].cpu().numpy().astype(np.float64)] + [o[0:1].cpu().numpy().astype(np.float64) for o in outs]
+    want = [ry[0]] + [r[0:1] for r in routs]
+    rows = [x[0].cpu().numpy().astype(np.float64)] + [t[0:1].cpu().numpy().astype(np.float64) for t in tin]
+    qpos = [np.arange(s)] + [np.array([s + t]) for t in range(len(outs))]
+    above = 0
+    for k in range(len(got)):
+        sub = _layer_on_cache(ows[0], rows[k], qpos[k], kval, vval, w.heads)
+        scale = np.max(np.abs(sub))
+        e_sub = np.abs(got[k] - sub) / scale
+        e_ref = np.abs(got[k] - want[k]) / max(np.max(np.abs(want[k])), 1e-30)
+        above += int(np.sum(e_ref > 1e-2))
+        record_property(f"max_err_vs_gpu_codes_{k}", float(e_sub.max()))
+        assert e_sub.max() <= 3e-3, f"output {k}: {e_sub.max()} against the layer on the GPU's cache"
+    record_property("outputs_above_1e-2_vs_oracle", above)
