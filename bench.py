@@ -568,7 +568,7 @@ def run_case(args, w, device):
         if mat == "wq":
             N *= 3
         prefill = name.startswith("prefill")
-        M = min(w.b * w.s, 8192) if prefill else w.b      # a few GB at most on the device
+        M = min(w.b * w.s, 8192) if prefill else (args.m or w.b)   # a few GB at most on the device
         per = K * N * (2 if prefill else Q4)
         copies = 1 if prefill else max(2, min(32, int(-(-l2 // per))))
         Ws = []
@@ -581,6 +581,8 @@ def run_case(args, w, device):
         ws = fg.workspace(max(fg.fg_linear_workspace_bytes(M, K, N, not prefill, dt), 1), dev)
         calls = [lambda W=W: fg.fg_linear(W, x, y, ws=ws) for W in Ws]
         shape = {"M": M, "K": K, "N": N, "copies": copies}
+        if not prefill:   # weights once (0.625 B each) + x in and y out (fp16)
+            shape["algorithmic_bytes"] = K * N * Q4 + 2 * M * (K + N)
     else:
         L = fg.Layer.from_dense(synth.layer_weights(w, 0, dev), w.heads, True)
         x = synth.prompt(w, device=dev)
@@ -649,6 +651,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle timing")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--m", type=int, default=None, help="rows of a decode-product case (default: the block size)")
     ap.add_argument("--case", choices=CASES, default=None,
                     help="time one kernel class at the workload's shapes (for profilers)")
     args = ap.parse_args()

@@ -163,9 +163,13 @@ fg_status fg_kv_append(const fg_kv* kv, const void* k_new, const void* v_new, in
  * [M][w->N]; y must not overlap x or r.
  * codec FG_CODEC_Q4G64 uses w->codes/mins/scales (dequantized on the fly,
  * rounded to the compute dtype), FG_CODEC_NONE uses w->dense ([K][N] in
- * dtype).  K and N must be multiples of 64.  fp16 with M >= 64 runs on the
- * tensor cores (split over K when the output has too few tiles, using ws);
- * other cases on the CUDA cores.  ws_bytes >= fg_linear_workspace_bytes. */
+ * dtype).  K and N must be multiples of 64.  fp16 on Q4G64 weights with a
+ * decode copy (w->packed): M <= 256 runs on the tensor cores (weights
+ * converted into tensor memory); without the copy, M >= 64 runs on the
+ * tensor cores after converting the weight to fp16 in ws.  fp16 dense
+ * weights with M >= 64 run on the tensor cores; other cases on the CUDA
+ * cores.  Products are split over K when the output has too few tiles,
+ * using ws.  ws_bytes >= fg_linear_workspace_bytes. */
 size_t fg_linear_workspace_bytes(int64_t M, int64_t K, int64_t N, fg_codec codec, fg_dtype dtype);
 fg_status fg_linear(const fg_wmat* w, fg_codec codec, fg_dtype dtype, const void* x, int64_t M,
                     const void* r, int32_t relu, void* y, void* ws, size_t ws_bytes,

@@ -599,24 +599,7 @@ fg_status launch_ts(TsParams& p, cudaStream_t st) {
     return check_launch("gemm_q4ts_kernel (launch)");
   const fg_status s = check_launch("gemm_q4ts_kernel");
   if (s != FG_OK || p.splits == 1) return s;
-  // the split sum over the whole GPU, programmatically after the product
-  const int64_t total = static_cast<int64_t>(p.M) * p.N / 4;
-  cudaLaunchConfig_t rc = {};
-  rc.gridDim = dim3(static_cast<unsigned>(std::min<int64_t>((total + 255) / 256, static_cast<int64_t>(num_sms()) * 8)));
-  rc.blockDim = dim3(256);
-  rc.stream = st;
-  rc.attrs = attr;
-  rc.numAttrs = 1;
-  trace_extra_launch();
-  // the kernel holds every split's load in registers: the smallest bucket
-  // that fits, so that few splits keep few registers
-  auto sum = p.splits <= 2 ? splitk_sum_kernel<2>
-             : p.splits <= 4 ? splitk_sum_kernel<4>
-             : p.splits <= 8 ? splitk_sum_kernel<8> : splitk_sum_kernel<kMaxSplits>;
-  if (cudaLaunchKernelEx(&rc, sum, static_cast<const float*>(p.part), p.splits, p.M, p.N, BNC * RB, p.n_tiles, p.R,
-                         p.ldr, p.relu, p.Y, p.ldy) != cudaSuccess)
-    return check_launch("splitk_sum_kernel (launch)");
-  return check_launch("splitk_sum_kernel");
+  return splitk_sum_launch(p.part, p.splits, p.M, p.N, BNC * RB, p.n_tiles, p.R, p.ldr, p.relu, p.Y, p.ldy, st);
 }
 
 int bt_for(int64_t M) { return M <= 32 ? 32 : (M <= 64 ? 64 : (M <= 128 ? 128 : 256)); }
@@ -647,6 +630,31 @@ int splits_for(int64_t M, int64_t N, int64_t K, int rb) {
 }
 
 }  // namespace
+
+fg_status splitk_sum_launch(const float* part, int splits, int64_t M, int64_t N, int nch, int n_tiles, const void* R,
+                            int64_t ldr, int relu, void* Y, int64_t ldy, cudaStream_t st) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  const int64_t total = M * N / 4;
+  cudaLaunchConfig_t rc = {};
+  rc.gridDim = dim3(static_cast<unsigned>(std::min<int64_t>((total + 255) / 256, static_cast<int64_t>(num_sms()) * 8)));
+  rc.blockDim = dim3(256);
+  rc.stream = st;
+  rc.attrs = attr;
+  rc.numAttrs = 1;
+  trace_extra_launch();
+  // the kernel holds every split's load in registers: the smallest bucket
+  // that fits, so that few splits keep few registers
+  auto sum = splits <= 2 ? splitk_sum_kernel<2>
+             : splits <= 4 ? splitk_sum_kernel<4>
+             : splits <= 8 ? splitk_sum_kernel<8> : splitk_sum_kernel<kMaxSplits>;
+  if (cudaLaunchKernelEx(&rc, sum, part, splits, static_cast<int>(M), static_cast<int>(N), nch, n_tiles,
+                         static_cast<const __half*>(R), static_cast<int>(ldr), relu, static_cast<__half*>(Y),
+                         static_cast<int>(ldy)) != cudaSuccess)
+    return check_launch("splitk_sum_kernel (launch)");
+  return check_launch("splitk_sum_kernel");
+}
 
 size_t gemm_q4ts_workspace_bytes(int64_t M, int64_t N, int64_t K) {
   size_t need = 0;

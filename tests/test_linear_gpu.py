@@ -60,6 +60,14 @@ CASES = [
     (64, 960, 512, True, False, True, torch.float16),         # 15 k tiles, 64-row block
     (96, 1088, 768, True, True, False, torch.float16),        # 17 k tiles, 128-row block
     (256, 960, 384, True, False, True, torch.float16),        # 15 k tiles, 256-row block
+    # blocks of a few sequences (padded to the kernel's 32-row MMA)
+    (2, 768, 2304, True, False, False, torch.float16),        # OPT-125M QKV, two sequences
+    (3, 4096, 4096, True, False, True, torch.float16),
+    (4, 16384, 4096, True, False, True, torch.float16),       # long K: sixteen splits
+    (6, 1024, 768, True, True, False, torch.float16),
+    (8, 4096, 16384, True, True, False, torch.float16),
+    (8, 1088, 512, True, False, True, torch.float16),         # 17 k tiles: ragged warp ranges
+    (1, 12288, 256, True, False, False, torch.float16),       # a single channel tile, no split of N
 ]
 
 # quantized fp16 products with at most 256 rows run on the decode-copy
@@ -112,7 +120,7 @@ def test_linear_repeatable(fg, fmt):
     assert torch.equal(y1, y2)
 
 
-@pytest.mark.parametrize("M", [32, 64, 128, 256])
+@pytest.mark.parametrize("M", [1, 3, 8, 32, 64, 128, 256])
 @pytest.mark.parametrize("fmt", [EXACT, F16META])
 def test_decode_product_restores_weights_bit_exactly(fg, M, fmt):
     """With one-hot rows x = e_k the product returns weight row k itself
