@@ -184,12 +184,31 @@ __device__ __forceinline__ void merge_warps(const WarpState<D>& W, float* red_m,
   }
 }
 
+// Each warp stages its own 16-token blocks in shared memory, kWStages deep,
+// with asynchronous copies (per-thread groups, no CTA barrier): the K and V
+// codes of the block's rows in 16-byte pieces, and each row's (scale, min)
+// pairs.  The warp reads a block from shared memory right before it uses
+// it, so no registers hold blocks in flight.
+constexpr int kWStages = 3;
+
 template <int D>
-__global__ void __launch_bounds__(128) decode_attn_mma_kernel(const DecodeArgs a) {
+struct WarpStage {
+  static constexpr int C = D / 2;            // code bytes of a row
+  static constexpr int NG = D / 64;
+  static constexpr int kMetaArr = 16 * NG * 4;   // one (scale or min) array of a block
+  static constexpr int kK = 0, kV = 16 * C;
+  static constexpr int kKs = 32 * C, kKm = kKs + kMetaArr, kVs = kKm + kMetaArr, kVm = kVs + kMetaArr;
+  static constexpr int kBytes = kVm + kMetaArr;
+};
+
+template <int D>
+__global__ void __launch_bounds__(128, 4) decode_attn_mma_kernel(const DecodeArgs a) {
   constexpr int NG = D / 64;   // 64-groups per head row
   constexpr int NT = D / 16;   // m16 tiles of value dims
+  using WS = WarpStage<D>;
   __shared__ float red_m[4], red_l[4];
   __shared__ float red_o[4][D];
+  __shared__ __align__(16) uint8_t wsm[4][kWStages][WS::kBytes];
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int gq = lane >> 2, tig = lane & 3;
@@ -209,7 +228,10 @@ __global__ void __launch_bounds__(128) decode_attn_mma_kernel(const DecodeArgs a
 
   // ---- Concat: quantize the new token's K and V into slot pos -----------------
   if (a.knew != nullptr && a.pos >= t0 && a.pos < t1) {
-    if (warp == 0) append_token<D>(a, slot0, bi, h, lane);
+    if (warp == 0) {
+      append_token<D>(a, slot0, bi, h, lane);
+      tc::fence_proxy_async_global();   // the new row, then the asynchronous copies that read it
+    }
     __syncthreads();
   }
 
@@ -232,53 +254,84 @@ __global__ void __launch_bounds__(128) decode_attn_mma_kernel(const DecodeArgs a
 #pragma unroll
   for (int i = 0; i < NT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
 
-  // loads of one 16-token block (issued a block ahead of its use)
-  auto load = [&](int blk, KVBlock<NG>& B) {
+  // block blk of this CTA's tokens into this warp's stage st
+  auto issue = [&](int blk, int st) {
     const int64_t tb = t0 + static_cast<int64_t>(blk) * 16;
-    // K rows of tokens gq and gq+8: per group, 8 bytes at 16*tig dims
+    uint8_t* s = wsm[warp][st];
+    constexpr int C = WS::C, kPieces = C / 16;   // 16-byte pieces of a row
 #pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const int64_t tok = tb + gq + 8 * r;
-      const int64_t slot = slot0 + tok;
-#pragma unroll
-      for (int g = 0; g < NG; ++g) {
-        if (tok < t1) {
-          B.kw[r][g] = __ldcs(reinterpret_cast<const uint2*>(a.kc + slot * (D / 2) + g * 32 + 8 * tig));
-          B.ksc[r][g] = a.kscale[slot * NG + g];
-          B.kmn[r][g] = a.kmin[slot * NG + g];
-          B.vsc[r][g] = a.vscale[slot * NG + g];
-          B.vmn[r][g] = a.vmin[slot * NG + g];
-        } else {
-          B.kw[r][g] = make_uint2(0u, 0u);
-          B.ksc[r][g] = B.kmn[r][g] = B.vsc[r][g] = B.vmn[r][g] = 0.0f;
-        }
+    for (int pc = lane; pc < 16 * kPieces; pc += 32) {
+      const int row = pc / kPieces, off = (pc % kPieces) * 16;
+      if (tb + row < t1) {
+        const int64_t src = (slot0 + tb + row) * C + off;
+        tc::cp_async16(s + WS::kK + row * C + off, a.kc + src);
+        tc::cp_async16(s + WS::kV + row * C + off, a.vc + src);
       }
     }
-    // V words of tokens 2tig, 2tig+1, 2tig+8, 2tig+9: per group, 4 bytes at 8*gq dims
+    // (scale, min) pairs: four arrays x 16 rows x NG floats, 4-byte copies
+    // (the arrays need only 4-byte alignment)
+#pragma unroll
+    for (int e = lane; e < 64 * NG; e += 32) {
+      const int arr = e / (16 * NG), f = e % (16 * NG);   // f: float of the block's NG * 16
+      if (tb + f / NG < t1) {
+        const float* base = arr == 0 ? a.kscale : arr == 1 ? a.kmin : arr == 2 ? a.vscale : a.vmin;
+        tc::cp_async4(s + WS::kKs + arr * WS::kMetaArr + f * 4, base + (slot0 + tb) * NG + f);
+      }
+    }
+    tc::cp_async_commit();
+  };
+
+  // block blk from stage st into registers, as process_block takes it (rows
+  // past t1 read as zero)
+  auto read = [&](int blk, int st, KVBlock<NG>& B) {
+    const int64_t tb = t0 + static_cast<int64_t>(blk) * 16;
+    const uint8_t* s = wsm[warp][st];
+    const float* ks = reinterpret_cast<const float*>(s + WS::kKs);
+    const float* km = reinterpret_cast<const float*>(s + WS::kKm);
+    const float* vs = reinterpret_cast<const float*>(s + WS::kVs);
+    const float* vm = reinterpret_cast<const float*>(s + WS::kVm);
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int row = gq + 8 * r;
+      const bool v = tb + row < t1;
+#pragma unroll
+      for (int g = 0; g < NG; ++g) {
+        B.kw[r][g] = v ? *reinterpret_cast<const uint2*>(s + WS::kK + row * WS::C + g * 32 + 8 * tig)
+                       : make_uint2(0u, 0u);
+        B.ksc[r][g] = v ? ks[row * NG + g] : 0.0f;
+        B.kmn[r][g] = v ? km[row * NG + g] : 0.0f;
+        B.vsc[r][g] = v ? vs[row * NG + g] : 0.0f;
+        B.vmn[r][g] = v ? vm[row * NG + g] : 0.0f;
+      }
+    }
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
-      const int64_t tok = tb + 2 * tig + (r & 1) + 8 * (r >> 1);
-      const int64_t slot = slot0 + tok;
+      const int row = 2 * tig + (r & 1) + 8 * (r >> 1);
+      const bool v = tb + row < t1;
 #pragma unroll
       for (int g = 0; g < NG; ++g)
-        B.vw[r][g] =
-            tok < t1 ? __ldcs(reinterpret_cast<const unsigned int*>(a.vc + slot * (D / 2) + g * 32 + 4 * gq)) : 0u;
+        B.vw[r][g] = v ? *reinterpret_cast<const uint32_t*>(s + WS::kV + row * WS::C + g * 32 + 4 * gq) : 0u;
     }
   };
 
-  auto process = [&](int blk, const KVBlock<NG>& B) {
+  // the pipeline: blocks wb0.. in stages j % kWStages, kWStages - 1 ahead
+#pragma unroll
+  for (int i = 0; i < kWStages - 1; ++i) {
+    if (wb0 + i < wb1) issue(wb0 + i, i);
+    else tc::cp_async_commit();
+  }
+  for (int blk = wb0; blk < wb1; ++blk) {
+    const int j = blk - wb0;
+    // stage (j + kWStages - 1) % kWStages was read in iteration j - 1, which
+    // ended with a warp barrier
+    if (blk + kWStages - 1 < wb1) issue(blk + kWStages - 1, (j + kWStages - 1) % kWStages);
+    else tc::cp_async_commit();
+    tc::cp_async_wait<kWStages - 1>();   // this lane's copies of block blk have landed
+    __syncwarp();                        // and every lane's
+    KVBlock<NG> B;
+    read(blk, j % kWStages, B);
     process_block<D>(W, t0 + static_cast<int64_t>(blk) * 16, t1, B, gq, tig);
-  };
-
-  // two block buffers: the next block's loads are in flight while this one computes
-  KVBlock<NG> buf0, buf1;
-  if (wb0 < wb1) load(wb0, buf0);
-  for (int blk = wb0; blk < wb1; blk += 2) {
-    if (blk + 1 < wb1) load(blk + 1, buf1);
-    process(blk, buf0);
-    if (blk + 1 >= wb1) break;
-    if (blk + 2 < wb1) load(blk + 2, buf0);
-    process(blk + 1, buf1);
+    __syncwarp();                        // stage j % kWStages is read
   }
 
   // the per-lane sums over this warp's tokens: run_l and cmn over the rows gq
