@@ -254,30 +254,40 @@ __global__ void __launch_bounds__(128, 4) decode_attn_mma_kernel(const DecodeArg
 #pragma unroll
   for (int i = 0; i < NT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
 
-  // block blk of this CTA's tokens into this warp's stage st
+  // block blk of this CTA's tokens into this warp's stage st.  The pieces a
+  // lane copies sit at the same offsets in every block (rows are contiguous):
+  // lane l copies 16-byte pieces l, l + 32, ... of the K and V codes and
+  // floats l, l + 32, ... of the four (scale, min) arrays' NG * 16.
+  constexpr int kPieces = 16 * WS::C / 16;                    // 16-byte pieces of a block's codes
+  constexpr int kMetaPer = (64 * NG + 31) / 32;               // pair floats a lane copies
+  const uint8_t* kc_l = a.kc + (slot0 + t0) * WS::C + 16 * lane;
+  const uint8_t* vc_l = a.vc + (slot0 + t0) * WS::C + 16 * lane;
+  const float* meta_l[kMetaPer];
+  int meta_dst[kMetaPer], meta_row[kMetaPer];
+#pragma unroll
+  for (int u = 0; u < kMetaPer; ++u) {
+    const int e = lane + 32 * u, arr = e / (16 * NG), f = e % (16 * NG);
+    const float* base = arr == 0 ? a.kscale : arr == 1 ? a.kmin : arr == 2 ? a.vscale : a.vmin;
+    meta_l[u] = base + (slot0 + t0) * NG + f;
+    meta_dst[u] = WS::kKs + arr * WS::kMetaArr + f * 4;
+    meta_row[u] = f / NG;
+  }
   auto issue = [&](int blk, int st) {
     const int64_t tb = t0 + static_cast<int64_t>(blk) * 16;
+    const int nrow = static_cast<int>(min(static_cast<int64_t>(16), t1 - tb));   // valid rows of the block
     uint8_t* s = wsm[warp][st];
-    constexpr int C = WS::C, kPieces = C / 16;   // 16-byte pieces of a row
+    const int64_t cb = static_cast<int64_t>(blk) * 16 * WS::C;
 #pragma unroll
-    for (int pc = lane; pc < 16 * kPieces; pc += 32) {
-      const int row = pc / kPieces, off = (pc % kPieces) * 16;
-      if (tb + row < t1) {
-        const int64_t src = (slot0 + tb + row) * C + off;
-        tc::cp_async16(s + WS::kK + row * C + off, a.kc + src);
-        tc::cp_async16(s + WS::kV + row * C + off, a.vc + src);
+    for (int pc = lane, u = 0; u < (kPieces + 31) / 32; pc += 32, ++u) {
+      if (pc < kPieces && pc / (WS::C / 16) < nrow) {
+        tc::cp_async16(s + WS::kK + 16 * pc, kc_l + cb + 512 * u);
+        tc::cp_async16(s + WS::kV + 16 * pc, vc_l + cb + 512 * u);
       }
     }
-    // (scale, min) pairs: four arrays x 16 rows x NG floats, 4-byte copies
-    // (the arrays need only 4-byte alignment)
+    const int64_t mb = static_cast<int64_t>(blk) * 16 * NG;
 #pragma unroll
-    for (int e = lane; e < 64 * NG; e += 32) {
-      const int arr = e / (16 * NG), f = e % (16 * NG);   // f: float of the block's NG * 16
-      if (tb + f / NG < t1) {
-        const float* base = arr == 0 ? a.kscale : arr == 1 ? a.kmin : arr == 2 ? a.vscale : a.vmin;
-        tc::cp_async4(s + WS::kKs + arr * WS::kMetaArr + f * 4, base + (slot0 + tb) * NG + f);
-      }
-    }
+    for (int u = 0; u < kMetaPer; ++u)
+      if (meta_row[u] < nrow) tc::cp_async4(s + meta_dst[u], meta_l[u] + mb);
     tc::cp_async_commit();
   };
 
@@ -286,6 +296,32 @@ __global__ void __launch_bounds__(128, 4) decode_attn_mma_kernel(const DecodeArg
   auto read = [&](int blk, int st, KVBlock<NG>& B) {
     const int64_t tb = t0 + static_cast<int64_t>(blk) * 16;
     const uint8_t* s = wsm[warp][st];
+    if (tb + 16 <= t1) {   // a full block: no row to mask
+      const float* ks = reinterpret_cast<const float*>(s + WS::kKs);
+      const float* km = reinterpret_cast<const float*>(s + WS::kKm);
+      const float* vs = reinterpret_cast<const float*>(s + WS::kVs);
+      const float* vm = reinterpret_cast<const float*>(s + WS::kVm);
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int row = gq + 8 * r;
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {
+          B.kw[r][g] = *reinterpret_cast<const uint2*>(s + WS::kK + row * WS::C + g * 32 + 8 * tig);
+          B.ksc[r][g] = ks[row * NG + g];
+          B.kmn[r][g] = km[row * NG + g];
+          B.vsc[r][g] = vs[row * NG + g];
+          B.vmn[r][g] = vm[row * NG + g];
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int row = 2 * tig + (r & 1) + 8 * (r >> 1);
+#pragma unroll
+        for (int g = 0; g < NG; ++g)
+          B.vw[r][g] = *reinterpret_cast<const uint32_t*>(s + WS::kV + row * WS::C + g * 32 + 4 * gq);
+      }
+      return;
+    }
     const float* ks = reinterpret_cast<const float*>(s + WS::kKs);
     const float* km = reinterpret_cast<const float*>(s + WS::kKm);
     const float* vs = reinterpret_cast<const float*>(s + WS::kVs);
