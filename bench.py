@@ -314,6 +314,16 @@ def run_ours(args, w, rank, world, device):
     y = torch.empty_like(x)
     outs = torch.empty_like(tin)
 
+    # decode steps replay CUDA graphs recorded by the first warm-up step
+    # (fg_decode_block_step_graphed); the profiled pass below runs them directly
+    graphs = None if args.no_graph else fg.GraphCache()
+
+    def decode_step(t_in, pos, out):
+        if graphs is not None and not args._prof:
+            fg.fg_decode_block_step_graphed(graphs, blk, t_in, pos, out, ws, st)
+        else:
+            fg.fg_decode_block_step(blk, t_in, pos, out, ws, st)
+
     def step(evs=None):
         if evs:
             evs[0].record(st)
@@ -323,7 +333,7 @@ def run_ours(args, w, rank, world, device):
             evs[1].record(st)
         fg.fg_profile_phase(1) if args._prof else None
         for t in range(w.n):
-            fg.fg_decode_block_step(blk, tin[t], w.s + t, outs[t], ws, st)
+            decode_step(tin[t], w.s + t, outs[t])
         if evs:
             evs[2].record(st)
 
@@ -376,7 +386,7 @@ def run_ours(args, w, rank, world, device):
     t_d = torch.empty_like(tin[0])
     e2e_ms = []
     h2d_step = d2h_step = 0
-    for k in range(args.steps):
+    for k in range(args.steps + 1):   # the first pass records the graphs of these buffers, untimed
         e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
         x_d.copy_(x_h, non_blocking=True)
         fg.fg_prefill_block(blk, x_d, y, ws, st)
@@ -385,12 +395,13 @@ def run_ours(args, w, rank, world, device):
         for t in range(w.n):
             t_d.copy_(tin_h[t], non_blocking=True)
             h2d_step += t_d.numel() * t_d.element_size()
-            fg.fg_decode_block_step(blk, t_d, w.s + t, outs[t], ws, st)
+            decode_step(t_d, w.s + t, outs[t])
             out_h[t].copy_(outs[t], non_blocking=True)
             d2h_step += outs[t].numel() * outs[t].element_size()
         e[1].record(st)
         torch.cuda.synchronize()
-        e2e_ms.append(e[0].elapsed_time(e[1]))
+        if k > 0:
+            e2e_ms.append(e[0].elapsed_time(e[1]))
     e2e_dec = max_over_ranks([sum(e2e_ms) / 1e3], world, dev)[0]
 
     # the same decode layer-steps on finite data: one layer of the stack, its
@@ -473,6 +484,7 @@ def run_ours(args, w, rank, world, device):
         "kernels": {f"{'prefill' if p == 0 else 'decode'}:{k}": {"launches": v[0], "ms": round(v[1], 3)}
                     for p, d in prof.items() for k, v in d.items()},
         "gpu_launches": int(n_launch), "nonfinite_decode_outputs": nonfinite,
+        "decode_path": "direct calls" if args.no_graph else "fg_decode_block_step_graphed (CUDA graph per step)",
         "cpu_baseline": cpu and {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample", "threads")},
         "e2e": {"value": w.b * w.n * K * world / e2e_dec, "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d_step, "d2h_bytes_per_step": d2h_step,
@@ -650,6 +662,7 @@ def main():
     ap.add_argument("--config", default="opt-6.7b", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle timing")
+    ap.add_argument("--no-graph", action="store_true", help="decode steps by direct calls, not replayed graphs")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--m", type=int, default=None, help="rows of a decode-product case (default: the block size)")
     ap.add_argument("--case", choices=CASES, default=None,

@@ -304,6 +304,26 @@ fg_status fg_decode_block_step(const fg_layer* layers, int32_t l, const void* t,
                                int64_t pos, const fg_kv* kvs, void* y, void* ws,
                                size_t ws_bytes, cudaStream_t stream);
 
+/* [S4] the zig-zag block's decode step replayed as a CUDA graph: the same
+ * arguments, results and errors as fg_decode_block_step.  The first call
+ * with a given set of arguments (every pointer and size, and the bytes of
+ * the layers[] and kvs[] structures) runs the step directly and then
+ * records its launches into a graph held by `cache`; later calls with the
+ * same arguments launch that graph, one host call per step.  Buffers the
+ * graphs refer to must stay allocated while `cache` holds them.  While
+ * fg_profile_start is active, or when `stream` is itself being captured,
+ * calls run the step directly and record nothing.  A cache may be shared by
+ * host threads; graphs launch on the stream each call names (recording uses
+ * a stream of the cache's own, on the current device: one device per
+ * cache). */
+typedef struct fg_graph_cache fg_graph_cache;
+fg_status fg_graph_cache_create(fg_graph_cache** cache);
+void fg_graph_cache_destroy(fg_graph_cache* cache);
+int64_t fg_graph_cache_size(const fg_graph_cache* cache);   /* graphs held */
+fg_status fg_decode_block_step_graphed(fg_graph_cache* cache, const fg_layer* layers, int32_t l, const void* t,
+                                       int64_t b, int64_t pos, const fg_kv* kvs, void* y, void* ws,
+                                       size_t ws_bytes, cudaStream_t stream);
+
 /* Synchronize `stream`, then report (and clear) the device error word that
  * kernels raise when a bounded wait runs out: FG_ERR_DEVICE_TIMEOUT, or
  * FG_ERR_CUDA if the synchronization itself failed. */

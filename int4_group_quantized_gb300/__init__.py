@@ -355,6 +355,43 @@ def fg_decode_block_step(block: Block, t: torch.Tensor, pos: int, y: torch.Tenso
                                      _ptr(y), _ptr(ws), ws.numel(), _stream(stream)), "fg_decode_block_step")
 
 
+_sig("fg_graph_cache_create", _INT, ctypes.POINTER(ctypes.c_void_p))
+_sig("fg_graph_cache_destroy", None, ctypes.c_void_p)
+_sig("fg_graph_cache_size", _I64, ctypes.c_void_p)
+_sig("fg_decode_block_step_graphed", _INT, ctypes.c_void_p, ctypes.POINTER(fg_layer), ctypes.c_int32, _P, _I64,
+     _I64, ctypes.POINTER(fg_kv), _P, _P, _SZ, _P)
+
+
+class GraphCache:
+    """The CUDA graphs of recorded decode steps (fg_graph_cache)."""
+
+    def __init__(self):
+        h = ctypes.c_void_p()
+        _check(_lib.fg_graph_cache_create(ctypes.byref(h)), "fg_graph_cache_create")
+        self._h = h
+
+    def __len__(self) -> int:
+        return int(_lib.fg_graph_cache_size(self._h))
+
+    def close(self) -> None:
+        if self._h:
+            _lib.fg_graph_cache_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def fg_decode_block_step_graphed(cache: GraphCache, block: Block, t: torch.Tensor, pos: int, y: torch.Tensor,
+                                 ws: torch.Tensor, stream=None) -> None:
+    _check(_lib.fg_decode_block_step_graphed(cache._h, block.larr, len(block.layers), _ptr(t), t.shape[0], int(pos),
+                                             block.karr, _ptr(y), _ptr(ws), ws.numel(), _stream(stream)),
+           "fg_decode_block_step_graphed")
+
+
 def fg_sync_status(stream=None) -> None:
     _check(_lib.fg_sync_status(_stream(stream)), "fg_sync_status")
 

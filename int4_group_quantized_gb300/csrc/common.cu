@@ -119,6 +119,9 @@ void trace_begin(int c, cudaStream_t st) {
 }
 
 void trace_extra_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+void count_launches(uint64_t n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+void count_launches_undo(uint64_t n) { g_launches.fetch_sub(n, std::memory_order_relaxed); }
+bool profiling() { return g_prof.on; }
 
 void trace_end(int c, cudaStream_t st) {
   (void)c;

@@ -62,6 +62,11 @@ void trace_end(int cls, cudaStream_t st);
 // A second kernel launched inside a Trace scope, timed as part of that
 // scope's launch (only the launch counter sees it).
 void trace_extra_launch();
+// The launch counter for kernels a CUDA graph runs (n per replay), and its
+// correction for launches only recorded into a graph.
+void count_launches(uint64_t n);
+void count_launches_undo(uint64_t n);
+bool profiling();   // fg_profile_start is active
 struct Trace {
   int cls;
   cudaStream_t st;
