@@ -118,13 +118,6 @@ size_t gemm_tc_workspace_bytes(int64_t M, int64_t N, int64_t K);
 bool gemm_q4ts_supported(const GemmArgs& a);
 fg_status gemm_q4ts(const GemmArgs& a, void* ws, size_t ws_bytes, cudaStream_t st);
 size_t gemm_q4ts_workspace_bytes(int64_t M, int64_t N, int64_t K);
-// The K-split sum of a decode product: fp32 partial blocks
-// [split][tile][M][nch] summed in split order over the whole GPU, then the
-// residual R (optional) and ReLU, into Y (fp16); launched with programmatic
-// stream serialization after the product.  Needs ldy, ldr multiples of 4
-// and Y, R 8-byte aligned.
-fg_status splitk_sum_launch(const float* part, int splits, int64_t M, int64_t N, int nch, int n_tiles, const void* R,
-                            int64_t ldr, int relu, void* Y, int64_t ldy, cudaStream_t st);
 // The decode copy of a [K][N] 4-bit weight read by gemm_q4ts (fg_pack_weight),
 // in fg_pack_format `format`, and its size.
 fg_status pack_weight(const uint8_t* codes, const float* mins, const float* scales, int64_t K, int64_t N,

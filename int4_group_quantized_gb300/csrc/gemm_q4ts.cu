@@ -22,10 +22,13 @@
 // Shared memory carries only what HBM delivers (codes, pairs) and X; the fp16
 // weights never touch it.
 //
-// K is split when there are too few channel tiles to fill the GPU: each
-// split bulk-copies its fp32 partial into its own workspace block
-// [split][tile][M][128], and splitk_sum_kernel, launched next on the same
-// stream, sums the blocks in split order and applies the epilogue.
+// K is split when there are too few channel tiles to fill the GPU.  The
+// splits of a channel tile form one thread-block cluster: each stages its
+// fp32 partial [M][128] in its own shared memory, then the cluster's CTAs
+// share the rows of the output, each summing every split's partial of its
+// rows over distributed shared memory in split (rank) order and applying the
+// epilogue.  No partial goes through global memory and no second kernel
+// runs.
 //
 // The kernel is launched with programmatic stream serialization: the weight
 // tiles of the first stages are requested and converted before
@@ -63,7 +66,7 @@ using namespace q4;
 constexpr int BK = 64;
 constexpr int BNC = 128;               // channels per row block (the MMA's M)
 constexpr int kDqWarp0 = 4;            // dequantization warps start here
-constexpr int kMaxSplits = 16;         // K splits of a decode product (splits_for)
+constexpr int kMaxSplits = 8;          // K splits of a decode product: a portable cluster
 // The copy producers run stages ahead and usually find their ring full; they
 // poll with this pause so that they leave the issue slots to the converters.
 constexpr uint32_t kProducerSleepNs = 100;
@@ -168,7 +171,6 @@ struct TsParams {
   const __half* R;
   int ldr;
   int relu;
-  float* part;              // [splits][M][N] fp32 when splits > 1
   unsigned int* err;
   uint32_t wait_limit;      // polls of a bounded wait (fg_set_wait_limit)
 };
@@ -488,12 +490,11 @@ __global__ void __launch_bounds__(TsCfg<BT, RB, FMT>::kThreads, TsCfg<BT, RB, FM
     return;
   }
 
-  // K splits: each split's partial, [M][NCH] fp32, goes to its own
-  // contiguous block of the workspace with one bulk copy from the drained
-  // rings; splitk_sum_kernel, the next launch, sums the blocks in split order.
+  // K splits: each split stages its partial, [M][NCH] fp32, in the drained
+  // rings; the cluster's ranks (= splits) then share the rows of Y, each
+  // summing every split's partial of its rows in split order over
+  // distributed shared memory.
   float* stage = reinterpret_cast<float*>(xring);   // the rings are free: every load and MMA is done
-  const size_t blk = static_cast<size_t>(p.M) * NCH;   // floats per partial block
-  float* myblk = p.part + (static_cast<size_t>(split) * p.n_tiles + nt) * blk;
   if (epi) {
 #pragma unroll 1
     for (int c0 = 0; c0 < BT && c0 < p.M; c0 += 32) {
@@ -505,71 +506,59 @@ __global__ void __launch_bounds__(TsCfg<BT, RB, FMT>::kThreads, TsCfg<BT, RB, FM
         if (c0 + e < p.M) stage[(c0 + e) * NCH + lch] = ok ? __uint_as_float(v[e]) : 0.0f;
     }
   }
-  fence_proxy_async_smem();   // the staged partial is visible to the bulk copy
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, C::kTmemCols);
   }
-  if (threadIdx.x == 0) {
-    bulk_store(myblk, stage, static_cast<uint32_t>(blk * 4));
-    bulk_commit();
-    bulk_wait_read_all();   // the source is read before the CTA (and its shared memory) goes away
-  }
-}
-
-// Y = epilogue(sum of the K splits' partial blocks in split order), over the
-// whole GPU.  Launched right after gemm_q4ts_kernel with programmatic stream
-// serialization: it may be scheduled early and waits for the partials.
-template <int MAXS>
-__global__ void __launch_bounds__(256) splitk_sum_kernel(const float* __restrict__ part, int splits, int M, int N,
-                                                         int nch, int n_tiles, const __half* __restrict__ R,
-                                                         int ldr, int relu, __half* __restrict__ Y, int ldy) {
-  griddep_launch();
-  griddep_wait();
-  const size_t blk = static_cast<size_t>(M) * nch;
-  const size_t sstride = static_cast<size_t>(n_tiles) * blk;
-  const int64_t total = static_cast<int64_t>(M) * N / 4;
-  for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < total;
-       e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t flat = 4 * e;
-    const int m = static_cast<int>(flat / N), n = static_cast<int>(flat % N);
-    const float* src = part + (static_cast<size_t>(n / nch) * M + m) * nch + n % nch;
-    // every split's load in flight at once (latency, not bandwidth, bounds
-    // this kernel), then the sum in split order
-    float4 v[MAXS];
+  cluster_sync();   // every split's partial is staged
+  {
+    // rank r reduces rows r, r + S, ... (S = splits): each item is four
+    // consecutive channels of one row, read from every split's partial
+    // (16 bytes each, all in flight at once) and summed in split order
+    const int S = p.splits;
+    const int r = static_cast<int>(cluster_ctarank());
+    const int rows = (p.M - r + S - 1) / S;
+    constexpr int kQuads = NCH / 4;
+    for (int it = threadIdx.x; it < rows * kQuads; it += C::kThreads) {
+      const int m = r + S * (it / kQuads), c = 4 * (it % kQuads);
+      const float* item = stage + m * NCH + c;   // the same offset in every split's shared memory
+      float4 v[kMaxSplits];
 #pragma unroll
-    for (int s = 0; s < MAXS; ++s)
-      if (s < splits) v[s] = __ldcg(reinterpret_cast<const float4*>(src + s * sstride));
-    float4 a4 = v[0];
+      for (int s = 0; s < kMaxSplits; ++s)
+        if (s < S) v[s] = ld_shared_cluster_v4(mapa_shared(item, s));
+      float4 y = v[0];
 #pragma unroll
-    for (int s = 1; s < MAXS; ++s)
-      if (s < splits) {
-        a4.x += v[s].x;
-        a4.y += v[s].y;
-        a4.z += v[s].z;
-        a4.w += v[s].w;
+      for (int s = 1; s < kMaxSplits; ++s)
+        if (s < S) {
+          y.x += v[s].x;
+          y.y += v[s].y;
+          y.z += v[s].z;
+          y.w += v[s].w;
+        }
+      const int ch = n0 + c;
+      if (p.R) {
+        const uint2 rr = *reinterpret_cast<const uint2*>(p.R + static_cast<size_t>(m) * p.ldr + ch);
+        const float2 r01 = __half22float2(*reinterpret_cast<const __half2*>(&rr.x));
+        const float2 r23 = __half22float2(*reinterpret_cast<const __half2*>(&rr.y));
+        y.x += r01.x;
+        y.y += r01.y;
+        y.z += r23.x;
+        y.w += r23.y;
       }
-    if (R) {
-      const uint2 rr = *reinterpret_cast<const uint2*>(R + static_cast<size_t>(m) * ldr + n);
-      const float2 r01 = __half22float2(*reinterpret_cast<const __half2*>(&rr.x));
-      const float2 r23 = __half22float2(*reinterpret_cast<const __half2*>(&rr.y));
-      a4.x += r01.x;
-      a4.y += r01.y;
-      a4.z += r23.x;
-      a4.w += r23.y;
+      if (p.relu) {
+        y.x = fmaxf(y.x, 0.0f);
+        y.y = fmaxf(y.y, 0.0f);
+        y.z = fmaxf(y.z, 0.0f);
+        y.w = fmaxf(y.w, 0.0f);
+      }
+      const __half2 y01 = __floats2half2_rn(y.x, y.y), y23 = __floats2half2_rn(y.z, y.w);
+      *reinterpret_cast<uint2*>(p.Y + static_cast<size_t>(m) * p.ldy + ch) =
+          make_uint2(*reinterpret_cast<const uint32_t*>(&y01), *reinterpret_cast<const uint32_t*>(&y23));
     }
-    if (relu) {
-      a4.x = fmaxf(a4.x, 0.0f);
-      a4.y = fmaxf(a4.y, 0.0f);
-      a4.z = fmaxf(a4.z, 0.0f);
-      a4.w = fmaxf(a4.w, 0.0f);
-    }
-    const __half2 y01 = __floats2half2_rn(a4.x, a4.y), y23 = __floats2half2_rn(a4.z, a4.w);
-    *reinterpret_cast<uint2*>(Y + static_cast<size_t>(m) * ldy + n) =
-        make_uint2(*reinterpret_cast<const uint32_t*>(&y01), *reinterpret_cast<const uint32_t*>(&y23));
   }
+  cluster_sync();   // no CTA leaves while another may still read its partial
 }
 
 template <int BT, int RB, int FMT>
@@ -590,16 +579,18 @@ fg_status launch_ts(TsParams& p, cudaStream_t st) {
   cfg.blockDim = dim3(C::kThreads);
   cfg.dynamicSmemBytes = C::kTotal;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;   // the K splits of a channel tile
+  attr[1].val.clusterDim.x = static_cast<unsigned>(p.splits);
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   if (cudaLaunchKernelEx(&cfg, gemm_q4ts_kernel<BT, RB, FMT>, p) != cudaSuccess)
     return check_launch("gemm_q4ts_kernel (launch)");
-  const fg_status s = check_launch("gemm_q4ts_kernel");
-  if (s != FG_OK || p.splits == 1) return s;
-  return splitk_sum_launch(p.part, p.splits, p.M, p.N, BNC * RB, p.n_tiles, p.R, p.ldr, p.relu, p.Y, p.ldy, st);
+  return check_launch("gemm_q4ts_kernel");
 }
 
 int bt_for(int64_t M) { return M <= 32 ? 32 : (M <= 64 ? 64 : (M <= 128 ? 128 : 256)); }
@@ -611,8 +602,9 @@ int rb_for(const GemmArgs&) { return 1; }
 
 // Split count: K is cut so that the CTAs fill the GPU's slots (one per SM
 // with two row blocks, two per SM with one) with the fewest waves of per-CTA
-// k tiles, plus a charge per split for its partial's round trip through L2.
-// Depends on the shape only.
+// k tiles, plus a charge per split for the cluster's reduction of its
+// partial.  At most kMaxSplits (one portable cluster).  Depends on the shape
+// only.
 int splits_for(int64_t M, int64_t N, int64_t K, int rb) {
   const int64_t tiles = N / (BNC * rb), ktiles = K / BK;
   const int64_t slots = (rb == 1 && M <= 128 ? 2 : 1) * static_cast<int64_t>(num_sms());
@@ -631,39 +623,7 @@ int splits_for(int64_t M, int64_t N, int64_t K, int rb) {
 
 }  // namespace
 
-fg_status splitk_sum_launch(const float* part, int splits, int64_t M, int64_t N, int nch, int n_tiles, const void* R,
-                            int64_t ldr, int relu, void* Y, int64_t ldy, cudaStream_t st) {
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  const int64_t total = M * N / 4;
-  cudaLaunchConfig_t rc = {};
-  rc.gridDim = dim3(static_cast<unsigned>(std::min<int64_t>((total + 255) / 256, static_cast<int64_t>(num_sms()) * 8)));
-  rc.blockDim = dim3(256);
-  rc.stream = st;
-  rc.attrs = attr;
-  rc.numAttrs = 1;
-  trace_extra_launch();
-  // the kernel holds every split's load in registers: the smallest bucket
-  // that fits, so that few splits keep few registers
-  auto sum = splits <= 2 ? splitk_sum_kernel<2>
-             : splits <= 4 ? splitk_sum_kernel<4>
-             : splits <= 8 ? splitk_sum_kernel<8> : splitk_sum_kernel<kMaxSplits>;
-  if (cudaLaunchKernelEx(&rc, sum, part, splits, static_cast<int>(M), static_cast<int>(N), nch, n_tiles,
-                         static_cast<const __half*>(R), static_cast<int>(ldr), relu, static_cast<__half*>(Y),
-                         static_cast<int>(ldy)) != cudaSuccess)
-    return check_launch("splitk_sum_kernel (launch)");
-  return check_launch("splitk_sum_kernel");
-}
-
-size_t gemm_q4ts_workspace_bytes(int64_t M, int64_t N, int64_t K) {
-  size_t need = 0;
-  for (int rb = 1; rb <= 2; ++rb) {   // whichever the weight segments allow
-    const int s = splits_for(M, N, K, rb);
-    if (s > 1) need = std::max(need, static_cast<size_t>(s) * M * N * 4);
-  }
-  return need;
-}
+size_t gemm_q4ts_workspace_bytes(int64_t, int64_t, int64_t) { return 0; }   // splits reduce in the cluster
 
 bool gemm_q4ts_supported(const GemmArgs& a) {
   if (a.dtype != FG_F16 || !a.quant || a.M < 1 || a.M > 256 || a.K % BK) return false;
@@ -679,6 +639,8 @@ bool gemm_q4ts_supported(const GemmArgs& a) {
 }
 
 fg_status gemm_q4ts(const GemmArgs& a, void* ws, size_t ws_bytes, cudaStream_t st) {
+  (void)ws;   // the K splits reduce inside their cluster: no workspace
+  (void)ws_bytes;
   TsParams p;
   memset(&p, 0, sizeof(p));
   const int bt = bt_for(a.M);
@@ -701,11 +663,6 @@ fg_status gemm_q4ts(const GemmArgs& a, void* ws, size_t ws_bytes, cudaStream_t s
     const int want = splits_for(a.M, a.N, a.K, rb);
     p.ktiles_per_split = (ktiles + want - 1) / want;
     p.splits = (ktiles + p.ktiles_per_split - 1) / p.ktiles_per_split;
-  }
-  if (p.splits > 1) {
-    const size_t need = static_cast<size_t>(p.splits) * a.M * a.N * 4;
-    if (!ws || ws_bytes < need) return fail(FG_ERR_WORKSPACE, "decode product needs %zu workspace bytes", need);
-    p.part = static_cast<float*>(ws);
   }
   p.Y = static_cast<__half*>(a.Y);
   p.ldy = static_cast<int>(a.ldy);
