@@ -107,52 +107,62 @@ struct KVDst {
   float* scales[2];
 };
 
-template <typename T>
+// A warp owns one (K or V, sequence, head) and a run of kKvTokens
+// consecutive tokens, so that the codes and (min, scale) pairs it writes are
+// contiguous in the cache (slot-major per head): 8 lanes per 64-group, the
+// groups of a head row side by side, 32 / (8 * groups per head) tokens at
+// a time, two such batches in flight.
+constexpr int kKvTokens = 32;
+
+template <typename T, int NG>
 __global__ void __launch_bounds__(256) kv_store_q4_kernel(const T* __restrict__ ksrc,
                                                           const T* __restrict__ vsrc, int64_t ld,
                                                           int64_t b, int64_t ntok, int64_t pos0,
-                                                          int h1, int heads, int d, int64_t cap,
-                                                          KVDst dst) {
-  // A warp takes whole token rows (one K or V row of h1 values): the row's
-  // indices are worked out once, then its 64-groups go 4 at a time, 8 lanes
-  // per group.  head_dim is 64 or 128, so heads and groups split by shifts.
+                                                          int heads, int64_t cap, KVDst dst) {
+  constexpr int D = 64 * NG;
+  constexpr int kTpi = 4 / NG;   // tokens per warp-wide batch
   const int lane = threadIdx.x & 31;
-  const int part = lane & 7;
-  const int gpr = h1 >> 6;                    // groups per row
-  const int dshift = d == 128 ? 7 : 6;        // log2(head_dim)
-  const int gph = d >> 6;                     // groups per head
-  const int64_t rows = b * ntok;
+  const int part = lane & 7, gi = (lane >> 3) % NG, tb = lane / (8 * NG);
+  const int64_t chunks = (ntok + kKvTokens - 1) / kKvTokens;
+  const int64_t items = 2 * b * heads * chunks;
   const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-  for (int64_t r = warp; r < 2 * rows; r += nwarps) {
-    const int which = r >= rows ? 1 : 0;
-    const int64_t row = r - which * rows;    // bi * ntok + ti
-    const int64_t bi = row / ntok, ti = row - bi * ntok;
-    const T* src = (which ? vsrc : ksrc) + row * ld;
-    const int64_t slot_base = bi * heads * cap + pos0 + ti;   // slot of head 0
+  for (int64_t it = warp; it < items; it += nwarps) {
+    const int64_t ch = it % chunks;
+    const int64_t bh = (it / chunks) % (b * heads);
+    const int which = static_cast<int>(it / (chunks * b * heads));
+    const int64_t bi = bh / heads;
+    const int h = static_cast<int>(bh % heads);
+    const int64_t t0 = ch * kKvTokens, t1 = min(ntok, t0 + kKvTokens);
+    const T* src = (which ? vsrc : ksrc) + (bi * ntok) * ld + h * D + gi * 64 + part * 8;
+    const int64_t slot0 = bh * cap + pos0;
     uint32_t* codes = dst.codes[which];
     float* mins = dst.mins[which];
     float* scales = dst.scales[which];
-    for (int gi0 = 0; gi0 < gpr; gi0 += 4) {
-      const int gi = gi0 + (lane >> 3);
-      const bool valid = gi < gpr;
-      float v[8];
-      if (valid) {
-        load8(src + gi * 64 + part * 8, v);
-      } else {
+    for (int64_t tt = t0; tt < t1; tt += 2 * kTpi) {
+      float v[2][8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = 0.0f;
+      for (int u = 0; u < 2; ++u) {
+        const int64_t ti = tt + u * kTpi + tb;
+        if (ti < t1) {
+          load8(src + ti * ld, v[u]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) v[u][e] = 0.0f;
+        }
       }
-      float mn, sc;
-      const uint32_t packed = quantize_group8(v, mn, sc);
-      if (valid) {
-        const int head = (gi * 64) >> dshift;
-        const int wg = gi - head * gph;
-        const int64_t slot = slot_base + static_cast<int64_t>(head) * cap;
-        codes[(slot * (d >> 1) + wg * 32) / 4 + part] = packed;
-        if (part == 0) {
-          mins[slot * gph + wg] = mn;
-          scales[slot * gph + wg] = sc;
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int64_t ti = tt + u * kTpi + tb;
+        float mn, sc;
+        const uint32_t packed = quantize_group8(v[u], mn, sc);   // every lane of the group takes part
+        if (ti < t1) {
+          const int64_t slot = slot0 + ti;
+          codes[(slot * (D / 2) + gi * 32) / 4 + part] = packed;
+          if (part == 0) {
+            mins[slot * NG + gi] = mn;
+            scales[slot * NG + gi] = sc;
+          }
         }
       }
     }
@@ -223,6 +233,8 @@ fg_status kv_store(const fg_kv& kv, const void* ksrc, const void* vsrc, int64_t 
   const int h1 = kv.heads * kv.head_dim;
   if (b == 0 || ntok == 0) return FG_OK;
   if (kv.codec == FG_CODEC_Q4G64) {
+    if (kv.head_dim != 64 && kv.head_dim != 128)
+      return fail(FG_ERR_UNSUPPORTED, "4-bit cache with head_dim %d (64 or 128)", kv.head_dim);
     KVDst dst;
     dst.codes[0] = reinterpret_cast<uint32_t*>(kv.k_codes);
     dst.codes[1] = reinterpret_cast<uint32_t*>(kv.v_codes);
@@ -230,16 +242,25 @@ fg_status kv_store(const fg_kv& kv, const void* ksrc, const void* vsrc, int64_t 
     dst.mins[1] = kv.v_mins;
     dst.scales[0] = kv.k_scales;
     dst.scales[1] = kv.v_scales;
-    const int grid = grid_for(2 * b * ntok, 8);   // a token row per warp, 8 warps per block
+    const int64_t items = 2 * b * kv.heads * ((ntok + kKvTokens - 1) / kKvTokens);
+    const int grid = grid_for(items, 8);   // a (K/V, sequence, head, token run) per warp, 8 warps per block
     Trace tr(KC_KV_STORE, st);
-    if (kv.dtype == FG_F16)
-      kv_store_q4_kernel<__half><<<grid, 256, 0, st>>>(
-          static_cast<const __half*>(ksrc), static_cast<const __half*>(vsrc), ld, b, ntok, pos0,
-          h1, kv.heads, kv.head_dim, kv.capacity, dst);
-    else
-      kv_store_q4_kernel<float><<<grid, 256, 0, st>>>(
-          static_cast<const float*>(ksrc), static_cast<const float*>(vsrc), ld, b, ntok, pos0, h1,
-          kv.heads, kv.head_dim, kv.capacity, dst);
+    const bool wide = kv.head_dim == 128;
+    if (kv.dtype == FG_F16) {
+      const __half* k = static_cast<const __half*>(ksrc);
+      const __half* v = static_cast<const __half*>(vsrc);
+      if (wide)
+        kv_store_q4_kernel<__half, 2><<<grid, 256, 0, st>>>(k, v, ld, b, ntok, pos0, kv.heads, kv.capacity, dst);
+      else
+        kv_store_q4_kernel<__half, 1><<<grid, 256, 0, st>>>(k, v, ld, b, ntok, pos0, kv.heads, kv.capacity, dst);
+    } else {
+      const float* k = static_cast<const float*>(ksrc);
+      const float* v = static_cast<const float*>(vsrc);
+      if (wide)
+        kv_store_q4_kernel<float, 2><<<grid, 256, 0, st>>>(k, v, ld, b, ntok, pos0, kv.heads, kv.capacity, dst);
+      else
+        kv_store_q4_kernel<float, 1><<<grid, 256, 0, st>>>(k, v, ld, b, ntok, pos0, kv.heads, kv.capacity, dst);
+    }
     return check_launch("kv_store_q4_kernel");
   }
   const int64_t n8 = 2 * b * ntok * (h1 / 8);

@@ -48,10 +48,21 @@ __device__ __forceinline__ uint32_t quantize_group8(const float (&v)[8], float& 
     mx = key_to_float(kmax);
   }
   const float r = __fsub_rn(mx, mn);
+  // u = ((x - min) / r) * 15 with each op rounded as written decides the
+  // code through rint.  One product t * (15 / r), with 15 / r rounded once
+  // per group, is within 4 ulp of u (relative; u <= 15, so within 3.6e-6);
+  // wherever it lies further than 1e-5 from a rounding boundary (k + 1/2)
+  // both round to the same integer, and elsewhere -- or for a group whose r
+  // is zero, infinite or NaN -- u itself is formed.  The codes equal those of
+  // the literal op order.
+  const float c15 = __fdiv_rn(15.0f, r);
+  const bool fast = r > 0.0f && r < INFINITY && c15 < INFINITY;
   uint32_t packed = 0;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const float u = __fmul_rn(__fdiv_rn(__fsub_rn(v[i], mn), r), 15.0f);
+    const float t = __fsub_rn(v[i], mn);
+    float u = __fmul_rn(t, c15);
+    if (!fast || fabsf(fabsf(__fsub_rn(u, rintf(u))) - 0.5f) < 1e-5f) u = __fmul_rn(__fdiv_rn(t, r), 15.0f);
     const float q = fminf(fmaxf(rintf(u), 0.0f), 15.0f);  // NaN -> 0
     packed |= static_cast<uint32_t>(q) << (4 * i);
   }
