@@ -410,6 +410,7 @@ def run_ours(args, w, rank, world, device):
     # a few layers: the page's layer has no normalisation); per-kernel device
     # time per layer-step, beside the chained run's
     finite, topk = finite_layer_steps(fg, w, layers[w.l // 2], dev, st, args.steps)
+    offload = None if args.no_offload else offload_timing(fg, w, layers, kvs, tin, ws, dev, st)
 
     if rank != 0:
         return
@@ -496,6 +497,7 @@ def run_ours(args, w, rank, world, device):
                                           for k, v in ((f"decode:{a}", b) for a, b in dec_prof.items())},
             "finite_us_per_layer_step": finite},
         "topk_attention_4bit_s": topk,
+        "offload_c2c": offload,
         "clocks": clocks, "wall_s_timed": t_wall,
     }
     print(json.dumps(line), flush=True)
@@ -527,6 +529,35 @@ def finite_layer_steps(fg, w, L, dev, st, steps: int) -> dict:
             total[name] = total.get(name, 0.0) + ms
     per_step = {name: round(ms / (w.n * max(1, steps)) * 1e3, 2) for name, ms in total.items()}
     return per_step, topk_attention_timing(fg, w, kv, dev, st)
+
+
+def offload_timing(fg, w, layers, kvs, tin, ws, dev, st, steps: int = 4) -> dict:
+    """Decode steps with every layer's decode copies in pinned host memory,
+    streamed over NVLink-C2C into a two-half device stage while the previous
+    layer computes (fg_decode_block_step_offload, Algorithm 1's overlap):
+    device time per step and the host-to-device rate it implies.  Runs on the
+    stack's caches after the timed region (it rewrites slots s..s+steps-1)."""
+    host = [L.offloaded(stored_too=False) for L in layers]
+    blk = fg.Block(host, kvs)
+    stage = fg.workspace(fg.fg_offload_stage_bytes(layers[0]), dev)
+    copy = torch.cuda.Stream(device=dev)
+    out = torch.empty_like(tin[0])
+    for t in range(2):   # warm-up
+        fg.fg_decode_block_step_offload(blk, tin[t], w.s + t, out, ws, stage, st, copy)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for t in range(steps):
+        fg.fg_decode_block_step_offload(blk, tin[t], w.s + t, out, ws, stage, st, copy)
+    e1.record(st)
+    e1.synchronize()
+    fg.fg_sync_status()
+    ms = e0.elapsed_time(e1) / steps
+    per_step = w.l * fg.fg_offload_stage_bytes(layers[0]) / 2
+    return {"steps": steps, "ms_per_step": round(ms, 3), "tokens_per_s": round(w.b / (ms * 1e-3), 1),
+            "h2d_bytes_per_step": per_step, "h2d_gbs": round(per_step / (ms * 1e-3) / 1e9, 1),
+            "definition": "decode copies of all layers in pinned host memory, copied layer by layer on a "
+                          "second stream while the previous layer computes; KV cache and activations in HBM"}
 
 
 def topk_attention_timing(fg, w, kv, dev, st, calls: int = 10) -> dict:
@@ -663,6 +694,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle timing")
     ap.add_argument("--no-graph", action="store_true", help="decode steps by direct calls, not replayed graphs")
+    ap.add_argument("--no-offload", action="store_true", help="skip the host-offloaded decode timing")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--m", type=int, default=None, help="rows of a decode-product case (default: the block size)")
     ap.add_argument("--case", choices=CASES, default=None,

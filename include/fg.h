@@ -304,6 +304,25 @@ fg_status fg_decode_block_step(const fg_layer* layers, int32_t l, const void* t,
                                int64_t pos, const fg_kv* kvs, void* y, void* ws,
                                size_t ws_bytes, cudaStream_t stream);
 
+/* [S4] Algorithm 1 on GB300: the zig-zag block's decode step with the
+ * weights offloaded to host memory (the Grace LPDDR behind NVLink-C2C).
+ * layers[] are fp16 4-bit layers whose decode copies (w->packed, all six
+ * matrices, one format) may live in host memory (pinned, or any memory
+ * cudaMemcpyAsync reads); the decode kernels read nothing else of a weight.
+ * Layer by layer, the six copies are copied on `copy_stream` into one of
+ * two halves of `stage` (device, 256-byte aligned, stage_bytes >=
+ * fg_offload_stage_bytes(&layers[0])) while `stream` computes the previous
+ * layer from the other half: the load of layer i+1 overlaps the compute of
+ * layer i.  Events order the halves between the two streams (a per-device
+ * set kept by the library: calls on one device must not overlap).  Same
+ * arguments, results and errors as fg_decode_block_step otherwise; the
+ * outputs are bit-identical to it.  copy_stream may equal stream (no
+ * overlap).  Layers that need no decode copy -> FG_ERR_UNSUPPORTED. */
+size_t fg_offload_stage_bytes(const fg_layer* L);
+fg_status fg_decode_block_step_offload(const fg_layer* layers, int32_t l, const void* t, int64_t b, int64_t pos,
+                                       const fg_kv* kvs, void* y, void* ws, size_t ws_bytes, void* stage,
+                                       size_t stage_bytes, cudaStream_t stream, cudaStream_t copy_stream);
+
 /* [S4] the zig-zag block's decode step replayed as a CUDA graph: the same
  * arguments, results and errors as fg_decode_block_step.  The first call
  * with a given set of arguments (every pointer and size, and the bytes of

@@ -250,6 +250,20 @@ class Layer:
     def nbytes(self) -> int:
         return sum(self.w[m].nbytes() for m in self.MATS)
 
+    def offloaded(self, stored_too: bool = True) -> "Layer":
+        """The same layer with its weight arrays in pinned host memory (for
+        fg_decode_block_step_offload, which streams the decode copies to the
+        device layer by layer).  stored_too=False moves only the decode
+        copies (the stored form stays where it is; a decode step reads only
+        the copies)."""
+        def host(t, move=True):
+            return None if t is None else (t.cpu().pin_memory() if move else t)
+        q = {m: QuantWeight(self.w[m].K, self.w[m].N, host(self.w[m].codes, stored_too),
+                            host(self.w[m].mins, stored_too), host(self.w[m].scales, stored_too),
+                            host(self.w[m].dense, stored_too), host(self.w[m].packed),
+                            self.w[m].packed_format) for m in self.MATS}
+        return Layer(q, self.h1, self.h2, self.heads, self.quantized, self.dtype)
+
 
 class KVCache:
     """[b][heads][capacity][head_dim] cache, Q4G64 or dense, on `device`."""
@@ -390,6 +404,27 @@ def fg_decode_block_step_graphed(cache: GraphCache, block: Block, t: torch.Tenso
     _check(_lib.fg_decode_block_step_graphed(cache._h, block.larr, len(block.layers), _ptr(t), t.shape[0], int(pos),
                                              block.karr, _ptr(y), _ptr(ws), ws.numel(), _stream(stream)),
            "fg_decode_block_step_graphed")
+
+
+_sig("fg_offload_stage_bytes", _SZ, ctypes.POINTER(fg_layer))
+_sig("fg_decode_block_step_offload", _INT, ctypes.POINTER(fg_layer), ctypes.c_int32, _P, _I64, _I64,
+     ctypes.POINTER(fg_kv), _P, _P, _SZ, _P, _SZ, _P, _P)
+
+
+def fg_offload_stage_bytes(layer: Layer) -> int:
+    return _lib.fg_offload_stage_bytes(ctypes.byref(layer.struct))
+
+
+def fg_decode_block_step_offload(block: Block, t: torch.Tensor, pos: int, y: torch.Tensor, ws: torch.Tensor,
+                                 stage: torch.Tensor, stream=None, copy_stream=None) -> None:
+    """A decode step of a block whose layers' weights live in host memory
+    (Layer.offloaded): the next layer's decode copies are copied into one half
+    of `stage` on copy_stream while this layer computes from the other."""
+    _check(_lib.fg_decode_block_step_offload(block.larr, len(block.layers), _ptr(t), t.shape[0], int(pos),
+                                             block.karr, _ptr(y), _ptr(ws), ws.numel(), _ptr(stage), stage.numel(),
+                                             _stream(stream), _stream(copy_stream if copy_stream is not None
+                                                                      else stream)),
+           "fg_decode_block_step_offload")
 
 
 def fg_sync_status(stream=None) -> None:

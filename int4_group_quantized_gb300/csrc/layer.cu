@@ -3,6 +3,8 @@
 // whole block resident, so one pass over a layer's weights serves every
 // sequence of the block).  Argument validation, workspace layout and the
 // sequence of kernel launches live here; the arithmetic is in the kernels.
+#include <mutex>
+
 #include "fg_internal.cuh"
 
 namespace fg {
@@ -512,6 +514,134 @@ fg_status fg_decode_block_step(const fg_layer* layers, int32_t l, const void* t,
     void* out = (i == l - 1) ? y : ping[i & 1];
     FG_TRY(run_decode(layers[i], in, b, pos, kvs[i], out, ws,
                       scratch_bytes(layers[i], b, kvs[i].capacity, true), stream));
+    in = out;
+  }
+  return FG_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Decode with the weights offloaded to host memory (FlexGen notes, "4. 卸载
+// 策略", Algorithm 1: the next layer's weights are loaded while the current
+// layer computes).  On GB300 host memory is the Grace LPDDR behind
+// NVLink-C2C.  The six decode copies of a layer are the only weight bytes a
+// decode step reads; they go, layer by layer, into one of two device stage
+// buffers on a copy stream, while the compute stream runs the previous
+// layer from the other buffer.  Two events per buffer order the pair: the
+// compute stream waits until a buffer is loaded, the copy stream until the
+// layer that last read it has finished.
+// ---------------------------------------------------------------------------
+namespace {
+
+struct StageLayout {
+  size_t off[6];
+  size_t bytes[6];
+  size_t total;
+};
+
+StageLayout stage_layout(const fg_layer& L) {
+  StageLayout S;
+  const fg_wmat* m[6] = {&L.wq, &L.wk, &L.wv, &L.wo, &L.w1, &L.w2};
+  size_t at = 0;
+  for (int i = 0; i < 6; ++i) {
+    S.off[i] = at;
+    S.bytes[i] = pack_weight_bytes(m[i]->K, m[i]->N, m[i]->packed_format);
+    at += up(S.bytes[i]);
+  }
+  S.total = at;
+  return S;
+}
+
+struct OffloadEvents {
+  cudaEvent_t loaded[2] = {nullptr, nullptr};
+  cudaEvent_t released[2] = {nullptr, nullptr};
+};
+
+fg_status offload_events(OffloadEvents** out) {
+  static std::mutex mu;
+  static OffloadEvents ev[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return fail(FG_ERR_CUDA, "cudaGetDevice");
+  std::lock_guard<std::mutex> lk(mu);
+  OffloadEvents& e = ev[dev];
+  for (int i = 0; i < 2; ++i) {
+    if (!e.loaded[i] && cudaEventCreateWithFlags(&e.loaded[i], cudaEventDisableTiming) != cudaSuccess)
+      return check_launch("cudaEventCreateWithFlags");
+    if (!e.released[i] && cudaEventCreateWithFlags(&e.released[i], cudaEventDisableTiming) != cudaSuccess)
+      return check_launch("cudaEventCreateWithFlags");
+  }
+  *out = &e;
+  return FG_OK;
+}
+
+}  // namespace
+
+extern "C" size_t fg_offload_stage_bytes(const fg_layer* L) {
+  if (check_layer(L) != FG_OK || !decode_needs_copies(*L)) return 0;
+  return 2 * stage_layout(*L).total;
+}
+
+extern "C" fg_status fg_decode_block_step_offload(const fg_layer* layers, int32_t l, const void* t, int64_t b,
+                                                  int64_t pos, const fg_kv* kvs, void* y, void* ws, size_t ws_bytes,
+                                                  void* stage, size_t stage_bytes, cudaStream_t stream,
+                                                  cudaStream_t copy_stream) {
+  if (!layers || !kvs || l <= 0) return fail(FG_ERR_ARG, "layers/kvs/l");
+  for (int32_t i = 0; i < l; ++i) {
+    FG_TRY(check_layer(&layers[i]));
+    if (!decode_needs_copies(layers[i]))
+      return fail(FG_ERR_UNSUPPORTED, "offloaded decode streams the decode copies of fp16 4-bit layers");
+    FG_TRY(check_decode_copies(layers[i]));
+    if (layers[i].h1 != layers[0].h1 || layers[i].h2 != layers[0].h2 ||
+        layers[i].wq.packed_format != layers[0].wq.packed_format)
+      return fail(FG_ERR_SHAPE, "layers differ in h1/h2/decode-copy format");
+    FG_TRY(check_kv(&kvs[i], b, layers[i].heads, layers[i].h1 / layers[i].heads, layers[i].codec,
+                    layers[i].dtype));
+    if (pos < 0 || pos >= kvs[i].capacity)
+      return fail(FG_ERR_CAPACITY, "pos %lld outside [0, %lld)", (long long)pos, (long long)kvs[i].capacity);
+  }
+  const StageLayout S = stage_layout(layers[0]);
+  if (!stage || stage_bytes < 2 * S.total) return fail(FG_ERR_WORKSPACE, "stage %zu < %zu bytes", stage_bytes, 2 * S.total);
+  if (!aligned(stage, kAlign)) return fail(FG_ERR_ALIGN, "stage needs 256-byte alignment");
+  if (b == 0) return FG_OK;
+  FG_TRY(check_act(t, "t"));
+  FG_TRY(check_act(y, "y"));
+  size_t layer_ws = 0;
+  for (int32_t i = 0; i < l; ++i) {
+    const size_t w = fg_decode_workspace_bytes(&layers[i], b, kvs[i].capacity);
+    layer_ws = w > layer_ws ? w : layer_ws;
+  }
+  const size_t act = up(b * layers[0].h1 * dtype_bytes(layers[0].dtype));
+  const size_t need = up(layer_ws) + 2 * act;
+  if (!ws || ws_bytes < need) return fail(FG_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes, need);
+  if (!aligned(ws, kAlign)) return fail(FG_ERR_ALIGN, "workspace needs 256-byte alignment");
+
+  OffloadEvents* E = nullptr;
+  FG_TRY(offload_events(&E));
+  char* buf[2] = {static_cast<char*>(stage), static_cast<char*>(stage) + S.total};
+  // layer j's six decode copies into buffer j % 2, once the layer that last
+  // read that buffer has finished
+  auto load = [&](int32_t j) -> fg_status {
+    const int s = j & 1;
+    if (cudaStreamWaitEvent(copy_stream, E->released[s], 0) != cudaSuccess) return check_launch("cudaStreamWaitEvent");
+    const fg_wmat* m[6] = {&layers[j].wq, &layers[j].wk, &layers[j].wv, &layers[j].wo, &layers[j].w1, &layers[j].w2};
+    for (int k = 0; k < 6; ++k)
+      if (cudaMemcpyAsync(buf[s] + S.off[k], m[k]->packed, S.bytes[k], cudaMemcpyDefault, copy_stream) != cudaSuccess)
+        return check_launch("cudaMemcpyAsync (decode copy to the stage)");
+    if (cudaEventRecord(E->loaded[s], copy_stream) != cudaSuccess) return check_launch("cudaEventRecord");
+    return FG_OK;
+  };
+  char* ping[2] = {static_cast<char*>(ws) + up(layer_ws), static_cast<char*>(ws) + up(layer_ws) + act};
+  const void* in = t;
+  FG_TRY(load(0));
+  for (int32_t i = 0; i < l; ++i) {
+    if (i + 1 < l) FG_TRY(load(i + 1));   // the next layer streams in while this one computes
+    const int s = i & 1;
+    if (cudaStreamWaitEvent(stream, E->loaded[s], 0) != cudaSuccess) return check_launch("cudaStreamWaitEvent");
+    fg_layer Ld = layers[i];   // the same layer, its decode copies read from the stage
+    fg_wmat* m[6] = {&Ld.wq, &Ld.wk, &Ld.wv, &Ld.wo, &Ld.w1, &Ld.w2};
+    for (int k = 0; k < 6; ++k) m[k]->packed = reinterpret_cast<const uint8_t*>(buf[s] + S.off[k]);
+    void* out = (i == l - 1) ? y : ping[i & 1];
+    FG_TRY(run_decode(Ld, in, b, pos, kvs[i], out, ws, scratch_bytes(Ld, b, kvs[i].capacity, true), stream));
+    if (cudaEventRecord(E->released[s], stream) != cudaSuccess) return check_launch("cudaEventRecord");
     in = out;
   }
   return FG_OK;

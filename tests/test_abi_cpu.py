@@ -165,6 +165,27 @@ def test_topk_attention_host_errors(fg):
     assert fg.topk_keep(528) == 53 and fg.topk_keep(530) == 53 and fg.topk_keep(1) == 1
 
 
+def test_offload_host_errors(fg):
+    """fg_decode_block_step_offload checks its arguments on the host first."""
+    L = fg.lib
+    P = ctypes.c_void_p(4096)
+    lay, kv = _layer(fg, packed=True), _kv(fg)
+    larr = (fg.fg_layer * 1)(lay)
+    karr = (fg.fg_kv * 1)(kv)
+    stage = L.fg_offload_stage_bytes(ctypes.byref(lay))
+    assert stage > 0
+    ws = L.fg_decode_block_workspace_bytes(ctypes.byref(lay), 2, 16)
+    args = lambda st_ptr, st_bytes, pos=3: (larr, 1, P, 2, pos, karr, P, ctypes.c_void_p(4096), ws, st_ptr,
+                                            st_bytes, None, None)
+    assert L.fg_decode_block_step_offload(*args(None, stage)) == 5            # no stage
+    assert L.fg_decode_block_step_offload(*args(P, stage - 1)) == 5           # stage too small
+    assert L.fg_decode_block_step_offload(*args(ctypes.c_void_p(4096 + 16), stage)) == 3   # alignment
+    assert L.fg_decode_block_step_offload(*args(P, stage, pos=16)) == 4       # pos at capacity
+    nocopy = _layer(fg, packed=False)
+    assert L.fg_decode_block_step_offload((fg.fg_layer * 1)(nocopy), 1, P, 2, 3, karr, P, P, ws, P, stage,
+                                          None, None) == 1                     # no decode copies
+
+
 def test_noalloc_scratch_bound_covers_every_cache(fg):
     """The built-in split scratch (1 MiB) holds what the split rule asks for,
     for every block size and cache capacity up to 4096 with head_dim 64 and
