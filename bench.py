@@ -554,10 +554,49 @@ def offload_timing(fg, w, layers, kvs, tin, ws, dev, st, steps: int = 4) -> dict
     fg.fg_sync_status()
     ms = e0.elapsed_time(e1) / steps
     per_step = w.l * fg.fg_offload_stage_bytes(layers[0]) / 2
-    return {"steps": steps, "ms_per_step": round(ms, 3), "tokens_per_s": round(w.b / (ms * 1e-3), 1),
-            "h2d_bytes_per_step": per_step, "h2d_gbs": round(per_step / (ms * 1e-3) / 1e9, 1),
-            "definition": "decode copies of all layers in pinned host memory, copied layer by layer on a "
-                          "second stream while the previous layer computes; KV cache and activations in HBM"}
+    res = {"steps": steps, "ms_per_step": round(ms, 3), "tokens_per_s": round(w.b / (ms * 1e-3), 1),
+           "h2d_bytes_per_step": per_step, "h2d_gbs": round(per_step / (ms * 1e-3) / 1e9, 1),
+           "definition": "decode copies of all layers in pinned host memory, copied layer by layer on a "
+                         "second stream while the previous layer computes; KV cache and activations in HBM"}
+    # the same weights read in place by the decode kernels' bulk copies over
+    # NVLink-C2C (no stage), where the pinned pages are mapped at the same
+    # address on the device
+    if all(_device_maps_host_at_same_address(L.w[m].packed.data_ptr()) for L in host for m in fg.Layer.MATS):
+        blk0 = fg.Block(host, kvs)
+        fg.fg_decode_block_step(blk0, tin[0], w.s, out, ws, st)
+        torch.cuda.synchronize()
+        e0.record(st)
+        for t in range(steps):
+            fg.fg_decode_block_step(blk0, tin[t], w.s + t, out, ws, st)
+        e1.record(st)
+        e1.synchronize()
+        fg.fg_sync_status()
+        zms = e0.elapsed_time(e1) / steps
+        res["in_place"] = {"ms_per_step": round(zms, 3), "tokens_per_s": round(w.b / (zms * 1e-3), 1),
+                           "host_read_gbs": round(per_step / (zms * 1e-3) / 1e9, 1)}
+    return res
+
+
+def _device_maps_host_at_same_address(ptr: int) -> bool:
+    """cudaPointerGetAttributes: pinned host memory whose device address is
+    the host address (so a kernel may read it through the pointer)."""
+    import ctypes
+
+    class Attr(ctypes.Structure):   # cudaPointerAttributes as the CUDA 13 runtime header declares it
+        _fields_ = [("type", ctypes.c_int), ("device", ctypes.c_int), ("devicePointer", ctypes.c_void_p),
+                    ("hostPointer", ctypes.c_void_p), ("reserved", ctypes.c_long * 8)]
+    for name in ("libcudart.so", "libcudart.so.13", "/usr/local/cuda/lib64/libcudart.so"):
+        try:
+            rt = ctypes.CDLL(name)
+            break
+        except OSError:
+            rt = None
+    if rt is None:
+        return False
+    a = Attr()
+    if rt.cudaPointerGetAttributes(ctypes.byref(a), ctypes.c_void_p(ptr)) != 0:
+        return False
+    return a.type == 1 and a.devicePointer == ptr and a.hostPointer == ptr
 
 
 def topk_attention_timing(fg, w, kv, dev, st, calls: int = 10) -> dict:
