@@ -58,10 +58,10 @@ PACK_BYTES = {0: Q4, 1: 0.5 + 4.0 / 64.0}
 TRAFFIC = {"gemm_q4_decode": {
     "sources": ("int4_group_quantized_gb300/csrc/gemm_q4ts.cu", "int4_group_quantized_gb300/csrc/q4_convert.cuh",
                 "int4_group_quantized_gb300/csrc/q4_dev.cuh", "int4_group_quantized_gb300/csrc/tc_ptx.cuh"),
-    "sha256_16": ("c933a8f2578eb58b", "bdc48444633d6cb6", "360d7c9967f0a780", "9dc843e43182b935"),
-    "dram_bytes": 32036864.0,
+    "sha256_16": ("3157f5bfb3e916e3", "bdc48444633d6cb6", "360d7c9967f0a780", "396e7d83852eb72d"),
+    "dram_bytes": 32036096.0,
     "algorithmic_bytes": 4096 * 12288 * Q4 + 2 * 64 * (4096 + 3 * 4096),
-    "capture": "ncu, x.[w_Q w_K w_V] M=64 K=4096 N=12288, mean of 4 launches"}}
+    "capture": "ncu, x.[w_Q w_K w_V] M=64 K=4096 N=12288, one launch (K splits reduced in the cluster)"}}
 
 
 def traffic_per_launch(kernel: str, algorithmic_per_launch: float):
