@@ -1,0 +1,377 @@
+// Causal prefill attention on tcgen05 (FlexGen notes, "背景知识": x_Out =
+// Softmax(x_Q x_K^T / sqrt(h1)) x_V per head, causal for generation;
+// "5. 近似方法": K and V are read back from the 4-bit cache as FP16).
+//
+// Input: the layer's Q|K|V buffer [b*s][ld] (fp16) in which the K and V
+// columns already hold the values the cache restores, fp16(fmaf(q, scale,
+// min)) (written back by the K/V store), so that the attention reads
+// exactly the cached values.  s is a multiple of 128.
+//
+// One CTA per (sequence, head, 128-query tile), flash-style over 128-key
+// tiles up to the diagonal:
+//   * a TMA thread loads Q once and K, V tiles into a two-stage ring (one
+//     tensor map over the buffer, boxes of 64 columns x 128 rows, 128-byte
+//     swizzle: K-major panels for Q and K, MN-major column blocks for V);
+//   * one thread issues S = Q K^T (M = N = 128, K = head_dim) into tensor
+//     memory, and O += P V (K = 128 keys) into a second tensor-memory block;
+//   * four softmax warps (one query row per thread) read S with tcgen05.ld,
+//     mask the diagonal tile, keep the running max and sum in base 2 and
+//     write P (fp16) into shared memory in the swizzled K-major layout the
+//     next MMA reads.  O is rescaled in tensor memory only when a row's max
+//     grows by more than 2^8 (otherwise P is formed against the stale max,
+//     which keeps it below 256 and the result the same up to rounding);
+//   * S of the next tile is computed while the softmax works on this one.
+// At the end the softmax warps divide O by the row sums and store fp16.
+// Every mbarrier wait is bounded; on timeout the CTA raises the library's
+// device error word, lets its copies and MMAs finish and frees its tensor
+// memory.
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <string.h>
+
+#include "fg_internal.cuh"
+#include "tc_ptx.cuh"
+
+namespace fg {
+
+// defined in gemm_tc.cu
+bool tc_make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+                 uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw);
+
+namespace {
+
+using namespace tc;
+
+constexpr int kTile = 128;          // queries per CTA, keys per tile
+constexpr int kThreads = 192;       // warp 0: TMA, warp 1: MMA + TMEM, warps 2..5: softmax
+constexpr int kSoftWarp0 = 2;
+constexpr float kRescale = 8.0f;    // log2 growth of a row max that forces a rescale of O
+
+struct PaParams {
+  CUtensorMap map;      // the Q|K|V buffer, box {64, 128}
+  __half* out;          // [b*s][ldo]
+  int ldo;
+  int s, heads, h1;
+  int qtiles;           // s / 128
+  float scale_log2;     // log2(e) / sqrt(head_dim)
+  unsigned int* err;
+  uint32_t wait_limit;
+};
+
+template <int D>
+struct PaSmem {
+  static constexpr int kPanels = D / 64;          // 64-column panels of a head row
+  static constexpr int kPanel = kTile * 128;      // 16 KiB: 128 rows x 128 bytes
+  static constexpr int kQ = kPanels * kPanel;
+  static constexpr int kK = kPanels * kPanel;
+  static constexpr int kV = kPanels * kPanel;     // MN-major: D/64 blocks of 128 keys x 64 dims
+  static constexpr int kP = 2 * kPanel;           // 128 queries x 128 keys, two K-major panels
+  static constexpr int kStage = kK + kV;
+  static constexpr int kBytes = 1024 + kQ + 2 * kStage + kP + 256;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) prefill_attn_tc_kernel(const __grid_constant__ PaParams p) {
+  using S = PaSmem<D>;
+  constexpr uint32_t kIdescS = idesc_f16(128, 128, 0, 0);   // A = Q (K-major), B = K (K-major)
+  constexpr uint32_t kIdescO = idesc_f16(128, D, 0, 1);     // A = P (K-major), B = V (MN-major)
+  constexpr uint32_t kTmemCols = 256;                       // S: columns 0..127, O: 128..128+D-1
+  constexpr uint32_t kO = 128;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = sm;
+  uint8_t* sKV = sQ + S::kQ;                 // two stages: [K panels][V blocks]
+  uint8_t* sP = sKV + 2 * S::kStage;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + S::kP);
+  uint64_t* qfull = bars;
+  uint64_t* kvfull = bars + 1;     // [2]
+  uint64_t* kvfree = bars + 3;     // [2] the PV MMA of the tile has read the stage
+  uint64_t* sfull = bars + 5;      // S of the tile is in tensor memory
+  uint64_t* sfree = bars + 6;      // four softmax warps have read S
+  uint64_t* pfull = bars + 7;      // four softmax warps have written P
+  uint64_t* odone = bars + 8;      // PV of the tile has completed
+  uint64_t* done = bars + 9;       // every MMA has completed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 10);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // longest query tiles first
+  const int qt = p.qtiles - 1 - static_cast<int>(blockIdx.x % p.qtiles);
+  const int bh = static_cast<int>(blockIdx.x / p.qtiles);
+  const int bi = bh / p.heads, h = bh % p.heads;
+  const int row0 = bi * p.s;              // the sequence's first row of the buffer
+  const int nkt = qt + 1;                 // key tiles up to the diagonal
+  const int colq = h * D, colk = p.h1 + h * D, colv = 2 * p.h1 + h * D;
+
+  if (threadIdx.x == 0) {
+    mbar_init(qfull, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&kvfull[i], 1);
+      mbar_init(&kvfree[i], 1);
+    }
+    mbar_init(sfull, 1);
+    mbar_init(sfree, 4);
+    mbar_init(pfull, 4);
+    mbar_init(odone, 1);
+    mbar_init(done, 1);
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+  if (warp == 0 && lane == 0) tma_prefetch_desc(&p.map);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ---- TMA: Q once, then K and V of each key tile -----------------------------
+    if (lane == 0) {
+      mbar_expect_tx(qfull, S::kQ);
+      for (int pn = 0; pn < S::kPanels; ++pn)
+        tma_load_2d(sQ + pn * S::kPanel, &p.map, colq + 64 * pn, row0 + qt * kTile, qfull);
+      int issued = 0;
+      for (int j = 0; j < nkt; ++j) {
+        const int st = j & 1;
+        if (!mbar_wait(&kvfree[st], ((j >> 1) & 1) ^ 1, p.wait_limit, abort_flag)) break;
+        uint8_t* stage = sKV + st * S::kStage;
+        mbar_expect_tx(&kvfull[st], S::kStage);
+        for (int pn = 0; pn < S::kPanels; ++pn) {
+          tma_load_2d(stage + pn * S::kPanel, &p.map, colk + 64 * pn, row0 + j * kTile, &kvfull[st]);
+          tma_load_2d(stage + S::kK + pn * S::kPanel, &p.map, colv + 64 * pn, row0 + j * kTile, &kvfull[st]);
+        }
+        ++issued;
+      }
+      volatile int dummy = 0;   // nothing in flight at exit
+      mbar_wait(qfull, 0, kDrainLimit, &dummy);
+      for (int j = (issued > 2 ? issued - 2 : 0); j < issued; ++j)
+        mbar_wait(&kvfull[j & 1], (j >> 1) & 1, kDrainLimit, &dummy);
+      if (*abort_flag) atomicOr(p.err, DEV_ERR_WAIT_TIMEOUT);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---- MMA issuer --------------------------------------------------------------
+    if (lane == 0) {
+      bool ok = mbar_wait(qfull, 0, p.wait_limit, abort_flag);
+      const uint32_t q_addr = smem_u32(sQ), p_addr = smem_u32(sP);
+      // S of tile j: needs K_j and a free S (tile j-1's scores read)
+      auto issue_s = [&](int j) -> bool {
+        const int st = j & 1;
+        if (!mbar_wait(&kvfull[st], (j >> 1) & 1, p.wait_limit, abort_flag)) return false;
+        if (j > 0 && !mbar_wait(sfree, (j - 1) & 1, p.wait_limit, abort_flag)) return false;
+        tc_fence_after();
+        const uint32_t k_addr = smem_u32(sKV + st * S::kStage);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * S::kPanel + (kk % 4) * 32;
+          mma_f16(tmem, smem_desc_sw128(q_addr + off, 16, 1024), smem_desc_sw128(k_addr + off, 16, 1024), kIdescS,
+                  kk > 0 ? 1u : 0u);
+        }
+        mma_commit(sfull);
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      for (int j = 0; j < nkt && ok; ++j) {
+        // the next tile's scores while the softmax works on this one
+        if (j + 1 < nkt) ok = issue_s(j + 1);
+        if (!ok) break;
+        if (!mbar_wait(pfull, j & 1, p.wait_limit, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t v_addr = smem_u32(sKV + (j & 1) * S::kStage + S::kK);
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk) {
+          // A = P: K-major panels of 64 keys; B = V: 64-dim blocks 16 KiB apart
+          // (leading byte offset), 8-key groups 1 KiB apart (stride)
+          const uint64_t a = smem_desc_sw128(p_addr + (kk / 4) * S::kPanel + (kk % 4) * 32, 16, 1024);
+          const uint64_t b = smem_desc_sw128(v_addr + kk * 2048, S::kPanel, 1024);
+          mma_f16(tmem + kO, a, b, kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(&kvfree[j & 1]);   // K_j and V_j are read
+        mma_commit(odone);
+      }
+      mma_commit(done);
+      if (!ok) atomicOr(p.err, DEV_ERR_WAIT_TIMEOUT);
+    }
+    __syncwarp();
+  } else if (warp >= kSoftWarp0) {
+    // ---- softmax warps: query row r = 32 * (warp % 4) + lane --------------------------
+    const int quarter = warp & 3;
+    const int r = 32 * quarter + lane;
+    const uint32_t trow = tmem + (static_cast<uint32_t>(32 * quarter) << 16);
+    const int qpos = qt * kTile + r;      // the query's position in its sequence
+    float m = -INFINITY, l = 0.0f;
+    bool ok = true;
+    uint8_t* prow = sP + r * 128;         // this row in each P panel
+    for (int j = 0; j < nkt; ++j) {
+      // tcgen05.ld/st are warp-collective: every branch around them is
+      // taken by the whole warp
+      if (ok) ok = mbar_wait(sfull, j & 1, p.wait_limit, abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+      tc_fence_after();
+      float sv[128];
+      if (ok) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t u[32];
+          tmem_ld_32x32b_x32(trow + 32 * c, u);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) sv[32 * c + e] = __uint_as_float(u[e]) * p.scale_log2;
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sfree);   // S may be overwritten by the next tile's scores
+      // causal mask on the diagonal tile: key 128j + c is visible iff <= qpos
+      float mx = -INFINITY;
+      const int kbase = j * kTile;
+#pragma unroll
+      for (int c = 0; c < 128; ++c) {
+        if (kbase + c > qpos) sv[c] = -INFINITY;
+        mx = fmaxf(mx, sv[c]);
+      }
+      // P may be written once the previous tile's PV has read it; O may be
+      // rescaled only then too
+      if (j > 0 && ok) ok = mbar_wait(odone, (j - 1) & 1, p.wait_limit, abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+      tc_fence_after();
+      if (j == 0) {
+        m = mx;
+      } else {
+        // rows whose max grew by more than 2^8 take the new max and scale
+        // their O by alpha; the other rows of the warp keep theirs (alpha 1)
+        const bool grow = mx > m + kRescale;
+        const float alpha = grow ? exp2f(m - mx) : 1.0f;
+        if (grow) {
+          l *= alpha;
+          m = mx;
+        }
+        if (__any_sync(0xffffffffu, grow) && ok) {
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t u[32];
+            tmem_ld_32x32b_x32(trow + kO + 32 * c, u);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) u[e] = __float_as_uint(__uint_as_float(u[e]) * alpha);
+            tmem_st_32x32b_x32(trow + kO + 32 * c, u);
+          }
+          tmem_st_wait();
+        }
+      }
+      // P = exp2(s - m) in fp16, 8 keys (one 16-byte chunk) at a time, into the
+      // swizzled K-major panels (chunk c8 of row r at c8 ^ (r % 8))
+      float lsum = 0.0f;
+#pragma unroll
+      for (int c8 = 0; c8 < 16; ++c8) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float p0 = exp2f(sv[8 * c8 + 2 * e] - m), p1 = exp2f(sv[8 * c8 + 2 * e + 1] - m);
+          const __half2 h2 = __floats2half2_rn(p0, p1);
+          lsum += __low2float(h2) + __high2float(h2);   // the weights the MMA multiplies
+          w[e] = *reinterpret_cast<const uint32_t*>(&h2);
+        }
+        const int panel = c8 >> 3, chunk = c8 & 7;
+        *reinterpret_cast<uint4*>(prow + panel * S::kPanel + ((chunk ^ (r & 7)) << 4)) =
+            make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      l += lsum;
+      fence_proxy_async_smem();   // P (generic writes) before the MMA reads it
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(pfull);
+    }
+    // ---- O / l -> fp16 ---------------------------------------------------------------
+    if (ok) ok = mbar_wait(odone, (nkt - 1) & 1, p.wait_limit, abort_flag);
+    ok = __all_sync(0xffffffffu, ok && !*abort_flag);
+    tc_fence_after();
+    if (ok) {
+      const float inv = 1.0f / l;
+      __half* dst = p.out + static_cast<size_t>(row0 + qpos) * p.ldo + h * D;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t u[32];
+        tmem_ld_32x32b_x32(trow + kO + 32 * c, u);
+        tmem_ld_wait();
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const __half2 h2 = __floats2half2_rn(__uint_as_float(u[8 * v + 2 * e]) * inv,
+                                                 __uint_as_float(u[8 * v + 2 * e + 1]) * inv);
+            w[e] = *reinterpret_cast<const uint32_t*>(&h2);
+          }
+          *reinterpret_cast<uint4*>(dst + 32 * c + 8 * v) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      }
+    }
+  }
+  // ---- teardown: every MMA done, then the tensor memory is freed ----------------------
+  if (warp == 1 && lane == 0) {
+    volatile int dummy = 0;
+    mbar_wait(done, 0, kDrainLimit, &dummy);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int D>
+fg_status launch_pa(const void* qkv, int64_t ld, int64_t b, int64_t s, int32_t heads, void* out, int64_t ldo,
+                    cudaStream_t st) {
+  using S = PaSmem<D>;
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    if (cudaFuncSetAttribute(prefill_attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kBytes) !=
+        cudaSuccess)
+      return check_launch("prefill_attn_tc smem attribute");
+    attr_set[dev] = true;
+  }
+  PaParams p;
+  memset(&p, 0, sizeof(p));
+  if (!tc_make_map(&p.map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, qkv, static_cast<uint64_t>(ld), static_cast<uint64_t>(b * s),
+                   static_cast<uint64_t>(ld) * 2, 64, kTile, CU_TENSOR_MAP_SWIZZLE_128B))
+    return fail(FG_ERR_CUDA, "tensor map for the Q|K|V buffer");
+  p.out = static_cast<__half*>(out);
+  p.ldo = static_cast<int>(ldo);
+  p.s = static_cast<int>(s);
+  p.heads = heads;
+  p.h1 = heads * D;
+  p.qtiles = static_cast<int>(s / kTile);
+  p.scale_log2 = static_cast<float>(1.4426950408889634074 / sqrt(static_cast<double>(D)));
+  p.err = device_error_word();
+  if (!p.err) return fail(FG_ERR_CUDA, "device error word");
+  p.wait_limit = wait_limit();
+  Trace tr(KC_ATTN_PREFILL, st);
+  const unsigned grid = static_cast<unsigned>(b * heads * p.qtiles);
+  prefill_attn_tc_kernel<D><<<grid, kThreads, S::kBytes, st>>>(p);
+  return check_launch("prefill_attn_tc_kernel");
+}
+
+}  // namespace
+
+bool prefill_attention_tc_supported(int64_t s, int32_t head_dim, fg_dtype dt) {
+  return dt == FG_F16 && s >= kTile && s % kTile == 0 && (head_dim == 64 || head_dim == 128);
+}
+
+fg_status prefill_attention_tc(const void* qkv, int64_t ld, int64_t b, int64_t s, int32_t heads, int32_t head_dim,
+                               void* out, int64_t ldo, cudaStream_t st) {
+  if (b == 0 || s == 0) return FG_OK;
+  if (!aligned(qkv, 16) || (ld * 2) % 16 || !aligned(out, 16) || ldo % 8)
+    return fail(FG_ERR_ALIGN, "prefill attention: 16-byte aligned buffers and rows");
+  if (head_dim == 128) return launch_pa<128>(qkv, ld, b, s, heads, out, ldo, st);
+  return launch_pa<64>(qkv, ld, b, s, heads, out, ldo, st);
+}
+
+}  // namespace fg

@@ -118,7 +118,7 @@ template <typename T, int NG>
 __global__ void __launch_bounds__(256) kv_store_q4_kernel(const T* __restrict__ ksrc,
                                                           const T* __restrict__ vsrc, int64_t ld,
                                                           int64_t b, int64_t ntok, int64_t pos0,
-                                                          int heads, int64_t cap, KVDst dst) {
+                                                          int heads, int64_t cap, KVDst dst, int write_back) {
   constexpr int D = 64 * NG;
   constexpr int kTpi = 4 / NG;   // tokens per warp-wide batch
   const int lane = threadIdx.x & 31;
@@ -162,6 +162,14 @@ __global__ void __launch_bounds__(256) kv_store_q4_kernel(const T* __restrict__ 
           if (part == 0) {
             mins[slot * NG + gi] = mn;
             scales[slot * NG + gi] = sc;
+          }
+          if (write_back) {
+            // the values attention reads back from the cache, fp16(fmaf(q,
+            // scale, min)), in place of the row just quantized
+            float r[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) r[e] = __fmaf_rn(static_cast<float>((packed >> (4 * e)) & 15u), sc, mn);
+            store8(const_cast<T*>(src) + ti * ld, r);
           }
         }
       }
@@ -229,7 +237,7 @@ fg_status dequant_rows(const uint8_t* codes, const float* mins, const float* sca
 }
 
 fg_status kv_store(const fg_kv& kv, const void* ksrc, const void* vsrc, int64_t ld, int64_t b,
-                   int64_t ntok, int64_t pos0, cudaStream_t st) {
+                   int64_t ntok, int64_t pos0, cudaStream_t st, bool write_back) {
   const int h1 = kv.heads * kv.head_dim;
   if (b == 0 || ntok == 0) return FG_OK;
   if (kv.codec == FG_CODEC_Q4G64) {
@@ -250,16 +258,16 @@ fg_status kv_store(const fg_kv& kv, const void* ksrc, const void* vsrc, int64_t 
       const __half* k = static_cast<const __half*>(ksrc);
       const __half* v = static_cast<const __half*>(vsrc);
       if (wide)
-        kv_store_q4_kernel<__half, 2><<<grid, 256, 0, st>>>(k, v, ld, b, ntok, pos0, kv.heads, kv.capacity, dst);
+        kv_store_q4_kernel<__half, 2><<<grid, 256, 0, st>>>(k, v, ld, b, ntok, pos0, kv.heads, kv.capacity, dst, write_back ? 1 : 0);
       else
-        kv_store_q4_kernel<__half, 1><<<grid, 256, 0, st>>>(k, v, ld, b, ntok, pos0, kv.heads, kv.capacity, dst);
+        kv_store_q4_kernel<__half, 1><<<grid, 256, 0, st>>>(k, v, ld, b, ntok, pos0, kv.heads, kv.capacity, dst, write_back ? 1 : 0);
     } else {
       const float* k = static_cast<const float*>(ksrc);
       const float* v = static_cast<const float*>(vsrc);
       if (wide)
-        kv_store_q4_kernel<float, 2><<<grid, 256, 0, st>>>(k, v, ld, b, ntok, pos0, kv.heads, kv.capacity, dst);
+        kv_store_q4_kernel<float, 2><<<grid, 256, 0, st>>>(k, v, ld, b, ntok, pos0, kv.heads, kv.capacity, dst, write_back ? 1 : 0);
       else
-        kv_store_q4_kernel<float, 1><<<grid, 256, 0, st>>>(k, v, ld, b, ntok, pos0, kv.heads, kv.capacity, dst);
+        kv_store_q4_kernel<float, 1><<<grid, 256, 0, st>>>(k, v, ld, b, ntok, pos0, kv.heads, kv.capacity, dst, write_back ? 1 : 0);
     }
     return check_launch("kv_store_q4_kernel");
   }

@@ -140,8 +140,16 @@ size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, fg_dtype dt, int qu
 // Store K/V rows of `T` tokens per sequence at slots pos0..pos0+T-1.  The
 // row of sequence bi, token ti starts at ksrc + (bi*T + ti)*ld (elements of
 // the cache dtype), likewise for vsrc.
+// write_back (4-bit fp16 cache): each source row is then overwritten with the
+// values the cache restores, fp16(fmaf(q, scale, min)).
 fg_status kv_store(const fg_kv& kv, const void* ksrc, const void* vsrc, int64_t ld, int64_t b,
-                   int64_t T, int64_t pos0, cudaStream_t st);
+                   int64_t T, int64_t pos0, cudaStream_t st, bool write_back = false);
+// Causal prefill attention on tcgen05 over a Q|K|V buffer [b*s][ld] whose K
+// and V columns hold the values the cache restores (kv_store with
+// write_back): s a multiple of 128, head_dim 64 or 128, fp16.
+bool prefill_attention_tc_supported(int64_t s, int32_t head_dim, fg_dtype dt);
+fg_status prefill_attention_tc(const void* qkv, int64_t ld, int64_t b, int64_t s, int32_t heads, int32_t head_dim,
+                               void* out, int64_t ldo, cudaStream_t st);
 
 // ---- attention -------------------------------------------------------------
 // Host-side argument checks of fg_decode_attention (no CUDA call).

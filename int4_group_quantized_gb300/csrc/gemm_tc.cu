@@ -192,7 +192,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
       mbar_wait(done, 0, kDrainLimit, &dummy);
     }
     tc_fence_after();
-    if (ok && !*abort_flag) {
+    // the TMEM loads are warp-collective: the whole warp takes this branch
+    if (__all_sync(0xffffffffu, ok && !*abort_flag)) {
       const int q = warp - kEpiWarp0;   // TMEM lanes 32q .. 32q+31
       for (int mt = 0; mt < MT; ++mt) {
         const int m = m0 + mt * 128 + q * 32 + lane;

@@ -217,9 +217,15 @@ fg_status run_prefill(const fg_layer& L, const void* x, int64_t b, int64_t s, co
   FG_TRY(gemm(product(P, x, h1, M, qkv, 3, B.qkv, 3 * h1, nullptr, 0, 0), B.scratch, scratch, st));
   // cache the prompt's K/V (quantized per token along the hidden dimension)
   const size_t e = dtype_bytes(L.dtype);
-  FG_TRY(kv_store(kv, B.qkv + h1 * e, B.qkv + 2 * h1 * e, 3 * h1, b, s, 0, st));
+  const int32_t d = static_cast<int32_t>(h1 / L.heads);
+  const bool tc = kv.codec == FG_CODEC_Q4G64 && prefill_attention_tc_supported(s, d, L.dtype);
+  // on the tensor-core path the K/V columns then hold what the cache restores
+  FG_TRY(kv_store(kv, B.qkv + h1 * e, B.qkv + 2 * h1 * e, 3 * h1, b, s, 0, st, tc));
   // Softmax(x_Q x_K^T / sqrt(d)) x_V, causal, K/V read back through the codec
-  FG_TRY(prefill_attention(kv, B.qkv, 3 * h1, b, s, B.att, h1, st));
+  if (tc)
+    FG_TRY(prefill_attention_tc(B.qkv, 3 * h1, b, s, L.heads, d, B.att, h1, st));
+  else
+    FG_TRY(prefill_attention(kv, B.qkv, 3 * h1, b, s, B.att, h1, st));
   // x_Out = (...) w_O + x
   FG_TRY(gemm(product(P, B.att, h1, M, &P.wo, 1, B.xo, h1, x, h1, 0), B.scratch, scratch, st));
   // relu(x_Out w_1)

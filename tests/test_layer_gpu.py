@@ -121,6 +121,22 @@ def test_fp16_small_ragged(fg):
     _compare(w, y, outs, oracle_block(w, raw, True, x, tin, list(range(w.b))), list(range(w.b)), 1e-2)
 
 
+@pytest.mark.parametrize("heads,head_dim,s", [(2, 128, 384), (4, 64, 256)])
+def test_prefill_tensor_core_attention_mixed_rescales(fg, heads, head_dim, s):
+    """fp16 prompts of a multiple of 128 tokens take the tcgen05 prefill
+    attention.  The prompt is scaled by 8 so that the scores reach ~47 in
+    base 2: at a later key tile the running max of some query rows of a warp
+    grows by more than 2^8 (their O is rescaled in tensor memory) while the
+    other rows keep theirs (~4% of the row-tiles of these inputs)."""
+    h1 = heads * head_dim
+    w = synth.Workload("tc16", 9, 1, h1, 2 * h1, heads, 2, s, 2, "f16")
+    raw = [synth.layer_weights(w, 0, "cuda")]
+    x = synth.prompt(w, device="cuda") * 8
+    tin = synth.decode_inputs(w, device="cuda")
+    y, outs, _ = run_gpu_block(fg, w, raw, True, x, tin)
+    _compare(w, y, outs, oracle_block(w, raw, True, x, tin, list(range(w.b))), list(range(w.b)), 1e-2)
+
+
 def test_opt125m_two_layer_chain(fg):
     """Two chained layers of the OPT-125M shape at the full block (b=32,
     s=512, n=32); the oracle recomputes sequences 0, 17 and 31.  Deeper
