@@ -168,7 +168,7 @@ __global__ void __launch_bounds__(256) kv_store_q4_kernel(const T* __restrict__ 
             // scale, min)), in place of the row just quantized
             float r[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) r[e] = __fmaf_rn(static_cast<float>((packed >> (4 * e)) & 15u), sc, mn);
+            for (int e = 0; e < 8; ++e) r[e] = __fmaf_rn(codec::code_float((packed >> (4 * e)) & 15u), sc, mn);
             store8(const_cast<T*>(src) + ti * ld, r);
           }
         }

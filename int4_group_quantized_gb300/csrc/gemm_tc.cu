@@ -13,9 +13,11 @@
 // past M are zero-filled by the TMA unit.
 //
 // Warp roles (256 threads): warp 0 issues TMA; warp 1 owns TMEM and one of
-// its lanes issues the MMAs; warps 4..7 drain the accumulator in the
-// epilogue.  Every wait is bounded: on timeout the CTA raises the library's
-// device error word and leaves.
+// its lanes issues the MMAs; then all eight warps drain the accumulator in
+// the epilogue (warp w: TMEM lanes 32(w%4).., half of the tile's columns).
+// Every wait is bounded: on timeout the CTA raises the library's device
+// error word and leaves.
+
 #include <cudaTypedefs.h>
 #include <string.h>
 
@@ -29,7 +31,6 @@ using namespace tc;
 
 constexpr int BK = 64;             // k per pipeline stage (one 128-byte swizzle row of fp16)
 constexpr int kThreads = 256;
-constexpr int kEpiWarp0 = 4;       // warps 4..7 drain TMEM
 constexpr int BN = 256;            // columns of a CTA tile
 
 struct TcParams {
@@ -182,24 +183,27 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     __syncwarp();
   }
 
-  // ---- epilogue ---------------------------------------------------------------------
-  if (warp >= kEpiWarp0) {
+  // ---- epilogue: all eight warps ------------------------------------------------------
+  {
     const bool ok = mbar_wait(done, 0, p.wait_limit, abort_flag);
     if (!ok) {
       // the MMA thread always commits `done`: wait for its MMAs to finish
       // before the tensor memory they write is freed
       volatile int dummy = 0;
       mbar_wait(done, 0, kDrainLimit, &dummy);
+      if (lane == 0) raise(p);
     }
     tc_fence_after();
     // the TMEM loads are warp-collective: the whole warp takes this branch
     if (__all_sync(0xffffffffu, ok && !*abort_flag)) {
-      const int q = warp - kEpiWarp0;   // TMEM lanes 32q .. 32q+31
+      const int q = warp & 3;                        // TMEM lanes 32q .. 32q+31
+      const int cb = warp >= 4 ? 0 : BN / 2;         // this warp's half of the columns
       for (int mt = 0; mt < MT; ++mt) {
         const int m = m0 + mt * 128 + q * 32 + lane;
-        for (int c0 = 0; c0 < BN; c0 += 32) {
+        const uint32_t trow = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + mt * BN;
+        for (int c0 = cb; c0 < cb + BN / 2; c0 += 32) {
           uint32_t r[32];
-          tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + mt * BN + c0, r);
+          tmem_ld_32x32b_x32(trow + c0, r);
           tmem_ld_wait();
           if (m >= p.M) continue;
           const int n = n0 + c0;

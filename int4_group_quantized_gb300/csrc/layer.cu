@@ -215,11 +215,12 @@ fg_status run_prefill(const fg_layer& L, const void* x, int64_t b, int64_t s, co
   const fg_wmat qkv[3] = {P.wq, P.wk, P.wv};
   // x_Q, x_K, x_V = x w_Q, x w_K, x w_V (one pass over the three matrices)
   FG_TRY(gemm(product(P, x, h1, M, qkv, 3, B.qkv, 3 * h1, nullptr, 0, 0), B.scratch, scratch, st));
-  // cache the prompt's K/V (quantized per token along the hidden dimension)
+  // cache the prompt's K/V (quantized per token along the hidden dimension);
+  // on the tensor-core attention path the K/V columns then hold what the
+  // cache restores
   const size_t e = dtype_bytes(L.dtype);
   const int32_t d = static_cast<int32_t>(h1 / L.heads);
   const bool tc = kv.codec == FG_CODEC_Q4G64 && prefill_attention_tc_supported(s, d, L.dtype);
-  // on the tensor-core path the K/V columns then hold what the cache restores
   FG_TRY(kv_store(kv, B.qkv + h1 * e, B.qkv + 2 * h1 * e, 3 * h1, b, s, 0, st, tc));
   // Softmax(x_Q x_K^T / sqrt(d)) x_V, causal, K/V read back through the codec
   if (tc)

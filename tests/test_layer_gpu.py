@@ -137,6 +137,39 @@ def test_prefill_tensor_core_attention_mixed_rescales(fg, heads, head_dim, s):
     _compare(w, y, outs, oracle_block(w, raw, True, x, tin, list(range(w.b))), list(range(w.b)), 1e-2)
 
 
+@pytest.mark.parametrize("heads,head_dim,s", [(2, 128, 256), (8, 64, 384)])
+def test_prefill_cache_equals_kv_append(fg, heads, head_dim, s):
+    """The prefill's K/V store (on the tensor-core attention path, which also
+    writes the cache-restored values back for the attention) fills the cache
+    with the codes, mins and scales fg_kv_append stores, bit for bit, for
+    the same K/V rows, computed here by separate x·w_K and x·w_V products on
+    the same weights (one tensor-core tile per 256 columns, the same
+    accumulation order).  h1 = 512 puts two column tiles in each of K and V."""
+    h1 = heads * head_dim
+    w = synth.Workload("kv16", 9, 1, h1, 2 * h1, heads, 2, s, 1, "f16")
+    raw = synth.layer_weights(w, 0, "cuda")
+    L = fg.Layer.from_dense(raw, heads, quantized=True)
+    x = synth.prompt(w, device="cuda") * 4
+    kv = fg.KVCache(w.b, heads, head_dim, s, True, torch.float16, "cuda")
+    y = torch.empty_like(x)
+    fg.fg_prefill_layer(L, x, kv, y, fg.workspace(fg.fg_prefill_workspace_bytes(L, w.b, s), "cuda"))
+    xs = x.reshape(w.b * s, h1)
+    rows = {}
+    for m in ("wk", "wv"):
+        W = fg.QuantWeight.from_dense(raw[m], True, pack=False)   # the prefill product: fp16 weights, tensor cores
+        rows[m] = torch.empty((w.b * s, h1), dtype=torch.float16, device="cuda")
+        fg.fg_linear(W, xs, rows[m])
+    k, v = rows["wk"].reshape(w.b, s, h1), rows["wv"].reshape(w.b, s, h1)
+    ref = fg.KVCache(w.b, heads, head_dim, s, True, torch.float16, "cuda")
+    for t in range(s):
+        fg.fg_kv_append(ref, k[:, t].contiguous(), v[:, t].contiguous(), t)
+    fg.fg_sync_status()
+    for name in ("k_codes", "v_codes"):
+        assert torch.equal(getattr(kv, name), getattr(ref, name)), name
+    for name in ("k_mins", "k_scales", "v_mins", "v_scales"):
+        assert torch.equal(getattr(kv, name).view(torch.int32), getattr(ref, name).view(torch.int32)), name
+
+
 def test_opt125m_two_layer_chain(fg):
     """Two chained layers of the OPT-125M shape at the full block (b=32,
     s=512, n=32); the oracle recomputes sequences 0, 17 and 31.  Deeper
