@@ -7,27 +7,35 @@
 // min)) (written back by the K/V store), so that the attention reads
 // exactly the cached values.  s is a multiple of 128.
 //
-// One CTA per (sequence, head, 128-query tile), flash-style over 128-key
-// tiles up to the diagonal:
-//   * a TMA thread loads Q once and K, V tiles into a two-stage ring (one
-//     tensor map over the buffer, boxes of 64 columns x 128 rows, 128-byte
-//     swizzle: K-major panels for Q and K, MN-major column blocks for V);
+// A persistent kernel: one CTA per SM takes the items (sequence, head,
+// 128-query tile), longest first, dealt round-robin over the CTAs, and runs
+// each flash-style over its 128-key tiles up to the diagonal:
+//   * a TMA thread loads Q of an item into one of two buffers and the K, V
+//     tiles into a two-stage ring that runs on across items (one tensor map
+//     over the buffer, boxes of 64 columns x 128 rows, 128-byte swizzle:
+//     K-major panels for Q and K, MN-major column blocks for V);
 //   * one thread issues S = Q K^T (M = N = 128, K = head_dim) into tensor
-//     memory, and O += P V (K = 128 keys) into a second tensor-memory block;
+//     memory and O += P V (K = 128 keys) into one of two O blocks (items
+//     alternate), S of the next tile -- of this item or the next -- while
+//     the softmax works on this one;
 //   * four softmax warps (one query row per thread) read S with tcgen05.ld,
 //     mask the diagonal tile, keep the running max and sum in base 2 and
 //     write P (fp16) into shared memory in the swizzled K-major layout the
 //     next MMA reads.  O is rescaled in tensor memory only when a row's max
 //     grows by more than 2^8 (otherwise P is formed against the stale max,
 //     which keeps it below 256 and the result the same up to rounding);
-//   * S of the next tile is computed while the softmax works on this one.
-// At the end the softmax warps divide O by the row sums and store fp16.
+//   * after an item's last tile the softmax warps divide its O by the row
+//     sums and store fp16, while the next item's S and P V proceed in the
+//     other O block.
+// The copy and MMA barriers count phases over the CTA's whole tile sequence.
 // Every mbarrier wait is bounded; on timeout the CTA raises the library's
 // device error word, lets its copies and MMAs finish and frees its tensor
 // memory.
 #include <cudaTypedefs.h>
 #include <math.h>
 #include <string.h>
+
+#include <algorithm>
 
 #include "fg_internal.cuh"
 #include "tc_ptx.cuh"
@@ -53,6 +61,8 @@ struct PaParams {
   int ldo;
   int s, heads, h1;
   int qtiles;           // s / 128
+  int bh;               // b * heads
+  int items;            // b * heads * qtiles
   float scale_log2;     // log2(e) / sqrt(head_dim)
   unsigned int* err;
   uint32_t wait_limit;
@@ -62,53 +72,81 @@ template <int D>
 struct PaSmem {
   static constexpr int kPanels = D / 64;          // 64-column panels of a head row
   static constexpr int kPanel = kTile * 128;      // 16 KiB: 128 rows x 128 bytes
-  static constexpr int kQ = kPanels * kPanel;
+  static constexpr int kQ = kPanels * kPanel;     // one Q buffer (two of them)
   static constexpr int kK = kPanels * kPanel;
   static constexpr int kV = kPanels * kPanel;     // MN-major: D/64 blocks of 128 keys x 64 dims
   static constexpr int kP = 2 * kPanel;           // 128 queries x 128 keys, two K-major panels
   static constexpr int kStage = kK + kV;
-  static constexpr int kBytes = 1024 + kQ + 2 * kStage + kP + 256;
+  static constexpr int kBytes = 1024 + 2 * kQ + 2 * kStage + kP + 256;
+  static_assert(kBytes <= 232448, "shared memory of one CTA");
 };
+
+// 2^x on the special-function unit (relative error ~2^-22; P is rounded to
+// fp16 right after, and 2^-inf = +0).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// acc + lo + hi of an fp16 pair, in fp32 (mixed-precision adds).
+__device__ __forceinline__ float add_pair_f16(float acc, uint32_t h2) {
+  float r;
+  asm("{ .reg .f16 a, b; .reg .f32 t; mov.b32 {a, b}, %1; add.rn.f32.f16 t, a, %2; add.rn.f32.f16 %0, b, t; }"
+      : "=f"(r)
+      : "r"(h2), "f"(acc));
+  return r;
+}
+
+// Item k of the longest-first order: query tile qt of (sequence bi, head h).
+struct PaItem {
+  int qt, bi, h;
+};
+__device__ __forceinline__ PaItem pa_item(const PaParams& p, int k) {
+  PaItem it;
+  it.qt = p.qtiles - 1 - k / p.bh;
+  const int bh = k % p.bh;
+  it.bi = bh / p.heads;
+  it.h = bh % p.heads;
+  return it;
+}
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) prefill_attn_tc_kernel(const __grid_constant__ PaParams p) {
   using S = PaSmem<D>;
   constexpr uint32_t kIdescS = idesc_f16(128, 128, 0, 0);   // A = Q (K-major), B = K (K-major)
   constexpr uint32_t kIdescO = idesc_f16(128, D, 0, 1);     // A = P (K-major), B = V (MN-major)
-  constexpr uint32_t kTmemCols = 256;                       // S: columns 0..127, O: 128..128+D-1
-  constexpr uint32_t kO = 128;
+  constexpr uint32_t kO = 128;                              // S: columns 0..127, O blocks from here
+  constexpr uint32_t kTmemCols = kO + 2 * D <= 256 ? 256 : 512;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sQ = sm;
-  uint8_t* sKV = sQ + S::kQ;                 // two stages: [K panels][V blocks]
+  uint8_t* sQ = sm;                          // two Q buffers
+  uint8_t* sKV = sQ + 2 * S::kQ;             // two stages: [K panels][V blocks]
   uint8_t* sP = sKV + 2 * S::kStage;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sP + S::kP);
-  uint64_t* qfull = bars;
-  uint64_t* kvfull = bars + 1;     // [2]
-  uint64_t* kvfree = bars + 3;     // [2] the PV MMA of the tile has read the stage
-  uint64_t* sfull = bars + 5;      // S of the tile is in tensor memory
-  uint64_t* sfree = bars + 6;      // four softmax warps have read S
-  uint64_t* pfull = bars + 7;      // four softmax warps have written P
-  uint64_t* odone = bars + 8;      // PV of the tile has completed
-  uint64_t* done = bars + 9;       // every MMA has completed
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 10);
+  uint64_t* qfull = bars;          // [2] Q of an item is in its buffer
+  uint64_t* qfree = bars + 2;      // [2] the item's S MMAs have read it
+  uint64_t* kvfull = bars + 4;     // [2]
+  uint64_t* kvfree = bars + 6;     // [2] the PV MMA of the tile has read the stage
+  uint64_t* sfull = bars + 8;      // S of the tile is in tensor memory
+  uint64_t* sfree = bars + 9;      // four softmax warps have read S
+  uint64_t* pfull = bars + 10;     // four softmax warps have written P
+  uint64_t* odone = bars + 11;     // PV of the tile has completed
+  uint64_t* ofree = bars + 12;     // [2] the softmax warps have stored the O block
+  uint64_t* done = bars + 14;      // every MMA has completed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // longest query tiles first
-  const int qt = p.qtiles - 1 - static_cast<int>(blockIdx.x % p.qtiles);
-  const int bh = static_cast<int>(blockIdx.x / p.qtiles);
-  const int bi = bh / p.heads, h = bh % p.heads;
-  const int row0 = bi * p.s;              // the sequence's first row of the buffer
-  const int nkt = qt + 1;                 // key tiles up to the diagonal
-  const int colq = h * D, colk = p.h1 + h * D, colv = 2 * p.h1 + h * D;
+  const int G = static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
-    mbar_init(qfull, 1);
     for (int i = 0; i < 2; ++i) {
+      mbar_init(&qfull[i], 1);
+      mbar_init(&qfree[i], 1);
       mbar_init(&kvfull[i], 1);
       mbar_init(&kvfree[i], 1);
+      mbar_init(&ofree[i], 4);
     }
     mbar_init(sfull, 1);
     mbar_init(sfree, 4);
@@ -126,42 +164,55 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_tc_kernel(const __gr
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
-    // ---- TMA: Q once, then K and V of each key tile -----------------------------
+    // ---- TMA: per item Q, then K and V of each key tile ---------------------------
     if (lane == 0) {
-      mbar_expect_tx(qfull, S::kQ);
-      for (int pn = 0; pn < S::kPanels; ++pn)
-        tma_load_2d(sQ + pn * S::kPanel, &p.map, colq + 64 * pn, row0 + qt * kTile, qfull);
-      int issued = 0;
-      for (int j = 0; j < nkt; ++j) {
-        const int st = j & 1;
-        if (!mbar_wait(&kvfree[st], ((j >> 1) & 1) ^ 1, p.wait_limit, abort_flag)) break;
-        uint8_t* stage = sKV + st * S::kStage;
-        mbar_expect_tx(&kvfull[st], S::kStage);
-        for (int pn = 0; pn < S::kPanels; ++pn) {
-          tma_load_2d(stage + pn * S::kPanel, &p.map, colk + 64 * pn, row0 + j * kTile, &kvfull[st]);
-          tma_load_2d(stage + S::kK + pn * S::kPanel, &p.map, colv + 64 * pn, row0 + j * kTile, &kvfull[st]);
+      int q_issued = 0, g_issued = 0;
+      bool ok = true;
+      for (int k = blockIdx.x; k < p.items && ok; k += G) {
+        const PaItem it = pa_item(p, k);
+        const int row0 = it.bi * p.s;
+        const int qb = q_issued & 1;
+        if (!mbar_wait(&qfree[qb], ((q_issued >> 1) & 1) ^ 1, p.wait_limit, abort_flag)) break;
+        mbar_expect_tx(&qfull[qb], S::kQ);
+        for (int pn = 0; pn < S::kPanels; ++pn)
+          tma_load_2d(sQ + qb * S::kQ + pn * S::kPanel, &p.map, it.h * D + 64 * pn, row0 + it.qt * kTile, &qfull[qb]);
+        ++q_issued;
+        for (int j = 0; j <= it.qt; ++j) {
+          const int st = g_issued & 1;
+          if (!mbar_wait(&kvfree[st], ((g_issued >> 1) & 1) ^ 1, p.wait_limit, abort_flag)) {
+            ok = false;
+            break;
+          }
+          uint8_t* stage = sKV + st * S::kStage;
+          mbar_expect_tx(&kvfull[st], S::kStage);
+          for (int pn = 0; pn < S::kPanels; ++pn) {
+            tma_load_2d(stage + pn * S::kPanel, &p.map, p.h1 + it.h * D + 64 * pn, row0 + j * kTile, &kvfull[st]);
+            tma_load_2d(stage + S::kK + pn * S::kPanel, &p.map, 2 * p.h1 + it.h * D + 64 * pn, row0 + j * kTile,
+                        &kvfull[st]);
+          }
+          ++g_issued;
         }
-        ++issued;
       }
       volatile int dummy = 0;   // nothing in flight at exit
-      mbar_wait(qfull, 0, kDrainLimit, &dummy);
-      for (int j = (issued > 2 ? issued - 2 : 0); j < issued; ++j)
-        mbar_wait(&kvfull[j & 1], (j >> 1) & 1, kDrainLimit, &dummy);
+      for (int u = (q_issued > 2 ? q_issued - 2 : 0); u < q_issued; ++u)
+        mbar_wait(&qfull[u & 1], (u >> 1) & 1, kDrainLimit, &dummy);
+      for (int u = (g_issued > 2 ? g_issued - 2 : 0); u < g_issued; ++u)
+        mbar_wait(&kvfull[u & 1], (u >> 1) & 1, kDrainLimit, &dummy);
       if (*abort_flag) atomicOr(p.err, DEV_ERR_WAIT_TIMEOUT);
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ---- MMA issuer --------------------------------------------------------------
+    // ---- MMA issuer, over the CTA's tile sequence -----------------------------------
     if (lane == 0) {
-      bool ok = mbar_wait(qfull, 0, p.wait_limit, abort_flag);
-      const uint32_t q_addr = smem_u32(sQ), p_addr = smem_u32(sP);
-      // S of tile j: needs K_j and a free S (tile j-1's scores read)
-      auto issue_s = [&](int j) -> bool {
-        const int st = j & 1;
-        if (!mbar_wait(&kvfull[st], (j >> 1) & 1, p.wait_limit, abort_flag)) return false;
-        if (j > 0 && !mbar_wait(sfree, (j - 1) & 1, p.wait_limit, abort_flag)) return false;
+      const uint32_t p_addr = smem_u32(sP);
+      // S of tile g (item n, Q buffer n & 1): needs K_g and a free S (tile
+      // g-1's scores read); after an item's last S its Q buffer is released
+      auto issue_s = [&](int g, int n, bool last) -> bool {
+        const int st = g & 1;
+        if (!mbar_wait(&kvfull[st], (g >> 1) & 1, p.wait_limit, abort_flag)) return false;
+        if (g > 0 && !mbar_wait(sfree, (g - 1) & 1, p.wait_limit, abort_flag)) return false;
         tc_fence_after();
-        const uint32_t k_addr = smem_u32(sKV + st * S::kStage);
+        const uint32_t q_addr = smem_u32(sQ + (n & 1) * S::kQ), k_addr = smem_u32(sKV + st * S::kStage);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk / 4) * S::kPanel + (kk % 4) * 32;
@@ -169,147 +220,190 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_tc_kernel(const __gr
                   kk > 0 ? 1u : 0u);
         }
         mma_commit(sfull);
+        if (last) mma_commit(&qfree[n & 1]);
         return true;
       };
-      if (ok) ok = issue_s(0);
-      for (int j = 0; j < nkt && ok; ++j) {
-        // the next tile's scores while the softmax works on this one
-        if (j + 1 < nkt) ok = issue_s(j + 1);
-        if (!ok) break;
-        if (!mbar_wait(pfull, j & 1, p.wait_limit, abort_flag)) {
+      bool ok = true;
+      int k = blockIdx.x, n = 0, j = 0, g = 0;
+      PaItem it = pa_item(p, k);
+      ok = mbar_wait(&qfull[0], 0, p.wait_limit, abort_flag) && issue_s(0, 0, it.qt == 0);
+      while (ok) {
+        // the tile after g: the next of this item, or the first of the next item
+        int kn = k, nn = n, jn = j + 1;
+        PaItem itn = it;
+        if (jn > it.qt) {
+          kn = k + G;
+          nn = n + 1;
+          jn = 0;
+          if (kn < p.items) itn = pa_item(p, kn);
+        }
+        const bool has_next = kn < p.items;
+        if (has_next) {
+          if (jn == 0 && !mbar_wait(&qfull[nn & 1], (nn >> 1) & 1, p.wait_limit, abort_flag)) {
+            ok = false;
+            break;
+          }
+          if (!issue_s(g + 1, nn, jn == itn.qt)) {
+            ok = false;
+            break;
+          }
+        }
+        // O[n & 1] += P_g V_g; the block's first P V overwrites it, once the
+        // softmax warps have stored the item that used it before
+        if (!mbar_wait(pfull, g & 1, p.wait_limit, abort_flag) ||
+            (j == 0 && !mbar_wait(&ofree[n & 1], ((n >> 1) & 1) ^ 1, p.wait_limit, abort_flag))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t v_addr = smem_u32(sKV + (j & 1) * S::kStage + S::kK);
+        const uint32_t v_addr = smem_u32(sKV + (g & 1) * S::kStage + S::kK);
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk) {
           // A = P: K-major panels of 64 keys; B = V: 64-dim blocks 16 KiB apart
           // (leading byte offset), 8-key groups 1 KiB apart (stride)
           const uint64_t a = smem_desc_sw128(p_addr + (kk / 4) * S::kPanel + (kk % 4) * 32, 16, 1024);
           const uint64_t b = smem_desc_sw128(v_addr + kk * 2048, S::kPanel, 1024);
-          mma_f16(tmem + kO, a, b, kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
+          mma_f16(tmem + kO + (n & 1) * D, a, b, kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(&kvfree[j & 1]);   // K_j and V_j are read
+        mma_commit(&kvfree[g & 1]);   // K_g and V_g are read
         mma_commit(odone);
+        if (!has_next) break;
+        k = kn;
+        n = nn;
+        j = jn;
+        it = itn;
+        ++g;
       }
       mma_commit(done);
       if (!ok) atomicOr(p.err, DEV_ERR_WAIT_TIMEOUT);
     }
     __syncwarp();
   } else if (warp >= kSoftWarp0) {
-    // ---- softmax warps: query row r = 32 * (warp % 4) + lane --------------------------
+    // ---- softmax warps: query row r = 32 * (warp % 4) + lane of each item -------------
     const int quarter = warp & 3;
     const int r = 32 * quarter + lane;
     const uint32_t trow = tmem + (static_cast<uint32_t>(32 * quarter) << 16);
-    const int qpos = qt * kTile + r;      // the query's position in its sequence
-    float m = -INFINITY, l = 0.0f;
-    bool ok = true;
     uint8_t* prow = sP + r * 128;         // this row in each P panel
-    for (int j = 0; j < nkt; ++j) {
-      // tcgen05.ld/st are warp-collective: every branch around them is
-      // taken by the whole warp
-      if (ok) ok = mbar_wait(sfull, j & 1, p.wait_limit, abort_flag);
-      ok = __all_sync(0xffffffffu, ok);
-      tc_fence_after();
-      float sv[128];
-      if (ok) {
+    bool ok = true;
+    int g = 0, n = 0;
+    for (int k = blockIdx.x; k < p.items && ok; k += G, ++n) {
+      const PaItem it = pa_item(p, k);
+      const uint32_t ob = kO + (n & 1) * D;
+      const int qpos = it.qt * kTile + r;   // the query's position in its sequence (row r of the tile)
+      float m = -INFINITY, l = 0.0f;
+      for (int j = 0; j <= it.qt; ++j, ++g) {
+        // tcgen05.ld/st are warp-collective: every branch around them is
+        // taken by the whole warp
+        if (ok) ok = mbar_wait(sfull, g & 1, p.wait_limit, abort_flag);
+        ok = __all_sync(0xffffffffu, ok);
+        tc_fence_after();
+        float sv[128];   // raw scores of the row (the scale is folded into the exponent below)
+        if (ok) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t u[32];
-          tmem_ld_32x32b_x32(trow + 32 * c, u);
-          tmem_ld_wait();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) sv[32 * c + e] = __uint_as_float(u[e]) * p.scale_log2;
-        }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(sfree);   // S may be overwritten by the next tile's scores
-      // causal mask on the diagonal tile: key 128j + c is visible iff <= qpos
-      float mx = -INFINITY;
-      const int kbase = j * kTile;
-#pragma unroll
-      for (int c = 0; c < 128; ++c) {
-        if (kbase + c > qpos) sv[c] = -INFINITY;
-        mx = fmaxf(mx, sv[c]);
-      }
-      // P may be written once the previous tile's PV has read it; O may be
-      // rescaled only then too
-      if (j > 0 && ok) ok = mbar_wait(odone, (j - 1) & 1, p.wait_limit, abort_flag);
-      ok = __all_sync(0xffffffffu, ok);
-      tc_fence_after();
-      if (j == 0) {
-        m = mx;
-      } else {
-        // rows whose max grew by more than 2^8 take the new max and scale
-        // their O by alpha; the other rows of the warp keep theirs (alpha 1)
-        const bool grow = mx > m + kRescale;
-        const float alpha = grow ? exp2f(m - mx) : 1.0f;
-        if (grow) {
-          l *= alpha;
-          m = mx;
-        }
-        if (__any_sync(0xffffffffu, grow) && ok) {
-#pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
+          for (int c = 0; c < 4; ++c) {
             uint32_t u[32];
-            tmem_ld_32x32b_x32(trow + kO + 32 * c, u);
+            tmem_ld_32x32b_x32(trow + 32 * c, u);
             tmem_ld_wait();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) u[e] = __float_as_uint(__uint_as_float(u[e]) * alpha);
-            tmem_st_32x32b_x32(trow + kO + 32 * c, u);
+            for (int e = 0; e < 32; ++e) sv[32 * c + e] = __uint_as_float(u[e]);
           }
-          tmem_st_wait();
         }
-      }
-      // P = exp2(s - m) in fp16, 8 keys (one 16-byte chunk) at a time, into the
-      // swizzled K-major panels (chunk c8 of row r at c8 ^ (r % 8))
-      float lsum = 0.0f;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sfree);   // S may be overwritten by the next tile's scores
+        // causal mask on the diagonal tile (the same for the whole warp): key
+        // 128j + c is visible iff c <= r there
+        if (j == it.qt) {
 #pragma unroll
-      for (int c8 = 0; c8 < 16; ++c8) {
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float p0 = exp2f(sv[8 * c8 + 2 * e] - m), p1 = exp2f(sv[8 * c8 + 2 * e + 1] - m);
-          const __half2 h2 = __floats2half2_rn(p0, p1);
-          lsum += __low2float(h2) + __high2float(h2);   // the weights the MMA multiplies
-          w[e] = *reinterpret_cast<const uint32_t*>(&h2);
+          for (int c = 0; c < 128; ++c)
+            if (c > r) sv[c] = -INFINITY;
         }
-        const int panel = c8 >> 3, chunk = c8 & 7;
-        *reinterpret_cast<uint4*>(prow + panel * S::kPanel + ((chunk ^ (r & 7)) << 4)) =
-            make_uint4(w[0], w[1], w[2], w[3]);
-      }
-      l += lsum;
-      fence_proxy_async_smem();   // P (generic writes) before the MMA reads it
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(pfull);
-    }
-    // ---- O / l -> fp16 ---------------------------------------------------------------
-    if (ok) ok = mbar_wait(odone, (nkt - 1) & 1, p.wait_limit, abort_flag);
-    ok = __all_sync(0xffffffffu, ok && !*abort_flag);
-    tc_fence_after();
-    if (ok) {
-      const float inv = 1.0f / l;
-      __half* dst = p.out + static_cast<size_t>(row0 + qpos) * p.ldo + h * D;
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 128; ++c) mx = fmaxf(mx, sv[c]);
+        mx *= p.scale_log2;   // in base-2 units, like m
+        // P may be written once the previous tile's PV (of any item) has read
+        // it; O may be rescaled only then too
+        if (g > 0 && ok) ok = mbar_wait(odone, (g - 1) & 1, p.wait_limit, abort_flag);
+        ok = __all_sync(0xffffffffu, ok);
+        tc_fence_after();
+        if (j == 0) {
+          m = mx;
+        } else {
+          // rows whose max grew by more than 2^8 take the new max and scale
+          // their O by alpha; the other rows of the warp keep theirs (alpha 1)
+          const bool grow = mx > m + kRescale;
+          const float alpha = grow ? ex2_approx(m - mx) : 1.0f;
+          if (grow) {
+            l *= alpha;
+            m = mx;
+          }
+          if (__any_sync(0xffffffffu, grow) && ok) {
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t u[32];
-        tmem_ld_32x32b_x32(trow + kO + 32 * c, u);
-        tmem_ld_wait();
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t u[32];
+              tmem_ld_32x32b_x32(trow + ob + 32 * c, u);
+              tmem_ld_wait();
 #pragma unroll
-        for (int v = 0; v < 4; ++v) {
+              for (int e = 0; e < 32; ++e) u[e] = __float_as_uint(__uint_as_float(u[e]) * alpha);
+              tmem_st_32x32b_x32(trow + ob + 32 * c, u);
+            }
+            tmem_st_wait();
+          }
+        }
+        // P = 2^(s * scale - m) in fp16, 8 keys (one 16-byte chunk) at a time,
+        // into the swizzled K-major panels (chunk c8 of row r at c8 ^ (r % 8));
+        // the row sum takes the fp16 weights the MMA multiplies
+        const float negm = -m;
+        float lsum = 0.0f;
+#pragma unroll
+        for (int c8 = 0; c8 < 16; ++c8) {
           uint32_t w[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const __half2 h2 = __floats2half2_rn(__uint_as_float(u[8 * v + 2 * e]) * inv,
-                                                 __uint_as_float(u[8 * v + 2 * e + 1]) * inv);
+            const __half2 h2 = __floats2half2_rn(ex2_approx(fmaf(sv[8 * c8 + 2 * e], p.scale_log2, negm)),
+                                                 ex2_approx(fmaf(sv[8 * c8 + 2 * e + 1], p.scale_log2, negm)));
             w[e] = *reinterpret_cast<const uint32_t*>(&h2);
+            lsum = add_pair_f16(lsum, w[e]);
           }
-          *reinterpret_cast<uint4*>(dst + 32 * c + 8 * v) = make_uint4(w[0], w[1], w[2], w[3]);
+          const int panel = c8 >> 3, chunk = c8 & 7;
+          *reinterpret_cast<uint4*>(prow + panel * S::kPanel + ((chunk ^ (r & 7)) << 4)) =
+              make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        l += lsum;
+        fence_proxy_async_smem();   // P (generic writes) before the MMA reads it
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(pfull);
+      }
+      // ---- the item's O / l -> fp16, then its O block is free -----------------------
+      if (ok) ok = mbar_wait(odone, (g - 1) & 1, p.wait_limit, abort_flag);
+      ok = __all_sync(0xffffffffu, ok && !*abort_flag);
+      tc_fence_after();
+      if (ok) {
+        const float inv = 1.0f / l;
+        __half* dst = p.out + static_cast<size_t>(it.bi * p.s + qpos) * p.ldo + it.h * D;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t u[32];
+          tmem_ld_32x32b_x32(trow + ob + 32 * c, u);
+          tmem_ld_wait();
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const __half2 h2 = __floats2half2_rn(__uint_as_float(u[8 * v + 2 * e]) * inv,
+                                                   __uint_as_float(u[8 * v + 2 * e + 1]) * inv);
+              w[e] = *reinterpret_cast<const uint32_t*>(&h2);
+            }
+            *reinterpret_cast<uint4*>(dst + 32 * c + 8 * v) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
         }
       }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ofree[n & 1]);
     }
   }
   // ---- teardown: every MMA done, then the tensor memory is freed ----------------------
@@ -349,12 +443,15 @@ fg_status launch_pa(const void* qkv, int64_t ld, int64_t b, int64_t s, int32_t h
   p.heads = heads;
   p.h1 = heads * D;
   p.qtiles = static_cast<int>(s / kTile);
+  p.bh = static_cast<int>(b * heads);
+  p.items = p.bh * p.qtiles;
   p.scale_log2 = static_cast<float>(1.4426950408889634074 / sqrt(static_cast<double>(D)));
   p.err = device_error_word();
   if (!p.err) return fail(FG_ERR_CUDA, "device error word");
   p.wait_limit = wait_limit();
   Trace tr(KC_ATTN_PREFILL, st);
-  const unsigned grid = static_cast<unsigned>(b * heads * p.qtiles);
+  // persistent: one CTA per SM (the shared memory admits no second one)
+  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(p.items, num_sms()));
   prefill_attn_tc_kernel<D><<<grid, kThreads, S::kBytes, st>>>(p);
   return check_launch("prefill_attn_tc_kernel");
 }
