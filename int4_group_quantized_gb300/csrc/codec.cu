@@ -111,8 +111,10 @@ struct KVDst {
 // consecutive tokens, so that the codes and (min, scale) pairs it writes are
 // contiguous in the cache (slot-major per head): 8 lanes per 64-group, the
 // groups of a head row side by side, 32 / (8 * groups per head) tokens at
-// a time, two such batches in flight.
+// a time, kKvBatches such batches in flight (four measured slower: fewer
+// warps fit).
 constexpr int kKvTokens = 32;
+constexpr int kKvBatches = 2;
 
 template <typename T, int NG>
 __global__ void __launch_bounds__(256) kv_store_q4_kernel(const T* __restrict__ ksrc,
@@ -136,13 +138,13 @@ __global__ void __launch_bounds__(256) kv_store_q4_kernel(const T* __restrict__ 
     const int64_t t0 = ch * kKvTokens, t1 = min(ntok, t0 + kKvTokens);
     const T* src = (which ? vsrc : ksrc) + (bi * ntok) * ld + h * D + gi * 64 + part * 8;
     const int64_t slot0 = bh * cap + pos0;
-    uint32_t* codes = dst.codes[which];
-    float* mins = dst.mins[which];
-    float* scales = dst.scales[which];
-    for (int64_t tt = t0; tt < t1; tt += 2 * kTpi) {
-      float v[2][8];
+    uint32_t* codes = which ? dst.codes[1] : dst.codes[0];   // selects: no local copy of the parameter
+    float* mins = which ? dst.mins[1] : dst.mins[0];
+    float* scales = which ? dst.scales[1] : dst.scales[0];
+    for (int64_t tt = t0; tt < t1; tt += kKvBatches * kTpi) {
+      float v[kKvBatches][8];
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
+      for (int u = 0; u < kKvBatches; ++u) {
         const int64_t ti = tt + u * kTpi + tb;
         if (ti < t1) {
           load8(src + ti * ld, v[u]);
@@ -152,7 +154,7 @@ __global__ void __launch_bounds__(256) kv_store_q4_kernel(const T* __restrict__ 
         }
       }
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
+      for (int u = 0; u < kKvBatches; ++u) {
         const int64_t ti = tt + u * kTpi + tb;
         float mn, sc;
         const uint32_t packed = quantize_group8(v[u], mn, sc);   // every lane of the group takes part
