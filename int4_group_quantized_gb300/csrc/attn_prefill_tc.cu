@@ -7,9 +7,10 @@
 // min)) (written back by the K/V store), so that the attention reads
 // exactly the cached values.  s is a multiple of 128.
 //
-// A persistent kernel: one CTA per SM takes the items (sequence, head,
-// 128-query tile), longest first, dealt round-robin over the CTAs, and runs
-// each flash-style over its 128-key tiles up to the diagonal:
+// A persistent kernel: one CTA per SM takes items (sequence, head,
+// 128-query tile) in units that pair a head's long and short query tiles,
+// dealt round-robin so that a head's units run side by side (see PaItem),
+// and runs each item flash-style over its 128-key tiles up to the diagonal:
 //   * a TMA thread loads Q of an item into one of two buffers and the K, V
 //     tiles into a two-stage ring that runs on across items (one tensor map
 //     over the buffer, boxes of 64 columns x 128 rows, 128-byte swizzle:
@@ -62,7 +63,9 @@ struct PaParams {
   int s, heads, h1;
   int qtiles;           // s / 128
   int bh;               // b * heads
-  int items;            // b * heads * qtiles
+  int npairs;           // qtiles / 2: paired query tiles per head
+  int pair_units;       // bh * npairs
+  int units;            // pair_units + (bh if qtiles is odd)
   float scale_log2;     // log2(e) / sqrt(head_dim)
   unsigned int* err;
   uint32_t wait_limit;
@@ -97,16 +100,44 @@ __device__ __forceinline__ float add_pair_f16(float acc, uint32_t h2) {
   return r;
 }
 
-// Item k of the longest-first order: query tile qt of (sequence bi, head h).
+// The work of a head (sequence bi, head h) is its query tiles qt = 0 ..
+// qtiles-1, qt costing qt+1 key tiles.  Units pair tile qtiles-1-p with tile
+// p (both cost qtiles+1 together); with an odd count the middle tile is a
+// unit of its own.  Units run head by head, pairs before singles, dealt
+// round-robin over the CTAs: every CTA gets the same work within one unit,
+// and the two units of a head land on neighbouring CTAs in the same round,
+// so that they read the head's K/V tiles from L2 rather than DRAM twice.
 struct PaItem {
   int qt, bi, h;
 };
-__device__ __forceinline__ PaItem pa_item(const PaParams& p, int k) {
+// Items of CTA c (its units in order, a pair unit's longer tile first).
+__device__ __forceinline__ int pa_pair_rounds(const PaParams& p, int c) {
+  return c < p.pair_units ? (p.pair_units - c + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x) : 0;
+}
+__device__ __forceinline__ int pa_items(const PaParams& p, int c) {
+  const int G = static_cast<int>(gridDim.x);
+  const int rp = pa_pair_rounds(p, c);
+  const int rall = c < p.units ? (p.units - c + G - 1) / G : 0;
+  return 2 * rp + (rall - rp);
+}
+__device__ __forceinline__ PaItem pa_item(const PaParams& p, int c, int i) {
+  const int G = static_cast<int>(gridDim.x);
+  const int rp = pa_pair_rounds(p, c);
+  int head, qt;
+  if (i < 2 * rp) {
+    const int u = c + (i >> 1) * G;
+    head = u / p.npairs;
+    const int pr = u - head * p.npairs;
+    qt = (i & 1) ? pr : p.qtiles - 1 - pr;
+  } else {
+    const int u = c + (rp + (i - 2 * rp)) * G;
+    head = u - p.pair_units;
+    qt = p.qtiles >> 1;
+  }
   PaItem it;
-  it.qt = p.qtiles - 1 - k / p.bh;
-  const int bh = k % p.bh;
-  it.bi = bh / p.heads;
-  it.h = bh % p.heads;
+  it.qt = qt;
+  it.bi = head / p.heads;
+  it.h = head % p.heads;
   return it;
 }
 
@@ -138,7 +169,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_tc_kernel(const __gr
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int G = static_cast<int>(gridDim.x);
+  const int c = static_cast<int>(blockIdx.x);
+  const int nitems = pa_items(p, c);   // the host launches no CTA without work
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
@@ -168,8 +200,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_tc_kernel(const __gr
     if (lane == 0) {
       int q_issued = 0, g_issued = 0;
       bool ok = true;
-      for (int k = blockIdx.x; k < p.items && ok; k += G) {
-        const PaItem it = pa_item(p, k);
+      for (int i = 0; i < nitems && ok; ++i) {
+        const PaItem it = pa_item(p, c, i);
         const int row0 = it.bi * p.s;
         const int qb = q_issued & 1;
         if (!mbar_wait(&qfree[qb], ((q_issued >> 1) & 1) ^ 1, p.wait_limit, abort_flag)) break;
@@ -223,21 +255,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_tc_kernel(const __gr
         if (last) mma_commit(&qfree[n & 1]);
         return true;
       };
-      bool ok = true;
-      int k = blockIdx.x, n = 0, j = 0, g = 0;
-      PaItem it = pa_item(p, k);
-      ok = mbar_wait(&qfull[0], 0, p.wait_limit, abort_flag) && issue_s(0, 0, it.qt == 0);
+      bool ok = nitems > 0;
+      int n = 0, j = 0, g = 0;   // item, its tile, the CTA's tile
+      PaItem it = pa_item(p, c, 0);
+      ok = ok && mbar_wait(&qfull[0], 0, p.wait_limit, abort_flag) && issue_s(0, 0, it.qt == 0);
       while (ok) {
         // the tile after g: the next of this item, or the first of the next item
-        int kn = k, nn = n, jn = j + 1;
+        int nn = n, jn = j + 1;
         PaItem itn = it;
         if (jn > it.qt) {
-          kn = k + G;
           nn = n + 1;
           jn = 0;
-          if (kn < p.items) itn = pa_item(p, kn);
+          if (nn < nitems) itn = pa_item(p, c, nn);
         }
-        const bool has_next = kn < p.items;
+        const bool has_next = nn < nitems;
         if (has_next) {
           if (jn == 0 && !mbar_wait(&qfull[nn & 1], (nn >> 1) & 1, p.wait_limit, abort_flag)) {
             ok = false;
@@ -268,7 +299,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_tc_kernel(const __gr
         mma_commit(&kvfree[g & 1]);   // K_g and V_g are read
         mma_commit(odone);
         if (!has_next) break;
-        k = kn;
         n = nn;
         j = jn;
         it = itn;
@@ -286,8 +316,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_tc_kernel(const __gr
     uint8_t* prow = sP + r * 128;         // this row in each P panel
     bool ok = true;
     int g = 0, n = 0;
-    for (int k = blockIdx.x; k < p.items && ok; k += G, ++n) {
-      const PaItem it = pa_item(p, k);
+    for (; n < nitems && ok; ++n) {
+      const PaItem it = pa_item(p, c, n);
       const uint32_t ob = kO + (n & 1) * D;
       const int qpos = it.qt * kTile + r;   // the query's position in its sequence (row r of the tile)
       float m = -INFINITY, l = 0.0f;
@@ -444,14 +474,17 @@ fg_status launch_pa(const void* qkv, int64_t ld, int64_t b, int64_t s, int32_t h
   p.h1 = heads * D;
   p.qtiles = static_cast<int>(s / kTile);
   p.bh = static_cast<int>(b * heads);
-  p.items = p.bh * p.qtiles;
+  p.npairs = p.qtiles / 2;
+  p.pair_units = p.bh * p.npairs;
+  p.units = p.pair_units + (p.qtiles % 2 ? p.bh : 0);
   p.scale_log2 = static_cast<float>(1.4426950408889634074 / sqrt(static_cast<double>(D)));
   p.err = device_error_word();
   if (!p.err) return fail(FG_ERR_CUDA, "device error word");
   p.wait_limit = wait_limit();
   Trace tr(KC_ATTN_PREFILL, st);
-  // persistent: one CTA per SM (the shared memory admits no second one)
-  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(p.items, num_sms()));
+  // persistent: one CTA per SM (the shared memory admits no second one),
+  // and no more CTAs than units
+  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(p.units, num_sms()));
   prefill_attn_tc_kernel<D><<<grid, kThreads, S::kBytes, st>>>(p);
   return check_launch("prefill_attn_tc_kernel");
 }
