@@ -274,7 +274,11 @@ size_t fg_decode_workspace_bytes(const fg_layer* L, int64_t b, int64_t capacity)
  * prompt tokens into slots 0..s-1 of kv (quantized per [S5]); attention is
  * causal and reads K/V back through the codec, so the new tokens see the
  * same values a later decode step reads.  Requires kv->b == b,
- * s <= kv->capacity, and ws_bytes >= fg_prefill_workspace_bytes(L, b, s). */
+ * s <= kv->capacity, and ws_bytes >= fg_prefill_workspace_bytes(L, b, s).
+ * fp16 layers with a 4-bit cache, s a multiple of 128 and head_dim 64 or
+ * 128 run the attention on the tensor cores (tcgen05), one CTA per SM;
+ * other prompts take the warp-level MMA kernel.  Both give the same values
+ * up to rounding. */
 fg_status fg_prefill_layer(const fg_layer* L, const void* x, int64_t b, int64_t s,
                            const fg_kv* kv, void* y, void* ws, size_t ws_bytes,
                            cudaStream_t stream);
